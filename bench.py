@@ -1,0 +1,434 @@
+#!/usr/bin/env python
+"""Benchmark of the Block-GTQ packed-cache decode path on GB300.
+
+One step = one decode step of the whole workload: for every layer, append the
+new token to the packed cache (bgtq_quantize_append) and run decode attention
+over the packed cache (bgtq_decode_attn).  The default workload is the
+Qwen2.5-3B-shaped 36-layer stack at 131072 cached tokens, K3V3 (2 KV heads,
+16 query heads, batch 1).  The step's launches are captured once in a CUDA
+graph and replayed.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gpu|reference]
+                  [--workload NAME]
+
+--impl reference times the CPU oracle (the plain restatement of the method)
+on the host cores, on a bounded sample of the same workload.  Under torchrun
+each rank runs an independent replica (the path shards by sequence/head with
+no exchange); value = all ranks' tokens / max-over-ranks time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "packed-KV decode attn: tokens/s & achieved HBM GB/s (% of peak) at 128K ctx"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_attn_qwen3b_36l_128k.txt")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    ap.add_argument("--workload", default="qwen3b_36l_128k")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--sample-seconds", type=float, default=12.0, help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+def env_rank():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ----------------------------------------------------------------------------- CPU oracle sample
+
+class OracleSample:
+    """The oracle's decode step on one (layer, head) sample of the workload.
+
+    One repetition unpacks and dequantises the sample's packed K/V cache,
+    runs float64 attention for the head's G queries, and encodes + packs one
+    new token.  Cost scales with the cached token-heads a step reads.
+    """
+
+    TOKENS = 8192
+
+    def __init__(self, workload: str):
+        from oracle import bgtq_oracle as O
+        from rope_aware_quantized_gb300 import synth, workloads
+        self.O = O
+        w = workloads.WORKLOADS[workload]
+        self.li = synth.layer_inputs(w.seed, 0, 1, w.group, self.TOKENS, w.rope_base, w.s_ln)
+        self.hs = O.head_state(workloads.calib_keys(w, 0, 0), w.bits_per_key, w.v_bits,
+                               workloads.plan_seed(w, 0), 0)
+        enc = O.encode_head(self.hs, self.li.k[0], self.li.v[0])
+        self.krec, self.vrec, self.krho, self.vrho = enc["krec"], enc["vrec"], enc["krho"], enc["vrho"]
+
+    def rep(self):
+        O, hs, li = self.O, self.hs, self.li
+        kcodes = O.unpack_k(self.krec, hs.kc, hs.bk)
+        vcodes = O.unpack_v(self.vrec, hs.bv, self.TOKENS)
+        khat = O.dequant(kcodes, self.krho, hs.kc)
+        vhat = O.dequant(vcodes, self.vrho, hs.vc)
+        O.attention(li.q, khat, vhat)
+        nk, _ = O.encode(li.k[0][:1], hs.kc)
+        O.pack_k(nk, hs.kc, hs.bk)
+        nv, _ = O.encode(li.v[0][:1], hs.vc)
+        O.pack_v(nv, hs.bv)
+
+
+def oracle_sample(workload: str, seconds: float):
+    s = OracleSample(workload)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        s.rep()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= 400:
+            break
+    return {"sec_per_token_head": el / (reps * s.TOKENS), "reps": reps, "tokens": s.TOKENS, "seconds": el}
+
+
+def single_thread_env():
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k] = "1"
+
+
+def cpu_baseline(workload: str, seconds: float):
+    """Run the oracle sample in a single-threaded child process."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env.pop("RANK", None)
+    env.pop("WORLD_SIZE", None)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", "--workload", workload,
+                        "--sample-seconds", str(seconds)], capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError("oracle sample failed:\n" + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_line_fields(workload: str, sample: dict):
+    from rope_aware_quantized_gb300 import workloads
+    w = workloads.WORKLOADS[workload]
+    token_heads = int(w.seq_lens().sum()) * w.n_kv * w.layers
+    step_s = sample["sec_per_token_head"] * token_heads
+    value = w.batch / step_s
+    desc = (f"oracle decode step on one (layer, head) of {sample['tokens']} cached tokens x {sample['reps']} reps "
+            f"({sample['seconds']:.1f} s): unpack + dequantise K/V, float64 attention for {w.group} queries, "
+            f"encode + pack 1 token; scaled to {token_heads} token-heads per step")
+    return value, step_s, desc
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        load = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_from_profile():
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current decode kernel source."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    src = os.path.join(ROOT, "rope_aware_quantized_gb300", "csrc", "decode_attn.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    vals = {}
+    for line in open(PROFILE_SUMMARY):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("decode_attn.cu sha256[:16]") != sha:
+        return None
+    try:
+        return float(vals["dram bytes per launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    import rope_aware_quantized_gb300 as bg
+    from rope_aware_quantized_gb300 import workloads
+
+    rank, local_rank, world = env_rank()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    bg._native.lib()
+    w = workloads.WORKLOADS[args.workload]
+    lens = w.seq_lens()
+    max_len = int(lens.max())
+    L, B = w.layers, w.batch
+
+    # device buffers of all layers' per-step inputs/outputs (views per layer)
+    q_all = torch.empty((L, B, w.n_q, 128), dtype=torch.float16, device="cuda")
+    nk_all = torch.empty((L, B, w.n_kv, 1, 128), dtype=torch.float16, device="cuda")
+    nv_all = torch.empty_like(nk_all)
+    out_all = torch.empty((L, B, w.n_q, 128), dtype=torch.float16, device="cuda")
+    layers = []
+    for l in range(L):
+        ls = workloads.build_layer(w, l)
+        q_all[l].copy_(ls.q)
+        nk_all[l].copy_(ls.new_k)
+        nv_all[l].copy_(ls.new_v)
+        ls.q, ls.new_k, ls.new_v = q_all[l], nk_all[l], nv_all[l]
+        layers.append(ls)
+    torch.cuda.synchronize()
+    ws = torch.zeros(bg.bgtq_decode_attn_workspace(layers[0].plan, B, max_len), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def step():
+        for l, ls in enumerate(layers):
+            bg.bgtq_quantize_append(ls.plan, ls.new_k, ls.new_v, ls.pos_new, ls.cache, status=status)
+            bg.bgtq_decode_attn(ls.plan, ls.q, ls.cache, ls.seq_lens, max_len, out_all[l], ws, status=status)
+
+    with torch.cuda.stream(stream):
+        step()
+        step()
+    torch.cuda.synchronize()
+    assert status.item() == 0, f"device status {status.item()}"
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    launches_per_step = 2 * L
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        graph.replay()
+    barrier()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * B / (ms / 1000.0)
+
+    # dominant kernel alone: CUDA events around each decode launch on its stream
+    durs = []
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            for l, ls in enumerate(layers):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                bg.bgtq_decode_attn(ls.plan, ls.q, ls.cache, ls.seq_lens, max_len, out_all[l], ws, status=status)
+                b.record(stream)
+                durs.append((a, b))
+    torch.cuda.synchronize()
+    launch_ms = statistics.mean(a.elapsed_time(b) for a, b in durs)
+    bpth = w.packed_bytes_per_token_head()
+    decode_bytes = int(lens.sum()) * w.n_kv * bpth + B * w.n_q * 128 * 2 * 2
+    peaks, peak_kind = load_peaks()
+    achieved = decode_bytes / (launch_ms / 1000.0) / 1e9
+    traffic = traffic_from_profile()
+    step_bytes = L * decode_bytes
+
+    # end to end: pinned host inputs -> device, graph replay, outputs -> host
+    hq = torch.empty(q_all.shape, dtype=q_all.dtype, pin_memory=True)
+    hk = torch.empty(nk_all.shape, dtype=nk_all.dtype, pin_memory=True)
+    hv = torch.empty(nv_all.shape, dtype=nv_all.dtype, pin_memory=True)
+    ho = torch.empty(out_all.shape, dtype=out_all.dtype, pin_memory=True)
+    hq.copy_(q_all)
+    hk.copy_(nk_all)
+    hv.copy_(nv_all)
+    torch.cuda.synchronize()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with torch.cuda.stream(stream):
+        x0.record(stream)
+        for _ in range(args.steps):
+            q_all.copy_(hq, non_blocking=True)
+            nk_all.copy_(hk, non_blocking=True)
+            nv_all.copy_(hv, non_blocking=True)
+            graph.replay()
+            ho.copy_(out_all, non_blocking=True)
+        x1.record(stream)
+    barrier()
+    e2e_ms = x0.elapsed_time(x1) / args.steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    assert status.item() == 0, f"device status {status.item()}"
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        s = cpu_baseline(args.workload, args.sample_seconds)
+        v, _, desc = cpu_line_fields(args.workload, s)
+        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        fp16_bytes = int(lens.sum()) * w.n_kv * 512 * L
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
+            "config": {
+                "workload": w.name, "layers": L, "kv_heads": w.n_kv, "q_heads": w.n_q, "head_dim": 128,
+                "context": int(max_len), "batch": B, "kv_bits": f"K{w.bits_per_key // 128}V{w.v_bits}",
+                "step": "per layer: quantize-append 1 token + decode attention (CUDA graph)",
+                "packed_bytes_per_step": step_bytes, "fp16_kv_bytes_per_step": fp16_bytes,
+                "compute": "fp16 mma operands (hi+lo split of q and p), fp32 accumulate; fp32 encoder",
+                "l2": "inputs larger than L2 (packed cache per step >> 129 MB L2), no flush",
+                "parallelism": f"replicas x{world}",
+            },
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                         "kernel": "decode_attn", "launch_ms": launch_ms, "bytes_per_launch": decode_bytes,
+                         "peak_kind": f"{peak_kind} (copy, burst)"},
+            "e2e": {"value": world * B / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "path": "pinned H2D of q/new K/V, graph of the API calls, D2H of out"},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+            "achieved_step_gbs": step_bytes / (ms / 1000.0) / 1e9,
+        }
+        if cpu:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- reference arm (CPU oracle)
+
+def run_reference(args):
+    rank, _, world = env_rank()
+    if rank != 0:
+        return
+    single_thread_env()
+    from rope_aware_quantized_gb300 import workloads
+    w = workloads.WORKLOADS[args.workload]
+    sample = OracleSample(args.workload)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        sample.rep()
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    per_th = statistics.mean(times) / sample.TOKENS
+    s = {"sec_per_token_head": per_th, "reps": len(times), "tokens": sample.TOKENS, "seconds": sum(times)}
+    value, step_s, desc = cpu_line_fields(args.workload, s)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_s * 1000.0, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "layers": w.layers, "kv_heads": w.n_kv, "q_heads": w.n_q,
+                   "context": int(w.seq_lens().max()), "batch": w.batch,
+                   "kv_bits": f"K{w.bits_per_key // 128}V{w.v_bits}"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.oracle_sample:
+        single_thread_env()
+        print(json.dumps(oracle_sample(args.workload, args.sample_seconds)), flush=True)
+        return
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,232 @@
+/*
+ * bgtq.h — C ABI of the Block-GTQ packed-cache decode library (GB300, sm_103a).
+ *
+ * The method: "RoPE-Aware Bit Allocation for KV-Cache Quantization".  Under
+ * RoPE a key's contribution to a logit is a sum over 2-D frequency blocks
+ * (English abstract); Block-GTQ scores each RoPE block of each (layer, KV
+ * head) with a label-free energy from calibration data and greedily assigns
+ * integer bit widths by marginal gain under the TQ-MSE 4^-b distortion rate
+ * (English abstract; paper review §1 Key Terms, §3 Method & Key Results).
+ * Values use uniform TQ-MSE.  The packed-cache serving path attends directly
+ * on the compressed cache, never materialising an fp16 KV cache (abstract;
+ * review §1 "Packed-Cache", Figure 2).
+ *
+ * Conventions for every entry point:
+ *   - Return value: BGTQ_OK (0) or a negative BGTQ_ERR_* code; the message of
+ *     the last failure on the calling thread is returned by bgtq_last_error().
+ *   - "device" pointers are CUDA device memory owned by the caller; "host"
+ *     pointers are ordinary host memory owned by the caller.  The library
+ *     allocates device memory only in bgtq_plan_create (its read-only tables,
+ *     freed by bgtq_plan_destroy).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Device work is enqueued asynchronously on it; no call
+ *     synchronises the host except bgtq_plan_create/destroy.
+ *   - head_dim must be 128.  Inputs must be finite: NaN/Inf inputs give
+ *     unspecified codes, never a fault.
+ *   - Errors discovered on the device (positions beyond the cache capacity,
+ *     sequence lengths beyond capacity) are OR-ed into an optional device
+ *     status word (BGTQ_STATUS_* bits) and the offending work is skipped.
+ *
+ * Cache layout of one layer (all caller-owned device memory, see
+ * bgtq_cache_bytes):
+ *   k_codes [B][H][capacity][16*bK] bytes  one K record per token
+ *   v_codes [B][H][capacity/2][32*bV] bytes one V record per token pair
+ *   k_norm, v_norm [B][H][capacity] float   per-token norms (side data)
+ * with bK = bits_per_key / 128, bV = v_bits, capacity even.
+ */
+#ifndef BGTQ_H
+#define BGTQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BGTQ_OK 0
+#define BGTQ_ERR_INVALID_ARG (-1)
+#define BGTQ_ERR_UNSUPPORTED (-2)
+#define BGTQ_ERR_CAPACITY (-3)
+#define BGTQ_ERR_WORKSPACE (-4)
+#define BGTQ_ERR_CUDA (-5)
+#define BGTQ_ERR_DEVICE_CHECK (-6)
+
+/* device status bits */
+#define BGTQ_STATUS_APPEND_CAPACITY 1 /* pos_start + t_new > capacity: that sequence was skipped */
+#define BGTQ_STATUS_SEQLEN_CAPACITY 2 /* seq_len > capacity or < 0: clamped */
+
+/* plan flags */
+#define BGTQ_PLAN_HOST_ONLY 1 /* build the tables on the host only (inspection, no GPU needed) */
+
+typedef struct bgtq_plan bgtq_plan;
+
+/* One layer's packed cache.  Passed by pointer; the struct itself is read on
+ * the host only. */
+typedef struct {
+    void* k_codes;    /* device, [B][H][capacity][16*bK] bytes */
+    float* k_norm;    /* device, [B][H][capacity] */
+    void* v_codes;    /* device, [B][H][capacity/2][32*bV] bytes */
+    float* v_norm;    /* device, [B][H][capacity] */
+    int64_t capacity; /* tokens per (sequence, head); must be even */
+} bgtq_cache;
+
+/* Message of the last failure on this thread ("" if none).  Never NULL. */
+const char* bgtq_last_error(void);
+
+/*
+ * bgtq_alloc_bits — Block-GTQ allocation for one (layer, KV head).
+ * Source: abstract ("computes a label-free energy score for each RoPE block
+ * and greedily allocates integer bit widths by marginal gain"), review §3
+ * (the gain uses the TQ-MSE 4^-b rate within the budget).
+ *   calib_keys_fp16  host, [n][head_dim] IEEE half bit patterns, keys as cached
+ *                    (RoPE applied)
+ *   bits_per_key     even, >= 0: bits spent per key (K3 = 384); every greedy
+ *                    step gives one bit to both coordinates of a block
+ *   b_max            1..8, largest width of a block
+ *   rope_layout      0 = half-split blocks (i, i+64), 1 = interleaved (2i, 2i+1)
+ *   block_bits_out   host, [head_dim/2] widths (sum = bits_per_key/2)
+ *   energy_out       host, [head_dim/2] float64 energies, may be NULL
+ * Energy: s_i = (1/n) sum_t (k_t[lo_i]^2 + k_t[hi_i]^2) in float64.  Greedy:
+ * the block maximising s_i*4^-b_i among b_i < b_max gets the next bit, ties
+ * to the smaller index.  Host only; never touches the GPU.
+ * Errors: INVALID_ARG for n <= 0, odd or oversized budgets, b_max out of range.
+ */
+int bgtq_alloc_bits(const uint16_t* calib_keys_fp16, int64_t n, int head_dim, int bits_per_key, int b_max,
+                    int rope_layout, uint8_t* block_bits_out, double* energy_out);
+
+/*
+ * bgtq_plan_create — codec tables of one layer (all KV heads).
+ * Source: TQ-MSE "rotates then quantises" with a near-optimal distortion rate
+ * (review §1 Key Terms); per-block widths from Block-GTQ (abstract).
+ *   n_kv_heads       KV heads of the layer (H)
+ *   group            query heads per KV head (G, 1..8); query head h reads
+ *                    KV head h / G
+ *   bits_per_key     multiple of 128 (bK = bits_per_key/128 words per lane slice)
+ *   v_bits           1..5, uniform value width
+ *   block_bits       host, [H][head_dim/2] widths from bgtq_alloc_bits
+ *   energy           host, [H][head_dim/2] energies from bgtq_alloc_bits
+ *   seed             per-layer seed of the random rotation signs
+ *   rope_layout      as in bgtq_alloc_bits
+ *   flags            0, or BGTQ_PLAN_HOST_ONLY
+ * Builds, per head: the codec order (width classes cut into aligned
+ * power-of-two rotation pieces), whitening, SplitMix64 rotation signs, the
+ * Lloyd-Max codebooks (fp16 centroids, float32 thresholds), the lane layout
+ * of the K record, and copies them to the current CUDA device (synchronous).
+ * Errors: INVALID_ARG (sizes, widths not summing to the budget);
+ * UNSUPPORTED (head_dim != 128, no balanced lane layout for an allocation);
+ * CUDA (device allocation or copy failed).
+ */
+int bgtq_plan_create(bgtq_plan** out, int head_dim, int n_kv_heads, int group, int bits_per_key, int v_bits,
+                     const uint8_t* block_bits, const double* energy, uint64_t seed, int rope_layout, int flags);
+
+/* Frees the plan and its device tables (synchronous).  NULL is accepted. */
+int bgtq_plan_destroy(bgtq_plan* plan);
+
+/*
+ * Host views of a plan's tables, for inspection and for checking them against
+ * an independent implementation.  The pointers stay valid until the plan is
+ * destroyed.  head in [0, H).
+ *   n_coded      coded coordinates of the head's keys (widths > 0)
+ *   perm         [128] codec index -> original dim (first n_coded valid)
+ *   width        [128] code width of each codec index
+ *   piece        [128] rotation piece size of each codec index
+ *   sign_k       [128] +1/-1 rotation signs of the keys (codec order)
+ *   sign_v       [128] +1/-1 rotation signs of the values
+ *   whiten       [128] float whitening multiplier of each codec index
+ *   dewhiten     [128] float de-whitening multiplier of each codec index
+ *   slot_pair    [4][16] K record lane layout: codec pair in each lane slot
+ *   slot_offset  [4][16] bit offset of each slot's field inside its lane slice
+ */
+typedef struct {
+    int n_coded;
+    const uint8_t* perm;
+    const uint8_t* width;
+    const uint8_t* piece;
+    const int8_t* sign_k;
+    const int8_t* sign_v;
+    const float* whiten;
+    const float* dewhiten;
+    const uint8_t* slot_pair;
+    const uint16_t* slot_offset;
+} bgtq_head_tables;
+
+int bgtq_plan_get_head(const bgtq_plan* plan, int head, bgtq_head_tables* out);
+
+/* Codebook of one width (0..8): 2^width fp16-exact centroids as floats and
+ * 2^width - 1 float thresholds (host pointers owned by the plan). */
+int bgtq_plan_get_codebook(const bgtq_plan* plan, int width, const float** centroids, const float** thresholds,
+                           int* n_levels);
+
+/* Byte sizes of one layer's cache buffers for `batch` sequences of `capacity`
+ * tokens (capacity even). */
+int bgtq_cache_bytes(const bgtq_plan* plan, int batch, int64_t capacity, size_t* k_codes_bytes,
+                     size_t* v_codes_bytes, size_t* norm_bytes);
+
+/*
+ * bgtq_quantize_append — encode and store new tokens (prefill chunk or one
+ * decode token).  Source: the packed cache is written from compressed K/V
+ * (abstract, packed-cache serving path); TQ-MSE encoder (review §1).
+ *   k_fp16, v_fp16   device, [batch][H][t_new][128] half (RoPE applied to K)
+ *   pos_start        device, [batch] int32: first cache position written for
+ *                    each sequence (not modified)
+ *   cache            host pointer to the layer's cache descriptor
+ *   dev_status       device int32 or NULL: BGTQ_STATUS_APPEND_CAPACITY is
+ *                    OR-ed in and the sequence skipped when pos_start +
+ *                    t_new > capacity or pos_start < 0
+ * Per token: rotate (whitened keys / raw values), store the float norm, code
+ * every coordinate against the Lloyd-Max thresholds, bit-pack at exactly the
+ * budget.  Bits of other tokens that share a V pair record are preserved.
+ * Errors: INVALID_ARG (null pointers, batch/t_new < 0, odd capacity,
+ * host-only plan); CUDA (launch failure).
+ */
+int bgtq_quantize_append(const bgtq_plan* plan, void* stream, const void* k_fp16, const void* v_fp16, int batch,
+                         int t_new, const int32_t* pos_start, const bgtq_cache* cache, int32_t* dev_status);
+
+/* Workspace bytes bgtq_decode_attn needs for `batch` sequences no longer than
+ * max_len.  The workspace must be zero-filled once before first use (its
+ * counters are returned to zero by every call). */
+int bgtq_decode_attn_workspace(const bgtq_plan* plan, int batch, int64_t max_len, size_t* bytes);
+
+/*
+ * bgtq_decode_attn — one decode step of attention on the packed cache.
+ * Source: packed-cache serving path that works on compressed K/V without an
+ * fp16 KV cache (abstract; review §1 "Packed-Cache", Figure 2).
+ *   q_fp16       device, [batch][H*G][128] half, RoPE applied
+ *   cache        host pointer to the layer's cache descriptor
+ *   seq_lens     device, [batch] int32 valid tokens per sequence (not modified);
+ *                values above capacity are clamped (status bit 2)
+ *   max_len      host upper bound of seq_lens (sizes the split-K grid)
+ *   out          device, [batch][H*G][128], half (out_dtype 0) or float (1)
+ *   softmax_scale  logit scale, e.g. 1/sqrt(128)
+ *   workspace    device scratch of bgtq_decode_attn_workspace bytes (zeroed
+ *                once before the first call)
+ *   dev_status   device int32 or NULL
+ * Computes o_g = sum_t softmax_t(scale * q_g . k_t) v_t over the dequantised
+ * cache: the query is rotated once into the codec domain, K/V codes are
+ * streamed from HBM and decoded by codebook lookup, the contractions run on
+ * tensor cores, and split-K partials are merged by the last CTA of each
+ * (sequence, head).  An empty sequence yields zeros.
+ * Errors: INVALID_ARG, WORKSPACE (too small), UNSUPPORTED (bK > 3 or G > 8),
+ * CUDA.
+ */
+int bgtq_decode_attn(const bgtq_plan* plan, void* stream, const void* q_fp16, const bgtq_cache* cache,
+                     const int32_t* seq_lens, int64_t max_len, int batch, void* out, int out_dtype,
+                     float softmax_scale, void* workspace, size_t ws_bytes, int32_t* dev_status);
+
+/*
+ * bgtq_dequant_debug — decode cached tokens [t0, t1) of (sequence b, head)
+ * back to float32, for inspection and parity checks.
+ *   k_out, v_out  device, [t1-t0][128] float (either may be NULL)
+ *   codec_domain  0: original dims (inverse rotation, de-whitening, scatter);
+ *                 1: codec-domain reconstruction rho * centroid per codec index
+ * Errors: INVALID_ARG (ranges outside the capacity, host-only plan), CUDA.
+ */
+int bgtq_dequant_debug(const bgtq_plan* plan, void* stream, const bgtq_cache* cache, int batch, int b, int head,
+                       int64_t t0, int64_t t1, float* k_out, float* v_out, int codec_domain);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BGTQ_H */

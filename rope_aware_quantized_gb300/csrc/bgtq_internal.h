@@ -1,0 +1,90 @@
+// Library-internal types shared by the host planner and the CUDA kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "bgtq.h"
+
+namespace bgtq {
+
+constexpr int kD = 128;      // head dim
+constexpr int kNB = 64;      // RoPE 2-D blocks per key
+constexpr int kWMax = 8;     // widest code
+constexpr int kPairMaxW = 5; // widest code decoded through the pair table
+
+// Pair table: entry (4^w + f) holds half2(c_w[f & (2^w-1)], c_w[f >> w]) for
+// w = 0..kPairMaxW, so a pre-shifted field f<<2 is OR-ed with (4^w)<<2.
+constexpr int kPairLutWords = 1 << (2 * kPairMaxW + 1);
+// Single table: entry (2^w + c) holds c_w[c] (fp16 bits) for w = 0..8.
+constexpr int kSingleLutHalves = 1 << (kWMax + 1);
+
+// Per-head device tables.  All arrays are in codec order unless noted.
+struct HeadTab {
+    int32_t n_coded;
+    uint32_t wide_mask;       // decode: slots decoded through the single table
+    int32_t pad[2];
+    uint8_t perm[kD];         // codec index -> original dim
+    uint8_t width[kD];        // code width per codec index (0 past n_coded)
+    uint8_t plog2[kD];        // log2 of the rotation piece size (0 past n_coded)
+    uint8_t slot_pair[4][16]; // decode lane layout: codec pair per (lane, slot)
+    uint8_t slot_w[4][16];    // width of that pair
+    uint8_t slot_sh[4][16];   // field shift inside the slot's 64-bit window
+    uint16_t pair_bit[kNB];   // absolute bit position of codec pair m in the K record
+    float whiten[kD];
+    float dewhiten[kD];
+    float inv_sqrt[kD];
+    float sign_k[kD];
+    float sign_v[kD];
+};
+
+struct DevTables {
+    HeadTab* heads = nullptr;     // [H]
+    float* cent = nullptr;        // [9][256] centroids (fp16-exact floats)
+    float* thr = nullptr;         // [9][256] thresholds (first 2^w - 1 used)
+    uint32_t* pair_lut = nullptr; // [kPairLutWords]
+    uint16_t* single_lut = nullptr; // [kSingleLutHalves]
+};
+
+}  // namespace bgtq
+
+struct bgtq_plan {
+    int H = 0, G = 0, bits_per_key = 0, bk = 0, bv = 0, rope_layout = 0, flags = 0;
+    uint64_t seed = 0;
+    int device = -1, num_sms = 0;
+    std::vector<bgtq::HeadTab> heads;
+    std::vector<float> cent[bgtq::kWMax + 1];
+    std::vector<float> thr[bgtq::kWMax + 1];
+    std::vector<uint32_t> pair_lut;
+    std::vector<uint16_t> single_lut;
+    // inspection copies (bgtq_plan_get_head)
+    std::vector<std::vector<int8_t>> sign_k8, sign_v8;
+    std::vector<std::vector<uint8_t>> piece;
+    std::vector<std::vector<uint16_t>> slot_off;
+    bgtq::DevTables dev;
+};
+
+namespace bgtq {
+
+int set_error(int code, const char* fmt, ...);
+
+// Kernel launchers (defined in the .cu files).  They only enqueue work.
+cudaError_t launch_quantize_append(const bgtq_plan& p, cudaStream_t s, const void* k, const void* v, int batch,
+                                   int t_new, const int32_t* pos_start, const bgtq_cache& c, int32_t* status);
+cudaError_t launch_dequant(const bgtq_plan& p, cudaStream_t s, const bgtq_cache& c, int batch, int b, int head,
+                           int64_t t0, int64_t t1, float* k_out, float* v_out, int codec_domain);
+
+struct SplitPlan {
+    int n_split = 1;
+    int tokens_per_split = 64;
+};
+SplitPlan decode_split(const bgtq_plan& p, int batch, int64_t max_len);
+size_t decode_workspace_bytes(const bgtq_plan& p, int batch, const SplitPlan& sp);
+cudaError_t launch_decode(const bgtq_plan& p, cudaStream_t s, const void* q, const bgtq_cache& c,
+                          const int32_t* seq_lens, int batch, const SplitPlan& sp, void* out, int out_dtype,
+                          float scale, void* ws, int32_t* status);
+
+}  // namespace bgtq

@@ -1,0 +1,499 @@
+// Split-K decode attention directly on the Block-GTQ packed cache.
+//
+// Method: "RoPE-Aware Bit Allocation for KV-Cache Quantization" — English
+// abstract and review §1 "Packed-Cache" / Figure 2: attention is computed on
+// the compressed K/V, no fp16 KV cache is materialised.
+//
+// Per CTA: one (sequence, KV head, token split).  Prologue: the G query heads
+// are rotated once into the key codec domain (de-whitening, signs, blockwise
+// Hadamard, 1/sqrt(piece), softmax scale and log2 e folded in) and split into
+// fp16 hi + lo parts that form the 16 rows of the mma A operand (rows 0..7 hi,
+// 8..15 lo).  Main loop, per warp and 16-token tile:
+//   S^T = Q_hilo . K_hat^T     8 k-chunks x 2 token n-tiles of m16n8k16 mma;
+//                              K_hat fragments come from a 64-bit window of
+//                              the lane's K record slice, one shift + mask +
+//                              one shared-memory pair-table lookup per 2 coords
+//   logits = (hi + lo rows) * rho_K * scale, online softmax per head (exp2)
+//   O_hilo += P_hilo . V_hat   16 dim n-tiles of m16n8k16 mma; P' = p*rho_V
+//                              split hi + lo into the A rows; V_hat fragments
+//                              come straight from the token-pair V records
+// Epilogue: per-CTA merge of the warps, partial (m, l, acc) to the workspace,
+// and the last CTA of the (sequence, head) merges all splits (log-sum-exp),
+// applies the inverse value rotation and writes the output.
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "bgtq_internal.h"
+
+namespace bgtq {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kTile = 16;
+constexpr int kGran = kWarps * kTile;  // tokens per CTA step; split granularity
+constexpr int kMaxSplit = 256;
+constexpr int kPartStride = 2 + kD;    // m, l, acc[128] per query head
+
+struct DecodeParams {
+    const __half* q;
+    const uint8_t* kc;
+    const float* kn;
+    const uint8_t* vc;
+    const float* vn;
+    int64_t cap;
+    const int32_t* seq_lens;
+    void* out;
+    int out_dtype;
+    float* part;
+    uint32_t* count;
+    const HeadTab* heads;
+    const uint32_t* pair_lut;
+    const uint16_t* single_lut;
+    float scale_log2;
+    float v_inv_sqrt;
+    int H, G, n_split, tps;
+    int32_t* status;
+};
+
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+// hi = fp16(x), lo = fp16(x - hi) for a pair of values
+__device__ __forceinline__ void split_hilo(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __half2 h = __floats2half2_rn(x0, x1);
+    const float2 hf = __half22float2(h);
+    hi = h2_bits(h);
+    lo = h2_bits(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
+}
+
+template <int BK>
+__device__ __forceinline__ uint32_t kword(const uint32_t (&kw)[BK], int i) {
+    return i < BK ? kw[i < BK ? i : 0] : 0u;
+}
+
+// Decoded fp16 pair of K slot `S` (compile-time) of the lane's record slice.
+template <int BK, int S>
+__device__ __forceinline__ uint32_t k_pair(const uint32_t (&kw)[BK], uint32_t sh, uint32_t mask, uint32_t base,
+                                           uint32_t wide, const uint32_t* s_pair, const uint16_t* s_single) {
+    constexpr bool kUpper = (BK == 3 && S >= 8);
+    static_assert(BK >= 1 && BK <= 3, "K record slices of 1..3 words");
+    const uint32_t lo = kUpper ? kword(kw, 1) : kword(kw, 0);
+    const uint32_t hi = kUpper ? kword(kw, 2) : kword(kw, 1);
+    const uint64_t win = ((uint64_t)hi << 32) | lo;
+    if (!((wide >> S) & 1u)) {
+        const uint32_t x = S == 0 ? (kword(kw, 0) << 2) : (uint32_t)(win >> sh);
+        const uint32_t addr = (x & mask) | base;
+        return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const char*>(s_pair) + addr);
+    }
+    const uint32_t x = S == 0 ? (kword(kw, 0) << 1) : (uint32_t)(win >> sh);
+    const uint32_t w = __popc(mask);
+    const uint32_t a0 = (x & mask) | base;
+    const uint32_t a1 = ((x >> w) & mask) | base;
+    const uint32_t h0 = *reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(s_single) + a0);
+    const uint32_t h1 = *reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(s_single) + a1);
+    return h0 | (h1 << 16);
+}
+
+// Decoded fp16 pair (even token, odd token) of V codec dim 16*g + ND from the
+// lane-group's BV words of a token-pair record.
+template <int BV, int ND>
+__device__ __forceinline__ uint32_t v_pair(const uint32_t (&vw)[BV], uint32_t vbase, const uint32_t* s_pair) {
+    constexpr int FB = 2 * BV;
+    constexpr int O = FB * ND;
+    constexpr int WI = O >> 5, SH = O & 31;
+    constexpr uint32_t MASK = ((1u << FB) - 1u) << 2;
+    uint32_t x;
+    if constexpr (SH == 0)
+        x = vw[WI] << 2;
+    else if constexpr (SH + FB <= 32)
+        x = vw[WI] >> (SH - 2);
+    else
+        x = __funnelshift_r(vw[WI], vw[WI + 1 < BV ? WI + 1 : WI], SH - 2);
+    const uint32_t addr = (x & MASK) | vbase;
+    return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const char*>(s_pair) + addr);
+}
+
+template <int BK, int BV, int C>
+__device__ __forceinline__ void s_chunk(float (&sacc)[2][4], const uint32_t (&qa)[8][4], const uint32_t (&kw)[2][BK],
+                                        const uint32_t (&ksh)[16], const uint32_t (&kmask)[16],
+                                        const uint32_t (&kbase)[16], uint32_t wide, const uint32_t* s_pair,
+                                        const uint16_t* s_single) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const uint32_t b0 = k_pair<BK, 2 * C>(kw[nt], ksh[2 * C], kmask[2 * C], kbase[2 * C], wide, s_pair, s_single);
+        const uint32_t b1 =
+            k_pair<BK, 2 * C + 1>(kw[nt], ksh[2 * C + 1], kmask[2 * C + 1], kbase[2 * C + 1], wide, s_pair, s_single);
+        mma16816(sacc[nt], qa[C], b0, b1);
+    }
+}
+
+template <int BV, int ND>
+__device__ __forceinline__ void pv_tile(float (&acc)[16][4], const uint32_t (&pa)[4], const uint32_t (&vw)[2][BV],
+                                        uint32_t vbase, const uint32_t* s_pair) {
+    const uint32_t b0 = v_pair<BV, ND>(vw[0], vbase, s_pair);
+    const uint32_t b1 = v_pair<BV, ND>(vw[1], vbase, s_pair);
+    mma16816(acc[ND], pa, b0, b1);
+}
+
+template <int BK, int BV>
+__global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) {
+    __shared__ __align__(16) uint32_t s_pair[kPairLutWords];
+    __shared__ __align__(16) uint16_t s_single[kSingleLutHalves];
+    __shared__ __align__(16) float s_q[8][kD];
+    __shared__ __align__(16) float s_o[kWarps][8][kD];
+    __shared__ float s_m[kWarps][8], s_l[kWarps][8];
+    __shared__ int s_last;
+
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int G = p.G;
+    const size_t unit = (size_t)b * p.H + h;
+    int seq = p.seq_lens[b];
+    if (seq < 0 || (int64_t)seq > p.cap) {
+        if (tid == 0 && split == 0 && h == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_SEQLEN_CAPACITY);
+        seq = seq < 0 ? 0 : (int)p.cap;
+    }
+    const int n_active = (seq + p.tps - 1) / p.tps;
+    if (seq == 0) {
+        if (split == 0) {
+            for (int i = tid; i < G * kD; i += kWarps * 32) {
+                const size_t o = ((size_t)b * p.H * G + (size_t)h * G) * kD + i;
+                if (p.out_dtype) static_cast<float*>(p.out)[o] = 0.0f;
+                else static_cast<__half*>(p.out)[o] = __float2half_rn(0.0f);
+            }
+        }
+        return;
+    }
+    if (split >= n_active) return;
+    const HeadTab* ht = p.heads + h;
+
+    for (int i = tid; i < kPairLutWords; i += kWarps * 32) s_pair[i] = __ldg(p.pair_lut + i);
+    for (int i = tid; i < kSingleLutHalves; i += kWarps * 32) s_single[i] = __ldg(p.single_lut + i);
+
+    // ---- query heads into the key codec domain
+    const int n_coded = ht->n_coded;
+    {
+        const int j = tid;
+        const int psz = 1 << ht->plog2[j];
+        const float f = ht->sign_k[j] * ht->dewhiten[j];
+        const int src = ht->perm[j];
+        const __half* qb = p.q + ((size_t)b * p.H * G + (size_t)h * G) * kD;
+        for (int gg = 0; gg < 8; ++gg)
+            s_q[gg][j] = (gg < G && j < n_coded) ? __half2float(qb[(size_t)gg * kD + src]) * f : 0.0f;
+        __syncthreads();
+        for (int hh = 1; hh < kD; hh <<= 1) {
+            float nv[8];
+#pragma unroll
+            for (int gg = 0; gg < 8; ++gg) {
+                const float mine = s_q[gg][j], other = s_q[gg][j ^ hh];
+                nv[gg] = psz > hh ? ((j & hh) ? other - mine : mine + other) : mine;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int gg = 0; gg < 8; ++gg) s_q[gg][j] = nv[gg];
+            __syncthreads();
+        }
+        const float sc = j < n_coded ? ht->inv_sqrt[j] * p.scale_log2 : 0.0f;
+#pragma unroll
+        for (int gg = 0; gg < 8; ++gg) s_q[gg][j] *= sc;
+        __syncthreads();
+    }
+    uint32_t qa[8][4];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const int m0 = ht->slot_pair[t][2 * c], m1 = ht->slot_pair[t][2 * c + 1];
+        const float x0 = s_q[g][(2 * m0) & (kD - 1)], x1 = s_q[g][(2 * m0 + 1) & (kD - 1)];
+        const float y0 = s_q[g][(2 * m1) & (kD - 1)], y1 = s_q[g][(2 * m1 + 1) & (kD - 1)];
+        const bool v0 = 2 * m0 < n_coded, v1 = 2 * m1 < n_coded;
+        split_hilo(v0 ? x0 : 0.0f, v0 ? x1 : 0.0f, qa[c][0], qa[c][1]);
+        split_hilo(v1 ? y0 : 0.0f, v1 ? y1 : 0.0f, qa[c][2], qa[c][3]);
+    }
+    // ---- per-lane K slot metadata
+    const uint32_t wide = ht->wide_mask;
+    uint32_t ksh[16], kmask[16], kbase[16];
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+        const uint32_t w = ht->slot_w[t][s];
+        const uint32_t sh = ht->slot_sh[t][s];
+        if ((wide >> s) & 1u) {
+            ksh[s] = sh > 0 ? sh - 1 : 0;
+            kmask[s] = ((1u << w) - 1u) << 1;
+            kbase[s] = (1u << w) << 1;
+        } else {
+            ksh[s] = sh > 1 ? sh - 2 : 0;
+            kmask[s] = ((1u << (2 * w)) - 1u) << 2;
+            kbase[s] = (1u << (2 * w)) << 2;
+        }
+    }
+    const uint32_t vbase = (1u << (2 * BV)) << 2;
+    __syncthreads();
+
+    // ---- main loop
+    const int t_begin = split * p.tps;
+    const int t_end = min(t_begin + p.tps, seq);
+    const uint8_t* kc = p.kc + unit * (size_t)p.cap * (16 * BK);
+    const uint8_t* vc = p.vc + unit * (size_t)(p.cap / 2) * (32 * BV);
+    const float* kn = p.kn + unit * (size_t)p.cap;
+    const float* vn = p.vn + unit * (size_t)p.cap;
+    float m_run = -INFINITY, l_run = 0.0f;
+    float acc[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+
+    for (int T0 = t_begin + warp * kTile; T0 < t_end; T0 += kWarps * kTile) {
+        uint32_t kw[2][BK];
+        float rk[2][2], rv[2][2];
+        uint32_t vw[2][BV];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int tok = min(T0 + 8 * nt + g, seq - 1);
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(kc + (size_t)tok * (16 * BK)) + BK * t;
+#pragma unroll
+            for (int i = 0; i < BK; ++i) kw[nt][i] = __ldg(src + i);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int tk = min(T0 + 8 * nt + 2 * t + e, seq - 1);
+                rk[nt][e] = __ldg(kn + tk);
+                rv[nt][e] = __ldg(vn + tk);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int pr = min((T0 >> 1) + 4 * r + t, (seq - 1) >> 1);
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(vc + (size_t)pr * (32 * BV)) + BV * g;
+#pragma unroll
+            for (int i = 0; i < BV; ++i) vw[r][i] = __ldg(src + i);
+        }
+        // S^T = Q . K^T
+        float sacc[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.0f;
+        s_chunk<BK, BV, 0>(sacc, qa, kw, ksh, kmask, kbase, wide, s_pair, s_single);
+        s_chunk<BK, BV, 1>(sacc, qa, kw, ksh, kmask, kbase, wide, s_pair, s_single);
+        s_chunk<BK, BV, 2>(sacc, qa, kw, ksh, kmask, kbase, wide, s_pair, s_single);
+        s_chunk<BK, BV, 3>(sacc, qa, kw, ksh, kmask, kbase, wide, s_pair, s_single);
+        s_chunk<BK, BV, 4>(sacc, qa, kw, ksh, kmask, kbase, wide, s_pair, s_single);
+        s_chunk<BK, BV, 5>(sacc, qa, kw, ksh, kmask, kbase, wide, s_pair, s_single);
+        s_chunk<BK, BV, 6>(sacc, qa, kw, ksh, kmask, kbase, wide, s_pair, s_single);
+        s_chunk<BK, BV, 7>(sacc, qa, kw, ksh, kmask, kbase, wide, s_pair, s_single);
+        // logits (log2 domain) and online softmax for head g
+        float lg[2][2];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int tok = T0 + 8 * nt + 2 * t + e;
+                const float v = (sacc[nt][e] + sacc[nt][2 + e]) * rk[nt][e];
+                lg[nt][e] = tok < t_end ? v : -INFINITY;
+                mx = fmaxf(mx, lg[nt][e]);
+            }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run, mx);
+        const float alpha = exp2f(m_run - m_new);
+        float pr[2][2], psum = 0.0f;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                pr[nt][e] = exp2f(lg[nt][e] - m_new);
+                psum += pr[nt][e];
+            }
+        l_run = l_run * alpha + psum;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            acc[i][0] *= alpha;
+            acc[i][1] *= alpha;
+            acc[i][2] *= alpha;
+            acc[i][3] *= alpha;
+        }
+        m_run = m_new;
+        uint32_t pa[4];
+        split_hilo(pr[0][0] * rv[0][0], pr[0][1] * rv[0][1], pa[0], pa[1]);
+        split_hilo(pr[1][0] * rv[1][0], pr[1][1] * rv[1][1], pa[2], pa[3]);
+        pv_tile<BV, 0>(acc, pa, vw, vbase, s_pair);
+        pv_tile<BV, 1>(acc, pa, vw, vbase, s_pair);
+        pv_tile<BV, 2>(acc, pa, vw, vbase, s_pair);
+        pv_tile<BV, 3>(acc, pa, vw, vbase, s_pair);
+        pv_tile<BV, 4>(acc, pa, vw, vbase, s_pair);
+        pv_tile<BV, 5>(acc, pa, vw, vbase, s_pair);
+        pv_tile<BV, 6>(acc, pa, vw, vbase, s_pair);
+        pv_tile<BV, 7>(acc, pa, vw, vbase, s_pair);
+        pv_tile<BV, 8>(acc, pa, vw, vbase, s_pair);
+        pv_tile<BV, 9>(acc, pa, vw, vbase, s_pair);
+        pv_tile<BV, 10>(acc, pa, vw, vbase, s_pair);
+        pv_tile<BV, 11>(acc, pa, vw, vbase, s_pair);
+        pv_tile<BV, 12>(acc, pa, vw, vbase, s_pair);
+        pv_tile<BV, 13>(acc, pa, vw, vbase, s_pair);
+        pv_tile<BV, 14>(acc, pa, vw, vbase, s_pair);
+        pv_tile<BV, 15>(acc, pa, vw, vbase, s_pair);
+    }
+
+    // ---- CTA merge of the warps
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    if (t == 0) {
+        s_m[warp][g] = m_run;
+        s_l[warp][g] = l_run;
+    }
+#pragma unroll
+    for (int nd = 0; nd < 16; ++nd) {
+        s_o[warp][g][16 * (2 * t) + nd] = acc[nd][0] + acc[nd][2];
+        s_o[warp][g][16 * (2 * t + 1) + nd] = acc[nd][1] + acc[nd][3];
+    }
+    __syncthreads();
+    float* part = p.part + (unit * p.n_split + split) * (size_t)G * kPartStride;
+    for (int gg = 0; gg < G; ++gg) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_m[w][gg]);
+        float L = 0.0f, O = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float f = s_m[w][gg] == -INFINITY ? 0.0f : exp2f(s_m[w][gg] - M);
+            L += s_l[w][gg] * f;
+            O += s_o[w][gg][tid] * f;
+        }
+        part[gg * kPartStride + 2 + tid] = O;
+        if (tid == 0) {
+            part[gg * kPartStride] = M;
+            part[gg * kPartStride + 1] = L;
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned prev = atomicAdd(p.count + unit, 1u);
+        s_last = (prev == (unsigned)(n_active - 1)) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    // ---- last CTA: merge all splits of this (sequence, head)
+    const float* base = p.part + unit * p.n_split * (size_t)G * kPartStride;
+    float* s_ml = &s_o[0][0][0];  // [n_active][G][2]
+    for (int i = tid; i < n_active * G; i += kWarps * 32) {
+        s_ml[2 * i] = __ldcg(base + (size_t)i * kPartStride);
+        s_ml[2 * i + 1] = __ldcg(base + (size_t)i * kPartStride + 1);
+    }
+    __syncthreads();
+    for (int gg = 0; gg < G; ++gg) {
+        float M = -INFINITY;
+        for (int s = 0; s < n_active; ++s) M = fmaxf(M, s_ml[2 * (s * G + gg)]);
+        float L = 0.0f, O = 0.0f;
+        for (int s = 0; s < n_active; ++s) {
+            const float ms = s_ml[2 * (s * G + gg)];
+            const float f = ms == -INFINITY ? 0.0f : exp2f(ms - M);
+            L += s_ml[2 * (s * G + gg) + 1] * f;
+            O += __ldcg(base + ((size_t)s * G + gg) * kPartStride + 2 + tid) * f;
+        }
+        s_q[gg][tid] = O / L;
+    }
+    __syncthreads();
+    // inverse value rotation: Hadamard-128, 1/sqrt(128), signs
+    for (int hh = 1; hh < kD; hh <<= 1) {
+        float nv[8];
+#pragma unroll
+        for (int gg = 0; gg < 8; ++gg) {
+            const float mine = s_q[gg][tid], other = s_q[gg][tid ^ hh];
+            nv[gg] = (tid & hh) ? other - mine : mine + other;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int gg = 0; gg < 8; ++gg) s_q[gg][tid] = nv[gg];
+        __syncthreads();
+    }
+    const float f = p.v_inv_sqrt * ht->sign_v[tid];
+    for (int gg = 0; gg < G; ++gg) {
+        const size_t o = ((size_t)b * p.H * G + (size_t)h * G + gg) * kD + tid;
+        const float val = s_q[gg][tid] * f;
+        if (p.out_dtype) static_cast<float*>(p.out)[o] = val;
+        else static_cast<__half*>(p.out)[o] = __float2half_rn(val);
+    }
+    if (tid == 0) p.count[unit] = 0;
+}
+
+template <int BK, int BV>
+cudaError_t launch_t(const DecodeParams& p, dim3 grid, cudaStream_t s) {
+    decode_kernel<BK, BV><<<grid, kWarps * 32, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+SplitPlan decode_split(const bgtq_plan& p, int batch, int64_t max_len) {
+    SplitPlan sp;
+    const int64_t units = std::max<int64_t>(1, (int64_t)batch * p.H);
+    const int64_t chunks = std::max<int64_t>(1, (max_len + kGran - 1) / kGran);
+    const int64_t target = 4 * (int64_t)std::max(1, p.num_sms);
+    int64_t ns = (target + units - 1) / units;
+    ns = std::max<int64_t>(1, std::min<int64_t>(ns, std::min<int64_t>(chunks, kMaxSplit)));
+    const int64_t tps = ((chunks + ns - 1) / ns) * kGran;
+    sp.tokens_per_split = (int)tps;
+    sp.n_split = (int)std::max<int64_t>(1, (std::max<int64_t>(max_len, 1) + tps - 1) / tps);
+    return sp;
+}
+
+size_t decode_workspace_bytes(const bgtq_plan& p, int batch, const SplitPlan& sp) {
+    const size_t units = (size_t)batch * p.H;
+    const size_t counters = ((units * sizeof(uint32_t)) + 255) / 256 * 256;
+    return counters + units * (size_t)sp.n_split * p.G * kPartStride * sizeof(float);
+}
+
+cudaError_t launch_decode(const bgtq_plan& pl, cudaStream_t s, const void* q, const bgtq_cache& c,
+                          const int32_t* seq_lens, int batch, const SplitPlan& sp, void* out, int out_dtype,
+                          float scale, void* ws, int32_t* status) {
+    DecodeParams p;
+    p.q = static_cast<const __half*>(q);
+    p.kc = static_cast<const uint8_t*>(c.k_codes);
+    p.kn = c.k_norm;
+    p.vc = static_cast<const uint8_t*>(c.v_codes);
+    p.vn = c.v_norm;
+    p.cap = c.capacity;
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.out_dtype = out_dtype;
+    const size_t units = (size_t)batch * pl.H;
+    const size_t counters = ((units * sizeof(uint32_t)) + 255) / 256 * 256;
+    p.count = static_cast<uint32_t*>(ws);
+    p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + counters);
+    p.heads = pl.dev.heads;
+    p.pair_lut = pl.dev.pair_lut;
+    p.single_lut = pl.dev.single_lut;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.v_inv_sqrt = (float)(1.0 / std::sqrt((double)kD));
+    p.H = pl.H;
+    p.G = pl.G;
+    p.n_split = sp.n_split;
+    p.tps = sp.tokens_per_split;
+    p.status = status;
+    dim3 grid((unsigned)sp.n_split, (unsigned)pl.H, (unsigned)batch);
+    const int key = pl.bk * 10 + pl.bv;
+    switch (key) {
+        case 11: return launch_t<1, 1>(p, grid, s);
+        case 12: return launch_t<1, 2>(p, grid, s);
+        case 13: return launch_t<1, 3>(p, grid, s);
+        case 14: return launch_t<1, 4>(p, grid, s);
+        case 21: return launch_t<2, 1>(p, grid, s);
+        case 22: return launch_t<2, 2>(p, grid, s);
+        case 23: return launch_t<2, 3>(p, grid, s);
+        case 24: return launch_t<2, 4>(p, grid, s);
+        case 31: return launch_t<3, 1>(p, grid, s);
+        case 32: return launch_t<3, 2>(p, grid, s);
+        case 33: return launch_t<3, 3>(p, grid, s);
+        case 34: return launch_t<3, 4>(p, grid, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace bgtq
