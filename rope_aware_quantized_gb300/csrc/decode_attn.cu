@@ -6,9 +6,9 @@
 //
 // Per CTA: one (sequence, KV head, token split).  Prologue: the G query heads
 // are rotated once into the key codec domain (de-whitening, signs, blockwise
-// Hadamard, 1/sqrt(piece), softmax scale and log2 e folded in) and split into
-// fp16 hi + lo parts that form the 16 rows of the mma A operand (rows 0..7 hi,
-// 8..15 lo).  Main loop, per warp and 16-token tile:
+// Hadamard, 1/sqrt(piece), softmax scale and log2 e folded in), scaled per
+// head by a power of two into the fp16 range, and split into fp16 hi + lo
+// parts that form the 16 rows of the mma A operand (rows 0..7 hi, 8..15 lo).  Main loop, per warp and 16-token tile:
 //   S^T = Q_hilo . K_hat^T     8 k-chunks x 2 token n-tiles of m16n8k16 mma;
 //                              K_hat fragments come from a 64-bit window of
 //                              the lane's K record slice, one shift + mask +
@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     __shared__ __align__(16) float s_q[8][kD];
     __shared__ __align__(16) float s_o[kWarps][8][kD];
     __shared__ float s_m[kWarps][8], s_l[kWarps][8];
+    __shared__ float s_qmax[kWarps][8], s_qscale[8], s_qunscale[8];
     __shared__ int s_last;
 
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -204,8 +205,32 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         const float sc = j < n_coded ? ht->inv_sqrt[j] * p.scale_log2 : 0.0f;
 #pragma unroll
         for (int gg = 0; gg < 8; ++gg) s_q[gg][j] *= sc;
+        // Per-head power-of-two scale so the fp16 hi/lo split cannot overflow
+        // (whitening moves a key block's scale into the query, so sigma*q can
+        // exceed the fp16 range): max |q| is brought to [2^13, 2^14); the
+        // logits are multiplied back by the exact inverse.
+#pragma unroll
+        for (int gg = 0; gg < 8; ++gg) {
+            float a = fabsf(s_q[gg][j]);
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+            if (lane == 0) s_qmax[warp][gg] = a;
+        }
+        __syncthreads();
+        if (tid < 8) {
+            const float a = fmaxf(fmaxf(s_qmax[0][tid], s_qmax[1][tid]), fmaxf(s_qmax[2][tid], s_qmax[3][tid]));
+            int e = 0;
+            if (a > 0.0f && isfinite(a)) frexpf(a, &e);
+            e = max(-100, min(100, e));
+            s_qscale[tid] = ldexpf(1.0f, 14 - e);
+            s_qunscale[tid] = ldexpf(1.0f, e - 14);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int gg = 0; gg < 8; ++gg) s_q[gg][j] *= s_qscale[gg];
         __syncthreads();
     }
+    const float q_unscale = s_qunscale[g];
     uint32_t qa[8][4];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
@@ -292,7 +317,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int tok = T0 + 8 * nt + 2 * t + e;
-                const float v = (sacc[nt][e] + sacc[nt][2 + e]) * rk[nt][e];
+                const float v = (sacc[nt][e] + sacc[nt][2 + e]) * (rk[nt][e] * q_unscale);
                 lg[nt][e] = tok < t_end ? v : -INFINITY;
                 mx = fmaxf(mx, lg[nt][e]);
             }

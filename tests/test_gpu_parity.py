@@ -199,6 +199,19 @@ def test_decode_fp16_output_and_split_invariance():
     check_close(got16[0], want, extra_abs=np.abs(want).max() * 2.0 ** -11)
 
 
+@pytest.mark.parametrize("qmul", [60.0, 1e-3])
+def test_decode_extreme_query_magnitudes(qmul):
+    """Whitening moves a block's scale into the query: sigma * q can leave the
+    fp16 range; the kernel must stay finite and accurate at both extremes."""
+    H, G, T = 1, 8, 900
+    li, plan, cache, heads = build(123, H, G, T, 384, 3, s_ln=1.5)
+    append(plan, cache, li, 0, T)
+    q = np.clip(li[0].q.astype(np.float64) * qmul, -60000, 60000).astype(np.float16)
+    got, _ = decode(plan, cache, dev(q[None]), dev(np.array([T], np.int32)), T)
+    assert np.all(np.isfinite(got))
+    check_close(got[0], oracle_out(heads, li[0], q, T, G))
+
+
 def test_decode_ragged_batch_with_empty_and_single_token_sequences():
     H, G, T = 2, 4, 1500
     li, plan, cache, heads = build(90, H, G, T, 256, 2, s_ln=1.2, batch=4, cap=1500)

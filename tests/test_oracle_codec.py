@@ -214,3 +214,30 @@ def test_v_pair_record_layout():
     assert words[0, 0] == 2 | (1 << 2)
     # dim 127 of pair 1 (token 2 even, no odd token): bits 508-509 -> word 15, bits 28-29
     assert words[1, 15] == 3 << 28
+
+
+def test_lane_layout_hand_example_uniform_widths():
+    """Uniform K2 (every pair 4 bits): worked by hand from the rule.  Ranks
+    equal pair indices; lane t first takes the pairs with rank = t (mod 4),
+    which already sum to the 32-bit slice, so lane t = {t, t+4, ..., t+60};
+    slots alternate even / odd positions of that list."""
+    kc = O.k_codec(np.full(O.NB, 2), np.ones(O.NB), 1, 0)
+    sp, off, wd = O.k_lane_layout(kc, 2)
+    for t in range(4):
+        lane = list(range(t, 64, 4))
+        assert sp[t] == lane[0::2] + lane[1::2]
+        assert off[t] == [4 * s for s in range(16)]
+    # the K record of a token with code pattern code_j = j mod 4: pair m holds
+    # (2m mod 4) | (2m+1 mod 4) << 2 = 0b1000 | ... computed field by field
+    codes = (np.arange(128) % 4)[None, :]
+    rec = O.pack_k(codes, kc, 2).view("<u4")[0]
+    # lane 0, slot 0 = pair 0: codes (0, 1) -> field 0 | 1 << 2 = 4 at bits 0-3
+    # lane 0, slot 1 = pair 8: codes (16 % 4, 17 % 4) = (0, 1) -> 4 at bits 4-7
+    assert rec[0] & 0xFF == 0x44
+    # every pair m has codes (2m % 4, (2m + 1) % 4) = (0|2, 1|3): field 4 or 14
+    for t in range(4):
+        word = int(rec[2 * t]) | (int(rec[2 * t + 1]) << 32)
+        for s in range(16):
+            m = sp[t][s]
+            want = (2 * m % 4) | (((2 * m + 1) % 4) << 2)
+            assert (word >> (4 * s)) & 0xF == want
