@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     ap.add_argument("--workload", default="qwen3b_36l_128k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="build only the first N layers (profiling)")
+    ap.add_argument("--eager", action="store_true", help="launch without a CUDA graph (profiling)")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--sample-seconds", type=float, default=12.0, help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -235,7 +237,7 @@ def run_gpu(args):
     w = workloads.WORKLOADS[args.workload]
     lens = w.seq_lens()
     max_len = int(lens.max())
-    L, B = w.layers, w.batch
+    L, B = (args.layers or w.layers), w.batch
 
     # device buffers of all layers' per-step inputs/outputs (views per layer)
     q_all = torch.empty((L, B, w.n_q, 128), dtype=torch.float16, device="cuda")
@@ -265,9 +267,15 @@ def run_gpu(args):
         step()
     torch.cuda.synchronize()
     assert status.item() == 0, f"device status {status.item()}"
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        step()
+    if args.eager:
+        class _Eager:
+            def replay(self):
+                step()
+        graph = _Eager()
+    else:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
     launches_per_step = 2 * L
 
     def barrier():
@@ -276,8 +284,9 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    for _ in range(args.warmup):
-        graph.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
     barrier()
     clocks = ClockSampler(local_rank)
     clocks.start()
@@ -359,9 +368,9 @@ def run_gpu(args):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
             "config": {
-                "workload": w.name, "layers": L, "kv_heads": w.n_kv, "q_heads": w.n_q, "head_dim": 128,
+                "workload": w.name if L == w.layers else f"{w.name}[first {L} layers]", "layers": L, "kv_heads": w.n_kv, "q_heads": w.n_q, "head_dim": 128,
                 "context": int(max_len), "batch": B, "kv_bits": f"K{w.bits_per_key // 128}V{w.v_bits}",
-                "step": "per layer: quantize-append 1 token + decode attention (CUDA graph)",
+                "step": "per layer: quantize-append 1 token + decode attention" + (" (eager)" if args.eager else " (CUDA graph)"),
                 "packed_bytes_per_step": step_bytes, "fp16_kv_bytes_per_step": fp16_bytes,
                 "compute": "fp16 mma operands (hi+lo split of q and p), fp32 accumulate; fp32 encoder",
                 "l2": "inputs larger than L2 (packed cache per step >> 129 MB L2), no flush",

@@ -17,9 +17,15 @@
 //   O_hilo += P_hilo . V_hat   16 dim n-tiles of m16n8k16 mma; P' = p*rho_V
 //                              split hi + lo into the A rows; V_hat fragments
 //                              come straight from the token-pair V records
-// Epilogue: per-CTA merge of the warps, partial (m, l, acc) to the workspace,
-// and the last CTA of the (sequence, head) merges all splits (log-sum-exp),
-// applies the inverse value rotation and writes the output.
+// Epilogue: the warps of a CTA merge in shared memory; the 8 CTAs of a
+// thread-block cluster (8 consecutive splits of one head) merge through
+// distributed shared memory, CTA r taking query head r, and write one
+// cluster partial (m, l, acc) per head to the workspace; the last cluster of
+// the (sequence, head) to finish (atomic ticket) merges the cluster partials
+// (log-sum-exp), applies the inverse value rotation and writes the output.
+// At entry every CTA asks the L2 to prefetch its whole token range, so the
+// HBM stream starts while the prologue runs.
+#include <cooperative_groups.h>
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -30,11 +36,13 @@
 namespace bgtq {
 namespace {
 
+namespace cg = cooperative_groups;
+
 constexpr int kWarps = 4;
-constexpr int kTile = 16;
-constexpr int kGran = kWarps * kTile;  // tokens per CTA step; split granularity
-constexpr int kMaxSplit = 256;
-constexpr int kPartStride = 2 + kD;    // m, l, acc[128] per query head
+constexpr int kTile = 16;         // tokens per warp iteration; splits start on a tile boundary
+constexpr int kCluster = 8;       // CTAs per thread-block cluster (consecutive splits of one head)
+constexpr int kMaxClusters = 64;  // clusters per (sequence, head)
+constexpr int kPartStride = 2 + kD;  // m, l, acc[128] per query head
 
 struct DecodeParams {
     const __half* q;
@@ -62,6 +70,28 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Bulk prefetch of [ptr, ptr + bytes) into L2 (16-byte aligned, multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
+// Prefetch the 16-byte-aligned part of [base, base + bytes) in 16 KB pieces
+// spread over the CTA's threads (the bulk prefetch needs 16-byte aligned
+// addresses and sizes, so the range is shrunk to the aligned interior).
+__device__ __forceinline__ void prefetch_range(const char* base, size_t bytes, int tid) {
+    constexpr size_t kChunk = 16384;
+    const uintptr_t a0 = (reinterpret_cast<uintptr_t>(base) + 15) & ~(uintptr_t)15;
+    const uintptr_t a1 = (reinterpret_cast<uintptr_t>(base) + bytes) & ~(uintptr_t)15;
+    if (a1 <= a0) return;
+    const size_t total = a1 - a0;
+    const size_t n = (total + kChunk - 1) / kChunk;
+    for (size_t i = tid; i < n; i += kWarps * 32) {
+        const size_t off = i * kChunk;
+        const size_t len = total - off < kChunk ? total - off : kChunk;
+        prefetch_l2(reinterpret_cast<const void*>(a0 + off), (uint32_t)len);
+    }
 }
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
@@ -144,13 +174,14 @@ __device__ __forceinline__ void pv_tile(float (&acc)[16][4], const uint32_t (&pa
 }
 
 template <int BK, int BV>
-__global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) {
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) {
     __shared__ __align__(16) uint32_t s_pair[kPairLutWords];
     __shared__ __align__(16) uint16_t s_single[kSingleLutHalves];
     __shared__ __align__(16) float s_q[8][kD];
     __shared__ __align__(16) float s_o[kWarps][8][kD];
     __shared__ float s_m[kWarps][8], s_l[kWarps][8];
     __shared__ float s_qmax[kWarps][8], s_qscale[8], s_qunscale[8];
+    __shared__ __align__(16) float s_part[8][kPartStride];
     __shared__ int s_last;
 
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -163,6 +194,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         seq = seq < 0 ? 0 : (int)p.cap;
     }
     const int n_active = (seq + p.tps - 1) / p.tps;
+    const int n_clusters = (n_active + kCluster - 1) / kCluster;
+    const int cid = split / kCluster;
     if (seq == 0) {
         if (split == 0) {
             for (int i = tid; i < G * kD; i += kWarps * 32) {
@@ -171,14 +204,36 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
                 else static_cast<__half*>(p.out)[o] = __float2half_rn(0.0f);
             }
         }
-        return;
+        return;  // every CTA of this (sequence, head) leaves here
     }
-    if (split >= n_active) return;
+    if (cid >= n_clusters) return;  // the whole cluster is past the sequence
+    cg::cluster_group cluster = cg::this_cluster();
+    const int crank = (int)cluster.block_rank();
+    const bool active = split < n_active;
     const HeadTab* ht = p.heads + h;
+    const int t_begin = split * p.tps;
+    const int t_end = min(t_begin + p.tps, seq);
+    const uint8_t* kc = p.kc + unit * (size_t)p.cap * (16 * BK);
+    const uint8_t* vc = p.vc + unit * (size_t)(p.cap / 2) * (32 * BV);
+    const float* kn = p.kn + unit * (size_t)p.cap;
+    const float* vn = p.vn + unit * (size_t)p.cap;
 
-    for (int i = tid; i < kPairLutWords; i += kWarps * 32) s_pair[i] = __ldg(p.pair_lut + i);
-    for (int i = tid; i < kSingleLutHalves; i += kWarps * 32) s_single[i] = __ldg(p.single_lut + i);
+    if (active) {
+        prefetch_range(reinterpret_cast<const char*>(kc + (size_t)t_begin * (16 * BK)),
+                       (size_t)(t_end - t_begin) * (16 * BK), tid);
+        prefetch_range(reinterpret_cast<const char*>(vc + (size_t)(t_begin / 2) * (32 * BV)),
+                       (size_t)((t_end - t_begin + 1) / 2) * (32 * BV), tid);
+        prefetch_range(reinterpret_cast<const char*>(kn + t_begin), (size_t)(t_end - t_begin) * 4, tid);
+        prefetch_range(reinterpret_cast<const char*>(vn + t_begin), (size_t)(t_end - t_begin) * 4, tid);
+        const uint4* lp = reinterpret_cast<const uint4*>(p.pair_lut);
+        uint4* sp = reinterpret_cast<uint4*>(s_pair);
+#pragma unroll
+        for (int i = 0; i < kPairLutWords / 4 / (kWarps * 32); ++i) sp[tid + i * kWarps * 32] = __ldg(lp + tid + i * kWarps * 32);
+        if (tid < kSingleLutHalves / 8)
+            reinterpret_cast<uint4*>(s_single)[tid] = __ldg(reinterpret_cast<const uint4*>(p.single_lut) + tid);
+    }
 
+    if (active) {
     // ---- query heads into the key codec domain
     const int n_coded = ht->n_coded;
     {
@@ -262,12 +317,6 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     __syncthreads();
 
     // ---- main loop
-    const int t_begin = split * p.tps;
-    const int t_end = min(t_begin + p.tps, seq);
-    const uint8_t* kc = p.kc + unit * (size_t)p.cap * (16 * BK);
-    const uint8_t* vc = p.vc + unit * (size_t)(p.cap / 2) * (32 * BV);
-    const float* kn = p.kn + unit * (size_t)p.cap;
-    const float* vn = p.vn + unit * (size_t)p.cap;
     float m_run = -INFINITY, l_run = 0.0f;
     float acc[16][4];
 #pragma unroll
@@ -363,7 +412,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         pv_tile<BV, 15>(acc, pa, vw, vbase, s_pair);
     }
 
-    // ---- CTA merge of the warps
+    // ---- CTA merge of the warps -> s_part
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
     if (t == 0) {
@@ -376,7 +425,6 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         s_o[warp][g][16 * (2 * t + 1) + nd] = acc[nd][1] + acc[nd][3];
     }
     __syncthreads();
-    float* part = p.part + (unit * p.n_split + split) * (size_t)G * kPartStride;
     for (int gg = 0; gg < G; ++gg) {
         float M = -INFINITY;
 #pragma unroll
@@ -388,64 +436,92 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             L += s_l[w][gg] * f;
             O += s_o[w][gg][tid] * f;
         }
-        part[gg * kPartStride + 2 + tid] = O;
+        s_part[gg][2 + tid] = O;
         if (tid == 0) {
-            part[gg * kPartStride] = M;
-            part[gg * kPartStride + 1] = L;
+            s_part[gg][0] = M;
+            s_part[gg][1] = L;
         }
     }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const unsigned prev = atomicAdd(p.count + unit, 1u);
-        s_last = (prev == (unsigned)(n_active - 1)) ? 1 : 0;
+    } else {
+        for (int gg = 0; gg < G; ++gg) {
+            s_part[gg][2 + tid] = 0.0f;
+            if (tid == 0) {
+                s_part[gg][0] = -INFINITY;
+                s_part[gg][1] = 0.0f;
+            }
+        }
     }
-    __syncthreads();
+
+    // ---- cluster merge: CTA rank r reduces query head r over the 8 CTAs
+    cluster.sync();
+    const size_t max_clusters = (size_t)p.n_split / kCluster;
+    float* cpart_base = p.part + unit * max_clusters * (size_t)G * kPartStride;
+    if (crank < G) {
+        float mc[kCluster];
+        float M = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kCluster; ++c) {
+            const float* rp = cluster.map_shared_rank(&s_part[crank][0], c);
+            mc[c] = rp[0];
+            M = fmaxf(M, mc[c]);
+        }
+        float L = 0.0f, O = 0.0f;
+#pragma unroll
+        for (int c = 0; c < kCluster; ++c) {
+            const float* rp = cluster.map_shared_rank(&s_part[crank][0], c);
+            const float f = mc[c] == -INFINITY ? 0.0f : exp2f(mc[c] - M);
+            L += rp[1] * f;
+            O += rp[2 + tid] * f;
+        }
+        float* dst = cpart_base + ((size_t)cid * G + crank) * kPartStride;
+        dst[2 + tid] = O;
+        if (tid == 0) {
+            dst[0] = M;
+            dst[1] = L;
+        }
+        __threadfence();
+    }
+    cluster.sync();
+    if (crank == 0 && tid == 0) {
+        const unsigned prev = atomicAdd(p.count + unit, 1u);
+        const int last = (prev == (unsigned)(n_clusters - 1)) ? 1 : 0;
+#pragma unroll
+        for (int c = 0; c < kCluster; ++c) *cluster.map_shared_rank(&s_last, c) = last;
+    }
+    cluster.sync();
     if (!s_last) return;
     __threadfence();
 
-    // ---- last CTA: merge all splits of this (sequence, head)
-    const float* base = p.part + unit * p.n_split * (size_t)G * kPartStride;
-    float* s_ml = &s_o[0][0][0];  // [n_active][G][2]
-    for (int i = tid; i < n_active * G; i += kWarps * 32) {
-        s_ml[2 * i] = __ldcg(base + (size_t)i * kPartStride);
-        s_ml[2 * i + 1] = __ldcg(base + (size_t)i * kPartStride + 1);
-    }
-    __syncthreads();
-    for (int gg = 0; gg < G; ++gg) {
+    // ---- last cluster: CTA r merges the cluster partials of query head r
+    if (crank >= G) return;
+    {
+        const int gg = crank;
         float M = -INFINITY;
-        for (int s = 0; s < n_active; ++s) M = fmaxf(M, s_ml[2 * (s * G + gg)]);
+        for (int c = 0; c < n_clusters; ++c) M = fmaxf(M, __ldcg(cpart_base + ((size_t)c * G + gg) * kPartStride));
         float L = 0.0f, O = 0.0f;
-        for (int s = 0; s < n_active; ++s) {
-            const float ms = s_ml[2 * (s * G + gg)];
-            const float f = ms == -INFINITY ? 0.0f : exp2f(ms - M);
-            L += s_ml[2 * (s * G + gg) + 1] * f;
-            O += __ldcg(base + ((size_t)s * G + gg) * kPartStride + 2 + tid) * f;
+        for (int c = 0; c < n_clusters; ++c) {
+            const float* src = cpart_base + ((size_t)c * G + gg) * kPartStride;
+            const float mcv = __ldcg(src);
+            const float f = mcv == -INFINITY ? 0.0f : exp2f(mcv - M);
+            L += __ldcg(src + 1) * f;
+            O += __ldcg(src + 2 + tid) * f;
         }
-        s_q[gg][tid] = O / L;
-    }
-    __syncthreads();
-    // inverse value rotation: Hadamard-128, 1/sqrt(128), signs
-    for (int hh = 1; hh < kD; hh <<= 1) {
-        float nv[8];
-#pragma unroll
-        for (int gg = 0; gg < 8; ++gg) {
-            const float mine = s_q[gg][tid], other = s_q[gg][tid ^ hh];
-            nv[gg] = (tid & hh) ? other - mine : mine + other;
+        s_q[0][tid] = O / L;
+        __syncthreads();
+        // inverse value rotation: Hadamard-128, 1/sqrt(128), signs
+        for (int hh = 1; hh < kD; hh <<= 1) {
+            const float mine = s_q[0][tid], other = s_q[0][tid ^ hh];
+            const float nv = (tid & hh) ? other - mine : mine + other;
+            __syncthreads();
+            s_q[0][tid] = nv;
+            __syncthreads();
         }
-        __syncthreads();
-#pragma unroll
-        for (int gg = 0; gg < 8; ++gg) s_q[gg][tid] = nv[gg];
-        __syncthreads();
-    }
-    const float f = p.v_inv_sqrt * ht->sign_v[tid];
-    for (int gg = 0; gg < G; ++gg) {
+        const float val = s_q[0][tid] * p.v_inv_sqrt * ht->sign_v[tid];
         const size_t o = ((size_t)b * p.H * G + (size_t)h * G + gg) * kD + tid;
-        const float val = s_q[gg][tid] * f;
         if (p.out_dtype) static_cast<float*>(p.out)[o] = val;
         else static_cast<__half*>(p.out)[o] = __float2half_rn(val);
     }
-    if (tid == 0) p.count[unit] = 0;
+    if (crank == 0 && tid == 0) p.count[unit] = 0;
 }
 
 template <int BK, int BV>
@@ -457,22 +533,28 @@ cudaError_t launch_t(const DecodeParams& p, dim3 grid, cudaStream_t s) {
 }  // namespace
 
 SplitPlan decode_split(const bgtq_plan& p, int batch, int64_t max_len) {
+    // About two CTAs per SM in total, at least 64 tokens per CTA, splits in
+    // whole clusters of 8 and whole 16-token tiles.
     SplitPlan sp;
     const int64_t units = std::max<int64_t>(1, (int64_t)batch * p.H);
-    const int64_t chunks = std::max<int64_t>(1, (max_len + kGran - 1) / kGran);
-    const int64_t target = 4 * (int64_t)std::max(1, p.num_sms);
-    int64_t ns = (target + units - 1) / units;
-    ns = std::max<int64_t>(1, std::min<int64_t>(ns, std::min<int64_t>(chunks, kMaxSplit)));
-    const int64_t tps = ((chunks + ns - 1) / ns) * kGran;
+    const int64_t len = std::max<int64_t>(max_len, 1);
+    int64_t ns = 2 * (int64_t)std::max(1, p.num_sms) / units;
+    ns = std::min<int64_t>(ns, (len + 63) / 64);
+    ns = std::min<int64_t>(ns, (int64_t)kCluster * kMaxClusters);
+    if (len >= 64 * kCluster) ns = std::max<int64_t>(ns, kCluster);
+    ns = std::max<int64_t>(ns, 1);
+    int64_t tps = (len + ns - 1) / ns;
+    tps = (tps + kTile - 1) / kTile * kTile;
+    const int64_t n = (len + tps - 1) / tps;
     sp.tokens_per_split = (int)tps;
-    sp.n_split = (int)std::max<int64_t>(1, (std::max<int64_t>(max_len, 1) + tps - 1) / tps);
+    sp.n_split = (int)((n + kCluster - 1) / kCluster * kCluster);
     return sp;
 }
 
 size_t decode_workspace_bytes(const bgtq_plan& p, int batch, const SplitPlan& sp) {
     const size_t units = (size_t)batch * p.H;
     const size_t counters = ((units * sizeof(uint32_t)) + 255) / 256 * 256;
-    return counters + units * (size_t)sp.n_split * p.G * kPartStride * sizeof(float);
+    return counters + units * (size_t)(sp.n_split / kCluster) * p.G * kPartStride * sizeof(float);
 }
 
 cudaError_t launch_decode(const bgtq_plan& pl, cudaStream_t s, const void* q, const bgtq_cache& c,

@@ -227,6 +227,16 @@ def test_decode_ragged_batch_with_empty_and_single_token_sequences():
         check_close(got[b], oracle_out(heads, li[b], q[b], int(lens[b]), G))
 
 
+def test_decode_capacity_not_multiple_of_four():
+    """Per-head norm rows then start 8 bytes off a 16-byte boundary."""
+    H, G, T = 3, 4, 1001
+    li, plan, cache, heads = build(21, H, G, T, 384, 3, s_ln=1.2, cap=1002)
+    append(plan, cache, li, 0, T)
+    got, st = decode(plan, cache, dev(li[0].q[None]), dev(np.array([T], np.int32)), T)
+    assert st == 0
+    check_close(got[0], oracle_out(heads, li[0], li[0].q, T, G))
+
+
 def test_decode_seq_len_beyond_capacity_is_clamped_and_flagged():
     H, G, T = 1, 4, 128
     li, plan, cache, heads = build(3, H, G, T, 384, 3, cap=128)
