@@ -215,6 +215,26 @@ int bgtq_decode_attn(const bgtq_plan* plan, void* stream, const void* q_fp16, co
                      float softmax_scale, void* workspace, size_t ws_bytes, int32_t* dev_status);
 
 /*
+ * bgtq_decode_attn_noalloc — bgtq_decode_attn for callers that cannot
+ * allocate device memory (a fixed memory budget, an allocator or pool that
+ * must not be bypassed, a host runtime without a device allocator).  The
+ * paper has no counterpart; this is a convenience of the library.
+ *   Same arguments and results as bgtq_decode_attn, minus the workspace: the
+ *   split-merge scratch is one built-in device array of 2 MiB that every GPU
+ *   which loads the library keeps until the process exits.  No call
+ *   allocates or frees memory.
+ *   The first call on a device looks up that array's address with the device
+ *   current; make it before any stream capture.  Every call shares the array
+ *   and it keeps the last call's contents (its counters are cleared by each
+ *   call), so calls that overlap on the GPU race; order them on one stream.
+ * Errors: as bgtq_decode_attn; WORKSPACE when the problem needs more than the
+ * built-in 2 MiB of scratch (then use bgtq_decode_attn with a workspace).
+ */
+int bgtq_decode_attn_noalloc(const bgtq_plan* plan, void* stream, const void* q_fp16, const bgtq_cache* cache,
+                             const int32_t* seq_lens, int64_t max_len, int batch, void* out, int out_dtype,
+                             float softmax_scale, int32_t* dev_status);
+
+/*
  * bgtq_dequant_debug — decode cached tokens [t0, t1) of (sequence b, head)
  * back to float32, for inspection and parity checks.
  *   k_out, v_out  device, [t1-t0][128] float (either may be NULL)

@@ -209,6 +209,24 @@ def bgtq_decode_attn(plan: Plan, q_fp16, cache: Cache, seq_lens, max_len: int, o
                                   workspace.numel() * workspace.element_size(), _ptr(status)))
 
 
+def bgtq_decode_attn_noalloc(plan: Plan, q_fp16, cache: Cache, seq_lens, max_len: int, out,
+                             softmax_scale: float | None = None, status=None, stream=None):
+    """bgtq_decode_attn without a workspace, for callers that cannot allocate
+    device memory; its merge scratch is the library's built-in 2 MiB array
+    (calls that overlap on the GPU race)."""
+    import torch
+    batch = q_fp16.shape[0]
+    if out.dtype == torch.float32:
+        out_dtype = 1
+    elif out.dtype == torch.float16:
+        out_dtype = 0
+    else:
+        raise ValueError("out must be float16 or float32")
+    scale = (1.0 / HEAD_DIM ** 0.5) if softmax_scale is None else softmax_scale
+    _check(lib().bgtq_decode_attn_noalloc(plan.handle, _stream(stream), _ptr(q_fp16), C.byref(cache.desc),
+                                          _ptr(seq_lens), max_len, batch, _ptr(out), out_dtype, scale, _ptr(status)))
+
+
 def bgtq_dequant_debug(plan: Plan, cache: Cache, b: int, head: int, t0: int, t1: int, k_out=None, v_out=None,
                        codec_domain: bool = False, stream=None):
     _check(lib().bgtq_dequant_debug(plan.handle, _stream(stream), C.byref(cache.desc), cache.batch, b, head, t0, t1,
@@ -217,5 +235,6 @@ def bgtq_dequant_debug(plan: Plan, cache: Cache, b: int, head: int, t0: int, t1:
 
 __all__ = [
     "BgtqError", "Plan", "Cache", "CacheView", "bgtq_alloc_bits", "bgtq_plan_create", "bgtq_cache_bytes",
-    "bgtq_quantize_append", "bgtq_decode_attn_workspace", "bgtq_decode_attn", "bgtq_dequant_debug",
+    "bgtq_quantize_append", "bgtq_decode_attn_workspace", "bgtq_decode_attn", "bgtq_decode_attn_noalloc",
+    "bgtq_dequant_debug",
 ]

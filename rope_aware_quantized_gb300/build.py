@@ -23,6 +23,7 @@ SOURCES = [
     ("bgtq_host.cpp", []),
     ("codec.cu", ["--fmad=false"]),
     ("decode_attn.cu", []),
+    ("decode_attn_noalloc.cu", []),
 ]
 
 
