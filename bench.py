@@ -210,12 +210,31 @@ def traffic_from_profile():
         if ":" in line:
             k, v = line.split(":", 1)
             vals[k.strip()] = v.strip()
-    if vals.get("decode_attn.cu sha256[:16]") != sha:
+    if vals.get("decode_attn.cu sha256 prefix") != sha:
         return None
     try:
         return float(vals["dram bytes per launch"])
     except (KeyError, ValueError):
         return None
+
+
+# ----------------------------------------------------------------------------- ranks
+
+def max_over_ranks(ms: float, dist=None, device="cpu") -> float:
+    """The slowest rank's time: every rank ends with the same value."""
+    if dist is None:
+        return float(ms)
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world: int, batch: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s of `world` independent replicas (weak scaling): each
+    replica decodes `batch` tokens per step; the job's step time is the
+    slowest replica's."""
+    return world * batch / (ms_per_step / 1000.0)
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -299,12 +318,8 @@ def run_gpu(args):
         e1.record(stream)
     barrier()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * B / (ms / 1000.0)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, "cuda")
+    value = replica_throughput(world, B, ms)
 
     # dominant kernel alone: CUDA events around each decode launch on its stream
     durs = []
@@ -348,11 +363,7 @@ def run_gpu(args):
             ho.copy_(out_all, non_blocking=True)
         x1.record(stream)
     barrier()
-    e2e_ms = x0.elapsed_time(x1) / args.steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(x0.elapsed_time(x1) / args.steps, dist, "cuda")
     assert status.item() == 0, f"device status {status.item()}"
 
     cpu = None
@@ -380,7 +391,7 @@ def run_gpu(args):
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                          "kernel": "decode_attn", "launch_ms": launch_ms, "bytes_per_launch": decode_bytes,
                          "peak_kind": f"{peak_kind} (copy, burst)"},
-            "e2e": {"value": world * B / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "e2e": {"value": replica_throughput(world, B, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "path": "pinned H2D of q/new K/V, graph of the API calls, D2H of out"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,

@@ -17,6 +17,7 @@ namespace bgtq {
 namespace {
 
 constexpr int kWarpsQ = 4;
+constexpr int kPairsPerWarp = 8;  // token pairs each warp of quantize_append encodes
 
 struct QParams {
     const __half* k;
@@ -86,7 +87,7 @@ __device__ __forceinline__ float warp_encode(float (&x)[4], const float (&sgn)[4
 #pragma unroll
         for (int s = 128; s >= 1; s >>= 1) {
             if (2 * s <= n) {
-                if (__ldg(tb + pos + s - 1) <= u) pos += s;
+                if (tb[pos + s - 1] <= u) pos += s;
             }
         }
         code[i] = pos;
@@ -95,6 +96,7 @@ __device__ __forceinline__ float warp_encode(float (&x)[4], const float (&sgn)[4
 }
 
 __global__ void __launch_bounds__(128) quantize_append_kernel(QParams p) {
+    __shared__ __align__(16) float s_thr[(kWMax + 1) * 256];
     __shared__ float xs[kWarpsQ][kD];
     __shared__ uint32_t krec[kWarpsQ][32];
     __shared__ uint32_t vrec[kWarpsQ][8 * kPairMaxW];
@@ -106,10 +108,10 @@ __global__ void __launch_bounds__(128) quantize_append_kernel(QParams p) {
         if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_APPEND_CAPACITY);
         return;
     }
-    const int64_t P = (int64_t)(ps >> 1) + (int64_t)blockIdx.x * kWarpsQ + warp;  // token-pair index
-    const int64_t pos0 = 2 * P;
-    const bool has[2] = {pos0 >= ps && pos0 < (int64_t)ps + p.t_new, pos0 + 1 >= ps && pos0 + 1 < (int64_t)ps + p.t_new};
-    if (!has[0] && !has[1]) return;
+    // Lloyd-Max thresholds of every width, staged once per block
+    for (int i = threadIdx.x; i < (kWMax + 1) * 256 / 4; i += kWarpsQ * 32)
+        reinterpret_cast<float4*>(s_thr)[i] = __ldg(reinterpret_cast<const float4*>(p.thr) + i);
+    __syncthreads();
     const HeadTab* ht = p.heads + h;
     const int n_coded = ht->n_coded;
     const size_t unit = (size_t)b * p.H + h;
@@ -135,76 +137,84 @@ __global__ void __launch_bounds__(128) quantize_append_kernel(QParams p) {
         vsg[i] = ht->sign_v[j];
         vis[i] = p.v_inv_sqrt;
     }
-    for (int i = lane; i < 8 * kPairMaxW; i += 32) {
-        vrec[warp][i] = 0;
-        vmask[warp][i] = 0;
-    }
-    for (int par = 0; par < 2; ++par) {
-        if (!has[par]) continue;
-        const int64_t pos = pos0 + par;
-        const size_t tok = (size_t)(pos - ps);
-        // ---- key
-        {
-            const __half2* src = reinterpret_cast<const __half2*>(p.k + (unit * p.t_new + tok) * kD) + 2 * lane;
-            const float2 a = __half22float2(src[0]), c = __half22float2(src[1]);
-            xs[warp][4 * lane + 0] = a.x;
-            xs[warp][4 * lane + 1] = a.y;
-            xs[warp][4 * lane + 2] = c.x;
-            xs[warp][4 * lane + 3] = c.y;
-            if (lane < 32) krec[warp][lane] = 0;
-            __syncwarp();
-            float x[4];
+    const int64_t P_first = (int64_t)(ps >> 1) + ((int64_t)blockIdx.x * kWarpsQ + warp) * kPairsPerWarp;
+    for (int it = 0; it < kPairsPerWarp; ++it) {
+        const int64_t P = P_first + it;  // token-pair index
+        const int64_t pos0 = 2 * P;
+        const bool has[2] = {pos0 >= ps && pos0 < (int64_t)ps + p.t_new, pos0 + 1 >= ps && pos0 + 1 < (int64_t)ps + p.t_new};
+        if (!has[0] && !has[1]) continue;
+        for (int i = lane; i < 8 * kPairMaxW; i += 32) {
+            vrec[warp][i] = 0;
+            vmask[warp][i] = 0;
+        }
+        for (int par = 0; par < 2; ++par) {
+            if (!has[par]) continue;
+            const int64_t pos = pos0 + par;
+            const size_t tok = (size_t)(pos - ps);
+            // ---- key
+            {
+                const __half2* src = reinterpret_cast<const __half2*>(p.k + (unit * p.t_new + tok) * kD) + 2 * lane;
+                const float2 a = __half22float2(src[0]), c = __half22float2(src[1]);
+                xs[warp][4 * lane + 0] = a.x;
+                xs[warp][4 * lane + 1] = a.y;
+                xs[warp][4 * lane + 2] = c.x;
+                xs[warp][4 * lane + 3] = c.y;
+                if (lane < 32) krec[warp][lane] = 0;
+                __syncwarp();
+                float x[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) x[i] = (4 * lane + i < n_coded) ? __fmul_rn(xs[warp][kperm[i]], kwh[i]) : 0.0f;
-            int code[4];
-            const float rho = warp_encode(x, ksg, kpl, kis, kw, n_coded, p.thr, lane, code);
+                for (int i = 0; i < 4; ++i) x[i] = (4 * lane + i < n_coded) ? __fmul_rn(xs[warp][kperm[i]], kwh[i]) : 0.0f;
+                int code[4];
+                const float rho = warp_encode(x, ksg, kpl, kis, kw, n_coded, s_thr, lane, code);
 #pragma unroll
-            for (int pr = 0; pr < 2; ++pr) {
-                const int j = 4 * lane + 2 * pr;
-                if (j + 1 < n_coded) {
-                    const int w = kw[2 * pr];
-                    const uint32_t field = (uint32_t)code[2 * pr] | ((uint32_t)code[2 * pr + 1] << w);
-                    const int bit = ht->pair_bit[j >> 1];
+                for (int pr = 0; pr < 2; ++pr) {
+                    const int j = 4 * lane + 2 * pr;
+                    if (j + 1 < n_coded) {
+                        const int w = kw[2 * pr];
+                        const uint32_t field = (uint32_t)code[2 * pr] | ((uint32_t)code[2 * pr + 1] << w);
+                        const int bit = ht->pair_bit[j >> 1];
+                        const int wi = bit >> 5, sh = bit & 31;
+                        atomicOr(&krec[warp][wi], field << sh);
+                        if (sh + 2 * w > 32) atomicOr(&krec[warp][wi + 1], field >> (32 - sh));
+                    }
+                }
+                __syncwarp();
+                uint32_t* dst = reinterpret_cast<uint32_t*>(p.kc + (unit * p.cap + pos) * (16 * p.bk));
+                if (lane < krec_words) dst[lane] = krec[warp][lane];
+                if (lane == 0) p.kn[unit * p.cap + pos] = rho;
+                __syncwarp();
+            }
+            // ---- value
+            {
+                const __half2* src = reinterpret_cast<const __half2*>(p.v + (unit * p.t_new + tok) * kD) + 2 * lane;
+                const float2 a = __half22float2(src[0]), c = __half22float2(src[1]);
+                float x[4] = {a.x, a.y, c.x, c.y};
+                int code[4];
+                const float rho = warp_encode(x, vsg, vpl, vis, vw, kD, s_thr, lane, code);
+                const uint32_t m1 = (1u << p.bv) - 1;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int j = 4 * lane + i;
+                    const int bit = 2 * p.bv * j + par * p.bv;
                     const int wi = bit >> 5, sh = bit & 31;
-                    atomicOr(&krec[warp][wi], field << sh);
-                    if (sh + 2 * w > 32) atomicOr(&krec[warp][wi + 1], field >> (32 - sh));
+                    atomicOr(&vrec[warp][wi], (uint32_t)code[i] << sh);
+                    atomicOr(&vmask[warp][wi], m1 << sh);
+                    if (sh + p.bv > 32) {
+                        atomicOr(&vrec[warp][wi + 1], (uint32_t)code[i] >> (32 - sh));
+                        atomicOr(&vmask[warp][wi + 1], m1 >> (32 - sh));
+                    }
                 }
+                if (lane == 0) p.vn[unit * p.cap + pos] = rho;
             }
-            __syncwarp();
-            uint32_t* dst = reinterpret_cast<uint32_t*>(p.kc + (unit * p.cap + pos) * (16 * p.bk));
-            if (lane < krec_words) dst[lane] = krec[warp][lane];
-            if (lane == 0) p.kn[unit * p.cap + pos] = rho;
-            __syncwarp();
         }
-        // ---- value
-        {
-            const __half2* src = reinterpret_cast<const __half2*>(p.v + (unit * p.t_new + tok) * kD) + 2 * lane;
-            const float2 a = __half22float2(src[0]), c = __half22float2(src[1]);
-            float x[4] = {a.x, a.y, c.x, c.y};
-            int code[4];
-            const float rho = warp_encode(x, vsg, vpl, vis, vw, kD, p.thr, lane, code);
-            const uint32_t m1 = (1u << p.bv) - 1;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int j = 4 * lane + i;
-                const int bit = 2 * p.bv * j + par * p.bv;
-                const int wi = bit >> 5, sh = bit & 31;
-                atomicOr(&vrec[warp][wi], (uint32_t)code[i] << sh);
-                atomicOr(&vmask[warp][wi], m1 << sh);
-                if (sh + p.bv > 32) {
-                    atomicOr(&vrec[warp][wi + 1], (uint32_t)code[i] >> (32 - sh));
-                    atomicOr(&vmask[warp][wi + 1], m1 >> (32 - sh));
-                }
-            }
-            if (lane == 0) p.vn[unit * p.cap + pos] = rho;
+        __syncwarp();
+        uint32_t* vdst = reinterpret_cast<uint32_t*>(p.vc + (unit * (p.cap / 2) + P) * (32 * p.bv));
+        for (int i = lane; i < vrec_words; i += 32) {
+            uint32_t val = vrec[warp][i];
+            if (!(has[0] && has[1])) val = (vdst[i] & ~vmask[warp][i]) | val;
+            vdst[i] = val;
         }
-    }
-    __syncwarp();
-    uint32_t* vdst = reinterpret_cast<uint32_t*>(p.vc + (unit * (p.cap / 2) + P) * (32 * p.bv));
-    for (int i = lane; i < vrec_words; i += 32) {
-        uint32_t val = vrec[warp][i];
-        if (!(has[0] && has[1])) val = (vdst[i] & ~vmask[warp][i]) | val;
-        vdst[i] = val;
+        __syncwarp();
     }
 }
 
@@ -336,7 +346,8 @@ cudaError_t launch_quantize_append(const bgtq_plan& pl, cudaStream_t s, const vo
     p.v_inv_sqrt = (float)(1.0 / std::sqrt((double)kD));
     p.status = status;
     const int64_t pairs = (int64_t)t_new / 2 + 1;
-    dim3 grid((unsigned)((pairs + kWarpsQ - 1) / kWarpsQ), (unsigned)pl.H, (unsigned)batch);
+    const int64_t per_block = (int64_t)kWarpsQ * kPairsPerWarp;
+    dim3 grid((unsigned)((pairs + per_block - 1) / per_block), (unsigned)pl.H, (unsigned)batch);
     quantize_append_kernel<<<grid, 32 * kWarpsQ, 0, s>>>(p);
     return cudaGetLastError();
 }

@@ -30,6 +30,8 @@
 
 #include <algorithm>
 #include <cmath>
+#include <map>
+#include <mutex>
 
 #include "bgtq_internal.h"
 
@@ -43,6 +45,17 @@ constexpr int kTile = 16;         // tokens per warp iteration; splits start on 
 constexpr int kCluster = 8;       // CTAs per thread-block cluster (consecutive splits of one head)
 constexpr int kMaxClusters = 64;  // clusters per (sequence, head)
 constexpr int kPartStride = 2 + kD;  // m, l, acc[128] per query head
+// Shared-memory decode tables (32-bit words).  Words [0, 2048): pair tables
+// of widths 0..5 shared by all lanes (entry 4^w + f).  Words [4096, 8192):
+// per-lane copies of the pair tables of widths 0..3 (entry e of lane L at
+// 4096 + 32 e + L), so lanes never collide on a bank.  Words [2048, 4096) are
+// unused by the tables; after the main loop the region is reused.
+constexpr int kTabWords = 8192;
+constexpr int kPrivWord = 4096;
+constexpr uint32_t kPrivByte = 4u * kPrivWord;
+constexpr int kPrivMaxW = 3;
+constexpr int kPrivEntries = 1 << (2 * kPrivMaxW + 1);   // 128
+constexpr float kHeadroom = 8.0f;  // log2 headroom of the softmax reference
 
 struct DecodeParams {
     const __half* q;
@@ -109,19 +122,32 @@ __device__ __forceinline__ uint32_t kword(const uint32_t (&kw)[BK], int i) {
     return i < BK ? kw[i < BK ? i : 0] : 0u;
 }
 
-// Decoded fp16 pair of K slot `S` (compile-time) of the lane's record slice.
-template <int BK, int S>
+__device__ __forceinline__ uint32_t lds32(const uint32_t* tab, uint32_t byte) {
+    return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const char*>(tab) + byte);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Decoded fp16 pair of K slot S (compile-time) of the lane's record slice.
+// (sh, mask, base) select the field and the table: the field is shifted so
+// that it lands pre-multiplied by the entry stride of its table (shared
+// tables: 4 bytes; per-lane tables: 128 bytes), masked and OR-ed with the
+// table's byte base.  Slots flagged in `wide` use the single-entry table.
+template <int BK, int S, bool kCheckWide>
 __device__ __forceinline__ uint32_t k_pair(const uint32_t (&kw)[BK], uint32_t sh, uint32_t mask, uint32_t base,
-                                           uint32_t wide, const uint32_t* s_pair, const uint16_t* s_single) {
+                                           uint32_t wide, const uint32_t* s_tab, const uint16_t* s_single) {
     constexpr bool kUpper = (BK == 3 && S >= 8);
     static_assert(BK >= 1 && BK <= 3, "K record slices of 1..3 words");
     const uint32_t lo = kUpper ? kword(kw, 1) : kword(kw, 0);
     const uint32_t hi = kUpper ? kword(kw, 2) : kword(kw, 1);
     const uint64_t win = ((uint64_t)hi << 32) | lo;
-    if (!((wide >> S) & 1u)) {
+    if (!kCheckWide || !((wide >> S) & 1u)) {
         const uint32_t x = S == 0 ? (kword(kw, 0) << 2) : (uint32_t)(win >> sh);
-        const uint32_t addr = (x & mask) | base;
-        return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const char*>(s_pair) + addr);
+        return lds32(s_tab, (x & mask) | base);
     }
     const uint32_t x = S == 0 ? (kword(kw, 0) << 1) : (uint32_t)(win >> sh);
     const uint32_t w = __popc(mask);
@@ -133,56 +159,96 @@ __device__ __forceinline__ uint32_t k_pair(const uint32_t (&kw)[BK], uint32_t sh
 }
 
 // Decoded fp16 pair (even token, odd token) of V codec dim 16*g + ND from the
-// lane-group's BV words of a token-pair record.
+// lane-group's BV words of a token-pair record (compile-time bit position).
 template <int BV, int ND>
-__device__ __forceinline__ uint32_t v_pair(const uint32_t (&vw)[BV], uint32_t vbase, const uint32_t* s_pair) {
+__device__ __forceinline__ uint32_t v_pair(const uint32_t (&vw)[BV], uint32_t vbase, const uint32_t* s_tab) {
     constexpr int FB = 2 * BV;
     constexpr int O = FB * ND;
     constexpr int WI = O >> 5, SH = O & 31;
-    constexpr uint32_t MASK = ((1u << FB) - 1u) << 2;
+    constexpr int PS = BV <= kPrivMaxW ? 7 : 2;  // entry stride 128 B (per-lane) or 4 B (shared)
+    constexpr uint32_t MASK = ((1u << FB) - 1u) << PS;
     uint32_t x;
-    if constexpr (SH == 0)
-        x = vw[WI] << 2;
-    else if constexpr (SH + FB <= 32)
-        x = vw[WI] >> (SH - 2);
-    else
-        x = __funnelshift_r(vw[WI], vw[WI + 1 < BV ? WI + 1 : WI], SH - 2);
-    const uint32_t addr = (x & MASK) | vbase;
-    return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const char*>(s_pair) + addr);
+    if constexpr (SH + FB <= 32) {
+        if constexpr (SH >= PS)
+            x = vw[WI] >> (SH - PS);
+        else
+            x = vw[WI] << (PS - SH);
+    } else {
+        x = __funnelshift_r(vw[WI], vw[WI + 1 < BV ? WI + 1 : WI], SH - PS);
+    }
+    return lds32(s_tab, (x & MASK) | vbase);
 }
 
-template <int BK, int BV, int C>
+template <int BK, int C, bool kAnyWide>
 __device__ __forceinline__ void s_chunk(float (&sacc)[2][4], const uint32_t (&qa)[8][4], const uint32_t (&kw)[2][BK],
                                         const uint32_t (&ksh)[16], const uint32_t (&kmask)[16],
-                                        const uint32_t (&kbase)[16], uint32_t wide, const uint32_t* s_pair,
+                                        const uint32_t (&kbase)[16], uint32_t wide, const uint32_t* s_tab,
                                         const uint16_t* s_single) {
+    constexpr bool kW0 = kAnyWide || (2 * C == 0) || (2 * C == 8);
+    constexpr bool kW1 = kAnyWide;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-        const uint32_t b0 = k_pair<BK, 2 * C>(kw[nt], ksh[2 * C], kmask[2 * C], kbase[2 * C], wide, s_pair, s_single);
-        const uint32_t b1 =
-            k_pair<BK, 2 * C + 1>(kw[nt], ksh[2 * C + 1], kmask[2 * C + 1], kbase[2 * C + 1], wide, s_pair, s_single);
+        const uint32_t b0 =
+            k_pair<BK, 2 * C, kW0>(kw[nt], ksh[2 * C], kmask[2 * C], kbase[2 * C], wide, s_tab, s_single);
+        const uint32_t b1 = k_pair<BK, 2 * C + 1, kW1>(kw[nt], ksh[2 * C + 1], kmask[2 * C + 1], kbase[2 * C + 1],
+                                                       wide, s_tab, s_single);
         mma16816(sacc[nt], qa[C], b0, b1);
     }
 }
 
 template <int BV, int ND>
 __device__ __forceinline__ void pv_tile(float (&acc)[16][4], const uint32_t (&pa)[4], const uint32_t (&vw)[2][BV],
-                                        uint32_t vbase, const uint32_t* s_pair) {
-    const uint32_t b0 = v_pair<BV, ND>(vw[0], vbase, s_pair);
-    const uint32_t b1 = v_pair<BV, ND>(vw[1], vbase, s_pair);
+                                        uint32_t vbase, const uint32_t* s_tab) {
+    const uint32_t b0 = v_pair<BV, ND>(vw[0], vbase, s_tab);
+    const uint32_t b1 = v_pair<BV, ND>(vw[1], vbase, s_tab);
     mma16816(acc[ND], pa, b0, b1);
 }
 
+// Global-memory operands of one 16-token tile for one lane.
 template <int BK, int BV>
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) {
-    __shared__ __align__(16) uint32_t s_pair[kPairLutWords];
+struct TileRegs {
+    uint32_t kw[2][BK];  // K record slice words of tokens T0 + g and T0 + 8 + g
+    float rk[2][2];      // key norms of tokens T0 + 8 nt + 2 t + e
+    float rv[2][2];      // value norms of the same tokens
+    uint32_t vw[2][BV];  // lane-group words of V pair records T0/2 + t and T0/2 + 4 + t
+
+    __device__ __forceinline__ void load(const uint8_t* kc, const uint8_t* vc, const float* kn, const float* vn,
+                                         int T0, int seq, int g, int t) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int tok = min(T0 + 8 * nt + g, seq - 1);
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(kc + (size_t)tok * (16 * BK)) + BK * t;
+#pragma unroll
+            for (int i = 0; i < BK; ++i) kw[nt][i] = __ldg(src + i);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int tk = min(T0 + 8 * nt + 2 * t + e, seq - 1);
+                rk[nt][e] = __ldg(kn + tk);
+                rv[nt][e] = __ldg(vn + tk);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int pr = min((T0 >> 1) + 4 * r + t, (seq - 1) >> 1);
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(vc + (size_t)pr * (32 * BV)) + BV * g;
+#pragma unroll
+            for (int i = 0; i < BV; ++i) vw[r][i] = __ldg(src + i);
+        }
+    }
+};
+
+template <int BK, int BV, bool kAnyWide>
+__global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) {
+    __shared__ __align__(16) uint32_t s_tab[kTabWords];
     __shared__ __align__(16) uint16_t s_single[kSingleLutHalves];
     __shared__ __align__(16) float s_q[8][kD];
-    __shared__ __align__(16) float s_o[kWarps][8][kD];
     __shared__ float s_m[kWarps][8], s_l[kWarps][8];
     __shared__ float s_qmax[kWarps][8], s_qscale[8], s_qunscale[8];
-    __shared__ __align__(16) float s_part[8][kPartStride];
     __shared__ int s_last;
+    // after the main loop the table region holds the warp partials and the
+    // CTA partial that the cluster reads
+    float (*s_o)[8][kD] = reinterpret_cast<float (*)[8][kD]>(s_tab + kPrivWord);
+    float (*s_part)[kPartStride] = reinterpret_cast<float (*)[kPartStride]>(s_tab);
 
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
@@ -226,9 +292,17 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kWarps * 32, 
         prefetch_range(reinterpret_cast<const char*>(kn + t_begin), (size_t)(t_end - t_begin) * 4, tid);
         prefetch_range(reinterpret_cast<const char*>(vn + t_begin), (size_t)(t_end - t_begin) * 4, tid);
         const uint4* lp = reinterpret_cast<const uint4*>(p.pair_lut);
-        uint4* sp = reinterpret_cast<uint4*>(s_pair);
+        uint4* sp = reinterpret_cast<uint4*>(s_tab);
 #pragma unroll
         for (int i = 0; i < kPairLutWords / 4 / (kWarps * 32); ++i) sp[tid + i * kWarps * 32] = __ldg(lp + tid + i * kWarps * 32);
+        // per-lane copies: entry e of lane L at kPrivWord + 32 e + L
+        uint4* pp = reinterpret_cast<uint4*>(s_tab + kPrivWord);
+#pragma unroll
+        for (int i = 0; i < kPrivEntries * 32 / 4 / (kWarps * 32); ++i) {
+            const int q4 = tid + i * kWarps * 32;
+            const uint32_t v = __ldg(p.pair_lut + (q4 >> 3));
+            pp[q4] = make_uint4(v, v, v, v);
+        }
         if (tid < kSingleLutHalves / 8)
             reinterpret_cast<uint4*>(s_single)[tid] = __ldg(reinterpret_cast<const uint4*>(p.single_lut) + tid);
     }
@@ -296,69 +370,50 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kWarps * 32, 
         split_hilo(v0 ? x0 : 0.0f, v0 ? x1 : 0.0f, qa[c][0], qa[c][1]);
         split_hilo(v1 ? y0 : 0.0f, v1 ? y1 : 0.0f, qa[c][2], qa[c][3]);
     }
-    // ---- per-lane K slot metadata
+    // ---- per-lane K slot metadata: field shift, mask and table base
     const uint32_t wide = ht->wide_mask;
     uint32_t ksh[16], kmask[16], kbase[16];
 #pragma unroll
     for (int s = 0; s < 16; ++s) {
         const uint32_t w = ht->slot_w[t][s];
         const uint32_t sh = ht->slot_sh[t][s];
-        if ((wide >> s) & 1u) {
+        if ((wide >> s) & 1u) {  // single-entry table, two lookups
             ksh[s] = sh > 0 ? sh - 1 : 0;
             kmask[s] = ((1u << w) - 1u) << 1;
             kbase[s] = (1u << w) << 1;
-        } else {
+        } else if (w <= (uint32_t)kPrivMaxW && sh >= 7 && s != 0) {  // per-lane pair table
+            ksh[s] = sh - 7;
+            kmask[s] = ((1u << (2 * w)) - 1u) << 7;
+            kbase[s] = kPrivByte + 4u * lane + ((1u << (2 * w)) << 7);
+        } else {  // shared pair table
             ksh[s] = sh > 1 ? sh - 2 : 0;
             kmask[s] = ((1u << (2 * w)) - 1u) << 2;
             kbase[s] = (1u << (2 * w)) << 2;
         }
     }
-    const uint32_t vbase = (1u << (2 * BV)) << 2;
+    const uint32_t vbase = BV <= kPrivMaxW ? kPrivByte + 4u * lane + ((1u << (2 * BV)) << 7) : (1u << (2 * BV)) << 2;
     __syncthreads();
 
-    // ---- main loop
-    float m_run = -INFINITY, l_run = 0.0f;
+    // ---- main loop: 16-token tiles, operands of the next tile loaded while
+    // the current one is decoded (ping-pong register buffers)
+    float m_ref = -INFINITY, l_run = 0.0f;  // softmax reference (running max + headroom), sum
     float acc[16][4];
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
 
-    for (int T0 = t_begin + warp * kTile; T0 < t_end; T0 += kWarps * kTile) {
-        uint32_t kw[2][BK];
-        float rk[2][2], rv[2][2];
-        uint32_t vw[2][BV];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int tok = min(T0 + 8 * nt + g, seq - 1);
-            const uint32_t* src = reinterpret_cast<const uint32_t*>(kc + (size_t)tok * (16 * BK)) + BK * t;
-#pragma unroll
-            for (int i = 0; i < BK; ++i) kw[nt][i] = __ldg(src + i);
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int tk = min(T0 + 8 * nt + 2 * t + e, seq - 1);
-                rk[nt][e] = __ldg(kn + tk);
-                rv[nt][e] = __ldg(vn + tk);
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int pr = min((T0 >> 1) + 4 * r + t, (seq - 1) >> 1);
-            const uint32_t* src = reinterpret_cast<const uint32_t*>(vc + (size_t)pr * (32 * BV)) + BV * g;
-#pragma unroll
-            for (int i = 0; i < BV; ++i) vw[r][i] = __ldg(src + i);
-        }
-        // S^T = Q . K^T
+    auto process = [&](const TileRegs<BK, BV>& tr, int T0) {
         float sacc[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.0f;
-        s_chunk<BK, BV, 0>(sacc, qa, kw, ksh, kmask, kbase, wide, s_pair, s_single);
-        s_chunk<BK, BV, 1>(sacc, qa, kw, ksh, kmask, kbase, wide, s_pair, s_single);
-        s_chunk<BK, BV, 2>(sacc, qa, kw, ksh, kmask, kbase, wide, s_pair, s_single);
-        s_chunk<BK, BV, 3>(sacc, qa, kw, ksh, kmask, kbase, wide, s_pair, s_single);
-        s_chunk<BK, BV, 4>(sacc, qa, kw, ksh, kmask, kbase, wide, s_pair, s_single);
-        s_chunk<BK, BV, 5>(sacc, qa, kw, ksh, kmask, kbase, wide, s_pair, s_single);
-        s_chunk<BK, BV, 6>(sacc, qa, kw, ksh, kmask, kbase, wide, s_pair, s_single);
-        s_chunk<BK, BV, 7>(sacc, qa, kw, ksh, kmask, kbase, wide, s_pair, s_single);
-        // logits (log2 domain) and online softmax for head g
+        s_chunk<BK, 0, kAnyWide>(sacc, qa, tr.kw, ksh, kmask, kbase, wide, s_tab, s_single);
+        s_chunk<BK, 1, kAnyWide>(sacc, qa, tr.kw, ksh, kmask, kbase, wide, s_tab, s_single);
+        s_chunk<BK, 2, kAnyWide>(sacc, qa, tr.kw, ksh, kmask, kbase, wide, s_tab, s_single);
+        s_chunk<BK, 3, kAnyWide>(sacc, qa, tr.kw, ksh, kmask, kbase, wide, s_tab, s_single);
+        s_chunk<BK, 4, kAnyWide>(sacc, qa, tr.kw, ksh, kmask, kbase, wide, s_tab, s_single);
+        s_chunk<BK, 5, kAnyWide>(sacc, qa, tr.kw, ksh, kmask, kbase, wide, s_tab, s_single);
+        s_chunk<BK, 6, kAnyWide>(sacc, qa, tr.kw, ksh, kmask, kbase, wide, s_tab, s_single);
+        s_chunk<BK, 7, kAnyWide>(sacc, qa, tr.kw, ksh, kmask, kbase, wide, s_tab, s_single);
+        // logits (log2 domain) of head g for tokens T0 + 8 nt + 2 t + e
         float lg[2][2];
         float mx = -INFINITY;
 #pragma unroll
@@ -366,51 +421,70 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kWarps * 32, 
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int tok = T0 + 8 * nt + 2 * t + e;
-                const float v = (sacc[nt][e] + sacc[nt][2 + e]) * (rk[nt][e] * q_unscale);
+                const float v = (sacc[nt][e] + sacc[nt][2 + e]) * (tr.rk[nt][e] * q_unscale);
                 lg[nt][e] = tok < t_end ? v : -INFINITY;
                 mx = fmaxf(mx, lg[nt][e]);
             }
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run, mx);
-        const float alpha = exp2f(m_run - m_new);
-        float pr[2][2], psum = 0.0f;
+        // The reference sits kHeadroom above the largest logit seen, so the
+        // weights stay <= 1 and the accumulator is rescaled only when a
+        // logit passes the reference.
+        if (__any_sync(0xffffffffu, mx > m_ref)) {
+            const float ref = mx > m_ref ? mx + kHeadroom : m_ref;
+            const float alpha = fast_exp2(m_ref - ref);
+            l_run *= alpha;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                acc[i][0] *= alpha;
+                acc[i][1] *= alpha;
+                acc[i][2] *= alpha;
+                acc[i][3] *= alpha;
+            }
+            m_ref = ref;
+        }
+        float pr[2][2];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                pr[nt][e] = exp2f(lg[nt][e] - m_new);
-                psum += pr[nt][e];
+                pr[nt][e] = fast_exp2(lg[nt][e] - m_ref);
+                l_run += pr[nt][e];
             }
-        l_run = l_run * alpha + psum;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            acc[i][0] *= alpha;
-            acc[i][1] *= alpha;
-            acc[i][2] *= alpha;
-            acc[i][3] *= alpha;
-        }
-        m_run = m_new;
         uint32_t pa[4];
-        split_hilo(pr[0][0] * rv[0][0], pr[0][1] * rv[0][1], pa[0], pa[1]);
-        split_hilo(pr[1][0] * rv[1][0], pr[1][1] * rv[1][1], pa[2], pa[3]);
-        pv_tile<BV, 0>(acc, pa, vw, vbase, s_pair);
-        pv_tile<BV, 1>(acc, pa, vw, vbase, s_pair);
-        pv_tile<BV, 2>(acc, pa, vw, vbase, s_pair);
-        pv_tile<BV, 3>(acc, pa, vw, vbase, s_pair);
-        pv_tile<BV, 4>(acc, pa, vw, vbase, s_pair);
-        pv_tile<BV, 5>(acc, pa, vw, vbase, s_pair);
-        pv_tile<BV, 6>(acc, pa, vw, vbase, s_pair);
-        pv_tile<BV, 7>(acc, pa, vw, vbase, s_pair);
-        pv_tile<BV, 8>(acc, pa, vw, vbase, s_pair);
-        pv_tile<BV, 9>(acc, pa, vw, vbase, s_pair);
-        pv_tile<BV, 10>(acc, pa, vw, vbase, s_pair);
-        pv_tile<BV, 11>(acc, pa, vw, vbase, s_pair);
-        pv_tile<BV, 12>(acc, pa, vw, vbase, s_pair);
-        pv_tile<BV, 13>(acc, pa, vw, vbase, s_pair);
-        pv_tile<BV, 14>(acc, pa, vw, vbase, s_pair);
-        pv_tile<BV, 15>(acc, pa, vw, vbase, s_pair);
+        split_hilo(pr[0][0] * tr.rv[0][0], pr[0][1] * tr.rv[0][1], pa[0], pa[1]);
+        split_hilo(pr[1][0] * tr.rv[1][0], pr[1][1] * tr.rv[1][1], pa[2], pa[3]);
+        pv_tile<BV, 0>(acc, pa, tr.vw, vbase, s_tab);
+        pv_tile<BV, 1>(acc, pa, tr.vw, vbase, s_tab);
+        pv_tile<BV, 2>(acc, pa, tr.vw, vbase, s_tab);
+        pv_tile<BV, 3>(acc, pa, tr.vw, vbase, s_tab);
+        pv_tile<BV, 4>(acc, pa, tr.vw, vbase, s_tab);
+        pv_tile<BV, 5>(acc, pa, tr.vw, vbase, s_tab);
+        pv_tile<BV, 6>(acc, pa, tr.vw, vbase, s_tab);
+        pv_tile<BV, 7>(acc, pa, tr.vw, vbase, s_tab);
+        pv_tile<BV, 8>(acc, pa, tr.vw, vbase, s_tab);
+        pv_tile<BV, 9>(acc, pa, tr.vw, vbase, s_tab);
+        pv_tile<BV, 10>(acc, pa, tr.vw, vbase, s_tab);
+        pv_tile<BV, 11>(acc, pa, tr.vw, vbase, s_tab);
+        pv_tile<BV, 12>(acc, pa, tr.vw, vbase, s_tab);
+        pv_tile<BV, 13>(acc, pa, tr.vw, vbase, s_tab);
+        pv_tile<BV, 14>(acc, pa, tr.vw, vbase, s_tab);
+        pv_tile<BV, 15>(acc, pa, tr.vw, vbase, s_tab);
+    };
+
+    constexpr int kStep = kWarps * kTile;
+    TileRegs<BK, BV> ta, tb;
+    int T0 = t_begin + warp * kTile;
+    if (T0 < t_end) ta.load(kc, vc, kn, vn, T0, seq, g, t);
+    for (; T0 < t_end; T0 += 2 * kStep) {
+        if (T0 + kStep < t_end) tb.load(kc, vc, kn, vn, T0 + kStep, seq, g, t);
+        process(ta, T0);
+        if (T0 + kStep >= t_end) break;
+        if (T0 + 2 * kStep < t_end) ta.load(kc, vc, kn, vn, T0 + 2 * kStep, seq, g, t);
+        process(tb, T0 + kStep);
     }
+    const float m_run = m_ref;
+    __syncthreads();  // the table region is reused below
 
     // ---- CTA merge of the warps -> s_part
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
@@ -524,21 +598,89 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kWarps * 32, 
     if (crank == 0 && tid == 0) p.count[unit] = 0;
 }
 
+template <int BK, int BV, bool kAnyWide>
+cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t s, cudaLaunchAttribute* attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    attr->id = cudaLaunchAttributeClusterDimension;
+    attr->val.clusterDim.x = kCluster;
+    attr->val.clusterDim.y = 1;
+    attr->val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
 template <int BK, int BV>
-cudaError_t launch_t(const DecodeParams& p, dim3 grid, cudaStream_t s) {
-    decode_kernel<BK, BV><<<grid, kWarps * 32, 0, s>>>(p);
-    return cudaGetLastError();
+cudaError_t launch_t(const DecodeParams& p, dim3 grid, cudaStream_t s, bool any_wide) {
+    cudaLaunchAttribute attr;
+    if (any_wide) {
+        cudaLaunchConfig_t cfg = launch_config<BK, BV, true>(grid, s, &attr);
+        return cudaLaunchKernelEx(&cfg, decode_kernel<BK, BV, true>, p);
+    }
+    cudaLaunchConfig_t cfg = launch_config<BK, BV, false>(grid, s, &attr);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<BK, BV, false>, p);
+}
+
+// CTAs of decode_kernel<BK, BV> that can be resident at once, in whole
+// clusters (cluster placement can leave SMs unusable, so this is at most
+// the SM count times the blocks per SM).
+template <int BK, int BV>
+int resident_ctas() {
+    cudaLaunchAttribute attr;
+    cudaLaunchConfig_t cfg = launch_config<BK, BV, false>(dim3(kCluster, 1, 1), nullptr, &attr);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, decode_kernel<BK, BV, false>, &cfg) != cudaSuccess || clusters <= 0) {
+        cudaGetLastError();
+        return 0;
+    }
+    return clusters * kCluster;
+}
+
+int resident_ctas_for(int bk, int bv) {
+    static std::mutex mu;
+    static std::map<std::pair<int, int>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int key = bk * 10 + bv;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find({dev, key});
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    switch (key) {
+        case 11: n = resident_ctas<1, 1>(); break;
+        case 12: n = resident_ctas<1, 2>(); break;
+        case 13: n = resident_ctas<1, 3>(); break;
+        case 14: n = resident_ctas<1, 4>(); break;
+        case 21: n = resident_ctas<2, 1>(); break;
+        case 22: n = resident_ctas<2, 2>(); break;
+        case 23: n = resident_ctas<2, 3>(); break;
+        case 24: n = resident_ctas<2, 4>(); break;
+        case 31: n = resident_ctas<3, 1>(); break;
+        case 32: n = resident_ctas<3, 2>(); break;
+        case 33: n = resident_ctas<3, 3>(); break;
+        case 34: n = resident_ctas<3, 4>(); break;
+        default: n = 0;
+    }
+    cache[{dev, key}] = n;
+    return n;
 }
 
 }  // namespace
 
 SplitPlan decode_split(const bgtq_plan& p, int batch, int64_t max_len) {
-    // About two CTAs per SM in total, at least 64 tokens per CTA, splits in
-    // whole clusters of 8 and whole 16-token tiles.
+    // One wave of resident CTAs in total (whole clusters of 8), at least 64
+    // tokens per CTA, splits in whole 16-token tiles.
     SplitPlan sp;
     const int64_t units = std::max<int64_t>(1, (int64_t)batch * p.H);
     const int64_t len = std::max<int64_t>(max_len, 1);
-    int64_t ns = 2 * (int64_t)std::max(1, p.num_sms) / units;
+    int64_t slots = (p.bk >= 1 && p.bk <= 3 && p.bv >= 1 && p.bv <= 4) ? resident_ctas_for(p.bk, p.bv) : 0;
+    if (slots <= 0) slots = 2 * (int64_t)std::max(1, p.num_sms);
+    int64_t ns = slots / units;
+    if (ns >= kCluster) ns = ns / kCluster * kCluster;
     ns = std::min<int64_t>(ns, (len + 63) / 64);
     ns = std::min<int64_t>(ns, (int64_t)kCluster * kMaxClusters);
     if (len >= 64 * kCluster) ns = std::max<int64_t>(ns, kCluster);
@@ -585,20 +727,24 @@ cudaError_t launch_decode(const bgtq_plan& pl, cudaStream_t s, const void* q, co
     p.tps = sp.tokens_per_split;
     p.status = status;
     dim3 grid((unsigned)sp.n_split, (unsigned)pl.H, (unsigned)batch);
+    // the fast instance checks only slots 0 and 8 (each lane's two widest
+    // pairs) for codes wider than the pair tables
+    bool any_wide = false;
+    for (const HeadTab& ht : pl.heads) any_wide |= (ht.wide_mask & ~((1u << 0) | (1u << 8))) != 0;
     const int key = pl.bk * 10 + pl.bv;
     switch (key) {
-        case 11: return launch_t<1, 1>(p, grid, s);
-        case 12: return launch_t<1, 2>(p, grid, s);
-        case 13: return launch_t<1, 3>(p, grid, s);
-        case 14: return launch_t<1, 4>(p, grid, s);
-        case 21: return launch_t<2, 1>(p, grid, s);
-        case 22: return launch_t<2, 2>(p, grid, s);
-        case 23: return launch_t<2, 3>(p, grid, s);
-        case 24: return launch_t<2, 4>(p, grid, s);
-        case 31: return launch_t<3, 1>(p, grid, s);
-        case 32: return launch_t<3, 2>(p, grid, s);
-        case 33: return launch_t<3, 3>(p, grid, s);
-        case 34: return launch_t<3, 4>(p, grid, s);
+        case 11: return launch_t<1, 1>(p, grid, s, any_wide);
+        case 12: return launch_t<1, 2>(p, grid, s, any_wide);
+        case 13: return launch_t<1, 3>(p, grid, s, any_wide);
+        case 14: return launch_t<1, 4>(p, grid, s, any_wide);
+        case 21: return launch_t<2, 1>(p, grid, s, any_wide);
+        case 22: return launch_t<2, 2>(p, grid, s, any_wide);
+        case 23: return launch_t<2, 3>(p, grid, s, any_wide);
+        case 24: return launch_t<2, 4>(p, grid, s, any_wide);
+        case 31: return launch_t<3, 1>(p, grid, s, any_wide);
+        case 32: return launch_t<3, 2>(p, grid, s, any_wide);
+        case 33: return launch_t<3, 3>(p, grid, s, any_wide);
+        case 34: return launch_t<3, 4>(p, grid, s, any_wide);
         default: return cudaErrorInvalidValue;
     }
 }
