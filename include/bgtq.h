@@ -21,6 +21,13 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Device work is enqueued asynchronously on it; no call
  *     synchronises the host except bgtq_plan_create/destroy.
+ *   - The quantize-append and decode kernels launch with programmatic
+ *     dependent launch: each may start while the previous kernel on the
+ *     stream is still running, does its plan-static set-up, and waits for
+ *     that kernel to finish before it reads q, k, v, pos_start or the cache.
+ *     The decode kernel reads seq_lens BEFORE that wait, so seq_lens must not
+ *     be written by a kernel that triggers its dependents early (no kernel
+ *     of this library writes it; ordinary kernels and copies are fine).
  *   - head_dim must be 128.  Inputs must be finite: NaN/Inf inputs give
  *     unspecified codes, never a fault.
  *   - Errors discovered on the device (positions beyond the cache capacity,

@@ -298,6 +298,7 @@ static void free_dev(bgtq_plan* p) {
     if (p->dev.thr) cudaFree(p->dev.thr);
     if (p->dev.pair_lut) cudaFree(p->dev.pair_lut);
     if (p->dev.single_lut) cudaFree(p->dev.single_lut);
+    if (p->dev.dec_image) cudaFree(p->dev.dec_image);
     p->dev = DevTables{};
 }
 
@@ -382,6 +383,34 @@ static int build_head(bgtq_plan* p, int h, const uint8_t* bits, const double* s)
             ht.slot_sh[t][sl] = (uint8_t)std::max(0, sh);
             if (wd[m] > kPairMaxW) ht.wide_mask |= 1u << sl;
         }
+    // decode lookup recipes: which table copy each (lane t, slot) uses
+    for (int t = 0; t < 4; ++t)
+        for (int sl = 0; sl < 16; ++sl) {
+            const uint32_t w = ht.slot_w[t][sl], sh = ht.slot_sh[t][sl];
+            uint32_t ex, mask, base, mult;
+            if ((ht.wide_mask >> sl) & 1u) {  // single-entry table, per-token-lane copy (16 B stride)
+                ex = 4;
+                mask = ((1u << w) - 1u) << 4;
+                base = 4u * kImgSingle + ((1u << w) << 4);
+                mult = 2u << 8;
+            } else if (w <= 3 && (sl == 0 || sh >= 7)) {  // per-lane pair table (128 B stride)
+                ex = 7;
+                mask = ((1u << (2 * w)) - 1u) << 7;
+                base = 4u * kImgPriv + ((1u << (2 * w)) << 7);
+                mult = 4u;
+            } else if (w == 4 && (sl == 0 || sh >= 5)) {  // per-token-lane width-4 table (32 B stride)
+                ex = 5;
+                mask = 255u << 5;
+                base = 4u * kImgG4;
+                mult = 4u << 8;
+            } else {  // shared pair table (4 B stride)
+                ex = 2;
+                mask = ((1u << (2 * w)) - 1u) << 2;
+                base = (1u << (2 * w)) << 2;
+                mult = 0;
+            }
+            ht.kmeta[t][sl] = SlotMeta{sl == 0 ? ex : sh - ex, mask, base, mult};
+        }
     return BGTQ_OK;
 }
 
@@ -415,6 +444,19 @@ static int build_codebooks(bgtq_plan* p) {
     for (int w = 0; w <= kWMax; ++w)
         for (int c = 0; c < (1 << w); ++c)
             p->single_lut[(1 << w) + c] = p->cent[w][c] == 0.0f ? 0 : double_to_half_bits(p->cent[w][c]);
+    // decode shared-memory image (layout in bgtq_internal.h)
+    p->dec_image.assign(kImgWords, 0);
+    for (int i = 0; i < kPairLutWords; ++i) p->dec_image[i] = p->pair_lut[i];
+    for (int f = 0; f < 256; ++f)
+        for (int g = 0; g < 8; ++g) p->dec_image[kImgG4 + 8 * f + g] = p->pair_lut[256 + f];
+    for (int e = 0; e < 128; ++e)
+        for (int l = 0; l < 32; ++l) p->dec_image[kImgPriv + 32 * e + l] = p->pair_lut[e];
+    for (int e = 0; e < kSingleLutHalves; ++e)
+        for (int g = 0; g < 8; ++g) {
+            const int half = 8 * e + g;
+            uint32_t& wd = p->dec_image[kImgSingle + half / 2];
+            wd |= (uint32_t)p->single_lut[e] << (16 * (half & 1));
+        }
     return BGTQ_OK;
 }
 
@@ -439,7 +481,8 @@ static int upload_plan(bgtq_plan* p) {
         (e = upload(&p->dev.cent, cent.data(), cent.size())) != cudaSuccess ||
         (e = upload(&p->dev.thr, thr.data(), thr.size())) != cudaSuccess ||
         (e = upload(&p->dev.pair_lut, p->pair_lut.data(), p->pair_lut.size())) != cudaSuccess ||
-        (e = upload(&p->dev.single_lut, p->single_lut.data(), p->single_lut.size())) != cudaSuccess) {
+        (e = upload(&p->dev.single_lut, p->single_lut.data(), p->single_lut.size())) != cudaSuccess ||
+        (e = upload(&p->dev.dec_image, p->dec_image.data(), p->dec_image.size())) != cudaSuccess) {
         free_dev(p);
         return set_error(BGTQ_ERR_CUDA, "plan upload: %s", cudaGetErrorString(e));
     }

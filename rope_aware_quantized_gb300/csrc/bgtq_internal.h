@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include <string>
@@ -22,6 +23,28 @@ constexpr int kPairLutWords = 1 << (2 * kPairMaxW + 1);
 // Single table: entry (2^w + c) holds c_w[c] (fp16 bits) for w = 0..8.
 constexpr int kSingleLutHalves = 1 << (kWMax + 1);
 
+// Shared-memory image of the decode tables (32-bit words), copied verbatim
+// by every decode CTA.  Arranged so that the lanes of a warp rarely collide
+// on a bank:
+//   [0, 2048)       pair tables of widths 0..5, shared by all lanes (entry 4^w + f)
+//   [2048, 4096)    8 copies of the width-4 pair table, one per token lane g
+//                   (entry 256 + f of copy g at 2048 + 8 f + g)
+//   [4096, 8192)    per-lane copies of the pair tables of widths 0..3
+//                   (entry e of lane L at 4096 + 32 e + L)
+//   [8192, 10240)   8 copies of the single-entry table by token lane g, as
+//                   fp16 halves (entry 2^w + c of copy g at half 8 (2^w + c) + g)
+constexpr int kImgG4 = 2048;
+constexpr int kImgPriv = 4096;
+constexpr int kImgSingle = 8192;
+constexpr int kImgWords = 10240;
+
+// How decode lane (g, t) extracts and looks up one K slot: the 64-bit window
+// is shifted right by `sh` (slot 0: its word is shifted left by `sh`), masked
+// with `mask` and OR-ed with base + (mult & 255) * lane + (mult >> 8) * g.
+struct SlotMeta {
+    uint32_t sh, mask, base, mult;
+};
+
 // Per-head device tables.  All arrays are in codec order unless noted.
 struct HeadTab {
     int32_t n_coded;
@@ -39,7 +62,11 @@ struct HeadTab {
     float inv_sqrt[kD];
     float sign_k[kD];
     float sign_v[kD];
+    SlotMeta kmeta[4][16];    // decode: lookup recipe of (lane t, slot)
 };
+
+static_assert(offsetof(HeadTab, kmeta) % 16 == 0 && sizeof(HeadTab) % 16 == 0,
+              "decode loads the lookup recipes with 16-byte loads");
 
 struct DevTables {
     HeadTab* heads = nullptr;     // [H]
@@ -47,6 +74,7 @@ struct DevTables {
     float* thr = nullptr;         // [9][256] thresholds (first 2^w - 1 used)
     uint32_t* pair_lut = nullptr; // [kPairLutWords]
     uint16_t* single_lut = nullptr; // [kSingleLutHalves]
+    uint32_t* dec_image = nullptr;  // [kImgWords] decode shared-memory image
 };
 
 }  // namespace bgtq
@@ -60,6 +88,7 @@ struct bgtq_plan {
     std::vector<float> thr[bgtq::kWMax + 1];
     std::vector<uint32_t> pair_lut;
     std::vector<uint16_t> single_lut;
+    std::vector<uint32_t> dec_image;
     // inspection copies (bgtq_plan_get_head)
     std::vector<std::vector<int8_t>> sign_k8, sign_v8;
     std::vector<std::vector<uint8_t>> piece;

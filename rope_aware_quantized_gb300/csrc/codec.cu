@@ -103,15 +103,19 @@ __global__ void __launch_bounds__(128) quantize_append_kernel(QParams p) {
     __shared__ uint32_t vmask[kWarpsQ][8 * kPairMaxW];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y, b = blockIdx.z;
+    // The next kernel may launch right away (programmatic dependent launch);
+    // the plan's tables are static, the inputs are read after the wait.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Lloyd-Max thresholds of every width, staged once per block
+    for (int i = threadIdx.x; i < (kWMax + 1) * 256 / 4; i += kWarpsQ * 32)
+        reinterpret_cast<float4*>(s_thr)[i] = __ldg(reinterpret_cast<const float4*>(p.thr) + i);
+    __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int ps = p.pos_start[b];
     if (ps < 0 || (int64_t)ps + p.t_new > p.cap) {
         if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_APPEND_CAPACITY);
         return;
     }
-    // Lloyd-Max thresholds of every width, staged once per block
-    for (int i = threadIdx.x; i < (kWMax + 1) * 256 / 4; i += kWarpsQ * 32)
-        reinterpret_cast<float4*>(s_thr)[i] = __ldg(reinterpret_cast<const float4*>(p.thr) + i);
-    __syncthreads();
     const HeadTab* ht = p.heads + h;
     const int n_coded = ht->n_coded;
     const size_t unit = (size_t)b * p.H + h;
@@ -348,8 +352,16 @@ cudaError_t launch_quantize_append(const bgtq_plan& pl, cudaStream_t s, const vo
     const int64_t pairs = (int64_t)t_new / 2 + 1;
     const int64_t per_block = (int64_t)kWarpsQ * kPairsPerWarp;
     dim3 grid((unsigned)((pairs + per_block - 1) / per_block), (unsigned)pl.H, (unsigned)batch);
-    quantize_append_kernel<<<grid, 32 * kWarpsQ, 0, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(32 * kWarpsQ, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quantize_append_kernel, p);
 }
 
 cudaError_t launch_dequant(const bgtq_plan& pl, cudaStream_t s, const bgtq_cache& c, int batch, int b, int head,

@@ -45,16 +45,8 @@ constexpr int kTile = 16;         // tokens per warp iteration; splits start on 
 constexpr int kCluster = 8;       // CTAs per thread-block cluster (consecutive splits of one head)
 constexpr int kMaxClusters = 64;  // clusters per (sequence, head)
 constexpr int kPartStride = 2 + kD;  // m, l, acc[128] per query head
-// Shared-memory decode tables (32-bit words).  Words [0, 2048): pair tables
-// of widths 0..5 shared by all lanes (entry 4^w + f).  Words [4096, 8192):
-// per-lane copies of the pair tables of widths 0..3 (entry e of lane L at
-// 4096 + 32 e + L), so lanes never collide on a bank.  Words [2048, 4096) are
-// unused by the tables; after the main loop the region is reused.
-constexpr int kTabWords = 8192;
-constexpr int kPrivWord = 4096;
-constexpr uint32_t kPrivByte = 4u * kPrivWord;
+constexpr uint32_t kPrivByte = 4u * kImgPriv;
 constexpr int kPrivMaxW = 3;
-constexpr int kPrivEntries = 1 << (2 * kPrivMaxW + 1);   // 128
 constexpr float kHeadroom = 8.0f;  // log2 headroom of the softmax reference
 
 struct DecodeParams {
@@ -72,6 +64,7 @@ struct DecodeParams {
     const HeadTab* heads;
     const uint32_t* pair_lut;
     const uint16_t* single_lut;
+    const uint32_t* dec_image;
     float scale_log2;
     float v_inv_sqrt;
     int H, G, n_split, tps;
@@ -84,6 +77,11 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// own set-up now / wait until the previous kernel's results are visible.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Bulk prefetch of [ptr, ptr + bytes) into L2 (16-byte aligned, multiple of 16).
 __device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
@@ -135,8 +133,9 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // Decoded fp16 pair of K slot S (compile-time) of the lane's record slice.
 // (sh, mask, base) select the field and the table: the field is shifted so
 // that it lands pre-multiplied by the entry stride of its table (shared
-// tables: 4 bytes; per-lane tables: 128 bytes), masked and OR-ed with the
-// table's byte base.  Slots flagged in `wide` use the single-entry table.
+// tables: 4 bytes; per-token-lane copies: 32 bytes; per-lane copies: 128
+// bytes), masked and OR-ed with the copy's byte base.  Slots flagged in
+// `wide` use the single-entry table (two lookups, 16-byte entry stride).
 template <int BK, int S, bool kCheckWide>
 __device__ __forceinline__ uint32_t k_pair(const uint32_t (&kw)[BK], uint32_t sh, uint32_t mask, uint32_t base,
                                            uint32_t wide, const uint32_t* s_tab, const uint16_t* s_single) {
@@ -145,11 +144,12 @@ __device__ __forceinline__ uint32_t k_pair(const uint32_t (&kw)[BK], uint32_t sh
     const uint32_t lo = kUpper ? kword(kw, 1) : kword(kw, 0);
     const uint32_t hi = kUpper ? kword(kw, 2) : kword(kw, 1);
     const uint64_t win = ((uint64_t)hi << 32) | lo;
+    // slot 0 starts at bit 0: its field is shifted left (by sh) instead
     if (!kCheckWide || !((wide >> S) & 1u)) {
-        const uint32_t x = S == 0 ? (kword(kw, 0) << 2) : (uint32_t)(win >> sh);
+        const uint32_t x = S == 0 ? (kword(kw, 0) << sh) : (uint32_t)(win >> sh);
         return lds32(s_tab, (x & mask) | base);
     }
-    const uint32_t x = S == 0 ? (kword(kw, 0) << 1) : (uint32_t)(win >> sh);
+    const uint32_t x = S == 0 ? (kword(kw, 0) << sh) : (uint32_t)(win >> sh);
     const uint32_t w = __popc(mask);
     const uint32_t a0 = (x & mask) | base;
     const uint32_t a1 = ((x >> w) & mask) | base;
@@ -204,6 +204,30 @@ __device__ __forceinline__ void pv_tile(float (&acc)[16][4], const uint32_t (&pa
     mma16816(acc[ND], pa, b0, b1);
 }
 
+// Blockwise Hadamard butterflies over the warp's 128 slots (lane L holds
+// slots 4L..4L+3): stage h pairs (j, j+h) inside pieces larger than h.
+__device__ __forceinline__ void rotate_warp(float (&x)[4], const int (&plog2)[4], int lane) {
+#pragma unroll
+    for (int h = 1; h <= 2; h <<= 1) {
+        float y[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float o = x[i ^ h];
+            y[i] = (1 << plog2[i]) > h ? ((i & h) ? o - x[i] : x[i] + o) : x[i];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = y[i];
+    }
+#pragma unroll
+    for (int h = 4; h < kD; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float o = __shfl_xor_sync(0xffffffffu, x[i], h >> 2);
+            if ((1 << plog2[i]) > h) x[i] = ((4 * lane + i) & h) ? o - x[i] : x[i] + o;
+        }
+    }
+}
+
 // Global-memory operands of one 16-token tile for one lane.
 template <int BK, int BV>
 struct TileRegs {
@@ -239,17 +263,21 @@ struct TileRegs {
 
 template <int BK, int BV, bool kAnyWide>
 __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) {
-    __shared__ __align__(16) uint32_t s_tab[kTabWords];
-    __shared__ __align__(16) uint16_t s_single[kSingleLutHalves];
+    __shared__ __align__(16) uint32_t s_tab[kImgWords];
+    const uint16_t* s_single = reinterpret_cast<const uint16_t*>(s_tab);
     __shared__ __align__(16) float s_q[8][kD];
     __shared__ float s_m[kWarps][8], s_l[kWarps][8];
     __shared__ float s_qmax[kWarps][8], s_qscale[8], s_qunscale[8];
     __shared__ int s_last;
     // after the main loop the table region holds the warp partials and the
     // CTA partial that the cluster reads
-    float (*s_o)[8][kD] = reinterpret_cast<float (*)[8][kD]>(s_tab + kPrivWord);
+    float (*s_o)[8][kD] = reinterpret_cast<float (*)[8][kD]>(s_tab + kImgPriv);
     float (*s_part)[kPartStride] = reinterpret_cast<float (*)[kPartStride]>(s_tab);
 
+    // The next kernel may launch right away; everything this kernel reads
+    // that an earlier kernel may still be writing (q, the cache) is read only
+    // after pdl_wait().  seq_lens is never written by this library's kernels.
+    pdl_trigger();
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
     const int G = p.G;
@@ -264,6 +292,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     const int cid = split / kCluster;
     if (seq == 0) {
         if (split == 0) {
+            pdl_wait();
             for (int i = tid; i < G * kD; i += kWarps * 32) {
                 const size_t o = ((size_t)b * p.H * G + (size_t)h * G) * kD + i;
                 if (p.out_dtype) static_cast<float*>(p.out)[o] = 0.0f;
@@ -291,72 +320,62 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
                        (size_t)((t_end - t_begin + 1) / 2) * (32 * BV), tid);
         prefetch_range(reinterpret_cast<const char*>(kn + t_begin), (size_t)(t_end - t_begin) * 4, tid);
         prefetch_range(reinterpret_cast<const char*>(vn + t_begin), (size_t)(t_end - t_begin) * 4, tid);
-        const uint4* lp = reinterpret_cast<const uint4*>(p.pair_lut);
-        uint4* sp = reinterpret_cast<uint4*>(s_tab);
+        // the table image: independent 16-byte loads, then the stores
+        constexpr int kPer = kImgWords / 4 / (kWarps * 32);
+        static_assert(kImgWords % (4 * kWarps * 32) == 0, "image size");
+        uint4 img[kPer];
+        const uint4* src = reinterpret_cast<const uint4*>(p.dec_image);
 #pragma unroll
-        for (int i = 0; i < kPairLutWords / 4 / (kWarps * 32); ++i) sp[tid + i * kWarps * 32] = __ldg(lp + tid + i * kWarps * 32);
-        // per-lane copies: entry e of lane L at kPrivWord + 32 e + L
-        uint4* pp = reinterpret_cast<uint4*>(s_tab + kPrivWord);
+        for (int i = 0; i < kPer; ++i) img[i] = __ldg(src + tid + i * kWarps * 32);
 #pragma unroll
-        for (int i = 0; i < kPrivEntries * 32 / 4 / (kWarps * 32); ++i) {
-            const int q4 = tid + i * kWarps * 32;
-            const uint32_t v = __ldg(p.pair_lut + (q4 >> 3));
-            pp[q4] = make_uint4(v, v, v, v);
-        }
-        if (tid < kSingleLutHalves / 8)
-            reinterpret_cast<uint4*>(s_single)[tid] = __ldg(reinterpret_cast<const uint4*>(p.single_lut) + tid);
+        for (int i = 0; i < kPer; ++i) reinterpret_cast<uint4*>(s_tab)[tid + i * kWarps * 32] = img[i];
     }
 
+    pdl_wait();  // q and the cache may have been written by the previous kernel
     if (active) {
-    // ---- query heads into the key codec domain
+    // ---- query heads into the key codec domain: warp w rotates heads 2w and
+    // 2w+1, lane L holding codec coordinates 4L..4L+3 (de-whitening, signs,
+    // blockwise Hadamard by shuffles, 1/sqrt(piece), softmax scale, log2 e)
     const int n_coded = ht->n_coded;
     {
-        const int j = tid;
-        const int psz = 1 << ht->plog2[j];
-        const float f = ht->sign_k[j] * ht->dewhiten[j];
-        const int src = ht->perm[j];
-        const __half* qb = p.q + ((size_t)b * p.H * G + (size_t)h * G) * kD;
-        for (int gg = 0; gg < 8; ++gg)
-            s_q[gg][j] = (gg < G && j < n_coded) ? __half2float(qb[(size_t)gg * kD + src]) * f : 0.0f;
-        __syncthreads();
-        for (int hh = 1; hh < kD; hh <<= 1) {
-            float nv[8];
+        int pl[4], src[4];
+        float f[4], sc[4];
 #pragma unroll
-            for (int gg = 0; gg < 8; ++gg) {
-                const float mine = s_q[gg][j], other = s_q[gg][j ^ hh];
-                nv[gg] = psz > hh ? ((j & hh) ? other - mine : mine + other) : mine;
-            }
-            __syncthreads();
-#pragma unroll
-            for (int gg = 0; gg < 8; ++gg) s_q[gg][j] = nv[gg];
-            __syncthreads();
+        for (int i = 0; i < 4; ++i) {
+            const int j = 4 * lane + i;
+            const bool coded = j < n_coded;
+            pl[i] = coded ? ht->plog2[j] : 0;
+            src[i] = ht->perm[j];
+            f[i] = coded ? ht->sign_k[j] * ht->dewhiten[j] : 0.0f;
+            sc[i] = coded ? ht->inv_sqrt[j] * p.scale_log2 : 0.0f;
         }
-        const float sc = j < n_coded ? ht->inv_sqrt[j] * p.scale_log2 : 0.0f;
+        const __half* qb = p.q + ((size_t)b * p.H * G + (size_t)h * G) * kD;
 #pragma unroll
-        for (int gg = 0; gg < 8; ++gg) s_q[gg][j] *= sc;
-        // Per-head power-of-two scale so the fp16 hi/lo split cannot overflow
-        // (whitening moves a key block's scale into the query, so sigma*q can
-        // exceed the fp16 range): max |q| is brought to [2^13, 2^14); the
-        // logits are multiplied back by the exact inverse.
+        for (int k = 0; k < 2; ++k) {
+            const int gg = 2 * warp + k;
+            float x[4];
 #pragma unroll
-        for (int gg = 0; gg < 8; ++gg) {
-            float a = fabsf(s_q[gg][j]);
+            for (int i = 0; i < 4; ++i) x[i] = gg < G ? __half2float(qb[(size_t)gg * kD + src[i]]) * f[i] : 0.0f;
+            rotate_warp(x, pl, lane);
+            float a = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                x[i] *= sc[i];
+                a = fmaxf(a, fabsf(x[i]));
+            }
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-            if (lane == 0) s_qmax[warp][gg] = a;
-        }
-        __syncthreads();
-        if (tid < 8) {
-            const float a = fmaxf(fmaxf(s_qmax[0][tid], s_qmax[1][tid]), fmaxf(s_qmax[2][tid], s_qmax[3][tid]));
+            // Per-head power-of-two scale so the fp16 hi/lo split cannot
+            // overflow (whitening moves a key block's scale into the query):
+            // max |q| is brought to [2^13, 2^14); logits are scaled back.
             int e = 0;
             if (a > 0.0f && isfinite(a)) frexpf(a, &e);
             e = max(-100, min(100, e));
-            s_qscale[tid] = ldexpf(1.0f, 14 - e);
-            s_qunscale[tid] = ldexpf(1.0f, e - 14);
-        }
-        __syncthreads();
+            const float qs = ldexpf(1.0f, 14 - e);
 #pragma unroll
-        for (int gg = 0; gg < 8; ++gg) s_q[gg][j] *= s_qscale[gg];
+            for (int i = 0; i < 4; ++i) s_q[gg][4 * lane + i] = x[i] * qs;
+            if (lane == 0) s_qunscale[gg] = ldexpf(1.0f, e - 14);
+        }
         __syncthreads();
     }
     const float q_unscale = s_qunscale[g];
@@ -370,26 +389,15 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         split_hilo(v0 ? x0 : 0.0f, v0 ? x1 : 0.0f, qa[c][0], qa[c][1]);
         split_hilo(v1 ? y0 : 0.0f, v1 ? y1 : 0.0f, qa[c][2], qa[c][3]);
     }
-    // ---- per-lane K slot metadata: field shift, mask and table base
+    // ---- per-lane K slot lookup recipes (precomputed in the plan)
     const uint32_t wide = ht->wide_mask;
     uint32_t ksh[16], kmask[16], kbase[16];
 #pragma unroll
     for (int s = 0; s < 16; ++s) {
-        const uint32_t w = ht->slot_w[t][s];
-        const uint32_t sh = ht->slot_sh[t][s];
-        if ((wide >> s) & 1u) {  // single-entry table, two lookups
-            ksh[s] = sh > 0 ? sh - 1 : 0;
-            kmask[s] = ((1u << w) - 1u) << 1;
-            kbase[s] = (1u << w) << 1;
-        } else if (w <= (uint32_t)kPrivMaxW && sh >= 7 && s != 0) {  // per-lane pair table
-            ksh[s] = sh - 7;
-            kmask[s] = ((1u << (2 * w)) - 1u) << 7;
-            kbase[s] = kPrivByte + 4u * lane + ((1u << (2 * w)) << 7);
-        } else {  // shared pair table
-            ksh[s] = sh > 1 ? sh - 2 : 0;
-            kmask[s] = ((1u << (2 * w)) - 1u) << 2;
-            kbase[s] = (1u << (2 * w)) << 2;
-        }
+        const uint4 m = __ldg(reinterpret_cast<const uint4*>(&ht->kmeta[t][s]));
+        ksh[s] = m.x;
+        kmask[s] = m.y;
+        kbase[s] = m.z + (m.w & 255u) * lane + (m.w >> 8) * g;
     }
     const uint32_t vbase = BV <= kPrivMaxW ? kPrivByte + 4u * lane + ((1u << (2 * BV)) << 7) : (1u << (2 * BV)) << 2;
     __syncthreads();
@@ -570,27 +578,40 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     if (crank >= G) return;
     {
         const int gg = crank;
-        float M = -INFINITY;
-        for (int c = 0; c < n_clusters; ++c) M = fmaxf(M, __ldcg(cpart_base + ((size_t)c * G + gg) * kPartStride));
-        float L = 0.0f, O = 0.0f;
-        for (int c = 0; c < n_clusters; ++c) {
+        float* s_ml = s_q[1];  // (m, l) of up to 64 cluster partials
+        for (int c = tid; c < n_clusters; c += kWarps * 32) {
             const float* src = cpart_base + ((size_t)c * G + gg) * kPartStride;
-            const float mcv = __ldcg(src);
-            const float f = mcv == -INFINITY ? 0.0f : exp2f(mcv - M);
-            L += __ldcg(src + 1) * f;
-            O += __ldcg(src + 2 + tid) * f;
+            s_ml[2 * c] = __ldcg(src);
+            s_ml[2 * c + 1] = __ldcg(src + 1);
         }
-        s_q[0][tid] = O / L;
         __syncthreads();
-        // inverse value rotation: Hadamard-128, 1/sqrt(128), signs
-        for (int hh = 1; hh < kD; hh <<= 1) {
-            const float mine = s_q[0][tid], other = s_q[0][tid ^ hh];
-            const float nv = (tid & hh) ? other - mine : mine + other;
-            __syncthreads();
-            s_q[0][tid] = nv;
-            __syncthreads();
+        float M = -INFINITY;
+        for (int c = 0; c < n_clusters; ++c) M = fmaxf(M, s_ml[2 * c]);
+        float L = 0.0f, O = 0.0f;
+#pragma unroll 8
+        for (int c = 0; c < n_clusters; ++c) {
+            const float mcv = s_ml[2 * c];
+            const float f = mcv == -INFINITY ? 0.0f : exp2f(mcv - M);
+            L += s_ml[2 * c + 1] * f;
+            O += __ldcg(cpart_base + ((size_t)c * G + gg) * kPartStride + 2 + tid) * f;
         }
-        const float val = s_q[0][tid] * p.v_inv_sqrt * ht->sign_v[tid];
+        // inverse value rotation (Hadamard-128, 1/sqrt(128), signs): thread
+        // tid holds dim tid; stages below 32 by shuffles, 32 and 64 via smem
+        float v = O / L;
+#pragma unroll
+        for (int hh = 1; hh < 32; hh <<= 1) {
+            const float o = __shfl_xor_sync(0xffffffffu, v, hh);
+            v = (tid & hh) ? o - v : v + o;
+        }
+#pragma unroll
+        for (int hh = 32; hh < kD; hh <<= 1) {
+            s_q[0][tid] = v;
+            __syncthreads();
+            const float o = s_q[0][tid ^ hh];
+            __syncthreads();
+            v = (tid & hh) ? o - v : v + o;
+        }
+        const float val = v * p.v_inv_sqrt * ht->sign_v[tid];
         const size_t o = ((size_t)b * p.H * G + (size_t)h * G + gg) * kD + tid;
         if (p.out_dtype) static_cast<float*>(p.out)[o] = val;
         else static_cast<__half*>(p.out)[o] = __float2half_rn(val);
@@ -599,29 +620,31 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
 }
 
 template <int BK, int BV, bool kAnyWide>
-cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t s, cudaLaunchAttribute* attr) {
+cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t s, cudaLaunchAttribute* attr /*[2]*/) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kWarps * 32, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
-    attr->id = cudaLaunchAttributeClusterDimension;
-    attr->val.clusterDim.x = kCluster;
-    attr->val.clusterDim.y = 1;
-    attr->val.clusterDim.z = 1;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cfg;
 }
 
 template <int BK, int BV>
 cudaError_t launch_t(const DecodeParams& p, dim3 grid, cudaStream_t s, bool any_wide) {
-    cudaLaunchAttribute attr;
+    cudaLaunchAttribute attr[2];
     if (any_wide) {
-        cudaLaunchConfig_t cfg = launch_config<BK, BV, true>(grid, s, &attr);
+        cudaLaunchConfig_t cfg = launch_config<BK, BV, true>(grid, s, attr);
         return cudaLaunchKernelEx(&cfg, decode_kernel<BK, BV, true>, p);
     }
-    cudaLaunchConfig_t cfg = launch_config<BK, BV, false>(grid, s, &attr);
+    cudaLaunchConfig_t cfg = launch_config<BK, BV, false>(grid, s, attr);
     return cudaLaunchKernelEx(&cfg, decode_kernel<BK, BV, false>, p);
 }
 
@@ -630,8 +653,9 @@ cudaError_t launch_t(const DecodeParams& p, dim3 grid, cudaStream_t s, bool any_
 // the SM count times the blocks per SM).
 template <int BK, int BV>
 int resident_ctas() {
-    cudaLaunchAttribute attr;
-    cudaLaunchConfig_t cfg = launch_config<BK, BV, false>(dim3(kCluster, 1, 1), nullptr, &attr);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = launch_config<BK, BV, false>(dim3(kCluster, 1, 1), nullptr, attr);
+    cfg.numAttrs = 1;  // occupancy: the cluster shape only
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, decode_kernel<BK, BV, false>, &cfg) != cudaSuccess || clusters <= 0) {
         cudaGetLastError();
@@ -672,8 +696,8 @@ int resident_ctas_for(int bk, int bv) {
 }  // namespace
 
 SplitPlan decode_split(const bgtq_plan& p, int batch, int64_t max_len) {
-    // One wave of resident CTAs in total (whole clusters of 8), at least 64
-    // tokens per CTA, splits in whole 16-token tiles.
+    // One wave of resident CTAs in total (whole clusters of 8), splits of
+    // whole 64-token steps (16 tokens for each of the 4 warps).
     SplitPlan sp;
     const int64_t units = std::max<int64_t>(1, (int64_t)batch * p.H);
     const int64_t len = std::max<int64_t>(max_len, 1);
@@ -685,8 +709,9 @@ SplitPlan decode_split(const bgtq_plan& p, int batch, int64_t max_len) {
     ns = std::min<int64_t>(ns, (int64_t)kCluster * kMaxClusters);
     if (len >= 64 * kCluster) ns = std::max<int64_t>(ns, kCluster);
     ns = std::max<int64_t>(ns, 1);
+    // whole 64-token steps so every warp of a CTA gets the same tile count
     int64_t tps = (len + ns - 1) / ns;
-    tps = (tps + kTile - 1) / kTile * kTile;
+    tps = (tps + kWarps * kTile - 1) / (kWarps * kTile) * (kWarps * kTile);
     const int64_t n = (len + tps - 1) / tps;
     sp.tokens_per_split = (int)tps;
     sp.n_split = (int)((n + kCluster - 1) / kCluster * kCluster);
@@ -719,6 +744,7 @@ cudaError_t launch_decode(const bgtq_plan& pl, cudaStream_t s, const void* q, co
     p.heads = pl.dev.heads;
     p.pair_lut = pl.dev.pair_lut;
     p.single_lut = pl.dev.single_lut;
+    p.dec_image = pl.dev.dec_image;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.v_inv_sqrt = (float)(1.0 / std::sqrt((double)kD));
     p.H = pl.H;
