@@ -2,8 +2,9 @@
 """Benchmark of the Block-GTQ packed-cache decode path on GB300.
 
 One step = one decode step of the whole workload: for every layer, append the
-new token to the packed cache (bgtq_quantize_append) and run decode attention
-over the packed cache (bgtq_decode_attn).  The default workload is the
+new token to the packed cache and run decode attention over the packed cache,
+in one launch (bgtq_decode_step; --two-call: bgtq_quantize_append followed by
+bgtq_decode_attn).  The default workload is the
 Qwen2.5-3B-shaped 36-layer stack at 131072 cached tokens, K3V3 (2 KV heads,
 16 query heads, batch 1).  The step's launches are captured once in a CUDA
 graph and replayed.  Prints one JSON line (rank 0).
@@ -49,6 +50,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="build only the first N layers (profiling)")
     ap.add_argument("--eager", action="store_true", help="launch without a CUDA graph (profiling)")
+    ap.add_argument("--two-call", action="store_true",
+                    help="per layer bgtq_quantize_append + bgtq_decode_attn instead of the fused bgtq_decode_step")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--sample-seconds", type=float, default=12.0, help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -239,6 +242,46 @@ def replica_throughput(world: int, batch: int, ms_per_step: float) -> float:
 
 # ----------------------------------------------------------------------------- GPU arm
 
+def measure_prefill(w, plan, tokens: int, peaks: dict, stream) -> dict:
+    """The quantize-append kernel alone on a prefill: `tokens` fp16 K/V rows
+    per (sequence, KV head) of one layer encoded into an empty packed cache in
+    one bgtq_quantize_append call (the inputs, 2 * batch * heads * tokens *
+    256 bytes, are larger than L2 at the default workload; no flush)."""
+    import torch
+
+    import rope_aware_quantized_gb300 as bg
+
+    B, H = w.batch, w.n_kv
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(20260)
+    k = torch.randn((B, H, tokens, 128), generator=gen, device="cuda").half()
+    v = torch.randn((B, H, tokens, 128), generator=gen, device="cuda").half()
+    cache = bg.Cache(plan, B, tokens + (tokens & 1))
+    pos = torch.zeros(B, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(8):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            bg.bgtq_quantize_append(plan, k, v, pos, cache, status=status)
+            b.record(stream)
+            times.append((a, b))
+    torch.cuda.synchronize()
+    assert status.item() == 0, f"append status {status.item()}"
+    ms = statistics.median(a.elapsed_time(b) for a, b in times[3:])
+    rows = B * H * tokens
+    read = rows * 128 * 2 * 2
+    written = rows * (16 * (w.bits_per_key // 128) + 16 * w.v_bits + 8)
+    gbs = (read + written) / (ms / 1000.0) / 1e9
+    del k, v, cache
+    return {"tokens_per_s": B * tokens / (ms / 1000.0), "ms_per_launch": ms, "tokens": tokens, "batch": B,
+            "kv_heads": H, "bytes_per_launch": read + written, "achieved": gbs, "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "bound": "hbm",
+            "bytes": "fp16 K and V rows read + packed K/V records and both norms written"}
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -276,10 +319,21 @@ def run_gpu(args):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     stream = torch.cuda.Stream()
 
-    def step():
-        for l, ls in enumerate(layers):
+    fused = not args.two_call
+    nk_tok = [nk_all[l][:, :, 0] for l in range(L)]  # [B][H][128] views of the new tokens
+    nv_tok = [nv_all[l][:, :, 0] for l in range(L)]
+
+    def layer_call(l, ls):
+        if fused:
+            bg.bgtq_decode_step(ls.plan, ls.q, nk_tok[l], nv_tok[l], ls.pos_new, ls.cache, ls.seq_lens, max_len,
+                                out_all[l], ws, status=status)
+        else:
             bg.bgtq_quantize_append(ls.plan, ls.new_k, ls.new_v, ls.pos_new, ls.cache, status=status)
             bg.bgtq_decode_attn(ls.plan, ls.q, ls.cache, ls.seq_lens, max_len, out_all[l], ws, status=status)
+
+    def step():
+        for l, ls in enumerate(layers):
+            layer_call(l, ls)
 
     with torch.cuda.stream(stream):
         step()
@@ -295,7 +349,7 @@ def run_gpu(args):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             step()
-    launches_per_step = 2 * L
+    launches_per_step = L if fused else 2 * L
 
     def barrier():
         torch.cuda.synchronize()
@@ -328,17 +382,27 @@ def run_gpu(args):
             for l, ls in enumerate(layers):
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-                bg.bgtq_decode_attn(ls.plan, ls.q, ls.cache, ls.seq_lens, max_len, out_all[l], ws, status=status)
+                if fused:
+                    bg.bgtq_decode_step(ls.plan, ls.q, nk_tok[l], nv_tok[l], ls.pos_new, ls.cache, ls.seq_lens,
+                                        max_len, out_all[l], ws, status=status)
+                else:
+                    bg.bgtq_decode_attn(ls.plan, ls.q, ls.cache, ls.seq_lens, max_len, out_all[l], ws, status=status)
                 b.record(stream)
                 durs.append((a, b))
     torch.cuda.synchronize()
     launch_ms = statistics.mean(a.elapsed_time(b) for a, b in durs)
     bpth = w.packed_bytes_per_token_head()
+    # packed K/V codes + norms of every cached token, q read and out written;
+    # the fused step also reads the new token and writes its records
     decode_bytes = int(lens.sum()) * w.n_kv * bpth + B * w.n_q * 128 * 2 * 2
+    if fused:
+        decode_bytes += B * w.n_kv * (2 * 256 + 16 * (w.bits_per_key // 128) + 16 * w.v_bits + 8)
     peaks, peak_kind = load_peaks()
     achieved = decode_bytes / (launch_ms / 1000.0) / 1e9
     traffic = traffic_from_profile()
     step_bytes = L * decode_bytes
+
+    prefill = measure_prefill(w, layers[0].plan, max_len, peaks, stream)
 
     # end to end: pinned host inputs -> device, graph replay, outputs -> host
     hq = torch.empty(q_all.shape, dtype=q_all.dtype, pin_memory=True)
@@ -381,7 +445,9 @@ def run_gpu(args):
             "config": {
                 "workload": w.name if L == w.layers else f"{w.name}[first {L} layers]", "layers": L, "kv_heads": w.n_kv, "q_heads": w.n_q, "head_dim": 128,
                 "context": int(max_len), "batch": B, "kv_bits": f"K{w.bits_per_key // 128}V{w.v_bits}",
-                "step": "per layer: quantize-append 1 token + decode attention" + (" (eager)" if args.eager else " (CUDA graph)"),
+                "step": ("per layer: bgtq_decode_step (quantize-append 1 token + decode attention, one launch)" if fused
+                         else "per layer: bgtq_quantize_append 1 token + bgtq_decode_attn")
+                        + (" (eager)" if args.eager else " (CUDA graph)"),
                 "packed_bytes_per_step": step_bytes, "fp16_kv_bytes_per_step": fp16_bytes,
                 "compute": "fp16 mma operands (hi+lo split of q and p), fp32 accumulate; fp32 encoder",
                 "l2": "inputs larger than L2 (packed cache per step >> 129 MB L2), no flush",
@@ -389,7 +455,7 @@ def run_gpu(args):
             },
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                         "kernel": "decode_attn", "launch_ms": launch_ms, "bytes_per_launch": decode_bytes,
+                         "kernel": "decode_step" if fused else "decode_attn", "launch_ms": launch_ms, "bytes_per_launch": decode_bytes,
                          "peak_kind": f"{peak_kind} (copy, burst)"},
             "e2e": {"value": replica_throughput(world, B, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "path": "pinned H2D of q/new K/V, graph of the API calls, D2H of out"},
@@ -397,6 +463,7 @@ def run_gpu(args):
             "clocks": clk,
             "achieved_step_gbs": step_bytes / (ms / 1000.0) / 1e9,
         }
+        line["append_prefill"] = prefill
         if cpu:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)

@@ -222,6 +222,29 @@ int bgtq_decode_attn(const bgtq_plan* plan, void* stream, const void* q_fp16, co
                      float softmax_scale, void* workspace, size_t ws_bytes, int32_t* dev_status);
 
 /*
+ * bgtq_decode_step — one decode step of one layer in a single launch: the
+ * new token of every sequence is quantize-appended to the packed cache and
+ * attention then runs over the updated cache.
+ * Source: the packed-cache serving path (abstract; review §1 "Packed-Cache",
+ * Figure 2): each step appends the new token's compressed K/V and attends on
+ * the compressed cache.
+ *   k_new_fp16, v_new_fp16  device, [batch][H][128] half: the new token
+ *   pos_new      device, [batch] int32 cache position of the new token (read
+ *                before the kernel waits for the previous kernel, like
+ *                seq_lens); usually seq_lens[b] - 1
+ *   all other arguments as bgtq_decode_attn (same workspace size)
+ * The result equals bgtq_quantize_append (t_new = 1, pos_start = pos_new)
+ * followed by bgtq_decode_attn: the same codes, norms and records are
+ * written and the attention sees them.  A position outside [0, capacity)
+ * appends nothing and sets BGTQ_STATUS_APPEND_CAPACITY.
+ * Errors: as bgtq_decode_attn.
+ */
+int bgtq_decode_step(const bgtq_plan* plan, void* stream, const void* q_fp16, const void* k_new_fp16,
+                     const void* v_new_fp16, const int32_t* pos_new, const bgtq_cache* cache,
+                     const int32_t* seq_lens, int64_t max_len, int batch, void* out, int out_dtype,
+                     float softmax_scale, void* workspace, size_t ws_bytes, int32_t* dev_status);
+
+/*
  * bgtq_decode_attn_noalloc — bgtq_decode_attn for callers that cannot
  * allocate device memory (a fixed memory budget, an allocator or pool that
  * must not be bypassed, a host runtime without a device allocator).  The

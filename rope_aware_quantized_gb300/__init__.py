@@ -209,6 +209,29 @@ def bgtq_decode_attn(plan: Plan, q_fp16, cache: Cache, seq_lens, max_len: int, o
                                   workspace.numel() * workspace.element_size(), _ptr(status)))
 
 
+def bgtq_decode_step(plan: Plan, q_fp16, k_new, v_new, pos_new, cache: Cache, seq_lens, max_len: int, out,
+                     workspace, softmax_scale: float | None = None, status=None, stream=None):
+    """One decode step of a layer in one launch: append the new token
+    (k_new/v_new: [B][H][128] float16 at pos_new: [B] int32), then attend
+    (q: [B][H*G][128] float16 over seq_lens tokens); out as bgtq_decode_attn."""
+    import torch
+    batch = q_fp16.shape[0]
+    if out.dtype == torch.float32:
+        out_dtype = 1
+    elif out.dtype == torch.float16:
+        out_dtype = 0
+    else:
+        raise ValueError("out must be float16 or float32")
+    if k_new.shape[-1] != HEAD_DIM or tuple(v_new.shape) != tuple(k_new.shape) or k_new.numel() != batch * plan.n_kv_heads * HEAD_DIM:
+        raise ValueError("k_new and v_new must be [B][H][128]")
+    if not (k_new.is_contiguous() and v_new.is_contiguous()):
+        raise ValueError("k_new and v_new must be contiguous")
+    scale = (1.0 / HEAD_DIM ** 0.5) if softmax_scale is None else softmax_scale
+    _check(lib().bgtq_decode_step(plan.handle, _stream(stream), _ptr(q_fp16), _ptr(k_new), _ptr(v_new), _ptr(pos_new),
+                                  C.byref(cache.desc), _ptr(seq_lens), max_len, batch, _ptr(out), out_dtype, scale,
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status)))
+
+
 def bgtq_decode_attn_noalloc(plan: Plan, q_fp16, cache: Cache, seq_lens, max_len: int, out,
                              softmax_scale: float | None = None, status=None, stream=None):
     """bgtq_decode_attn without a workspace, for callers that cannot allocate
@@ -235,6 +258,7 @@ def bgtq_dequant_debug(plan: Plan, cache: Cache, b: int, head: int, t0: int, t1:
 
 __all__ = [
     "BgtqError", "Plan", "Cache", "CacheView", "bgtq_alloc_bits", "bgtq_plan_create", "bgtq_cache_bytes",
-    "bgtq_quantize_append", "bgtq_decode_attn_workspace", "bgtq_decode_attn", "bgtq_decode_attn_noalloc",
+    "bgtq_quantize_append", "bgtq_decode_attn_workspace", "bgtq_decode_attn", "bgtq_decode_step",
+    "bgtq_decode_attn_noalloc",
     "bgtq_dequant_debug",
 ]

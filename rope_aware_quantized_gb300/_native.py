@@ -42,6 +42,9 @@ EXPORTS = {
     "bgtq_decode_attn_workspace": (C.c_int, [C.c_void_p, C.c_int, C.c_int64, C.POINTER(C.c_size_t)]),
     "bgtq_decode_attn": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.POINTER(BgtqCache), C.c_void_p, C.c_int64,
                                    C.c_int, C.c_void_p, C.c_int, C.c_float, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "bgtq_decode_step": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                   C.POINTER(BgtqCache), C.c_void_p, C.c_int64, C.c_int, C.c_void_p, C.c_int, C.c_float,
+                                   C.c_void_p, C.c_size_t, C.c_void_p]),
     "bgtq_decode_attn_noalloc": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.POINTER(BgtqCache), C.c_void_p,
                                            C.c_int64, C.c_int, C.c_void_p, C.c_int, C.c_float, C.c_void_p]),
     "bgtq_dequant_debug": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(BgtqCache), C.c_int, C.c_int, C.c_int,

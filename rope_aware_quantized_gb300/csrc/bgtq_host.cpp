@@ -654,6 +654,30 @@ int bgtq_decode_attn(const bgtq_plan* p, void* stream, const void* q, const bgtq
     return BGTQ_OK;
 }
 
+int bgtq_decode_step(const bgtq_plan* p, void* stream, const void* q, const void* k_new, const void* v_new,
+                     const int32_t* pos_new, const bgtq_cache* c, const int32_t* seq_lens, int64_t max_len, int batch,
+                     void* out, int out_dtype, float scale, void* ws, size_t ws_bytes, int32_t* status) {
+    int rc = check_plan(p);
+    if (rc) return rc;
+    if ((rc = check_cache(p, c))) return rc;
+    if (batch < 0 || max_len < 0) return set_error(BGTQ_ERR_INVALID_ARG, "batch and max_len must be >= 0");
+    if (batch == 0) return BGTQ_OK;
+    if (!q || !k_new || !v_new || !pos_new || !seq_lens || !out || !ws)
+        return set_error(BGTQ_ERR_INVALID_ARG, "NULL pointer");
+    if (out_dtype != 0 && out_dtype != 1) return set_error(BGTQ_ERR_INVALID_ARG, "out_dtype must be 0 (half) or 1 (float)");
+    if (p->bk > 3) return set_error(BGTQ_ERR_UNSUPPORTED, "decode supports bits_per_key <= 384");
+    if (p->bv > 4) return set_error(BGTQ_ERR_UNSUPPORTED, "decode supports v_bits <= 4");
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return set_error(BGTQ_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
+    if (max_len > c->capacity) max_len = c->capacity;
+    SplitPlan sp = decode_split(*p, batch, max_len);
+    size_t need = decode_workspace_bytes(*p, batch, sp);
+    if (ws_bytes < need) return set_error(BGTQ_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+    cudaError_t e = launch_decode(*p, (cudaStream_t)stream, q, *c, seq_lens, batch, sp, out, out_dtype, scale, ws, status,
+                                  k_new, v_new, pos_new);
+    if (e != cudaSuccess) return set_error(BGTQ_ERR_CUDA, "decode_step launch: %s", cudaGetErrorString(e));
+    return BGTQ_OK;
+}
+
 int bgtq_dequant_debug(const bgtq_plan* p, void* stream, const bgtq_cache* c, int batch, int b, int head, int64_t t0,
                        int64_t t1, float* k_out, float* v_out, int codec_domain) {
     int rc = check_plan(p);

@@ -112,8 +112,14 @@ struct SplitPlan {
 };
 SplitPlan decode_split(const bgtq_plan& p, int batch, int64_t max_len);
 size_t decode_workspace_bytes(const bgtq_plan& p, int batch, const SplitPlan& sp);
+// bytes of per-(sequence, KV head, query head) arrival counters at the front
+// of the decode workspace (they must be zero before a call; calls leave them zero)
+size_t decode_counter_bytes(const bgtq_plan& p, int batch);
+// k_new/v_new/pos_new non-null: the fused step (append one token per
+// sequence, then attend); null: attention only.
 cudaError_t launch_decode(const bgtq_plan& p, cudaStream_t s, const void* q, const bgtq_cache& c,
                           const int32_t* seq_lens, int batch, const SplitPlan& sp, void* out, int out_dtype,
-                          float scale, void* ws, int32_t* status);
+                          float scale, void* ws, int32_t* status, const void* k_new = nullptr,
+                          const void* v_new = nullptr, const int32_t* pos_new = nullptr);
 
 }  // namespace bgtq

@@ -4,20 +4,21 @@
 // Method: "RoPE-Aware Bit Allocation for KV-Cache Quantization" — review §1
 // Key Terms (TQ-MSE rotates then quantises; the packed cache stores
 // compressed K/V) and English abstract (per-block integer widths for keys,
-// uniform TQ-MSE for values).  One warp encodes one token: lane L holds codec
-// coordinates 4L..4L+3.  Every float operation is a single correctly rounded
+// uniform TQ-MSE for values).  A warp encodes tokens two at a time: lane L
+// holds codec coordinates 4L..4L+3 of each.  Every float operation is a single correctly rounded
 // IEEE operation in a fixed order (this file is built with --fmad=false and
 // uses explicit _rn intrinsics), so codes, norms and decoded values are
 // bit-identical to any implementation that follows the same steps.
 #include <cuda_fp16.h>
 
 #include "bgtq_internal.h"
+#include "encode.cuh"
 
 namespace bgtq {
 namespace {
 
 constexpr int kWarpsQ = 4;
-constexpr int kPairsPerWarp = 8;  // token pairs each warp of quantize_append encodes
+constexpr int kPairsPerBlock = 16;  // token pairs each quantize_append block encodes
 
 struct QParams {
     const __half* k;
@@ -36,189 +37,153 @@ struct QParams {
     int32_t* status;
 };
 
-// Randomized Hadamard on the warp's 128 slots: stages h = 1, 2, 4, ..., 64,
-// pair (j, j+h) inside a piece larger than h becomes (a + b, a - b).
-__device__ __forceinline__ void warp_butterflies(float (&x)[4], const int (&plog2)[4], int lane) {
-#pragma unroll
-    for (int h = 1; h <= 2; h <<= 1) {
-        float y[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int partner = i ^ h;
-            const bool active = (1 << plog2[i]) > h;
-            y[i] = !active ? x[i] : ((i & h) ? __fsub_rn(x[partner], x[i]) : __fadd_rn(x[i], x[partner]));
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) x[i] = y[i];
-    }
-#pragma unroll
-    for (int h = 4; h < 128; h <<= 1) {
-        const int lm = h >> 2;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float other = __shfl_xor_sync(0xffffffffu, x[i], lm);
-            const int j = 4 * lane + i;
-            if ((1 << plog2[i]) > h) x[i] = (j & h) ? __fsub_rn(other, x[i]) : __fadd_rn(x[i], other);
-        }
-    }
-}
-
-// Encode one token held as x[4] per lane (already whitened for keys).
-// Returns the codes of the lane's four coordinates and the norm rho.
-__device__ __forceinline__ float warp_encode(float (&x)[4], const float (&sgn)[4], const int (&plog2)[4],
-                                             const float (&inv_sqrt)[4], const int (&width)[4], int n_coded,
-                                             const float* __restrict__ thr, int lane, int (&code)[4]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) x[i] = __fmul_rn(x[i], sgn[i]);
-    warp_butterflies(x, plog2, lane);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) x[i] = __fmul_rn(x[i], inv_sqrt[i]);
-    float part = __fadd_rn(__fadd_rn(__fmul_rn(x[0], x[0]), __fmul_rn(x[1], x[1])),
-                           __fadd_rn(__fmul_rn(x[2], x[2]), __fmul_rn(x[3], x[3])));
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, m));
-    const float rho = __fsqrt_rn(__fdiv_rn(part, (float)n_coded));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float u = rho > 0.0f ? __fdiv_rn(x[i], rho) : 0.0f;
-        const int n = 1 << width[i];
-        const float* tb = thr + 256 * width[i];
-        int pos = 0;
-#pragma unroll
-        for (int s = 128; s >= 1; s >>= 1) {
-            if (2 * s <= n) {
-                if (tb[pos + s - 1] <= u) pos += s;
-            }
-        }
-        code[i] = pos;
-    }
-    return rho;
-}
-
+// One block appends up to kPairsPerBlock token pairs of one (sequence, head).
+// Warps 0 and 1 encode keys (the even and the odd token of each pair, two
+// pairs at a time), warps 2 and 3 encode values (alternate pairs, both tokens
+// of a pair at once, since a V record holds a token pair).  Each warp loads
+// the rows of its next group before encoding the current one.  A pair that
+// is only half appended has its V record merged in place with atomic AND/OR,
+// so nothing is read back.
 __global__ void __launch_bounds__(128) quantize_append_kernel(QParams p) {
-    __shared__ __align__(16) float s_thr[(kWMax + 1) * 256];
-    __shared__ float xs[kWarpsQ][kD];
-    __shared__ uint32_t krec[kWarpsQ][32];
-    __shared__ uint32_t vrec[kWarpsQ][8 * kPairMaxW];
-    __shared__ uint32_t vmask[kWarpsQ][8 * kPairMaxW];
+    __shared__ float s_thr[kThrCompact];
+    __shared__ uint32_t rec[kWarpsQ][2][8 * kPairMaxW];  // records being assembled per warp
+    __shared__ uint32_t rmask[2][8 * kPairMaxW];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y, b = blockIdx.z;
-    // The next kernel may launch right away (programmatic dependent launch);
-    // the plan's tables are static, the inputs are read after the wait.
+    // The next kernel may launch right away (programmatic dependent launch).
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // Lloyd-Max thresholds of every width, staged once per block
-    for (int i = threadIdx.x; i < (kWMax + 1) * 256 / 4; i += kWarpsQ * 32)
-        reinterpret_cast<float4*>(s_thr)[i] = __ldg(reinterpret_cast<const float4*>(p.thr) + i);
+
+    // ---- plan-static set-up, before waiting for the previous kernel
+    stage_thresholds(s_thr, p.thr, threadIdx.x, kWarpsQ * 32);
+    const HeadTab* ht = p.heads + h;
+    const size_t unit = (size_t)b * p.H + h;
+    const bool is_k = warp < 2;
+    EncLane el;
+    enc_lane_load(el, ht, is_k, p.bv, p.v_inv_sqrt, lane);
     __syncthreads();
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // pos_start is read before the wait: no kernel of this library writes it
     const int ps = p.pos_start[b];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (ps < 0 || (int64_t)ps + p.t_new > p.cap) {
         if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_APPEND_CAPACITY);
         return;
     }
-    const HeadTab* ht = p.heads + h;
-    const int n_coded = ht->n_coded;
-    const size_t unit = (size_t)b * p.H + h;
-    const int krec_words = 4 * p.bk, vrec_words = 8 * p.bv;
+    const int64_t end = (int64_t)ps + p.t_new;
+    const int64_t P0 = (int64_t)(ps >> 1) + (int64_t)blockIdx.x * kPairsPerBlock;
 
-    // per-lane key codec metadata (codec coordinates 4*lane + i)
-    int kpl[4], kw[4], kperm[4];
-    float ksg[4], kis[4], kwh[4];
-    int vpl[4], vw[4];
-    float vsg[4], vis[4];
+    if (is_k) {
+        // ---- keys: warp w encodes tokens 2P + w of pairs P = P0 + i, i + 1
+        const int krec_words = 4 * p.bk;
+        auto load = [&](int i, __half (&xh)[2][4]) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int j = 4 * lane + i;
-        const bool coded = j < n_coded;
-        kpl[i] = coded ? ht->plog2[j] : 0;
-        kw[i] = coded ? ht->width[j] : 0;
-        kperm[i] = ht->perm[j];
-        ksg[i] = ht->sign_k[j];
-        kis[i] = ht->inv_sqrt[j];
-        kwh[i] = ht->whiten[j];
-        vpl[i] = 7;
-        vw[i] = p.bv;
-        vsg[i] = ht->sign_v[j];
-        vis[i] = p.v_inv_sqrt;
-    }
-    const int64_t P_first = (int64_t)(ps >> 1) + ((int64_t)blockIdx.x * kWarpsQ + warp) * kPairsPerWarp;
-    for (int it = 0; it < kPairsPerWarp; ++it) {
-        const int64_t P = P_first + it;  // token-pair index
-        const int64_t pos0 = 2 * P;
-        const bool has[2] = {pos0 >= ps && pos0 < (int64_t)ps + p.t_new, pos0 + 1 >= ps && pos0 + 1 < (int64_t)ps + p.t_new};
-        if (!has[0] && !has[1]) continue;
-        for (int i = lane; i < 8 * kPairMaxW; i += 32) {
-            vrec[warp][i] = 0;
-            vmask[warp][i] = 0;
+            for (int n = 0; n < 2; ++n) {
+                const int64_t pos = 2 * (P0 + i + n) + warp;
+                if (pos >= ps && pos < end) {
+                    const __half* row = p.k + (unit * p.t_new + (size_t)(pos - ps)) * kD;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) xh[n][k] = row[el.src[k]];
+                }
+            }
+        };
+        __half cur[2][4], nxt[2][4];
+        load(0, cur);
+        for (int i = 0; i < kPairsPerBlock; i += 2) {
+            if (2 * (P0 + i) + warp >= end) break;
+            if (i + 2 < kPairsPerBlock) load(i + 2, nxt);
+            bool has[2];
+            float x[2][4];
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+                const int64_t pos = 2 * (P0 + i + n) + warp;
+                has[n] = pos >= ps && pos < end;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) x[n][k] = has[n] ? __fmul_rn(__half2float(cur[n][k]), el.wh[k]) : 0.0f;
+            }
+            int code[2][4];
+            float rho[2];
+            for (int k = lane; k < 2 * 8 * kPairMaxW; k += 32) (&rec[warp][0][0])[k] = 0;
+            __syncwarp();
+            warp_encode_n<2>(x, el.sg, el.pl, el.is, el.wd, el.n_coded, s_thr, code, rho);
+#pragma unroll
+            for (int n = 0; n < 2; ++n) pack_k_fields(rec[warp][n], code[n], el, lane);
+            __syncwarp();
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+                if (!has[n]) continue;
+                const int64_t pos = 2 * (P0 + i + n) + warp;
+                uint32_t* dst = reinterpret_cast<uint32_t*>(p.kc + (unit * p.cap + pos) * (16 * p.bk));
+                if (lane < krec_words) dst[lane] = rec[warp][n][lane];
+                if (lane == 0) p.kn[unit * p.cap + pos] = rho[n];
+            }
+            __syncwarp();
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) cur[n][k] = nxt[n][k];
         }
+        return;
+    }
+
+    // ---- values: warp 2 + r encodes both tokens of pairs P0 + r, P0 + r + 2, ...
+    const int r = warp - 2;
+    const int vrec_words = 8 * p.bv;
+    uint32_t* vrec = rec[warp][0];
+    uint32_t* vmask = rmask[r];
+    auto load = [&](int i, uint2 (&xr)[2]) {
+        const int64_t pos0 = 2 * (P0 + i);
+#pragma unroll
+        for (int par = 0; par < 2; ++par) {
+            const int64_t pos = pos0 + par;
+            if (pos >= ps && pos < end)
+                xr[par] = *(reinterpret_cast<const uint2*>(p.v + (unit * p.t_new + (size_t)(pos - ps)) * kD) + lane);
+        }
+    };
+    uint2 cur[2] = {make_uint2(0, 0), make_uint2(0, 0)}, nxt[2] = {make_uint2(0, 0), make_uint2(0, 0)};
+    load(r, cur);
+    for (int i = r; i < kPairsPerBlock; i += 2) {
+        const int64_t P = P0 + i;
+        const int64_t pos0 = 2 * P;
+        if (pos0 >= end) break;
+        if (i + 2 < kPairsPerBlock) load(i + 2, nxt);
+        const bool has[2] = {pos0 >= ps, pos0 + 1 < end};
+        float x[2][4];
+#pragma unroll
+        for (int par = 0; par < 2; ++par) {
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&cur[par].x));
+            const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&cur[par].y));
+            x[par][0] = has[par] ? a.x : 0.0f;
+            x[par][1] = has[par] ? a.y : 0.0f;
+            x[par][2] = has[par] ? c.x : 0.0f;
+            x[par][3] = has[par] ? c.y : 0.0f;
+        }
+        for (int k = lane; k < 8 * kPairMaxW; k += 32) {
+            vrec[k] = 0;
+            vmask[k] = 0;
+        }
+        __syncwarp();
+        int code[2][4];
+        float rho[2];
+        warp_encode_n<2>(x, el.sg, el.pl, el.is, el.wd, kD, s_thr, code, rho);
+#pragma unroll
         for (int par = 0; par < 2; ++par) {
             if (!has[par]) continue;
-            const int64_t pos = pos0 + par;
-            const size_t tok = (size_t)(pos - ps);
-            // ---- key
-            {
-                const __half2* src = reinterpret_cast<const __half2*>(p.k + (unit * p.t_new + tok) * kD) + 2 * lane;
-                const float2 a = __half22float2(src[0]), c = __half22float2(src[1]);
-                xs[warp][4 * lane + 0] = a.x;
-                xs[warp][4 * lane + 1] = a.y;
-                xs[warp][4 * lane + 2] = c.x;
-                xs[warp][4 * lane + 3] = c.y;
-                if (lane < 32) krec[warp][lane] = 0;
-                __syncwarp();
-                float x[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) x[i] = (4 * lane + i < n_coded) ? __fmul_rn(xs[warp][kperm[i]], kwh[i]) : 0.0f;
-                int code[4];
-                const float rho = warp_encode(x, ksg, kpl, kis, kw, n_coded, s_thr, lane, code);
-#pragma unroll
-                for (int pr = 0; pr < 2; ++pr) {
-                    const int j = 4 * lane + 2 * pr;
-                    if (j + 1 < n_coded) {
-                        const int w = kw[2 * pr];
-                        const uint32_t field = (uint32_t)code[2 * pr] | ((uint32_t)code[2 * pr + 1] << w);
-                        const int bit = ht->pair_bit[j >> 1];
-                        const int wi = bit >> 5, sh = bit & 31;
-                        atomicOr(&krec[warp][wi], field << sh);
-                        if (sh + 2 * w > 32) atomicOr(&krec[warp][wi + 1], field >> (32 - sh));
-                    }
-                }
-                __syncwarp();
-                uint32_t* dst = reinterpret_cast<uint32_t*>(p.kc + (unit * p.cap + pos) * (16 * p.bk));
-                if (lane < krec_words) dst[lane] = krec[warp][lane];
-                if (lane == 0) p.kn[unit * p.cap + pos] = rho;
-                __syncwarp();
-            }
-            // ---- value
-            {
-                const __half2* src = reinterpret_cast<const __half2*>(p.v + (unit * p.t_new + tok) * kD) + 2 * lane;
-                const float2 a = __half22float2(src[0]), c = __half22float2(src[1]);
-                float x[4] = {a.x, a.y, c.x, c.y};
-                int code[4];
-                const float rho = warp_encode(x, vsg, vpl, vis, vw, kD, s_thr, lane, code);
-                const uint32_t m1 = (1u << p.bv) - 1;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int j = 4 * lane + i;
-                    const int bit = 2 * p.bv * j + par * p.bv;
-                    const int wi = bit >> 5, sh = bit & 31;
-                    atomicOr(&vrec[warp][wi], (uint32_t)code[i] << sh);
-                    atomicOr(&vmask[warp][wi], m1 << sh);
-                    if (sh + p.bv > 32) {
-                        atomicOr(&vrec[warp][wi + 1], (uint32_t)code[i] >> (32 - sh));
-                        atomicOr(&vmask[warp][wi + 1], m1 >> (32 - sh));
-                    }
-                }
-                if (lane == 0) p.vn[unit * p.cap + pos] = rho;
-            }
+            pack_v_fields(vrec, vmask, code[par], par, p.bv, lane);
+            if (lane == 0) p.vn[unit * p.cap + pos0 + par] = rho[par];
         }
         __syncwarp();
         uint32_t* vdst = reinterpret_cast<uint32_t*>(p.vc + (unit * (p.cap / 2) + P) * (32 * p.bv));
-        for (int i = lane; i < vrec_words; i += 32) {
-            uint32_t val = vrec[warp][i];
-            if (!(has[0] && has[1])) val = (vdst[i] & ~vmask[warp][i]) | val;
-            vdst[i] = val;
+        for (int k = lane; k < vrec_words; k += 32) {
+            if (has[0] && has[1]) {
+                vdst[k] = vrec[k];
+            } else {
+                // merge the appended half into the record without reading it
+                atomicAnd(vdst + k, ~vmask[k]);
+                atomicOr(vdst + k, vrec[k]);
+            }
         }
         __syncwarp();
+        cur[0] = nxt[0];
+        cur[1] = nxt[1];
     }
 }
 
@@ -350,7 +315,7 @@ cudaError_t launch_quantize_append(const bgtq_plan& pl, cudaStream_t s, const vo
     p.v_inv_sqrt = (float)(1.0 / std::sqrt((double)kD));
     p.status = status;
     const int64_t pairs = (int64_t)t_new / 2 + 1;
-    const int64_t per_block = (int64_t)kWarpsQ * kPairsPerWarp;
+    const int64_t per_block = kPairsPerBlock;
     dim3 grid((unsigned)((pairs + per_block - 1) / per_block), (unsigned)pl.H, (unsigned)batch);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;

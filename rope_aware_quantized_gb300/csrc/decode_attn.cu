@@ -34,6 +34,7 @@
 #include <mutex>
 
 #include "bgtq_internal.h"
+#include "encode.cuh"
 
 namespace bgtq {
 namespace {
@@ -51,10 +52,10 @@ constexpr float kHeadroom = 8.0f;  // log2 headroom of the softmax reference
 
 struct DecodeParams {
     const __half* q;
-    const uint8_t* kc;
-    const float* kn;
-    const uint8_t* vc;
-    const float* vn;
+    uint8_t* kc;  // written only by the fused step (the new token)
+    float* kn;
+    uint8_t* vc;
+    float* vn;
     int64_t cap;
     const int32_t* seq_lens;
     void* out;
@@ -69,6 +70,12 @@ struct DecodeParams {
     float v_inv_sqrt;
     int H, G, n_split, tps;
     int32_t* status;
+    // fused step: one new token per (sequence, KV head) quantize-appended at
+    // pos_new[b] before attention (k_new == nullptr: attention only)
+    const __half* k_new;
+    const __half* v_new;
+    const int32_t* pos_new;
+    const float* thr;
 };
 
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -228,7 +235,8 @@ __device__ __forceinline__ void rotate_warp(float (&x)[4], const int (&plog2)[4]
     }
 }
 
-// Global-memory operands of one 16-token tile for one lane.
+// Global-memory operands of one 16-token tile for one lane.  Loaded through
+// L2 (ld.global.cg): the fused step writes the new token in the same kernel.
 template <int BK, int BV>
 struct TileRegs {
     uint32_t kw[2][BK];  // K record slice words of tokens T0 + g and T0 + 8 + g
@@ -243,12 +251,12 @@ struct TileRegs {
             const int tok = min(T0 + 8 * nt + g, seq - 1);
             const uint32_t* src = reinterpret_cast<const uint32_t*>(kc + (size_t)tok * (16 * BK)) + BK * t;
 #pragma unroll
-            for (int i = 0; i < BK; ++i) kw[nt][i] = __ldg(src + i);
+            for (int i = 0; i < BK; ++i) kw[nt][i] = __ldcg(src + i);
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int tk = min(T0 + 8 * nt + 2 * t + e, seq - 1);
-                rk[nt][e] = __ldg(kn + tk);
-                rv[nt][e] = __ldg(vn + tk);
+                rk[nt][e] = __ldcg(kn + tk);
+                rv[nt][e] = __ldcg(vn + tk);
             }
         }
 #pragma unroll
@@ -256,27 +264,79 @@ struct TileRegs {
             const int pr = min((T0 >> 1) + 4 * r + t, (seq - 1) >> 1);
             const uint32_t* src = reinterpret_cast<const uint32_t*>(vc + (size_t)pr * (32 * BV)) + BV * g;
 #pragma unroll
-            for (int i = 0; i < BV; ++i) vw[r][i] = __ldg(src + i);
+            for (int i = 0; i < BV; ++i) vw[r][i] = __ldcg(src + i);
         }
     }
 };
+
+// Fused step: quantize-append the new token of (sequence, KV head) `unit` at
+// `pos`, warp 0 the key and warp 1 the value (the same encoder steps as the
+// quantize-append kernel, so the codes are identical).  The value record of
+// the token pair is merged in place with atomic AND/OR.
+template <int BK, int BV>
+__device__ __forceinline__ void append_new_token(const DecodeParams& p, const EncLane& el, size_t unit, int pos,
+                                                 const float* s_thr, uint32_t (*s_enc)[8 * kPairMaxW], int warp,
+                                                 int lane) {
+    if (warp == 0) {
+        const __half* row = p.k_new + unit * kD;
+        float x[1][4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) x[0][k] = __fmul_rn(__half2float(row[el.src[k]]), el.wh[k]);
+        for (int k = lane; k < 8 * kPairMaxW; k += 32) s_enc[0][k] = 0;
+        __syncwarp();
+        int code[1][4];
+        float rho[1];
+        warp_encode_n<1>(x, el.sg, el.pl, el.is, el.wd, el.n_coded, s_thr, code, rho);
+        pack_k_fields(s_enc[0], code[0], el, lane);
+        __syncwarp();
+        uint32_t* dst = reinterpret_cast<uint32_t*>(p.kc + (unit * p.cap + pos) * (16 * BK));
+        if (lane < 4 * BK) dst[lane] = s_enc[0][lane];
+        if (lane == 0) p.kn[unit * p.cap + pos] = rho[0];
+    } else if (warp == 1) {
+        const uint2 raw = *(reinterpret_cast<const uint2*>(p.v_new + unit * kD) + lane);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+        const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+        float x[1][4] = {{a.x, a.y, c.x, c.y}};
+        for (int k = lane; k < 8 * kPairMaxW; k += 32) {
+            s_enc[1][k] = 0;
+            s_enc[2][k] = 0;
+        }
+        __syncwarp();
+        int code[1][4];
+        float rho[1];
+        warp_encode_n<1>(x, el.sg, el.pl, el.is, el.wd, kD, s_thr, code, rho);
+        pack_v_fields(s_enc[1], s_enc[2], code[0], pos & 1, BV, lane);
+        __syncwarp();
+        uint32_t* vdst = reinterpret_cast<uint32_t*>(p.vc + (unit * (p.cap / 2) + (pos >> 1)) * (32 * BV));
+        for (int k = lane; k < 8 * BV; k += 32) {
+            atomicAnd(vdst + k, ~s_enc[2][k]);
+            atomicOr(vdst + k, s_enc[1][k]);
+        }
+        if (lane == 0) p.vn[unit * p.cap + pos] = rho[0];
+    }
+}
+
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 template <int BK, int BV, bool kAnyWide>
 __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) {
     __shared__ __align__(16) uint32_t s_tab[kImgWords];
     const uint16_t* s_single = reinterpret_cast<const uint16_t*>(s_tab);
     __shared__ __align__(16) float s_q[8][kD];
-    __shared__ float s_m[kWarps][8], s_l[kWarps][8];
-    __shared__ float s_qmax[kWarps][8], s_qscale[8], s_qunscale[8];
+    __shared__ float s_qunscale[8];
     __shared__ int s_last;
-    // after the main loop the table region holds the warp partials and the
-    // CTA partial that the cluster reads
-    float (*s_o)[8][kD] = reinterpret_cast<float (*)[8][kD]>(s_tab + kImgPriv);
-    float (*s_part)[kPartStride] = reinterpret_cast<float (*)[kPartStride]>(s_tab);
+    __shared__ float s_thr[kThrCompact];                 // fused step: encoder thresholds
+    __shared__ uint32_t s_enc[3][8 * kPairMaxW];          // fused step: records being assembled
+    // after the main loop the table region holds the per-warp partials of
+    // the 8 query heads (m, l, acc[128]) that the cluster reads
+    float (*s_wp)[8][kPartStride] = reinterpret_cast<float (*)[8][kPartStride]>(s_tab);
+    static_assert(kWarps * 8 * kPartStride <= kImgWords, "partials fit in the table region");
 
     // The next kernel may launch right away; everything this kernel reads
-    // that an earlier kernel may still be writing (q, the cache) is read only
-    // after pdl_wait().  seq_lens is never written by this library's kernels.
+    // that an earlier kernel may still be writing (q, the cache, the
+    // workspace) is read only after pdl_wait().  seq_lens is never written by
+    // this library's kernels.  Every CTA passes pdl_wait() before it exits.
     pdl_trigger();
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
@@ -284,15 +344,34 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     const size_t unit = (size_t)b * p.H + h;
     int seq = p.seq_lens[b];
     if (seq < 0 || (int64_t)seq > p.cap) {
+        pdl_wait();
         if (tid == 0 && split == 0 && h == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_SEQLEN_CAPACITY);
         seq = seq < 0 ? 0 : (int)p.cap;
     }
     const int n_active = (seq + p.tps - 1) / p.tps;
     const int n_clusters = (n_active + kCluster - 1) / kCluster;
     const int cid = split / kCluster;
+    // fused step: the CTA whose token range holds the new position appends
+    // the new token before attending (split 0 when the position is not
+    // attended).  pos_new is read before the wait, like seq_lens.
+    bool owner = false, pos_bad = false;
+    int pos = 0;
+    EncLane el;
+    if (p.k_new) {
+        pos = p.pos_new[b];
+        pos_bad = pos < 0 || (int64_t)pos + 1 > p.cap;
+        owner = !pos_bad && split == (pos < seq ? pos / p.tps : 0);
+        if (owner) {
+            stage_thresholds(s_thr, p.thr, tid, kWarps * 32);
+            if (warp < 2) enc_lane_load(el, p.heads + h, warp == 0, BV, p.v_inv_sqrt, lane);
+            __syncthreads();
+        }
+    }
     if (seq == 0) {
+        pdl_wait();
+        if (pos_bad && split == 0 && h == 0 && tid == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_APPEND_CAPACITY);
+        if (owner) append_new_token<BK, BV>(p, el, unit, pos, s_thr, s_enc, warp, lane);
         if (split == 0) {
-            pdl_wait();
             for (int i = tid; i < G * kD; i += kWarps * 32) {
                 const size_t o = ((size_t)b * p.H * G + (size_t)h * G) * kD + i;
                 if (p.out_dtype) static_cast<float*>(p.out)[o] = 0.0f;
@@ -301,7 +380,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         }
         return;  // every CTA of this (sequence, head) leaves here
     }
-    if (cid >= n_clusters) return;  // the whole cluster is past the sequence
+    if (cid >= n_clusters) {  // the whole cluster is past the sequence
+        pdl_wait();
+        return;
+    }
     cg::cluster_group cluster = cg::this_cluster();
     const int crank = (int)cluster.block_rank();
     const bool active = split < n_active;
@@ -313,6 +395,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     const float* kn = p.kn + unit * (size_t)p.cap;
     const float* vn = p.vn + unit * (size_t)p.cap;
 
+    // ---- plan-static set-up, before waiting for the previous kernel: L2
+    // prefetch of the token range, the table image, the per-lane recipes
+    const int n_coded = ht->n_coded;
+    int q_pl[4], q_src[4];
+    float q_f[4], q_sc[4];
+    uint32_t ksh[16], kmask[16], kbase[16];
+    uint32_t slot_pairs[4];
     if (active) {
         prefetch_range(reinterpret_cast<const char*>(kc + (size_t)t_begin * (16 * BK)),
                        (size_t)(t_end - t_begin) * (16 * BK), tid);
@@ -329,39 +418,60 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         for (int i = 0; i < kPer; ++i) img[i] = __ldg(src + tid + i * kWarps * 32);
 #pragma unroll
         for (int i = 0; i < kPer; ++i) reinterpret_cast<uint4*>(s_tab)[tid + i * kWarps * 32] = img[i];
-    }
-
-    pdl_wait();  // q and the cache may have been written by the previous kernel
-    if (active) {
-    // ---- query heads into the key codec domain: warp w rotates heads 2w and
-    // 2w+1, lane L holding codec coordinates 4L..4L+3 (de-whitening, signs,
-    // blockwise Hadamard by shuffles, 1/sqrt(piece), softmax scale, log2 e)
-    const int n_coded = ht->n_coded;
-    {
-        int pl[4], src[4];
-        float f[4], sc[4];
+        // query rotation recipe of the lane's codec coordinates 4L..4L+3
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int j = 4 * lane + i;
             const bool coded = j < n_coded;
-            pl[i] = coded ? ht->plog2[j] : 0;
-            src[i] = ht->perm[j];
-            f[i] = coded ? ht->sign_k[j] * ht->dewhiten[j] : 0.0f;
-            sc[i] = coded ? ht->inv_sqrt[j] * p.scale_log2 : 0.0f;
+            q_pl[i] = coded ? ht->plog2[j] : 0;
+            q_src[i] = ht->perm[j];
+            q_f[i] = coded ? ht->sign_k[j] * ht->dewhiten[j] : 0.0f;
+            q_sc[i] = coded ? ht->inv_sqrt[j] * p.scale_log2 : 0.0f;
         }
+        // K slot lookup recipes and codec pairs of the lane's slots
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+            const uint4 m = __ldg(reinterpret_cast<const uint4*>(&ht->kmeta[t][s]));
+            ksh[s] = m.x;
+            kmask[s] = m.y;
+            kbase[s] = m.z + (m.w & 255u) * lane + (m.w >> 8) * g;
+        }
+        const uint4 sp = __ldg(reinterpret_cast<const uint4*>(&ht->slot_pair[t][0]));
+        slot_pairs[0] = sp.x;
+        slot_pairs[1] = sp.y;
+        slot_pairs[2] = sp.z;
+        slot_pairs[3] = sp.w;
+    }
+
+    pdl_wait();  // q, the cache and the workspace may belong to the previous kernel
+    if (pos_bad && split == 0 && h == 0 && tid == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_APPEND_CAPACITY);
+    if (owner) append_new_token<BK, BV>(p, el, unit, pos, s_thr, s_enc, warp, lane);
+    float m_ref = -INFINITY, l_run = 0.0f;  // softmax reference (running max + headroom), sum
+    float acc[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+    if (active) {
+    // ---- query heads into the key codec domain: warp w rotates heads 2w and
+    // 2w+1, lane L holding codec coordinates 4L..4L+3 (de-whitening, signs,
+    // blockwise Hadamard by shuffles, 1/sqrt(piece), softmax scale, log2 e)
+    {
         const __half* qb = p.q + ((size_t)b * p.H * G + (size_t)h * G) * kD;
+        float x[2][4];
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int gg = 2 * warp + k;
-            float x[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) x[i] = gg < G ? __half2float(qb[(size_t)gg * kD + src[i]]) * f[i] : 0.0f;
-            rotate_warp(x, pl, lane);
+            for (int i = 0; i < 4; ++i) x[k][i] = gg < G ? __half2float(qb[(size_t)gg * kD + q_src[i]]) * q_f[i] : 0.0f;
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int gg = 2 * warp + k;
+            rotate_warp(x[k], q_pl, lane);
             float a = 0.0f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                x[i] *= sc[i];
-                a = fmaxf(a, fabsf(x[i]));
+                x[k][i] *= q_sc[i];
+                a = fmaxf(a, fabsf(x[k][i]));
             }
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
@@ -373,42 +483,28 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             e = max(-100, min(100, e));
             const float qs = ldexpf(1.0f, 14 - e);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) s_q[gg][4 * lane + i] = x[i] * qs;
+            for (int i = 0; i < 4; ++i) s_q[gg][4 * lane + i] = x[k][i] * qs;
             if (lane == 0) s_qunscale[gg] = ldexpf(1.0f, e - 14);
         }
-        __syncthreads();
+        __syncthreads();  // s_q, s_qunscale, the table image (and a fused step's new token) are complete
     }
     const float q_unscale = s_qunscale[g];
     uint32_t qa[8][4];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-        const int m0 = ht->slot_pair[t][2 * c], m1 = ht->slot_pair[t][2 * c + 1];
+        const int m0 = (slot_pairs[c >> 1] >> (16 * (c & 1))) & 255;
+        const int m1 = (slot_pairs[c >> 1] >> (16 * (c & 1) + 8)) & 255;
         const float x0 = s_q[g][(2 * m0) & (kD - 1)], x1 = s_q[g][(2 * m0 + 1) & (kD - 1)];
         const float y0 = s_q[g][(2 * m1) & (kD - 1)], y1 = s_q[g][(2 * m1 + 1) & (kD - 1)];
         const bool v0 = 2 * m0 < n_coded, v1 = 2 * m1 < n_coded;
         split_hilo(v0 ? x0 : 0.0f, v0 ? x1 : 0.0f, qa[c][0], qa[c][1]);
         split_hilo(v1 ? y0 : 0.0f, v1 ? y1 : 0.0f, qa[c][2], qa[c][3]);
     }
-    // ---- per-lane K slot lookup recipes (precomputed in the plan)
     const uint32_t wide = ht->wide_mask;
-    uint32_t ksh[16], kmask[16], kbase[16];
-#pragma unroll
-    for (int s = 0; s < 16; ++s) {
-        const uint4 m = __ldg(reinterpret_cast<const uint4*>(&ht->kmeta[t][s]));
-        ksh[s] = m.x;
-        kmask[s] = m.y;
-        kbase[s] = m.z + (m.w & 255u) * lane + (m.w >> 8) * g;
-    }
     const uint32_t vbase = BV <= kPrivMaxW ? kPrivByte + 4u * lane + ((1u << (2 * BV)) << 7) : (1u << (2 * BV)) << 2;
-    __syncthreads();
 
     // ---- main loop: 16-token tiles, operands of the next tile loaded while
     // the current one is decoded (ping-pong register buffers)
-    float m_ref = -INFINITY, l_run = 0.0f;  // softmax reference (running max + headroom), sum
-    float acc[16][4];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
-
     auto process = [&](const TileRegs<BK, BV>& tr, int T0) {
         float sacc[2][4];
 #pragma unroll
@@ -491,96 +587,77 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         if (T0 + 2 * kStep < t_end) ta.load(kc, vc, kn, vn, T0 + 2 * kStep, seq, g, t);
         process(tb, T0 + kStep);
     }
-    const float m_run = m_ref;
-    __syncthreads();  // the table region is reused below
+    }  // active
 
-    // ---- CTA merge of the warps -> s_part
+    // ---- the warp's partial (m, l, acc) of its 8 query heads -> s_wp[warp]
+    __syncthreads();  // every warp is done with the tables
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
     if (t == 0) {
-        s_m[warp][g] = m_run;
-        s_l[warp][g] = l_run;
+        s_wp[warp][g][0] = m_ref;
+        s_wp[warp][g][1] = l_run;
     }
 #pragma unroll
     for (int nd = 0; nd < 16; ++nd) {
-        s_o[warp][g][16 * (2 * t) + nd] = acc[nd][0] + acc[nd][2];
-        s_o[warp][g][16 * (2 * t + 1) + nd] = acc[nd][1] + acc[nd][3];
-    }
-    __syncthreads();
-    for (int gg = 0; gg < G; ++gg) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_m[w][gg]);
-        float L = 0.0f, O = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const float f = s_m[w][gg] == -INFINITY ? 0.0f : exp2f(s_m[w][gg] - M);
-            L += s_l[w][gg] * f;
-            O += s_o[w][gg][tid] * f;
-        }
-        s_part[gg][2 + tid] = O;
-        if (tid == 0) {
-            s_part[gg][0] = M;
-            s_part[gg][1] = L;
-        }
-    }
-    } else {
-        for (int gg = 0; gg < G; ++gg) {
-            s_part[gg][2 + tid] = 0.0f;
-            if (tid == 0) {
-                s_part[gg][0] = -INFINITY;
-                s_part[gg][1] = 0.0f;
-            }
-        }
+        s_wp[warp][g][2 + 16 * (2 * t) + nd] = acc[nd][0] + acc[nd][2];
+        s_wp[warp][g][2 + 16 * (2 * t + 1) + nd] = acc[nd][1] + acc[nd][3];
     }
 
-    // ---- cluster merge: CTA rank r reduces query head r over the 8 CTAs
+    // ---- cluster merge: CTA rank r reduces query head r over the 32 warp
+    // partials of the cluster (8 CTAs x 4 warps), read through distributed
+    // shared memory; lane i of every warp handles partial i's (m, l)
     cluster.sync();
     const size_t max_clusters = (size_t)p.n_split / kCluster;
     float* cpart_base = p.part + unit * max_clusters * (size_t)G * kPartStride;
-    if (crank < G) {
-        float mc[kCluster];
-        float M = -INFINITY;
+    const int r = crank;
+    float Mc = -INFINITY, Lc = 0.0f, Oc = 0.0f;
+    if (r < G) {
+        const float* src = cluster.map_shared_rank(&s_wp[lane & 3][r][0], lane >> 2);
+        const float mi = src[0], li = src[1];
+        float M = mi;
 #pragma unroll
-        for (int c = 0; c < kCluster; ++c) {
-            const float* rp = cluster.map_shared_rank(&s_part[crank][0], c);
-            mc[c] = rp[0];
-            M = fmaxf(M, mc[c]);
-        }
-        float L = 0.0f, O = 0.0f;
+        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float fi = mi == -INFINITY ? 0.0f : exp2f(mi - M);
+        float L = li * fi;
 #pragma unroll
-        for (int c = 0; c < kCluster; ++c) {
-            const float* rp = cluster.map_shared_rank(&s_part[crank][0], c);
-            const float f = mc[c] == -INFINITY ? 0.0f : exp2f(mc[c] - M);
-            L += rp[1] * f;
-            O += rp[2 + tid] * f;
+        for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        const float* base[kCluster];
+#pragma unroll
+        for (int c = 0; c < kCluster; ++c) base[c] = cluster.map_shared_rank(&s_wp[0][r][2 + tid], c);
+        float O = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float f = __shfl_sync(0xffffffffu, fi, i);
+            O += f * base[i >> 2][(i & 3) * 8 * kPartStride];
         }
-        float* dst = cpart_base + ((size_t)cid * G + crank) * kPartStride;
-        dst[2 + tid] = O;
+        Mc = M;
+        Lc = L;
+        Oc = O;
+    }
+    cluster_arrive();  // this CTA has finished reading the other CTAs' partials
+    int last = 0;
+    if (r < G) {
+        float* dst = cpart_base + ((size_t)cid * G + r) * kPartStride;
+        dst[2 + tid] = Oc;
         if (tid == 0) {
-            dst[0] = M;
-            dst[1] = L;
+            dst[0] = Mc;
+            dst[1] = Lc;
         }
         __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+            const unsigned prev = atomicAdd(p.count + unit * G + r, 1u);
+            s_last = (prev == (unsigned)(n_clusters - 1)) ? 1 : 0;
+        }
+        __syncthreads();
+        last = s_last;
     }
-    cluster.sync();
-    if (crank == 0 && tid == 0) {
-        const unsigned prev = atomicAdd(p.count + unit, 1u);
-        const int last = (prev == (unsigned)(n_clusters - 1)) ? 1 : 0;
-#pragma unroll
-        for (int c = 0; c < kCluster; ++c) *cluster.map_shared_rank(&s_last, c) = last;
-    }
-    cluster.sync();
-    if (!s_last) return;
-    __threadfence();
-
-    // ---- last cluster: CTA r merges the cluster partials of query head r
-    if (crank >= G) return;
-    {
-        const int gg = crank;
-        float* s_ml = s_q[1];  // (m, l) of up to 64 cluster partials
+    if (last) {
+        // ---- last cluster partial of query head r: merge all of them
+        __threadfence();
+        float* s_ml = s_q[0];  // (m, l) of up to 64 cluster partials (s_q is no longer read)
         for (int c = tid; c < n_clusters; c += kWarps * 32) {
-            const float* src = cpart_base + ((size_t)c * G + gg) * kPartStride;
+            const float* src = cpart_base + ((size_t)c * G + r) * kPartStride;
             s_ml[2 * c] = __ldcg(src);
             s_ml[2 * c + 1] = __ldcg(src + 1);
         }
@@ -593,7 +670,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             const float mcv = s_ml[2 * c];
             const float f = mcv == -INFINITY ? 0.0f : exp2f(mcv - M);
             L += s_ml[2 * c + 1] * f;
-            O += __ldcg(cpart_base + ((size_t)c * G + gg) * kPartStride + 2 + tid) * f;
+            O += __ldcg(cpart_base + ((size_t)c * G + r) * kPartStride + 2 + tid) * f;
         }
         // inverse value rotation (Hadamard-128, 1/sqrt(128), signs): thread
         // tid holds dim tid; stages below 32 by shuffles, 32 and 64 via smem
@@ -603,20 +680,22 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             const float o = __shfl_xor_sync(0xffffffffu, v, hh);
             v = (tid & hh) ? o - v : v + o;
         }
+        float* s_x = s_q[1];
 #pragma unroll
         for (int hh = 32; hh < kD; hh <<= 1) {
-            s_q[0][tid] = v;
+            s_x[tid] = v;
             __syncthreads();
-            const float o = s_q[0][tid ^ hh];
+            const float o = s_x[tid ^ hh];
             __syncthreads();
             v = (tid & hh) ? o - v : v + o;
         }
         const float val = v * p.v_inv_sqrt * ht->sign_v[tid];
-        const size_t o = ((size_t)b * p.H * G + (size_t)h * G + gg) * kD + tid;
+        const size_t o = ((size_t)b * p.H * G + (size_t)h * G + r) * kD + tid;
         if (p.out_dtype) static_cast<float*>(p.out)[o] = val;
         else static_cast<__half*>(p.out)[o] = __float2half_rn(val);
+        if (tid == 0) p.count[unit * G + r] = 0;
     }
-    if (crank == 0 && tid == 0) p.count[unit] = 0;
+    cluster_wait();  // no CTA leaves while another may still read its partials
 }
 
 template <int BK, int BV, bool kAnyWide>
@@ -703,6 +782,10 @@ SplitPlan decode_split(const bgtq_plan& p, int batch, int64_t max_len) {
     const int64_t len = std::max<int64_t>(max_len, 1);
     int64_t slots = (p.bk >= 1 && p.bk <= 3 && p.bv >= 1 && p.bv <= 4) ? resident_ctas_for(p.bk, p.bv) : 0;
     if (slots <= 0) slots = 2 * (int64_t)std::max(1, p.num_sms);
+    // Leave one cluster's room for a kernel that programmatic dependent
+    // launch starts early next to this one, so that every cluster of this
+    // grid can be resident at once.
+    if (slots > 2 * kCluster) slots -= kCluster;
     int64_t ns = slots / units;
     if (ns >= kCluster) ns = ns / kCluster * kCluster;
     ns = std::min<int64_t>(ns, (len + 63) / 64);
@@ -718,27 +801,31 @@ SplitPlan decode_split(const bgtq_plan& p, int batch, int64_t max_len) {
     return sp;
 }
 
+size_t decode_counter_bytes(const bgtq_plan& p, int batch) {
+    return (((size_t)batch * p.H * p.G * sizeof(uint32_t)) + 255) / 256 * 256;
+}
+
 size_t decode_workspace_bytes(const bgtq_plan& p, int batch, const SplitPlan& sp) {
     const size_t units = (size_t)batch * p.H;
-    const size_t counters = ((units * sizeof(uint32_t)) + 255) / 256 * 256;
+    const size_t counters = decode_counter_bytes(p, batch);
     return counters + units * (size_t)(sp.n_split / kCluster) * p.G * kPartStride * sizeof(float);
 }
 
 cudaError_t launch_decode(const bgtq_plan& pl, cudaStream_t s, const void* q, const bgtq_cache& c,
                           const int32_t* seq_lens, int batch, const SplitPlan& sp, void* out, int out_dtype,
-                          float scale, void* ws, int32_t* status) {
+                          float scale, void* ws, int32_t* status, const void* k_new, const void* v_new,
+                          const int32_t* pos_new) {
     DecodeParams p;
     p.q = static_cast<const __half*>(q);
-    p.kc = static_cast<const uint8_t*>(c.k_codes);
+    p.kc = static_cast<uint8_t*>(c.k_codes);
     p.kn = c.k_norm;
-    p.vc = static_cast<const uint8_t*>(c.v_codes);
+    p.vc = static_cast<uint8_t*>(c.v_codes);
     p.vn = c.v_norm;
     p.cap = c.capacity;
     p.seq_lens = seq_lens;
     p.out = out;
     p.out_dtype = out_dtype;
-    const size_t units = (size_t)batch * pl.H;
-    const size_t counters = ((units * sizeof(uint32_t)) + 255) / 256 * 256;
+    const size_t counters = decode_counter_bytes(pl, batch);
     p.count = static_cast<uint32_t*>(ws);
     p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + counters);
     p.heads = pl.dev.heads;
@@ -752,6 +839,10 @@ cudaError_t launch_decode(const bgtq_plan& pl, cudaStream_t s, const void* q, co
     p.n_split = sp.n_split;
     p.tps = sp.tokens_per_split;
     p.status = status;
+    p.k_new = static_cast<const __half*>(k_new);
+    p.v_new = static_cast<const __half*>(v_new);
+    p.pos_new = pos_new;
+    p.thr = pl.dev.thr;
     dim3 grid((unsigned)sp.n_split, (unsigned)pl.H, (unsigned)batch);
     // the fast instance checks only slots 0 and 8 (each lane's two widest
     // pairs) for codes wider than the pair tables

@@ -83,9 +83,8 @@ extern "C" int bgtq_decode_attn_noalloc(const bgtq_plan* p, void* stream, const 
     void* scratch = nullptr;
     int rc = scratch_address(&scratch);
     if (rc) return rc;
-    // the per-(sequence, head) arrival counters at the front must start at zero
-    const size_t units = (size_t)batch * p->H;
-    const size_t counter_bytes = ((units * sizeof(uint32_t)) + 255) / 256 * 256;
+    // the arrival counters at the front must start at zero
+    const size_t counter_bytes = decode_counter_bytes(*p, batch);
     cudaError_t e = cudaMemsetAsync(scratch, 0, counter_bytes, (cudaStream_t)stream);
     if (e != cudaSuccess) return set_error(BGTQ_ERR_CUDA, "clearing scratch counters: %s", cudaGetErrorString(e));
     e = launch_decode(*p, (cudaStream_t)stream, q, *c, seq_lens, batch, sp, out, out_dtype, scale, scratch, status);
