@@ -69,7 +69,9 @@ extern "C" {
 typedef struct bgtq_plan bgtq_plan;
 
 /* One layer's packed cache.  Passed by pointer; the struct itself is read on
- * the host only. */
+ * the host only.  k_codes and v_codes must be 16-byte aligned (the kernels
+ * copy whole records with 16-byte asynchronous copies), the norms 4-byte
+ * aligned; INVALID_ARG otherwise. */
 typedef struct {
     void* k_codes;    /* device, [B][H][capacity][16*bK] bytes */
     float* k_norm;    /* device, [B][H][capacity] */

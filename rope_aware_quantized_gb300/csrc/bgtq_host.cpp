@@ -499,6 +499,10 @@ static int check_cache(const bgtq_plan* p, const bgtq_cache* c) {
     if (!c || !c->k_codes || !c->k_norm || !c->v_codes || !c->v_norm)
         return set_error(BGTQ_ERR_INVALID_ARG, "cache descriptor or one of its buffers is NULL");
     if (c->capacity <= 0 || (c->capacity & 1)) return set_error(BGTQ_ERR_INVALID_ARG, "capacity must be even and > 0");
+    if ((reinterpret_cast<uintptr_t>(c->k_codes) & 15) || (reinterpret_cast<uintptr_t>(c->v_codes) & 15))
+        return set_error(BGTQ_ERR_INVALID_ARG, "k_codes and v_codes must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(c->k_norm) & 3) || (reinterpret_cast<uintptr_t>(c->v_norm) & 3))
+        return set_error(BGTQ_ERR_INVALID_ARG, "k_norm and v_norm must be 4-byte aligned");
     (void)p;
     return BGTQ_OK;
 }

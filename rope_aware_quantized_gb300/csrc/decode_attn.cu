@@ -235,8 +235,69 @@ __device__ __forceinline__ void rotate_warp(float (&x)[4], const int (&plog2)[4]
     }
 }
 
-// Global-memory operands of one 16-token tile for one lane.  Loaded through
-// L2 (ld.global.cg): the fused step writes the new token in the same kernel.
+// Staging of 16-token tiles in shared memory: every warp keeps kStages
+// tiles in flight with cp.async (enough bytes in flight per SM to cover the
+// HBM latency), then reads its operands from the staged copy.  One staged
+// tile: 16 K records, 8 V pair records, 16 key norms, 16 value norms.
+constexpr int kStages = 4;
+
+template <int BK, int BV>
+struct StageLayout {
+    static constexpr int kK = 16 * 16 * BK;
+    static constexpr int kV = 8 * 32 * BV;
+    static constexpr int kN = kK + kV;  // key norms, then value norms
+    static constexpr int kBytes = kN + 2 * 16 * 4;
+    static_assert(kK % 16 == 0 && kV % 16 == 0, "16-byte copies");
+};
+
+// Dynamic shared memory of decode_kernel<BK, BV>: the table image, the
+// rotated queries, then kStages staged tiles per warp.
+constexpr int kSmemTab = 0;
+constexpr int kSmemQ = kImgWords * 4;
+constexpr int kSmemStage = kSmemQ + 8 * kD * 4;
+template <int BK, int BV>
+constexpr int decode_smem_bytes() {
+    return kSmemStage + kWarps * kStages * StageLayout<BK, BV>::kBytes;
+}
+
+// 16-byte (or, for the norms, 4-byte) asynchronous copy global -> shared;
+// `valid` false copies nothing and zero-fills.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// The warp copies tile [T0, T0 + 16) into the stage at shared address `st`;
+// tokens at or beyond `seq` are zero-filled (never read from global).
+template <int BK, int BV>
+__device__ __forceinline__ void stage_tile(uint32_t st, const uint8_t* kc, const uint8_t* vc, const float* kn,
+                                           const float* vn, int T0, int seq, int lane) {
+    using SL = StageLayout<BK, BV>;
+    const uint8_t* ksrc = kc + (size_t)T0 * (16 * BK);
+#pragma unroll
+    for (int c = lane; c < 16 * BK; c += 32) {
+        const bool ok = T0 + c / BK < seq;
+        cp_async16(st + 16 * c, ok ? ksrc + 16 * c : kc, ok);
+    }
+    const uint8_t* vsrc = vc + (size_t)(T0 >> 1) * (32 * BV);
+#pragma unroll
+    for (int c = lane; c < 16 * BV; c += 32) {
+        const bool ok = T0 + 2 * (c / (2 * BV)) < seq;
+        cp_async16(st + SL::kK + 16 * c, ok ? vsrc + 16 * c : vc, ok);
+    }
+    const int tk = T0 + (lane & 15);
+    const bool ok = tk < seq;
+    const float* nsrc = lane < 16 ? kn : vn;
+    cp_async4(st + SL::kN + 4 * lane, ok ? nsrc + tk : nsrc, ok);
+}
+
+// Operands of one 16-token tile for one lane, read from its staged copy.
 template <int BK, int BV>
 struct TileRegs {
     uint32_t kw[2][BK];  // K record slice words of tokens T0 + g and T0 + 8 + g
@@ -244,27 +305,25 @@ struct TileRegs {
     float rv[2][2];      // value norms of the same tokens
     uint32_t vw[2][BV];  // lane-group words of V pair records T0/2 + t and T0/2 + 4 + t
 
-    __device__ __forceinline__ void load(const uint8_t* kc, const uint8_t* vc, const float* kn, const float* vn,
-                                         int T0, int seq, int g, int t) {
+    __device__ __forceinline__ void read(const uint8_t* st, int g, int t) {
+        using SL = StageLayout<BK, BV>;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            const int tok = min(T0 + 8 * nt + g, seq - 1);
-            const uint32_t* src = reinterpret_cast<const uint32_t*>(kc + (size_t)tok * (16 * BK)) + BK * t;
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(st + (8 * nt + g) * (16 * BK)) + BK * t;
 #pragma unroll
-            for (int i = 0; i < BK; ++i) kw[nt][i] = __ldcg(src + i);
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int tk = min(T0 + 8 * nt + 2 * t + e, seq - 1);
-                rk[nt][e] = __ldcg(kn + tk);
-                rv[nt][e] = __ldcg(vn + tk);
-            }
+            for (int i = 0; i < BK; ++i) kw[nt][i] = src[i];
+            const float2 k2 = *reinterpret_cast<const float2*>(st + SL::kN + 4 * (8 * nt + 2 * t));
+            const float2 v2 = *reinterpret_cast<const float2*>(st + SL::kN + 64 + 4 * (8 * nt + 2 * t));
+            rk[nt][0] = k2.x;
+            rk[nt][1] = k2.y;
+            rv[nt][0] = v2.x;
+            rv[nt][1] = v2.y;
         }
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-            const int pr = min((T0 >> 1) + 4 * r + t, (seq - 1) >> 1);
-            const uint32_t* src = reinterpret_cast<const uint32_t*>(vc + (size_t)pr * (32 * BV)) + BV * g;
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(st + SL::kK + (4 * r + t) * (32 * BV)) + BV * g;
 #pragma unroll
-            for (int i = 0; i < BV; ++i) vw[r][i] = __ldcg(src + i);
+            for (int i = 0; i < BV; ++i) vw[r][i] = src[i];
         }
     }
 };
@@ -321,9 +380,10 @@ __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.w
 
 template <int BK, int BV, bool kAnyWide>
 __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) {
-    __shared__ __align__(16) uint32_t s_tab[kImgWords];
+    extern __shared__ __align__(16) uint8_t dsmem[];
+    uint32_t* s_tab = reinterpret_cast<uint32_t*>(dsmem + kSmemTab);
     const uint16_t* s_single = reinterpret_cast<const uint16_t*>(s_tab);
-    __shared__ __align__(16) float s_q[8][kD];
+    float (*s_q)[kD] = reinterpret_cast<float (*)[kD]>(dsmem + kSmemQ);
     __shared__ float s_qunscale[8];
     __shared__ int s_last;
     __shared__ float s_thr[kThrCompact];                 // fused step: encoder thresholds
@@ -451,21 +511,24 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
     if (active) {
-    // ---- query heads into the key codec domain: warp w rotates heads 2w and
-    // 2w+1, lane L holding codec coordinates 4L..4L+3 (de-whitening, signs,
-    // blockwise Hadamard by shuffles, 1/sqrt(piece), softmax scale, log2 e)
+    // ---- query heads into the key codec domain: warp w rotates heads
+    // kHPW w .. kHPW w + kHPW - 1, lane L holding codec coordinates 4L..4L+3
+    // (de-whitening, signs, blockwise Hadamard by shuffles, 1/sqrt(piece),
+    // softmax scale, log2 e)
     {
+        constexpr int kHPW = (8 + kWarps - 1) / kWarps;
         const __half* qb = p.q + ((size_t)b * p.H * G + (size_t)h * G) * kD;
-        float x[2][4];
+        float x[kHPW][4];
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int gg = 2 * warp + k;
+        for (int k = 0; k < kHPW; ++k) {
+            const int gg = kHPW * warp + k;
 #pragma unroll
             for (int i = 0; i < 4; ++i) x[k][i] = gg < G ? __half2float(qb[(size_t)gg * kD + q_src[i]]) * q_f[i] : 0.0f;
         }
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int gg = 2 * warp + k;
+        for (int k = 0; k < kHPW; ++k) {
+            const int gg = kHPW * warp + k;
+            if (gg >= 8) break;
             rotate_warp(x[k], q_pl, lane);
             float a = 0.0f;
 #pragma unroll
@@ -576,17 +639,32 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         pv_tile<BV, 15>(acc, pa, tr.vw, vbase, s_tab);
     };
 
+    // warp w takes tiles T0 = t_begin + 16 w + kStep k; kStages - 1 of them are
+    // being copied while one is processed
     constexpr int kStep = kWarps * kTile;
-    TileRegs<BK, BV> ta, tb;
-    int T0 = t_begin + warp * kTile;
-    if (T0 < t_end) ta.load(kc, vc, kn, vn, T0, seq, g, t);
-    for (; T0 < t_end; T0 += 2 * kStep) {
-        if (T0 + kStep < t_end) tb.load(kc, vc, kn, vn, T0 + kStep, seq, g, t);
-        process(ta, T0);
-        if (T0 + kStep >= t_end) break;
-        if (T0 + 2 * kStep < t_end) ta.load(kc, vc, kn, vn, T0 + 2 * kStep, seq, g, t);
-        process(tb, T0 + kStep);
+    using SL = StageLayout<BK, BV>;
+    const int T0w = t_begin + warp * kTile;
+    const int n_tiles = T0w < t_end ? (t_end - T0w + kStep - 1) / kStep : 0;
+    uint8_t* st_base = dsmem + kSmemStage + warp * (kStages * SL::kBytes);
+    const uint32_t st_addr = (uint32_t)__cvta_generic_to_shared(st_base);
+#pragma unroll
+    for (int k = 0; k < kStages - 1; ++k) {
+        if (k < n_tiles) stage_tile<BK, BV>(st_addr + k * SL::kBytes, kc, vc, kn, vn, T0w + k * kStep, seq, lane);
+        cp_async_commit();
     }
+    for (int k = 0; k < n_tiles; ++k) {
+        const int kn_ = k + kStages - 1;
+        if (kn_ < n_tiles)
+            stage_tile<BK, BV>(st_addr + (kn_ % kStages) * SL::kBytes, kc, vc, kn, vn, T0w + kn_ * kStep, seq, lane);
+        cp_async_commit();
+        cp_async_wait<kStages - 1>();
+        __syncwarp();
+        TileRegs<BK, BV> tr;
+        tr.read(st_base + (k % kStages) * SL::kBytes, g, t);
+        process(tr, T0w + k * kStep);
+        __syncwarp();  // the stage is refilled next
+    }
+    cp_async_wait<0>();
     }  // active
 
     // ---- the warp's partial (m, l, acc) of its 8 query heads -> s_wp[warp]
@@ -603,45 +681,73 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         s_wp[warp][g][2 + 16 * (2 * t + 1) + nd] = acc[nd][1] + acc[nd][3];
     }
 
-    // ---- cluster merge: CTA rank r reduces query head r over the 32 warp
-    // partials of the cluster (8 CTAs x 4 warps), read through distributed
-    // shared memory; lane i of every warp handles partial i's (m, l)
+    // ---- cluster merge: CTA rank r reduces query heads r, r + kCluster, ...
+    // over the kCluster * kWarps warp partials of the cluster, read through
+    // distributed shared memory (lane i of a warp takes the (m, l) of partials
+    // i, i + 32, ...; threads tid < 128 hold one dim of acc each)
+    constexpr int kParts = kCluster * kWarps;
+    constexpr int kPerLane = (kParts + 31) / 32;
+    constexpr int kHeadsPerCta = (8 + kCluster - 1) / kCluster;
     cluster.sync();
     const size_t max_clusters = (size_t)p.n_split / kCluster;
     float* cpart_base = p.part + unit * max_clusters * (size_t)G * kPartStride;
-    const int r = crank;
-    float Mc = -INFINITY, Lc = 0.0f, Oc = 0.0f;
-    if (r < G) {
-        const float* src = cluster.map_shared_rank(&s_wp[lane & 3][r][0], lane >> 2);
-        const float mi = src[0], li = src[1];
-        float M = mi;
+    float Mc[kHeadsPerCta], Lc[kHeadsPerCta], Oc[kHeadsPerCta];
+#pragma unroll
+    for (int j = 0; j < kHeadsPerCta; ++j) {
+        const int hh = crank + j * kCluster;
+        Mc[j] = -INFINITY;
+        Lc[j] = 0.0f;
+        Oc[j] = 0.0f;
+        if (hh >= G) continue;
+        float mi[kPerLane], li[kPerLane], fi[kPerLane];
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kPerLane; ++k) {
+            const int i = lane + 32 * k;
+            mi[k] = -INFINITY;
+            li[k] = 0.0f;
+            if (i < kParts) {
+                const float* src = cluster.map_shared_rank(&s_wp[i % kWarps][hh][0], i / kWarps);
+                mi[k] = src[0];
+                li[k] = src[1];
+            }
+            M = fmaxf(M, mi[k]);
+        }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        const float fi = mi == -INFINITY ? 0.0f : exp2f(mi - M);
-        float L = li * fi;
+        float L = 0.0f;
+#pragma unroll
+        for (int k = 0; k < kPerLane; ++k) {
+            fi[k] = mi[k] == -INFINITY ? 0.0f : exp2f(mi[k] - M);
+            L += li[k] * fi[k];
+        }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-        const float* base[kCluster];
-#pragma unroll
-        for (int c = 0; c < kCluster; ++c) base[c] = cluster.map_shared_rank(&s_wp[0][r][2 + tid], c);
         float O = 0.0f;
+        if (tid < kD) {
+            const float* base[kCluster];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float f = __shfl_sync(0xffffffffu, fi, i);
-            O += f * base[i >> 2][(i & 3) * 8 * kPartStride];
+            for (int c = 0; c < kCluster; ++c) base[c] = cluster.map_shared_rank(&s_wp[0][hh][2 + tid], c);
+#pragma unroll
+            for (int i = 0; i < kParts; ++i) {
+                const float f = __shfl_sync(0xffffffffu, fi[i / 32], i % 32);
+                O += f * base[i / kWarps][(i % kWarps) * 8 * kPartStride];
+            }
         }
-        Mc = M;
-        Lc = L;
-        Oc = O;
+        Mc[j] = M;
+        Lc[j] = L;
+        Oc[j] = O;
     }
     cluster_arrive();  // this CTA has finished reading the other CTAs' partials
-    int last = 0;
-    if (r < G) {
+#pragma unroll
+    for (int j = 0; j < kHeadsPerCta; ++j) {
+        const int r = crank + j * kCluster;
+        if (r >= G) continue;
         float* dst = cpart_base + ((size_t)cid * G + r) * kPartStride;
-        dst[2 + tid] = Oc;
+        if (tid < kD) dst[2 + tid] = Oc[j];
         if (tid == 0) {
-            dst[0] = Mc;
-            dst[1] = Lc;
+            dst[0] = Mc[j];
+            dst[1] = Lc[j];
         }
         __threadfence();
         __syncthreads();
@@ -650,9 +756,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             s_last = (prev == (unsigned)(n_clusters - 1)) ? 1 : 0;
         }
         __syncthreads();
-        last = s_last;
-    }
-    if (last) {
+        if (!s_last) continue;
         // ---- last cluster partial of query head r: merge all of them
         __threadfence();
         float* s_ml = s_q[0];  // (m, l) of up to 64 cluster partials (s_q is no longer read)
@@ -662,40 +766,66 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             s_ml[2 * c + 1] = __ldcg(src + 1);
         }
         __syncthreads();
-        float M = -INFINITY;
-        for (int c = 0; c < n_clusters; ++c) M = fmaxf(M, s_ml[2 * c]);
-        float L = 0.0f, O = 0.0f;
+        float v = 0.0f;
+        if (tid < kD) {
+            float M = -INFINITY;
+            for (int c = 0; c < n_clusters; ++c) M = fmaxf(M, s_ml[2 * c]);
+            float L = 0.0f, O = 0.0f;
 #pragma unroll 8
-        for (int c = 0; c < n_clusters; ++c) {
-            const float mcv = s_ml[2 * c];
-            const float f = mcv == -INFINITY ? 0.0f : exp2f(mcv - M);
-            L += s_ml[2 * c + 1] * f;
-            O += __ldcg(cpart_base + ((size_t)c * G + r) * kPartStride + 2 + tid) * f;
-        }
-        // inverse value rotation (Hadamard-128, 1/sqrt(128), signs): thread
-        // tid holds dim tid; stages below 32 by shuffles, 32 and 64 via smem
-        float v = O / L;
+            for (int c = 0; c < n_clusters; ++c) {
+                const float mcv = s_ml[2 * c];
+                const float f = mcv == -INFINITY ? 0.0f : exp2f(mcv - M);
+                L += s_ml[2 * c + 1] * f;
+                O += __ldcg(cpart_base + ((size_t)c * G + r) * kPartStride + 2 + tid) * f;
+            }
+            // inverse value rotation (Hadamard-128, 1/sqrt(128), signs):
+            // thread tid holds dim tid; stages below 32 by shuffles, 32 and
+            // 64 through shared memory
+            v = O / L;
 #pragma unroll
-        for (int hh = 1; hh < 32; hh <<= 1) {
-            const float o = __shfl_xor_sync(0xffffffffu, v, hh);
-            v = (tid & hh) ? o - v : v + o;
+            for (int hh = 1; hh < 32; hh <<= 1) {
+                const float o = __shfl_xor_sync(0xffffffffu, v, hh);
+                v = (tid & hh) ? o - v : v + o;
+            }
         }
         float* s_x = s_q[1];
 #pragma unroll
         for (int hh = 32; hh < kD; hh <<= 1) {
-            s_x[tid] = v;
+            if (tid < kD) s_x[tid] = v;
             __syncthreads();
-            const float o = s_x[tid ^ hh];
+            const float o = tid < kD ? s_x[tid ^ hh] : 0.0f;
             __syncthreads();
             v = (tid & hh) ? o - v : v + o;
         }
-        const float val = v * p.v_inv_sqrt * ht->sign_v[tid];
-        const size_t o = ((size_t)b * p.H * G + (size_t)h * G + r) * kD + tid;
-        if (p.out_dtype) static_cast<float*>(p.out)[o] = val;
-        else static_cast<__half*>(p.out)[o] = __float2half_rn(val);
+        if (tid < kD) {
+            const float val = v * p.v_inv_sqrt * ht->sign_v[tid];
+            const size_t o = ((size_t)b * p.H * G + (size_t)h * G + r) * kD + tid;
+            if (p.out_dtype) static_cast<float*>(p.out)[o] = val;
+            else static_cast<__half*>(p.out)[o] = __float2half_rn(val);
+        }
         if (tid == 0) p.count[unit * G + r] = 0;
     }
     cluster_wait();  // no CTA leaves while another may still read its partials
+}
+
+// The dynamic shared memory of both instances of decode_kernel<BK, BV> is
+// raised above the 48 KB default once per device.
+template <int BK, int BV>
+cudaError_t ensure_smem_attr() {
+    static std::mutex mu;
+    static bool done[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev]) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<BK, BV, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         decode_smem_bytes<BK, BV>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(decode_kernel<BK, BV, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 decode_smem_bytes<BK, BV>());
+    if (e == cudaSuccess) done[dev] = true;
+    return e;
 }
 
 template <int BK, int BV, bool kAnyWide>
@@ -703,7 +833,7 @@ cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t s, cudaLaunchAttribute*
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kWarps * 32, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = decode_smem_bytes<BK, BV>();
     cfg.stream = s;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kCluster;
@@ -718,6 +848,8 @@ cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t s, cudaLaunchAttribute*
 
 template <int BK, int BV>
 cudaError_t launch_t(const DecodeParams& p, dim3 grid, cudaStream_t s, bool any_wide) {
+    cudaError_t e = ensure_smem_attr<BK, BV>();
+    if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[2];
     if (any_wide) {
         cudaLaunchConfig_t cfg = launch_config<BK, BV, true>(grid, s, attr);
@@ -732,6 +864,10 @@ cudaError_t launch_t(const DecodeParams& p, dim3 grid, cudaStream_t s, bool any_
 // the SM count times the blocks per SM).
 template <int BK, int BV>
 int resident_ctas() {
+    if (ensure_smem_attr<BK, BV>() != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = launch_config<BK, BV, false>(dim3(kCluster, 1, 1), nullptr, attr);
     cfg.numAttrs = 1;  // occupancy: the cluster shape only
@@ -775,26 +911,26 @@ int resident_ctas_for(int bk, int bv) {
 }  // namespace
 
 SplitPlan decode_split(const bgtq_plan& p, int batch, int64_t max_len) {
-    // One wave of resident CTAs in total (whole clusters of 8), splits of
-    // whole 64-token steps (16 tokens for each of the 4 warps).
+    // One wave of resident CTAs in total (whole clusters), every split a
+    // whole number of steps (kTile tokens for each warp of the CTA).
+    constexpr int64_t kStepTok = kWarps * kTile;
     SplitPlan sp;
     const int64_t units = std::max<int64_t>(1, (int64_t)batch * p.H);
     const int64_t len = std::max<int64_t>(max_len, 1);
     int64_t slots = (p.bk >= 1 && p.bk <= 3 && p.bv >= 1 && p.bv <= 4) ? resident_ctas_for(p.bk, p.bv) : 0;
-    if (slots <= 0) slots = 2 * (int64_t)std::max(1, p.num_sms);
+    if (slots <= 0) slots = std::max(1, p.num_sms);
     // Leave one cluster's room for a kernel that programmatic dependent
     // launch starts early next to this one, so that every cluster of this
     // grid can be resident at once.
     if (slots > 2 * kCluster) slots -= kCluster;
     int64_t ns = slots / units;
     if (ns >= kCluster) ns = ns / kCluster * kCluster;
-    ns = std::min<int64_t>(ns, (len + 63) / 64);
+    ns = std::min<int64_t>(ns, (len + kStepTok - 1) / kStepTok);
     ns = std::min<int64_t>(ns, (int64_t)kCluster * kMaxClusters);
-    if (len >= 64 * kCluster) ns = std::max<int64_t>(ns, kCluster);
+    if (len >= kStepTok * kCluster) ns = std::max<int64_t>(ns, kCluster);
     ns = std::max<int64_t>(ns, 1);
-    // whole 64-token steps so every warp of a CTA gets the same tile count
     int64_t tps = (len + ns - 1) / ns;
-    tps = (tps + kWarps * kTile - 1) / (kWarps * kTile) * (kWarps * kTile);
+    tps = (tps + kStepTok - 1) / kStepTok * kStepTok;
     const int64_t n = (len + tps - 1) / tps;
     sp.tokens_per_split = (int)tps;
     sp.n_split = (int)((n + kCluster - 1) / kCluster * kCluster);
