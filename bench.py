@@ -37,7 +37,7 @@ sys.path.insert(0, ROOT)
 METRIC = "packed-KV decode attn: tokens/s & achieved HBM GB/s (% of peak) at 128K ctx"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_attn_qwen3b_36l_128k.txt")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_step_qwen3b_128k.txt")
 
 
 def parse_args():
@@ -201,19 +201,31 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def code_digest(path: str) -> str:
+    """sha256 prefix of a source file's code: // comments, surrounding
+    whitespace and blank lines removed, so comment edits keep a profile valid."""
+    import re
+    lines = []
+    for line in open(path, encoding="utf-8"):
+        line = re.sub(r"//.*$", "", line).strip()
+        if line:
+            lines.append(line)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
 def traffic_from_profile():
     """dram bytes per launch from the committed ncu summary, if it was taken on
     the current decode kernel source."""
     if not os.path.exists(PROFILE_SUMMARY):
         return None
     src = os.path.join(ROOT, "rope_aware_quantized_gb300", "csrc", "decode_attn.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    sha = code_digest(src)
     vals = {}
     for line in open(PROFILE_SUMMARY):
         if ":" in line:
             k, v = line.split(":", 1)
             vals[k.strip()] = v.strip()
-    if vals.get("decode_attn.cu sha256 prefix") != sha:
+    if (vals.get("decode_attn.cu code sha256 prefix", "").split() or [""])[0] != sha:
         return None
     try:
         return float(vals["dram bytes per launch"])

@@ -1,14 +1,21 @@
-// Split-K decode attention directly on the Block-GTQ packed cache.
+// Split-K decode attention directly on the Block-GTQ packed cache, and the
+// fused decode step (append the new token, then attend).
 //
 // Method: "RoPE-Aware Bit Allocation for KV-Cache Quantization" — English
 // abstract and review §1 "Packed-Cache" / Figure 2: attention is computed on
 // the compressed K/V, no fp16 KV cache is materialised.
 //
-// Per CTA: one (sequence, KV head, token split).  Prologue: the G query heads
-// are rotated once into the key codec domain (de-whitening, signs, blockwise
-// Hadamard, 1/sqrt(piece), softmax scale and log2 e folded in), scaled per
-// head by a power of two into the fp16 range, and split into fp16 hi + lo
-// parts that form the 16 rows of the mma A operand (rows 0..7 hi, 8..15 lo).  Main loop, per warp and 16-token tile:
+// Per CTA: one (sequence, KV head, token split), 4 warps; thread-block
+// clusters of 8 consecutive splits.  Before waiting for the previous kernel
+// (programmatic dependent launch) a CTA prefetches its token range into L2,
+// copies the plan's table image into shared memory and loads its per-lane
+// lookup recipes.  After the wait: the fused step's owning CTA quantize-
+// appends the new token; the G query heads are rotated once into the key
+// codec domain (de-whitening, signs, blockwise Hadamard, 1/sqrt(piece),
+// softmax scale and log2 e folded in), scaled per head by a power of two into
+// the fp16 range, and split into fp16 hi + lo parts that form the 16 rows of
+// the mma A operand (rows 0..7 hi, 8..15 lo).  Main loop, per warp and
+// 16-token tile, tiles staged in shared memory by cp.async:
 //   S^T = Q_hilo . K_hat^T     8 k-chunks x 2 token n-tiles of m16n8k16 mma;
 //                              K_hat fragments come from a 64-bit window of
 //                              the lane's K record slice, one shift + mask +
@@ -17,14 +24,12 @@
 //   O_hilo += P_hilo . V_hat   16 dim n-tiles of m16n8k16 mma; P' = p*rho_V
 //                              split hi + lo into the A rows; V_hat fragments
 //                              come straight from the token-pair V records
-// Epilogue: the warps of a CTA merge in shared memory; the 8 CTAs of a
-// thread-block cluster (8 consecutive splits of one head) merge through
-// distributed shared memory, CTA r taking query head r, and write one
-// cluster partial (m, l, acc) per head to the workspace; the last cluster of
-// the (sequence, head) to finish (atomic ticket) merges the cluster partials
-// (log-sum-exp), applies the inverse value rotation and writes the output.
-// At entry every CTA asks the L2 to prefetch its whole token range, so the
-// HBM stream starts while the prologue runs.
+// Epilogue: each warp leaves its partial (m, l, acc) in shared memory; CTA
+// rank r of the cluster reduces query head r over the cluster's 32 warp
+// partials through distributed shared memory and writes one cluster partial
+// to the workspace; the last cluster partial of each (sequence, head, query
+// head) to arrive (atomic ticket) triggers the final log-sum-exp merge, the
+// inverse value rotation and the output store.
 #include <cooperative_groups.h>
 #include <cuda_fp16.h>
 
@@ -756,54 +761,73 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             s_last = (prev == (unsigned)(n_clusters - 1)) ? 1 : 0;
         }
         __syncthreads();
-        if (!s_last) continue;
-        // ---- last cluster partial of query head r: merge all of them
+        if (!s_last || warp != 0) continue;
+        // ---- last cluster partial of query head r: warp 0 merges all of
+        // them (lane holds dims lane + 32 i), 8 partials per batch of
+        // independent loads, online rescaling between batches
         __threadfence();
-        float* s_ml = s_q[0];  // (m, l) of up to 64 cluster partials (s_q is no longer read)
-        for (int c = tid; c < n_clusters; c += kWarps * 32) {
-            const float* src = cpart_base + ((size_t)c * G + r) * kPartStride;
-            s_ml[2 * c] = __ldcg(src);
-            s_ml[2 * c + 1] = __ldcg(src + 1);
-        }
-        __syncthreads();
-        float v = 0.0f;
-        if (tid < kD) {
-            float M = -INFINITY;
-            for (int c = 0; c < n_clusters; ++c) M = fmaxf(M, s_ml[2 * c]);
-            float L = 0.0f, O = 0.0f;
-#pragma unroll 8
-            for (int c = 0; c < n_clusters; ++c) {
-                const float mcv = s_ml[2 * c];
-                const float f = mcv == -INFINITY ? 0.0f : exp2f(mcv - M);
-                L += s_ml[2 * c + 1] * f;
-                O += __ldcg(cpart_base + ((size_t)c * G + r) * kPartStride + 2 + tid) * f;
-            }
-            // inverse value rotation (Hadamard-128, 1/sqrt(128), signs):
-            // thread tid holds dim tid; stages below 32 by shuffles, 32 and
-            // 64 through shared memory
-            v = O / L;
+        float M = -INFINITY, L = 0.0f, O[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int c0 = 0; c0 < n_clusters; c0 += 8) {
+            float mc[8], lc[8], oc[8][4];
 #pragma unroll
-            for (int hh = 1; hh < 32; hh <<= 1) {
-                const float o = __shfl_xor_sync(0xffffffffu, v, hh);
-                v = (tid & hh) ? o - v : v + o;
+            for (int j = 0; j < 8; ++j) {
+                const int c = c0 + j;
+                mc[j] = -INFINITY;
+                lc[j] = 0.0f;
+                oc[j][0] = oc[j][1] = oc[j][2] = oc[j][3] = 0.0f;
+                if (c < n_clusters) {
+                    const float* src = cpart_base + ((size_t)c * G + r) * kPartStride;
+                    mc[j] = __ldcg(src);
+                    lc[j] = __ldcg(src + 1);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) oc[j][i] = __ldcg(src + 2 + lane + 32 * i);
+                }
+            }
+            float Mn = M;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) Mn = fmaxf(Mn, mc[j]);
+            const float a = M == -INFINITY ? 0.0f : exp2f(M - Mn);
+            L *= a;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) O[i] *= a;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float f = mc[j] == -INFINITY ? 0.0f : exp2f(mc[j] - Mn);
+                L += lc[j] * f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) O[i] += oc[j][i] * f;
+            }
+            M = Mn;
+        }
+        // inverse value rotation (Hadamard-128, 1/sqrt(128), signs): stages
+        // 1..16 by shuffles, 32 and 64 between the lane's four dims
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = O[i] / L;
+#pragma unroll
+        for (int hh = 1; hh < 32; hh <<= 1) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float o = __shfl_xor_sync(0xffffffffu, v[i], hh);
+                v[i] = (lane & hh) ? o - v[i] : v[i] + o;
             }
         }
-        float* s_x = s_q[1];
-#pragma unroll
-        for (int hh = 32; hh < kD; hh <<= 1) {
-            if (tid < kD) s_x[tid] = v;
-            __syncthreads();
-            const float o = tid < kD ? s_x[tid ^ hh] : 0.0f;
-            __syncthreads();
-            v = (tid & hh) ? o - v : v + o;
+        {
+            const float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+            v[0] = a0 + a2;
+            v[2] = a0 - a2;
+            v[1] = a1 + a3;
+            v[3] = a1 - a3;
         }
-        if (tid < kD) {
-            const float val = v * p.v_inv_sqrt * ht->sign_v[tid];
-            const size_t o = ((size_t)b * p.H * G + (size_t)h * G + r) * kD + tid;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int d = lane + 32 * i;
+            const float val = v[i] * p.v_inv_sqrt * ht->sign_v[d];
+            const size_t o = ((size_t)b * p.H * G + (size_t)h * G + r) * kD + d;
             if (p.out_dtype) static_cast<float*>(p.out)[o] = val;
             else static_cast<__half*>(p.out)[o] = __float2half_rn(val);
         }
-        if (tid == 0) p.count[unit * G + r] = 0;
+        if (lane == 0) p.count[unit * G + r] = 0;
     }
     cluster_wait();  // no CTA leaves while another may still read its partials
 }
