@@ -22,6 +22,9 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = [
     ("bgtq_host.cpp", []),
     ("codec.cu", ["--fmad=false"]),
+    ("codec_bulk_k1.cu", ["--fmad=false"]),
+    ("codec_bulk_k2.cu", ["--fmad=false"]),
+    ("codec_bulk_k3.cu", ["--fmad=false"]),
     ("decode_attn.cu", []),
     ("decode_attn_noalloc.cu", []),
 ]

@@ -20,22 +20,6 @@ namespace {
 constexpr int kWarpsQ = 4;
 constexpr int kPairsPerBlock = 16;  // token pairs each quantize_append block encodes
 
-struct QParams {
-    const __half* k;
-    const __half* v;
-    int t_new, H;
-    const int32_t* pos_start;
-    uint8_t* kc;
-    float* kn;
-    uint8_t* vc;
-    float* vn;
-    int64_t cap;
-    const HeadTab* heads;
-    const float* thr;
-    int bk, bv;
-    float v_inv_sqrt;
-    int32_t* status;
-};
 
 // One block appends up to kPairsPerBlock token pairs of one (sequence, head).
 // Warps 0 and 1 encode keys (the even and the odd token of each pair, two
@@ -314,18 +298,23 @@ cudaError_t launch_quantize_append(const bgtq_plan& pl, cudaStream_t s, const vo
     p.bv = pl.bv;
     p.v_inv_sqrt = (float)(1.0 / std::sqrt((double)kD));
     p.status = status;
-    const int64_t pairs = (int64_t)t_new / 2 + 1;
-    const int64_t per_block = kPairsPerBlock;
-    dim3 grid((unsigned)((pairs + per_block - 1) / per_block), (unsigned)pl.H, (unsigned)batch);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(32 * kWarpsQ, 1, 1);
     cfg.stream = s;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
+    // Bulk appends (prefill) take the token-per-thread kernel, which reads
+    // whole fp16 rows with 16-byte loads; small appends (decode) and other
+    // widths the warp-per-token kernel.
+    const bool aligned = ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15) == 0;
+    if (t_new >= kBulkMinTokens && aligned && pl.bk >= 1 && pl.bk <= 3 && pl.bv >= 1 && pl.bv <= 4)
+        return launch_quantize_append_bulk(p, pl.bk, pl.bv, batch, s);
+    const int64_t pairs = (int64_t)t_new / 2 + 1;
+    const int64_t per_block = kPairsPerBlock;
+    cfg.gridDim = dim3((unsigned)((pairs + per_block - 1) / per_block), (unsigned)pl.H, (unsigned)batch);
+    cfg.blockDim = dim3(32 * kWarpsQ, 1, 1);
     return cudaLaunchKernelEx(&cfg, quantize_append_kernel, p);
 }
 

@@ -53,7 +53,14 @@ constexpr int kMaxClusters = 64;  // clusters per (sequence, head)
 constexpr int kPartStride = 2 + kD;  // m, l, acc[128] per query head
 constexpr uint32_t kPrivByte = 4u * kImgPriv;
 constexpr int kPrivMaxW = 3;
-constexpr float kHeadroom = 8.0f;  // log2 headroom of the softmax reference
+// Softmax reference (log2 domain): set kLift above the largest logit when it
+// is moved, moved again only when a logit passes it by more than kSlack.  The
+// weights p then stay in (0, 2^kSlack] and the largest is >= 2^-kLift after a
+// move, so P' = p * rho_V stays in the fp16 normal range for value norms
+// from ~1e-3 to ~4e3, and the accumulator is rescaled only when the maximum
+// grows by more than kLift + kSlack.
+constexpr float kLift = 4.0f;
+constexpr float kSlack = 4.0f;
 
 struct DecodeParams {
     const __half* q;
@@ -511,7 +518,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     pdl_wait();  // q, the cache and the workspace may belong to the previous kernel
     if (pos_bad && split == 0 && h == 0 && tid == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_APPEND_CAPACITY);
     if (owner) append_new_token<BK, BV>(p, el, unit, pos, s_thr, s_enc, warp, lane);
-    float m_ref = -INFINITY, l_run = 0.0f;  // softmax reference (running max + headroom), sum
+    float m_ref = -INFINITY, l_run = 0.0f;  // softmax reference (see kLift, kSlack), sum
     float acc[16][4];
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
@@ -599,11 +606,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             }
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        // The reference sits kHeadroom above the largest logit seen, so the
-        // weights stay <= 1 and the accumulator is rescaled only when a
-        // logit passes the reference.
-        if (__any_sync(0xffffffffu, mx > m_ref)) {
-            const float ref = mx > m_ref ? mx + kHeadroom : m_ref;
+        if (__any_sync(0xffffffffu, mx > m_ref + kSlack)) {
+            const float ref = mx > m_ref + kSlack ? mx + kLift : m_ref;
             const float alpha = fast_exp2(m_ref - ref);
             l_run *= alpha;
 #pragma unroll

@@ -15,6 +15,30 @@
 #include "bgtq_internal.h"
 
 namespace bgtq {
+
+// Parameter block of the quantize-append kernels.
+struct QParams {
+    const __half* k;
+    const __half* v;
+    int t_new, H;
+    const int32_t* pos_start;
+    uint8_t* kc;
+    float* kn;
+    uint8_t* vc;
+    float* vn;
+    int64_t cap;
+    const HeadTab* heads;
+    const float* thr;
+    int bk, bv;
+    float v_inv_sqrt;
+    int32_t* status;
+};
+
+// Appends at least this long (and of the widths below) take the
+// token-per-thread bulk kernel; it launches it on `s`.
+constexpr int kBulkMinTokens = 64;
+cudaError_t launch_quantize_append_bulk(const QParams& p, int bk, int bv, int batch, cudaStream_t s);
+
 namespace {
 
 // Randomized Hadamard on the warp's 128 slots of N tokens at once: stages

@@ -212,6 +212,27 @@ def test_decode_extreme_query_magnitudes(qmul):
     check_close(got[0], oracle_out(heads, li[0], q, T, G))
 
 
+@pytest.mark.parametrize("vmul", [0.01, 100.0])
+def test_decode_value_magnitudes(vmul):
+    """P' = p * rho_V enters the tensor cores as fp16 hi + lo: value norms two
+    decades below and above unit scale must stay accurate (no fp16
+    subnormals or overflow in the weights)."""
+    H, G, T = 2, 8, 2000
+    li, plan, cache, heads = build(321, H, G, T, 384, 3, s_ln=1.2)
+    li = [synth.LayerInputs(li[0].k, (li[0].v.astype(np.float64) * vmul).astype(np.float16), li[0].q,
+                            li[0].calib, li[0].sigma)]
+    append(plan, cache, li, 0, T)
+    for qmul in (1.0, 0.05):  # peaked and flat softmax
+        q = (li[0].q.astype(np.float32) * qmul).astype(np.float16)
+        got, st = decode(plan, cache, dev(q[None]), dev(np.array([T], np.int32)), T)
+        assert st == 0 and np.all(np.isfinite(got))
+        want = oracle_out(heads, li[0], q, T, G)
+        err = np.abs(got[0] - want)
+        rel = np.linalg.norm(got[0] - want) / np.linalg.norm(want)
+        assert err.max() <= MAX_ABS * max(1.0, vmul), f"max abs {err.max():.3e}"
+        assert rel <= REL_L2, f"rel l2 {rel:.3e}"
+
+
 def test_decode_ragged_batch_with_empty_and_single_token_sequences():
     H, G, T = 2, 4, 1500
     li, plan, cache, heads = build(90, H, G, T, 256, 2, s_ln=1.2, batch=4, cap=1500)
