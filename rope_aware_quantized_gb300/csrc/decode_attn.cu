@@ -50,6 +50,7 @@ constexpr int kWarps = 4;
 constexpr int kTile = 16;         // tokens per warp iteration; splits start on a tile boundary
 constexpr int kCluster = 8;       // CTAs per thread-block cluster (consecutive splits of one head)
 constexpr int kMaxClusters = 64;  // clusters per (sequence, head)
+constexpr int64_t kMaxSplitTokens = 4096;  // longest token split of one CTA
 constexpr int kPartStride = 2 + kD;  // m, l, acc[128] per query head
 constexpr uint32_t kPrivByte = 4u * kImgPriv;
 constexpr int kPrivMaxW = 3;
@@ -953,6 +954,11 @@ SplitPlan decode_split(const bgtq_plan& p, int batch, int64_t max_len) {
     if (slots > 2 * kCluster) slots -= kCluster;
     int64_t ns = slots / units;
     if (ns >= kCluster) ns = ns / kCluster * kCluster;
+    // Splits longer than kMaxSplitTokens are cut further (several waves):
+    // in a ragged batch the long sequences then spread over many CTAs
+    // instead of one CTA each, and the short sequences' extra splits exit
+    // at once.
+    ns = std::max<int64_t>(ns, (len + kMaxSplitTokens - 1) / kMaxSplitTokens);
     ns = std::min<int64_t>(ns, (len + kStepTok - 1) / kStepTok);
     ns = std::min<int64_t>(ns, (int64_t)kCluster * kMaxClusters);
     if (len >= kStepTok * kCluster) ns = std::max<int64_t>(ns, kCluster);
