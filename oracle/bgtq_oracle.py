@@ -603,3 +603,33 @@ def encode_head(hs: HeadState, k_fp16, v_fp16):
 
 def decode_attention_head(hs: HeadState, q_fp16, khat, vhat, scale=1.0 / math.sqrt(D)):
     return attention(q_fp16, khat, vhat, scale)
+
+
+# =============================================================================
+# RoPE-logit fidelity diagnostic (review §3: Block-GTQ lowers the error of the
+# RoPE logits against uniform TQ-MSE at matched bit budgets; abstract: the
+# logit is a sum over 2-D frequency blocks, which is why per-block widths
+# help).  Reading R19: the figure is the mean absolute error of the attention
+# logits, scale * q.k_hat against scale * q.k over the cached tokens, per
+# query head; the baseline is uniform TQ-MSE on the keys at the same budget.
+# =============================================================================
+
+
+def uniform_head_state(bits_per_key: int, v_bits: int, seed: int, head: int, rope_layout: int = 0) -> HeadState:
+    """Uniform TQ-MSE keys at the budget of `bits_per_key`: every block gets
+    bK = bits_per_key / 128 bits and all energies are equal (s_i = 2, so the
+    whitening w_i = sqrt(2 / s_i) is the identity), which leaves a single
+    rotation piece over all 128 coordinates, as for values (reading R17)."""
+    bk = bits_per_key // 128
+    bits = np.full(NB, bk, dtype=np.int64)
+    s = np.full(NB, 2.0)
+    return HeadState(k_codec(bits, s, seed, head, rope_layout), v_codec(v_bits, seed, head), bits, s, bk, v_bits)
+
+
+def logit_mae(q_fp16: np.ndarray, k_fp16: np.ndarray, khat: np.ndarray, scale: float = 1.0 / math.sqrt(D)):
+    """(1/T) sum_t |scale q.k_t - scale q.khat_t| for every query row, float64.
+    q [G][128], k [T][128] (the keys as given), khat [T][128] (dequantised)."""
+    q = q_fp16.astype(np.float64)
+    exact = scale * (k_fp16.astype(np.float64) @ q.T)      # [T][G]
+    approx = scale * (khat.astype(np.float64) @ q.T)
+    return np.abs(exact - approx).mean(axis=0)
