@@ -267,6 +267,29 @@ int bgtq_decode_attn_noalloc(const bgtq_plan* plan, void* stream, const void* q_
                              float softmax_scale, int32_t* dev_status);
 
 /*
+ * bgtq_logit_mae — RoPE-logit fidelity diagnostic: for every query head, the
+ * mean absolute error of the attention logits computed from the packed keys
+ * against the keys as given,
+ *   mae[b][g] = (1/t) sum_{s < t} | softmax_scale (q_g . k_s - q_g . khat_s) |
+ * over cache positions 0..t-1 (khat = the dequantised cached key).
+ * Source: review §3 Method & Key Results (Block-GTQ lowers the RoPE-logit
+ * error against uniform TQ-MSE at matched budgets; plan a uniform baseline
+ * with every block at bK bits and equal energies); English abstract (the
+ * logit is a sum over 2-D frequency blocks).
+ *   q_fp16      device, [batch][H*G][128] half
+ *   k_fp16      device, [batch][H][t][128] half (8-byte aligned): the keys
+ *               that were appended at positions 0..t-1
+ *   cache       host pointer to the descriptor of the cache holding them
+ *   mae         device, [batch][H*G] float, overwritten
+ * q.khat is computed in the key codec domain as the decode kernel does; the
+ * result is float32 (summation order not fixed).
+ * Errors: INVALID_ARG (t > capacity, NULL, misaligned k, host-only plan),
+ * UNSUPPORTED (G > 8), CUDA.
+ */
+int bgtq_logit_mae(const bgtq_plan* plan, void* stream, const void* q_fp16, const void* k_fp16,
+                   const bgtq_cache* cache, int64_t t, int batch, float softmax_scale, float* mae);
+
+/*
  * bgtq_dequant_debug — decode cached tokens [t0, t1) of (sequence b, head)
  * back to float32, for inspection and parity checks.
  *   k_out, v_out  device, [t1-t0][128] float (either may be NULL)

@@ -250,6 +250,17 @@ def bgtq_decode_attn_noalloc(plan: Plan, q_fp16, cache: Cache, seq_lens, max_len
                                           _ptr(seq_lens), max_len, batch, _ptr(out), out_dtype, scale, _ptr(status)))
 
 
+def bgtq_logit_mae(plan: Plan, q_fp16, k_fp16, cache, t: int, out, softmax_scale: float | None = None, stream=None):
+    """RoPE-logit fidelity: out [B][H*G] float32 = mean over positions 0..t-1 of
+    |scale q.k - scale q.khat| (k_fp16: [B][H][t][128], the appended keys)."""
+    batch = q_fp16.shape[0]
+    if not k_fp16.is_contiguous() or k_fp16.shape[-1] != HEAD_DIM or k_fp16.shape[-2] != t:
+        raise ValueError("k must be a contiguous [B][H][t][128] tensor")
+    scale = (1.0 / HEAD_DIM ** 0.5) if softmax_scale is None else softmax_scale
+    _check(lib().bgtq_logit_mae(plan.handle, _stream(stream), _ptr(q_fp16), _ptr(k_fp16), C.byref(cache.desc), t,
+                                batch, scale, _ptr(out)))
+
+
 def bgtq_dequant_debug(plan: Plan, cache: Cache, b: int, head: int, t0: int, t1: int, k_out=None, v_out=None,
                        codec_domain: bool = False, stream=None):
     _check(lib().bgtq_dequant_debug(plan.handle, _stream(stream), C.byref(cache.desc), cache.batch, b, head, t0, t1,
@@ -259,6 +270,6 @@ def bgtq_dequant_debug(plan: Plan, cache: Cache, b: int, head: int, t0: int, t1:
 __all__ = [
     "BgtqError", "Plan", "Cache", "CacheView", "bgtq_alloc_bits", "bgtq_plan_create", "bgtq_cache_bytes",
     "bgtq_quantize_append", "bgtq_decode_attn_workspace", "bgtq_decode_attn", "bgtq_decode_step",
-    "bgtq_decode_attn_noalloc",
+    "bgtq_decode_attn_noalloc", "bgtq_logit_mae",
     "bgtq_dequant_debug",
 ]

@@ -27,6 +27,7 @@ SOURCES = [
     ("codec_bulk_k3.cu", ["--fmad=false"]),
     ("decode_attn.cu", []),
     ("decode_attn_noalloc.cu", []),
+    ("fidelity.cu", []),
 ]
 
 

@@ -682,6 +682,28 @@ int bgtq_decode_step(const bgtq_plan* p, void* stream, const void* q, const void
     return BGTQ_OK;
 }
 
+int bgtq_logit_mae(const bgtq_plan* p, void* stream, const void* q, const void* k, const bgtq_cache* c, int64_t t,
+                   int batch, float scale, float* mae) {
+    int rc = check_plan(p);
+    if (rc) return rc;
+    if ((rc = check_cache(p, c))) return rc;
+    if (batch < 0 || t < 0) return set_error(BGTQ_ERR_INVALID_ARG, "batch and t must be >= 0");
+    if (t > c->capacity) return set_error(BGTQ_ERR_INVALID_ARG, "t exceeds the cache capacity");
+    if (batch == 0) return BGTQ_OK;
+    if (!q || !k || !mae) return set_error(BGTQ_ERR_INVALID_ARG, "NULL pointer");
+    if (reinterpret_cast<uintptr_t>(k) & 7) return set_error(BGTQ_ERR_INVALID_ARG, "k must be 8-byte aligned");
+    if (p->G > 8) return set_error(BGTQ_ERR_UNSUPPORTED, "at most 8 query heads per KV head");
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return set_error(BGTQ_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
+    if (t == 0) {
+        cudaError_t e = cudaMemsetAsync(mae, 0, sizeof(float) * (size_t)batch * p->H * p->G, (cudaStream_t)stream);
+        if (e != cudaSuccess) return set_error(BGTQ_ERR_CUDA, "logit_mae: %s", cudaGetErrorString(e));
+        return BGTQ_OK;
+    }
+    cudaError_t e = launch_logit_mae(*p, (cudaStream_t)stream, q, k, *c, t, batch, scale, mae);
+    if (e != cudaSuccess) return set_error(BGTQ_ERR_CUDA, "logit_mae launch: %s", cudaGetErrorString(e));
+    return BGTQ_OK;
+}
+
 int bgtq_dequant_debug(const bgtq_plan* p, void* stream, const bgtq_cache* c, int batch, int b, int head, int64_t t0,
                        int64_t t1, float* k_out, float* v_out, int codec_domain) {
     int rc = check_plan(p);

@@ -106,6 +106,9 @@ cudaError_t launch_quantize_append(const bgtq_plan& p, cudaStream_t s, const voi
 cudaError_t launch_dequant(const bgtq_plan& p, cudaStream_t s, const bgtq_cache& c, int batch, int b, int head,
                            int64_t t0, int64_t t1, float* k_out, float* v_out, int codec_domain);
 
+cudaError_t launch_logit_mae(const bgtq_plan& p, cudaStream_t s, const void* q, const void* k, const bgtq_cache& c,
+                             int64_t t, int batch, float scale, float* out);
+
 struct SplitPlan {
     int n_split = 1;
     int tokens_per_split = 64;
