@@ -633,3 +633,26 @@ def logit_mae(q_fp16: np.ndarray, k_fp16: np.ndarray, khat: np.ndarray, scale: f
     exact = scale * (k_fp16.astype(np.float64) @ q.T)      # [T][G]
     approx = scale * (khat.astype(np.float64) @ q.T)
     return np.abs(exact - approx).mean(axis=0)
+
+
+# =============================================================================
+# fp16 recent-key buffer (abstract: the AIME result is stated "without an fp16
+# recent-key buffer", so the option exists).  Reading R20: the last W cached
+# keys of each (sequence, KV head) are also kept in fp16, and attention uses
+# those exact keys for positions [T - W, T) and the dequantised keys before
+# that; values stay packed.
+# =============================================================================
+
+
+def keys_with_recent(khat: np.ndarray, k_fp16: np.ndarray, w: int) -> np.ndarray:
+    """khat [T][128] with rows max(0, T - w) .. T - 1 replaced by the fp16 keys."""
+    t = khat.shape[0]
+    out = khat.astype(np.float64).copy()
+    lo = max(0, t - w)
+    out[lo:] = k_fp16[lo:t].astype(np.float64)
+    return out
+
+
+def attention_recent(q_fp16, khat, vhat, k_fp16, w: int, scale: float = 1.0 / math.sqrt(D)):
+    """Decode attention over the packed cache with an fp16 recent-key buffer of w keys."""
+    return attention(q_fp16, keys_with_recent(khat, k_fp16, w), vhat, scale)
