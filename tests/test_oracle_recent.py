@@ -23,15 +23,15 @@ def _case(seed=4, t=300):
 
 def test_zero_buffer_is_plain_attention():
     li, enc = _case()
-    a = O.attention_recent(li.q[0], enc["khat"], enc["vhat"], li.k[0], 0)
-    b = O.attention(li.q[0], enc["khat"], enc["vhat"])
+    a = O.attention_recent(li.q[:4], enc["khat"], enc["vhat"], li.k[0], 0)
+    b = O.attention(li.q[:4], enc["khat"], enc["vhat"])
     assert np.array_equal(a, b)
 
 
 def test_full_buffer_is_exact_key_attention():
     li, enc = _case(t=50)
-    got = O.attention_recent(li.q[0], enc["khat"], enc["vhat"], li.k[0], 64)
-    logits = li.q[0].astype(np.float64) @ li.k[0].astype(np.float64).T / math.sqrt(128)
+    got = O.attention_recent(li.q[:4], enc["khat"], enc["vhat"], li.k[0], 64)
+    logits = li.q[:4].astype(np.float64) @ li.k[0].astype(np.float64).T / math.sqrt(128)
     want = softmax(logits, axis=1) @ enc["vhat"].astype(np.float64)
     assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
 
