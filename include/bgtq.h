@@ -78,6 +78,14 @@ typedef struct {
     void* v_codes;    /* device, [B][H][capacity/2][32*bV] bytes */
     float* v_norm;    /* device, [B][H][capacity] */
     int64_t capacity; /* tokens per (sequence, head); must be even */
+    /* Optional fp16 recent-key buffer (abstract: results are quoted "without
+     * an fp16 recent-key buffer", so the option exists).  recent = W > 0:
+     * every append also copies the fp16 keys of its last W tokens into ring
+     * slot (position mod W) of k_recent, and decode uses those exact keys for
+     * positions [seq_len - W, seq_len) (values stay packed).  recent = 0:
+     * none (k_recent may be NULL). */
+    void* k_recent;   /* device, [B][H][recent][128] half, 16-byte aligned */
+    int64_t recent;   /* W, 0 <= W <= capacity */
 } bgtq_cache;
 
 /* Message of the last failure on this thread ("" if none).  Never NULL. */

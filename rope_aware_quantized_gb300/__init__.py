@@ -139,29 +139,35 @@ def bgtq_cache_bytes(plan: Plan, batch: int, capacity: int):
 class Cache:
     """One layer's packed cache in caller-owned torch CUDA tensors."""
 
-    def __init__(self, plan: Plan, batch: int, capacity: int, device="cuda"):
+    def __init__(self, plan: Plan, batch: int, capacity: int, device="cuda", recent: int = 0):
+        """recent = W > 0 adds an fp16 recent-key buffer of W keys per (sequence, KV head)."""
         import torch
         if capacity % 2:
             raise ValueError("capacity must be even")
         kb, vb, nb = bgtq_cache_bytes(plan, batch, capacity)
-        self.batch, self.capacity = batch, capacity
+        self.batch, self.capacity, self.recent = batch, capacity, recent
         self.k_codes = torch.zeros(kb, dtype=torch.uint8, device=device)
         self.v_codes = torch.zeros(vb, dtype=torch.uint8, device=device)
         self.k_norm = torch.zeros(nb // 4, dtype=torch.float32, device=device)
         self.v_norm = torch.zeros(nb // 4, dtype=torch.float32, device=device)
+        rb = batch * plan.n_kv_heads * recent * HEAD_DIM * 2
+        self.k_recent = torch.zeros(max(rb // 2, 8), dtype=torch.float16, device=device)
         self.desc = BgtqCache(self.k_codes.data_ptr(), self.k_norm.data_ptr(), self.v_codes.data_ptr(),
-                              self.v_norm.data_ptr(), capacity)
-        self._per_seq = (kb // max(batch, 1), vb // max(batch, 1), nb // max(batch, 1))
+                              self.v_norm.data_ptr(), capacity, self.k_recent.data_ptr() if recent else None,
+                              recent)
+        self._per_seq = (kb // max(batch, 1), vb // max(batch, 1), nb // max(batch, 1), rb // max(batch, 1))
 
     def sequence_view(self, b: int) -> "CacheView":
         """Descriptor of sequence b alone (batch 1), per the documented layout."""
-        kb, vb, nb = self._per_seq
+        kb, vb, nb, rb = self._per_seq
         return CacheView(BgtqCache(self.k_codes.data_ptr() + b * kb, self.k_norm.data_ptr() + b * nb,
                                    self.v_codes.data_ptr() + b * vb, self.v_norm.data_ptr() + b * nb,
-                                   self.capacity), self.capacity)
+                                   self.capacity, self.k_recent.data_ptr() + b * rb if self.recent else None,
+                                   self.recent), self.capacity)
 
     def nbytes(self) -> int:
-        return sum(t.numel() * t.element_size() for t in (self.k_codes, self.v_codes, self.k_norm, self.v_norm))
+        return sum(t.numel() * t.element_size() for t in (self.k_codes, self.v_codes, self.k_norm, self.v_norm)) + \
+            (self.k_recent.numel() * 2 if self.recent else 0)
 
 
 class CacheView:

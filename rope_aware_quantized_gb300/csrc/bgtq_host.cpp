@@ -503,6 +503,10 @@ static int check_cache(const bgtq_plan* p, const bgtq_cache* c) {
         return set_error(BGTQ_ERR_INVALID_ARG, "k_codes and v_codes must be 16-byte aligned");
     if ((reinterpret_cast<uintptr_t>(c->k_norm) & 3) || (reinterpret_cast<uintptr_t>(c->v_norm) & 3))
         return set_error(BGTQ_ERR_INVALID_ARG, "k_norm and v_norm must be 4-byte aligned");
+    if (c->recent < 0 || c->recent > c->capacity)
+        return set_error(BGTQ_ERR_INVALID_ARG, "recent must be in [0, capacity]");
+    if (c->recent > 0 && (!c->k_recent || (reinterpret_cast<uintptr_t>(c->k_recent) & 15)))
+        return set_error(BGTQ_ERR_INVALID_ARG, "k_recent must be a 16-byte aligned buffer when recent > 0");
     (void)p;
     return BGTQ_OK;
 }
@@ -624,6 +628,8 @@ int bgtq_quantize_append(const bgtq_plan* p, void* stream, const void* k, const 
     if (batch < 0 || t_new < 0) return set_error(BGTQ_ERR_INVALID_ARG, "batch and t_new must be >= 0");
     if (batch == 0 || t_new == 0) return BGTQ_OK;
     if (!k || !v || !pos_start) return set_error(BGTQ_ERR_INVALID_ARG, "NULL input pointer");
+    if (c->recent > 0 && ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 7))
+        return set_error(BGTQ_ERR_INVALID_ARG, "k and v must be 8-byte aligned when the cache has a recent-key buffer");
     cudaError_t e = launch_quantize_append(*p, (cudaStream_t)stream, k, v, batch, t_new, pos_start, *c, status);
     if (e != cudaSuccess) return set_error(BGTQ_ERR_CUDA, "quantize_append launch: %s", cudaGetErrorString(e));
     return BGTQ_OK;
@@ -668,6 +674,8 @@ int bgtq_decode_step(const bgtq_plan* p, void* stream, const void* q, const void
     if (batch == 0) return BGTQ_OK;
     if (!q || !k_new || !v_new || !pos_new || !seq_lens || !out || !ws)
         return set_error(BGTQ_ERR_INVALID_ARG, "NULL pointer");
+    if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 7)
+        return set_error(BGTQ_ERR_INVALID_ARG, "k_new and v_new must be 8-byte aligned");
     if (out_dtype != 0 && out_dtype != 1) return set_error(BGTQ_ERR_INVALID_ARG, "out_dtype must be 0 (half) or 1 (float)");
     if (p->bk > 3) return set_error(BGTQ_ERR_UNSUPPORTED, "decode supports bits_per_key <= 384");
     if (p->bv > 4) return set_error(BGTQ_ERR_UNSUPPORTED, "decode supports v_bits <= 4");

@@ -98,6 +98,11 @@ __global__ void __launch_bounds__(128) quantize_append_kernel(QParams p) {
                 uint32_t* dst = reinterpret_cast<uint32_t*>(p.kc + (unit * p.cap + pos) * (16 * p.bk));
                 if (lane < krec_words) dst[lane] = rec[warp][n][lane];
                 if (lane == 0) p.kn[unit * p.cap + pos] = rho[n];
+                if (p.recent > 0 && pos >= end - p.recent) {
+                    // fp16 recent-key ring: the key as given, slot pos mod W
+                    const uint2 nat = *(reinterpret_cast<const uint2*>(p.k + (unit * p.t_new + (size_t)(pos - ps)) * kD) + lane);
+                    *(reinterpret_cast<uint2*>(p.k_recent + (unit * p.recent + pos % p.recent) * kD) + lane) = nat;
+                }
             }
             __syncwarp();
 #pragma unroll
@@ -298,6 +303,8 @@ cudaError_t launch_quantize_append(const bgtq_plan& pl, cudaStream_t s, const vo
     p.bv = pl.bv;
     p.v_inv_sqrt = (float)(1.0 / std::sqrt((double)kD));
     p.status = status;
+    p.k_recent = static_cast<__half*>(c.k_recent);
+    p.recent = c.recent;
     cudaLaunchConfig_t cfg = {};
     cfg.stream = s;
     cudaLaunchAttribute attr;

@@ -169,6 +169,12 @@ __global__ void __launch_bounds__(kBulkTok) quantize_append_bulk_kernel(QParams 
             row[4 * i + 2] = w4.z;
             row[4 * i + 3] = w4.w;
         }
+        if (p.recent > 0 && pos >= end - p.recent) {
+            // fp16 recent-key ring: the key as given, slot pos mod W
+            uint4* rdst = reinterpret_cast<uint4*>(p.k_recent + (unit * p.recent + pos % p.recent) * kD);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) rdst[i] = make_uint4(row[4 * i], row[4 * i + 1], row[4 * i + 2], row[4 * i + 3]);
+        }
         const __half* rowh = reinterpret_cast<const __half*>(row);
         float z[kD];
 #pragma unroll

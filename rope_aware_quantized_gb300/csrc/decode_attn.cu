@@ -89,6 +89,10 @@ struct DecodeParams {
     const __half* v_new;
     const int32_t* pos_new;
     const float* thr;
+    // fp16 recent-key ring [B][H][recent][128] (recent > 0): exact keys for
+    // positions [seq - recent, seq); written by the fused step's append
+    __half* k_recent;
+    int64_t recent;
 };
 
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -351,6 +355,9 @@ __device__ __forceinline__ void append_new_token(const DecodeParams& p, const En
                                                  int lane) {
     if (warp == 0) {
         const __half* row = p.k_new + unit * kD;
+        if (p.recent > 0)  // fp16 recent-key ring: the new key as given, slot pos mod W
+            *(reinterpret_cast<uint2*>(p.k_recent + (unit * p.recent + pos % p.recent) * kD) + lane) =
+                *(reinterpret_cast<const uint2*>(row) + lane);
         float x[1][4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) x[0][k] = __fmul_rn(__half2float(row[el.src[k]]), el.wh[k]);
@@ -401,6 +408,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     __shared__ int s_last;
     __shared__ float s_thr[kThrCompact];                 // fused step: encoder thresholds
     __shared__ uint32_t s_enc[3][8 * kPairMaxW];          // fused step: records being assembled
+    __shared__ uint2 s_qo[8][32];                         // recent-key buffer: A fragments of q as given
     // after the main loop the table region holds the per-warp partials of
     // the 8 query heads (m, l, acc[128]) that the cluster reads
     float (*s_wp)[8][kPartStride] = reinterpret_cast<float (*)[8][kPartStride]>(s_tab);
@@ -463,6 +471,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     const HeadTab* ht = p.heads + h;
     const int t_begin = split * p.tps;
     const int t_end = min(t_begin + p.tps, seq);
+    const int wstart = p.recent > 0 ? max(0, seq - (int)p.recent) : seq;  // first position of the fp16 keys
     const uint8_t* kc = p.kc + unit * (size_t)p.cap * (16 * BK);
     const uint8_t* vc = p.vc + unit * (size_t)(p.cap / 2) * (32 * BV);
     const float* kn = p.kn + unit * (size_t)p.cap;
@@ -562,6 +571,17 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             for (int i = 0; i < 4; ++i) s_q[gg][4 * lane + i] = x[k][i] * qs;
             if (lane == 0) s_qunscale[gg] = ldexpf(1.0f, e - 14);
         }
+        // fp16 recent-key buffer: the query heads as given (fp16) as mma A
+        // fragments, rows 0..7 = heads (rows 8..15 zero), k-chunk c = dims
+        // 16c..16c+15; warp w builds chunks 2w, 2w + 1
+        if (kAnyWide && p.recent > 0 && t_end > wstart) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int c = 2 * warp + k;
+                const uint32_t* qw = reinterpret_cast<const uint32_t*>(qb + (size_t)min(g, G - 1) * kD + 16 * c + 2 * t);
+                s_qo[c][lane] = g < G ? make_uint2(__ldg(qw), __ldg(qw + 4)) : make_uint2(0u, 0u);
+            }
+        }
         __syncthreads();  // s_q, s_qunscale, the table image (and a fused step's new token) are complete
     }
     const float q_unscale = s_qunscale[g];
@@ -595,7 +615,6 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         s_chunk<BK, 7, kAnyWide>(sacc, qa, tr.kw, ksh, kmask, kbase, wide, s_tab, s_single);
         // logits (log2 domain) of head g for tokens T0 + 8 nt + 2 t + e
         float lg[2][2];
-        float mx = -INFINITY;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -603,8 +622,40 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
                 const int tok = T0 + 8 * nt + 2 * t + e;
                 const float v = (sacc[nt][e] + sacc[nt][2 + e]) * (tr.rk[nt][e] * q_unscale);
                 lg[nt][e] = tok < t_end ? v : -INFINITY;
-                mx = fmaxf(mx, lg[nt][e]);
             }
+        if (kAnyWide && p.recent > 0 && T0 + kTile > wstart) {
+            // (general instance only) the tile reaches into the fp16 recent-key buffer: those tokens'
+            // logits come from their exact keys (q as given . k, on the
+            // tensor cores; B fragments read from the ring slot pos mod W)
+            float s16[2][4];
+            const __half* ring[2];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                s16[nt][0] = s16[nt][1] = s16[nt][2] = s16[nt][3] = 0.0f;
+                const int tk = min(max(T0 + 8 * nt + g, wstart), seq - 1);
+                ring[nt] = p.k_recent + (unit * (size_t)p.recent + (size_t)(tk % p.recent)) * kD + 2 * t;
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint2 a = s_qo[c][lane];
+                const uint32_t af[4] = {a.x, 0u, a.y, 0u};
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const uint32_t* kr = reinterpret_cast<const uint32_t*>(ring[nt] + 16 * c);
+                    mma16816(s16[nt], af, __ldcg(kr), __ldcg(kr + 4));
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int tok = T0 + 8 * nt + 2 * t + e;
+                    if (tok >= wstart && tok < t_end) lg[nt][e] = s16[nt][e] * p.scale_log2;
+                }
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) mx = fmaxf(mx, fmaxf(lg[nt][0], lg[nt][1]));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
         if (__any_sync(0xffffffffu, mx > m_ref + kSlack)) {
@@ -1013,10 +1064,13 @@ cudaError_t launch_decode(const bgtq_plan& pl, cudaStream_t s, const void* q, co
     p.v_new = static_cast<const __half*>(v_new);
     p.pos_new = pos_new;
     p.thr = pl.dev.thr;
+    p.k_recent = static_cast<__half*>(c.k_recent);
+    p.recent = c.recent;
     dim3 grid((unsigned)sp.n_split, (unsigned)pl.H, (unsigned)batch);
     // the fast instance checks only slots 0 and 8 (each lane's two widest
-    // pairs) for codes wider than the pair tables
-    bool any_wide = false;
+    // pairs) for codes wider than the pair tables and has no recent-key
+    // buffer path; the general instance handles both
+    bool any_wide = c.recent > 0;
     for (const HeadTab& ht : pl.heads) any_wide |= (ht.wide_mask & ~((1u << 0) | (1u << 8))) != 0;
     const int key = pl.bk * 10 + pl.bv;
     switch (key) {

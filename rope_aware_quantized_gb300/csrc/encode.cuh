@@ -32,6 +32,8 @@ struct QParams {
     int bk, bv;
     float v_inv_sqrt;
     int32_t* status;
+    __half* k_recent;  // fp16 recent-key ring [B][H][recent][128] (recent > 0)
+    int64_t recent;
 };
 
 // Appends at least this long (and of the widths below) take the
