@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="build only the first N layers (profiling)")
     ap.add_argument("--eager", action="store_true", help="launch without a CUDA graph (profiling)")
+    ap.add_argument("--recent", type=int, default=0,
+                    help="keep the last W keys of every sequence in an fp16 recent-key buffer as well")
     ap.add_argument("--two-call", action="store_true",
                     help="per layer bgtq_quantize_append + bgtq_decode_attn instead of the fused bgtq_decode_step")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
@@ -320,7 +322,7 @@ def run_gpu(args):
     out_all = torch.empty((L, B, w.n_q, 128), dtype=torch.float16, device="cuda")
     layers = []
     for l in range(L):
-        ls = workloads.build_layer(w, l)
+        ls = workloads.build_layer(w, l, recent=args.recent)
         q_all[l].copy_(ls.q)
         nk_all[l].copy_(ls.new_k)
         nv_all[l].copy_(ls.new_v)
@@ -409,6 +411,8 @@ def run_gpu(args):
     decode_bytes = int(lens.sum()) * w.n_kv * bpth + B * w.n_q * 128 * 2 * 2
     if fused:
         decode_bytes += B * w.n_kv * (2 * 256 + 16 * (w.bits_per_key // 128) + 16 * w.v_bits + 8)
+    if args.recent:  # the fp16 keys of the window are read as well
+        decode_bytes += int(np.minimum(lens, args.recent).sum()) * w.n_kv * 256
     peaks, peak_kind = load_peaks()
     achieved = decode_bytes / (launch_ms / 1000.0) / 1e9
     traffic = traffic_from_profile()
@@ -464,6 +468,7 @@ def run_gpu(args):
                 "compute": "fp16 mma operands (hi+lo split of q and p), fp32 accumulate; fp32 encoder",
                 "l2": "inputs larger than L2 (packed cache per step >> 129 MB L2), no flush",
                 "parallelism": f"replicas x{world}",
+                **({"recent_fp16_keys": args.recent} if args.recent else {}),
             },
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,

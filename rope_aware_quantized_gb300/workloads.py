@@ -71,7 +71,7 @@ class LayerState:
 
 
 def build_layer(w: Workload, layer: int, device="cuda", keep_host=(), capacity: int | None = None,
-                prefill_chunk: int = 1 << 16) -> LayerState:
+                prefill_chunk: int = 1 << 16, recent: int = 0) -> LayerState:
     """Calibrate, plan, allocate and prefill one layer.
 
     Each sequence b holds tokens 0 .. len_b - 2 after the prefill; the decode
@@ -89,7 +89,7 @@ def build_layer(w: Workload, layer: int, device="cuda", keep_host=(), capacity: 
         bits.append(b)
         energy.append(e)
     plan = bgtq_plan_create(np.stack(bits), np.stack(energy), w.group, w.bits_per_key, w.v_bits, plan_seed(w, layer))
-    cache = Cache(plan, w.batch, cap, device)
+    cache = Cache(plan, w.batch, cap, device, recent=recent)
     q = torch.empty((w.batch, w.n_q, 128), dtype=torch.float16, device=device)
     new_k = torch.empty((w.batch, w.n_kv, 1, 128), dtype=torch.float16, device=device)
     new_v = torch.empty_like(new_k)
