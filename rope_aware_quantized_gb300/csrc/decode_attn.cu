@@ -398,8 +398,20 @@ __device__ __forceinline__ void append_new_token(const DecodeParams& p, const En
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
-template <int BK, int BV, bool kAnyWide>
+template <bool B>
+struct BoolTag {
+    static constexpr bool value = B;
+};
+
+// Instances (kKind): 0 = fast (slots 0 and 8 alone may hold codes wider
+// than the pair tables; no recent-key buffer), 1 = fast with the fp16
+// recent-key buffer, 2 = general (any slot wide) with the buffer.  The buffer
+// path is a separate instance so that the instance without it carries none
+// of its code.
+template <int BK, int BV, int kKind>
 __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) {
+    constexpr bool kAnyWide = kKind == 2;
+    constexpr bool kWinPath = kKind >= 1;
     extern __shared__ __align__(16) uint8_t dsmem[];
     uint32_t* s_tab = reinterpret_cast<uint32_t*>(dsmem + kSmemTab);
     const uint16_t* s_single = reinterpret_cast<const uint16_t*>(s_tab);
@@ -432,7 +444,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     const int n_active = (seq + p.tps - 1) / p.tps;
     const int n_clusters = (n_active + kCluster - 1) / kCluster;
     const int cid = split / kCluster;
-    // fused step: the CTA whose token range holds the new position appends
+    // Split s < n_active attends token range n_active - 1 - s (tokens
+    // tps r .. tps (r + 1) - 1 of range r).  CTAs start in split order, so
+    // the newest tokens, and in a fused step the append, go to the CTA that
+    // starts first.
+    // Fused step: the CTA whose token range holds the new position appends
     // the new token before attending (split 0 when the position is not
     // attended).  pos_new is read before the wait, like seq_lens.
     bool owner = false, pos_bad = false;
@@ -441,7 +457,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     if (p.k_new) {
         pos = p.pos_new[b];
         pos_bad = pos < 0 || (int64_t)pos + 1 > p.cap;
-        owner = !pos_bad && split == (pos < seq ? pos / p.tps : 0);
+        owner = !pos_bad && split == (pos < seq ? n_active - 1 - pos / p.tps : 0);
         if (owner) {
             stage_thresholds(s_thr, p.thr, tid, kWarps * 32);
             if (warp < 2) enc_lane_load(el, p.heads + h, warp == 0, BV, p.v_inv_sqrt, lane);
@@ -469,7 +485,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     const int crank = (int)cluster.block_rank();
     const bool active = split < n_active;
     const HeadTab* ht = p.heads + h;
-    const int t_begin = split * p.tps;
+    const int t_begin = active ? (n_active - 1 - split) * p.tps : seq;
     const int t_end = min(t_begin + p.tps, seq);
     const int wstart = p.recent > 0 ? max(0, seq - (int)p.recent) : seq;  // first position of the fp16 keys
     const uint8_t* kc = p.kc + unit * (size_t)p.cap * (16 * BK);
@@ -574,7 +590,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         // fp16 recent-key buffer: the query heads as given (fp16) as mma A
         // fragments, rows 0..7 = heads (rows 8..15 zero), k-chunk c = dims
         // 16c..16c+15; warp w builds chunks 2w, 2w + 1
-        if (kAnyWide && p.recent > 0 && t_end > wstart) {
+        if (kWinPath && p.recent > 0 && t_end > wstart) {
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 const int c = 2 * warp + k;
@@ -600,8 +616,30 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     const uint32_t vbase = BV <= kPrivMaxW ? kPrivByte + 4u * lane + ((1u << (2 * BV)) << 7) : (1u << (2 * BV)) << 2;
 
     // ---- main loop: 16-token tiles, operands of the next tile loaded while
-    // the current one is decoded (ping-pong register buffers)
-    auto process = [&](const TileRegs<BK, BV>& tr, int T0) {
+    // the current one is decoded (ping-pong register buffers).  kWin: the
+    // tile reaches into the fp16 recent-key buffer.
+    auto process = [&](const TileRegs<BK, BV>& tr, int T0, auto win) {
+        constexpr bool kWin = decltype(win)::value;
+        // recent-key buffer tile: its fp16 keys, as mma B fragments of ring
+        // slot pos mod W (token row g of 8-token group nt).  The fast
+        // instance fetches them first, so that the fetch overlaps the
+        // packed-key decode below; the general one (no registers to spare)
+        // right before use.
+        uint32_t kb[2][8][2];
+        auto load_kb = [&]() {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int tk = min(max(T0 + 8 * nt + g, wstart), seq - 1);
+                const uint32_t* kr = reinterpret_cast<const uint32_t*>(
+                    p.k_recent + (unit * (size_t)p.recent + (size_t)(tk % p.recent)) * kD + 2 * t);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    kb[nt][c][0] = __ldcg(kr + 8 * c);
+                    kb[nt][c][1] = __ldcg(kr + 8 * c + 4);
+                }
+            }
+        };
+        if constexpr (kWin && !kAnyWide) load_kb();
         float sacc[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.0f;
@@ -623,27 +661,20 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
                 const float v = (sacc[nt][e] + sacc[nt][2 + e]) * (tr.rk[nt][e] * q_unscale);
                 lg[nt][e] = tok < t_end ? v : -INFINITY;
             }
-        if (kAnyWide && p.recent > 0 && T0 + kTile > wstart) {
-            // (general instance only) the tile reaches into the fp16 recent-key buffer: those tokens'
-            // logits come from their exact keys (q as given . k, on the
-            // tensor cores; B fragments read from the ring slot pos mod W)
+        if constexpr (kWin) {
+            // the tokens of the tile inside the fp16 recent-key buffer take
+            // their logits from their exact keys (q as given . k, on the
+            // tensor cores)
+            if constexpr (kAnyWide) load_kb();
             float s16[2][4];
-            const __half* ring[2];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                s16[nt][0] = s16[nt][1] = s16[nt][2] = s16[nt][3] = 0.0f;
-                const int tk = min(max(T0 + 8 * nt + g, wstart), seq - 1);
-                ring[nt] = p.k_recent + (unit * (size_t)p.recent + (size_t)(tk % p.recent)) * kD + 2 * t;
-            }
+            for (int nt = 0; nt < 2; ++nt) s16[nt][0] = s16[nt][1] = s16[nt][2] = s16[nt][3] = 0.0f;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const uint2 a = s_qo[c][lane];
                 const uint32_t af[4] = {a.x, 0u, a.y, 0u};
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const uint32_t* kr = reinterpret_cast<const uint32_t*>(ring[nt] + 16 * c);
-                    mma16816(s16[nt], af, __ldcg(kr), __ldcg(kr + 4));
-                }
+                for (int nt = 0; nt < 2; ++nt) mma16816(s16[nt], af, kb[nt][c][0], kb[nt][c][1]);
             }
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
@@ -713,7 +744,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         if (k < n_tiles) stage_tile<BK, BV>(st_addr + k * SL::kBytes, kc, vc, kn, vn, T0w + k * kStep, seq, lane);
         cp_async_commit();
     }
-    for (int k = 0; k < n_tiles; ++k) {
+    auto step = [&](int k, auto win) {
         const int kn_ = k + kStages - 1;
         if (kn_ < n_tiles)
             stage_tile<BK, BV>(st_addr + (kn_ % kStages) * SL::kBytes, kc, vc, kn, vn, T0w + kn_ * kStep, seq, lane);
@@ -722,9 +753,19 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         __syncwarp();
         TileRegs<BK, BV> tr;
         tr.read(st_base + (k % kStages) * SL::kBytes, g, t);
-        process(tr, T0w + k * kStep);
+        process(tr, T0w + k * kStep, win);
         __syncwarp();  // the stage is refilled next
+    };
+    // the tiles that reach into the fp16 recent-key buffer are the warp's
+    // last few; the loop over the others carries no trace of the buffer
+    int n_fast = n_tiles;
+    if (kWinPath && p.recent > 0) {
+        const int d = wstart - kTile - T0w;
+        n_fast = d < 0 ? 0 : min(n_tiles, d / kStep + 1);
     }
+    for (int k = 0; k < n_fast; ++k) step(k, BoolTag<false>{});
+    if constexpr (kWinPath)
+        for (int k = n_fast; k < n_tiles; ++k) step(k, BoolTag<true>{});
     cp_async_wait<0>();
     }  // active
 
@@ -888,8 +929,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     cluster_wait();  // no CTA leaves while another may still read its partials
 }
 
-// The dynamic shared memory of both instances of decode_kernel<BK, BV> is
-// raised above the 48 KB default once per device.
+// The dynamic shared memory of the three instances of decode_kernel<BK, BV>
+// is raised above the 48 KB default once per device.
 template <int BK, int BV>
 cudaError_t ensure_smem_attr() {
     static std::mutex mu;
@@ -899,16 +940,19 @@ cudaError_t ensure_smem_attr() {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (done[dev]) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<BK, BV, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<BK, BV, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          decode_smem_bytes<BK, BV>());
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(decode_kernel<BK, BV, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(decode_kernel<BK, BV, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 decode_smem_bytes<BK, BV>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(decode_kernel<BK, BV, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  decode_smem_bytes<BK, BV>());
     if (e == cudaSuccess) done[dev] = true;
     return e;
 }
 
-template <int BK, int BV, bool kAnyWide>
+template <int BK, int BV>
 cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t s, cudaLaunchAttribute* attr /*[2]*/) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -927,16 +971,14 @@ cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t s, cudaLaunchAttribute*
 }
 
 template <int BK, int BV>
-cudaError_t launch_t(const DecodeParams& p, dim3 grid, cudaStream_t s, bool any_wide) {
+cudaError_t launch_t(const DecodeParams& p, dim3 grid, cudaStream_t s, int kind) {
     cudaError_t e = ensure_smem_attr<BK, BV>();
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[2];
-    if (any_wide) {
-        cudaLaunchConfig_t cfg = launch_config<BK, BV, true>(grid, s, attr);
-        return cudaLaunchKernelEx(&cfg, decode_kernel<BK, BV, true>, p);
-    }
-    cudaLaunchConfig_t cfg = launch_config<BK, BV, false>(grid, s, attr);
-    return cudaLaunchKernelEx(&cfg, decode_kernel<BK, BV, false>, p);
+    cudaLaunchConfig_t cfg = launch_config<BK, BV>(grid, s, attr);
+    if (kind == 2) return cudaLaunchKernelEx(&cfg, decode_kernel<BK, BV, 2>, p);
+    if (kind == 1) return cudaLaunchKernelEx(&cfg, decode_kernel<BK, BV, 1>, p);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<BK, BV, 0>, p);
 }
 
 // CTAs of decode_kernel<BK, BV> that can be resident at once, in whole
@@ -949,10 +991,10 @@ int resident_ctas() {
         return 0;
     }
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = launch_config<BK, BV, false>(dim3(kCluster, 1, 1), nullptr, attr);
+    cudaLaunchConfig_t cfg = launch_config<BK, BV>(dim3(kCluster, 1, 1), nullptr, attr);
     cfg.numAttrs = 1;  // occupancy: the cluster shape only
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, decode_kernel<BK, BV, false>, &cfg) != cudaSuccess || clusters <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, decode_kernel<BK, BV, 2>, &cfg) != cudaSuccess || clusters <= 0) {
         cudaGetLastError();
         return 0;
     }
@@ -1068,24 +1110,25 @@ cudaError_t launch_decode(const bgtq_plan& pl, cudaStream_t s, const void* q, co
     p.recent = c.recent;
     dim3 grid((unsigned)sp.n_split, (unsigned)pl.H, (unsigned)batch);
     // the fast instance checks only slots 0 and 8 (each lane's two widest
-    // pairs) for codes wider than the pair tables and has no recent-key
-    // buffer path; the general instance handles both
-    bool any_wide = c.recent > 0;
+    // pairs) for codes wider than the pair tables; the general instance
+    // checks every slot
+    bool any_wide = false;
     for (const HeadTab& ht : pl.heads) any_wide |= (ht.wide_mask & ~((1u << 0) | (1u << 8))) != 0;
+    const int kind = any_wide ? 2 : (c.recent > 0 ? 1 : 0);
     const int key = pl.bk * 10 + pl.bv;
     switch (key) {
-        case 11: return launch_t<1, 1>(p, grid, s, any_wide);
-        case 12: return launch_t<1, 2>(p, grid, s, any_wide);
-        case 13: return launch_t<1, 3>(p, grid, s, any_wide);
-        case 14: return launch_t<1, 4>(p, grid, s, any_wide);
-        case 21: return launch_t<2, 1>(p, grid, s, any_wide);
-        case 22: return launch_t<2, 2>(p, grid, s, any_wide);
-        case 23: return launch_t<2, 3>(p, grid, s, any_wide);
-        case 24: return launch_t<2, 4>(p, grid, s, any_wide);
-        case 31: return launch_t<3, 1>(p, grid, s, any_wide);
-        case 32: return launch_t<3, 2>(p, grid, s, any_wide);
-        case 33: return launch_t<3, 3>(p, grid, s, any_wide);
-        case 34: return launch_t<3, 4>(p, grid, s, any_wide);
+        case 11: return launch_t<1, 1>(p, grid, s, kind);
+        case 12: return launch_t<1, 2>(p, grid, s, kind);
+        case 13: return launch_t<1, 3>(p, grid, s, kind);
+        case 14: return launch_t<1, 4>(p, grid, s, kind);
+        case 21: return launch_t<2, 1>(p, grid, s, kind);
+        case 22: return launch_t<2, 2>(p, grid, s, kind);
+        case 23: return launch_t<2, 3>(p, grid, s, kind);
+        case 24: return launch_t<2, 4>(p, grid, s, kind);
+        case 31: return launch_t<3, 1>(p, grid, s, kind);
+        case 32: return launch_t<3, 2>(p, grid, s, kind);
+        case 33: return launch_t<3, 3>(p, grid, s, kind);
+        case 34: return launch_t<3, 4>(p, grid, s, kind);
         default: return cudaErrorInvalidValue;
     }
 }

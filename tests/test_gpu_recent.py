@@ -100,3 +100,33 @@ def test_recent_buffer_ragged_batch():
     got = decode(plan, cache, dev(q), dev(lens), T)
     for b in range(3):
         check_close(got[b], want_out(heads, li[b], q[b], int(lens[b]), G, W))
+
+
+@pytest.mark.parametrize("layout", ["uniform3", "wide8"])
+def test_recent_buffer_both_kernel_paths(layout):
+    """Explicit widths that fix which decode path runs: every block at 3 bits
+    (no code wider than the pair tables: the fast path) and 24 blocks at 8
+    bits with the rest at 0 (wide codes in many slots: the general path),
+    both at 384 bits per key."""
+    H, G, T, W, v_bits = 2, 8, 2500, 200, 3
+    li = synth.layer_inputs(808, 0, H, G, T, 1e5, 1.2)
+    energy = np.stack([bg.bgtq_alloc_bits(li.calib[h], 384)[1] for h in range(H)])
+    if layout == "uniform3":
+        bits = np.full((H, 64), 3, np.uint8)
+    else:
+        bits = np.zeros((H, 64), np.uint8)
+        bits[0, :24] = 8
+        bits[1, 40:] = 8
+    pseed = 0xA11CE
+    plan = bg.bgtq_plan_create(bits, energy, G, 384, v_bits, pseed)
+    cache = bg.Cache(plan, 1, T, recent=W)
+    heads = [O.HeadState(O.k_codec(bits[h].astype(np.int64), energy[h], pseed, h), O.v_codec(v_bits, pseed, h),
+                         bits[h].astype(np.int64), energy[h], 3, v_bits) for h in range(H)]
+    bg.bgtq_quantize_append(plan, dev(li.k[None]), dev(li.v[None]), dev(np.array([0], np.int32)), cache)
+    got = decode(plan, cache, dev(li.q[None]), dev(np.array([T], np.int32)), T)
+    check_close(got[0], want_out(heads, li, li.q, T, G, W))
+    # the same cache without the window path gives the packed-key result
+    plain = bg.Cache(plan, 1, T)
+    bg.bgtq_quantize_append(plan, dev(li.k[None]), dev(li.v[None]), dev(np.array([0], np.int32)), plain)
+    got0 = decode(plan, plain, dev(li.q[None]), dev(np.array([T], np.int32)), T)
+    check_close(got0[0], want_out(heads, li, li.q, T, G, 0))
