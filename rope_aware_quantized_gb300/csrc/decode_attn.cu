@@ -107,6 +107,15 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Ticket of the split merge: fetch-and-add with release (the CTA's partial,
+// ordered before it by a CTA barrier, is visible before the count moves) and
+// acquire (the last arriver then sees every other partial) at GPU scope.
+__device__ __forceinline__ unsigned ticket_acq_rel(unsigned* ptr) {
+    unsigned old;
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(ptr) : "memory");
+    return old;
+}
+
 // Bulk prefetch of [ptr, ptr + bytes) into L2 (16-byte aligned, multiple of 16).
 __device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(ptr), "r"(bytes) : "memory");
@@ -423,8 +432,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     __shared__ uint2 s_qo[8][32];                         // recent-key buffer: A fragments of q as given
     // after the main loop the table region holds the per-warp partials of
     // the 8 query heads (m, l, acc[128]) that the cluster reads
+    // and then the CTA's merged partial of the 8 heads
     float (*s_wp)[8][kPartStride] = reinterpret_cast<float (*)[8][kPartStride]>(s_tab);
-    static_assert(kWarps * 8 * kPartStride <= kImgWords, "partials fit in the table region");
+    float (*s_cp)[kPartStride] = reinterpret_cast<float (*)[kPartStride]>(s_tab + kWarps * 8 * kPartStride);
+    static_assert((kWarps + 1) * 8 * kPartStride <= kImgWords, "partials fit in the table region");
 
     // The next kernel may launch right away; everything this kernel reads
     // that an earlier kernel may still be writing (q, the cache, the
@@ -783,13 +794,45 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         s_wp[warp][g][2 + 16 * (2 * t + 1) + nd] = acc[nd][1] + acc[nd][3];
     }
 
+    // ---- CTA merge: thread tid merges query head tid / 16, dims
+    // 8 (tid % 16) .. + 7, over the 4 warps -> s_cp
+    static_assert(kWarps * 32 == 16 * 8, "CTA merge: 16 threads per head, 8 dims each");
+    __syncthreads();
+    {
+        const int hh = tid >> 4, d0 = 8 * (tid & 15);
+        float mw[kWarps], fw[kWarps];
+        float M = -INFINITY, L = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            mw[w] = s_wp[w][hh][0];
+            M = fmaxf(M, mw[w]);
+        }
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            fw[w] = mw[w] == -INFINITY ? 0.0f : exp2f(mw[w] - M);
+            L += s_wp[w][hh][1] * fw[w];
+        }
+        float o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            o[i] = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) o[i] += fw[w] * s_wp[w][hh][2 + d0 + i];
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s_cp[hh][2 + d0 + i] = o[i];
+        if ((tid & 15) == 0) {
+            s_cp[hh][0] = M;
+            s_cp[hh][1] = L;
+        }
+    }
+
     // ---- cluster merge: CTA rank r reduces query heads r, r + kCluster, ...
-    // over the kCluster * kWarps warp partials of the cluster, read through
-    // distributed shared memory (lane i of a warp takes the (m, l) of partials
-    // i, i + 32, ...; threads tid < 128 hold one dim of acc each)
-    constexpr int kParts = kCluster * kWarps;
-    constexpr int kPerLane = (kParts + 31) / 32;
+    // over the kCluster CTA partials of the cluster, read through distributed
+    // shared memory (lane c < kCluster takes the (m, l) of CTA c; thread tid
+    // holds dim tid of acc)
     constexpr int kHeadsPerCta = (8 + kCluster - 1) / kCluster;
+    static_assert(kCluster <= 32 && kWarps * 32 >= kD, "cluster merge layout");
     cluster.sync();
     const size_t max_clusters = (size_t)p.n_split / kCluster;
     float* cpart_base = p.part + unit * max_clusters * (size_t)G * kPartStride;
@@ -801,40 +844,26 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         Lc[j] = 0.0f;
         Oc[j] = 0.0f;
         if (hh >= G) continue;
-        float mi[kPerLane], li[kPerLane], fi[kPerLane];
-        float M = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < kPerLane; ++k) {
-            const int i = lane + 32 * k;
-            mi[k] = -INFINITY;
-            li[k] = 0.0f;
-            if (i < kParts) {
-                const float* src = cluster.map_shared_rank(&s_wp[i % kWarps][hh][0], i / kWarps);
-                mi[k] = src[0];
-                li[k] = src[1];
-            }
-            M = fmaxf(M, mi[k]);
+        float mi = -INFINITY, li = 0.0f;
+        if (lane < kCluster) {
+            const float* src = cluster.map_shared_rank(&s_cp[hh][0], lane);
+            mi = src[0];
+            li = src[1];
         }
+        float M = mi;
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float L = 0.0f;
-#pragma unroll
-        for (int k = 0; k < kPerLane; ++k) {
-            fi[k] = mi[k] == -INFINITY ? 0.0f : exp2f(mi[k] - M);
-            L += li[k] * fi[k];
-        }
+        const float fi = mi == -INFINITY ? 0.0f : exp2f(mi - M);
+        float L = li * fi;
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
         float O = 0.0f;
         if (tid < kD) {
-            const float* base[kCluster];
+            float x[kCluster];
 #pragma unroll
-            for (int c = 0; c < kCluster; ++c) base[c] = cluster.map_shared_rank(&s_wp[0][hh][2 + tid], c);
+            for (int c = 0; c < kCluster; ++c) x[c] = *cluster.map_shared_rank(&s_cp[hh][2 + tid], c);
 #pragma unroll
-            for (int i = 0; i < kParts; ++i) {
-                const float f = __shfl_sync(0xffffffffu, fi[i / 32], i % 32);
-                O += f * base[i / kWarps][(i % kWarps) * 8 * kPartStride];
-            }
+            for (int c = 0; c < kCluster; ++c) O += __shfl_sync(0xffffffffu, fi, c) * x[c];
         }
         Mc[j] = M;
         Lc[j] = L;
@@ -851,23 +880,22 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             dst[0] = Mc[j];
             dst[1] = Lc[j];
         }
-        __threadfence();
-        __syncthreads();
+        __syncthreads();  // the partial is written before thread 0 releases it
         if (tid == 0) {
-            const unsigned prev = atomicAdd(p.count + unit * G + r, 1u);
+            const unsigned prev = ticket_acq_rel(p.count + unit * G + r);
             s_last = (prev == (unsigned)(n_clusters - 1)) ? 1 : 0;
         }
-        __syncthreads();
+        __syncthreads();  // thread 0's acquire is ordered before warp 0's loads below
         if (!s_last || warp != 0) continue;
         // ---- last cluster partial of query head r: warp 0 merges all of
-        // them (lane holds dims lane + 32 i), 8 partials per batch of
+        // them (lane holds dims lane + 32 i), kBatch partials per batch of
         // independent loads, online rescaling between batches
-        __threadfence();
+        constexpr int kBatch = 16;
         float M = -INFINITY, L = 0.0f, O[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int c0 = 0; c0 < n_clusters; c0 += 8) {
-            float mc[8], lc[8], oc[8][4];
+        for (int c0 = 0; c0 < n_clusters; c0 += kBatch) {
+            float mc[kBatch], lc[kBatch], oc[kBatch][4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < kBatch; ++j) {
                 const int c = c0 + j;
                 mc[j] = -INFINITY;
                 lc[j] = 0.0f;
@@ -882,13 +910,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             }
             float Mn = M;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) Mn = fmaxf(Mn, mc[j]);
+            for (int j = 0; j < kBatch; ++j) Mn = fmaxf(Mn, mc[j]);
             const float a = M == -INFINITY ? 0.0f : exp2f(M - Mn);
             L *= a;
 #pragma unroll
             for (int i = 0; i < 4; ++i) O[i] *= a;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < kBatch; ++j) {
                 const float f = mc[j] == -INFINITY ? 0.0f : exp2f(mc[j] - Mn);
                 L += lc[j] * f;
 #pragma unroll
