@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--eager", action="store_true", help="launch without a CUDA graph (profiling)")
     ap.add_argument("--recent", type=int, default=0,
                     help="keep the last W keys of every sequence in an fp16 recent-key buffer as well")
+    ap.add_argument("--page-tokens", type=int, default=0,
+                    help="paged cache: pages of P tokens in a shuffled pool instead of contiguous rows")
     ap.add_argument("--two-call", action="store_true",
                     help="per layer bgtq_quantize_append + bgtq_decode_attn instead of the fused bgtq_decode_step")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
@@ -322,7 +324,7 @@ def run_gpu(args):
     out_all = torch.empty((L, B, w.n_q, 128), dtype=torch.float16, device="cuda")
     layers = []
     for l in range(L):
-        ls = workloads.build_layer(w, l, recent=args.recent)
+        ls = workloads.build_layer(w, l, recent=args.recent, page_tokens=args.page_tokens)
         q_all[l].copy_(ls.q)
         nk_all[l].copy_(ls.new_k)
         nv_all[l].copy_(ls.new_v)
@@ -469,6 +471,7 @@ def run_gpu(args):
                 "l2": "inputs larger than L2 (packed cache per step >> 129 MB L2), no flush",
                 "parallelism": f"replicas x{world}",
                 **({"recent_fp16_keys": args.recent} if args.recent else {}),
+                **({"page_tokens": args.page_tokens} if args.page_tokens else {}),
             },
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,

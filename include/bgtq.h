@@ -40,6 +40,10 @@
  *   v_codes [B][H][capacity/2][32*bV] bytes one V record per token pair
  *   k_norm, v_norm [B][H][capacity] float   per-token norms (side data)
  * with bK = bits_per_key / 128, bV = v_bits, capacity even.
+ * A paged cache (page_table != NULL in bgtq_cache) stores the same records in
+ * pools of pages of P tokens: the arrays above with [B] -> [n_pages] and
+ * capacity -> P, and sequence b's position pos in page page_table[b][pos / P]
+ * at row pos mod P.  Size the pools with bgtq_cache_bytes(plan, n_pages, P).
  */
 #ifndef BGTQ_H
 #define BGTQ_H
@@ -62,6 +66,8 @@ extern "C" {
 /* device status bits */
 #define BGTQ_STATUS_APPEND_CAPACITY 1 /* pos_start + t_new > capacity: that sequence was skipped */
 #define BGTQ_STATUS_SEQLEN_CAPACITY 2 /* seq_len > capacity or < 0: clamped */
+#define BGTQ_STATUS_PAGE_RANGE 4      /* a page_table entry outside [0, n_pages) was met: writes to that
+                                         page skipped, reads use page 0 (output unspecified) */
 
 /* plan flags */
 #define BGTQ_PLAN_HOST_ONLY 1 /* build the tables on the host only (inspection, no GPU needed) */
@@ -86,6 +92,17 @@ typedef struct {
      * none (k_recent may be NULL). */
     void* k_recent;   /* device, [B][H][recent][128] half, 16-byte aligned */
     int64_t recent;   /* W, 0 <= W <= capacity */
+    /* Optional paging (serving without a per-sequence reservation; NULL =
+     * contiguous, the fields below ignored).  page_table[b][i] is the pool
+     * page that holds positions i P .. i P + P - 1 of sequence b; a page
+     * that an append writes must not be mapped twice.
+     * page_table is read by the decode kernel before it waits for the previous
+     * kernel (like seq_lens): it must not be written by a kernel that triggers
+     * its dependents early.  capacity must equal max_pages * page_tokens. */
+    const int32_t* page_table; /* device, [B][max_pages] */
+    int64_t max_pages;         /* entries per row of page_table, >= 1 */
+    int64_t page_tokens;       /* P: a power of two, 16 <= P <= 2^20 */
+    int64_t n_pages;           /* pages in the pools, >= 1 */
 } bgtq_cache;
 
 /* Message of the last failure on this thread ("" if none).  Never NULL. */

@@ -22,6 +22,7 @@ HEAD_DIM = 128
 BGTQ_PLAN_HOST_ONLY = 1
 STATUS_APPEND_CAPACITY = 1
 STATUS_SEQLEN_CAPACITY = 2
+STATUS_PAGE_RANGE = 4
 
 
 class BgtqError(RuntimeError):
@@ -137,33 +138,58 @@ def bgtq_cache_bytes(plan: Plan, batch: int, capacity: int):
 
 
 class Cache:
-    """One layer's packed cache in caller-owned torch CUDA tensors."""
+    """One layer's packed cache in caller-owned torch CUDA tensors.
 
-    def __init__(self, plan: Plan, batch: int, capacity: int, device="cuda", recent: int = 0):
+    Contiguous (page_tokens = 0): [batch][H][capacity] records.  Paged
+    (page_tokens = P > 0): pools of n_pages pages of P tokens and a page table
+    [batch][capacity / P] (int32, device); by default n_pages = batch *
+    capacity / P and sequence b's page i is page b * (capacity / P) + i;
+    write `page_table` in place (its rows: pool page of each P positions,
+    -1 = unmapped) to map them otherwise."""
+
+    def __init__(self, plan: Plan, batch: int, capacity: int, device="cuda", recent: int = 0,
+                 page_tokens: int = 0, n_pages: int = 0):
         """recent = W > 0 adds an fp16 recent-key buffer of W keys per (sequence, KV head)."""
         import torch
         if capacity % 2:
             raise ValueError("capacity must be even")
-        kb, vb, nb = bgtq_cache_bytes(plan, batch, capacity)
-        self.batch, self.capacity, self.recent = batch, capacity, recent
+        self.batch, self.capacity, self.recent, self.page_tokens = batch, capacity, recent, page_tokens
+        self.page_table = None
+        if page_tokens:
+            if capacity % page_tokens:
+                raise ValueError("a paged cache needs capacity to be a multiple of page_tokens")
+            self.max_pages = capacity // page_tokens
+            self.n_pages = n_pages or batch * self.max_pages
+            kb, vb, nb = bgtq_cache_bytes(plan, self.n_pages, page_tokens)
+            ident = torch.arange(batch * self.max_pages, dtype=torch.int32, device=device)
+            self.page_table = torch.where(ident < self.n_pages, ident, torch.full_like(ident, -1))
+            self.page_table = self.page_table.view(batch, self.max_pages).contiguous()
+        else:
+            self.max_pages, self.n_pages = 0, 0
+            kb, vb, nb = bgtq_cache_bytes(plan, batch, capacity)
         self.k_codes = torch.zeros(kb, dtype=torch.uint8, device=device)
         self.v_codes = torch.zeros(vb, dtype=torch.uint8, device=device)
         self.k_norm = torch.zeros(nb // 4, dtype=torch.float32, device=device)
         self.v_norm = torch.zeros(nb // 4, dtype=torch.float32, device=device)
         rb = batch * plan.n_kv_heads * recent * HEAD_DIM * 2
         self.k_recent = torch.zeros(max(rb // 2, 8), dtype=torch.float16, device=device)
-        self.desc = BgtqCache(self.k_codes.data_ptr(), self.k_norm.data_ptr(), self.v_codes.data_ptr(),
-                              self.v_norm.data_ptr(), capacity, self.k_recent.data_ptr() if recent else None,
-                              recent)
+        self.desc = self._desc(0, 0, 0, 0, 0)
         self._per_seq = (kb // max(batch, 1), vb // max(batch, 1), nb // max(batch, 1), rb // max(batch, 1))
+
+    def _desc(self, ko, vo, no, ro, po) -> BgtqCache:
+        pt = self.page_table
+        return BgtqCache(self.k_codes.data_ptr() + ko, self.k_norm.data_ptr() + no, self.v_codes.data_ptr() + vo,
+                         self.v_norm.data_ptr() + no, self.capacity,
+                         self.k_recent.data_ptr() + ro if self.recent else None, self.recent,
+                         pt.data_ptr() + po if pt is not None else None, self.max_pages, self.page_tokens,
+                         self.n_pages)
 
     def sequence_view(self, b: int) -> "CacheView":
         """Descriptor of sequence b alone (batch 1), per the documented layout."""
         kb, vb, nb, rb = self._per_seq
-        return CacheView(BgtqCache(self.k_codes.data_ptr() + b * kb, self.k_norm.data_ptr() + b * nb,
-                                   self.v_codes.data_ptr() + b * vb, self.v_norm.data_ptr() + b * nb,
-                                   self.capacity, self.k_recent.data_ptr() + b * rb if self.recent else None,
-                                   self.recent), self.capacity)
+        if self.page_table is not None:  # same pools, row b of the page table
+            return CacheView(self._desc(0, 0, 0, b * rb, b * self.max_pages * 4), self.capacity)
+        return CacheView(self._desc(b * kb, b * vb, b * nb, b * rb, 0), self.capacity)
 
     def nbytes(self) -> int:
         return sum(t.numel() * t.element_size() for t in (self.k_codes, self.v_codes, self.k_norm, self.v_norm)) + \

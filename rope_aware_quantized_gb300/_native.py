@@ -16,7 +16,9 @@ _LIB = None
 
 class BgtqCache(C.Structure):
     _fields_ = [("k_codes", C.c_void_p), ("k_norm", C.c_void_p), ("v_codes", C.c_void_p),
-                ("v_norm", C.c_void_p), ("capacity", C.c_int64), ("k_recent", C.c_void_p), ("recent", C.c_int64)]
+                ("v_norm", C.c_void_p), ("capacity", C.c_int64), ("k_recent", C.c_void_p), ("recent", C.c_int64),
+                ("page_table", C.c_void_p), ("max_pages", C.c_int64), ("page_tokens", C.c_int64),
+                ("n_pages", C.c_int64)]
 
 
 class BgtqHeadTables(C.Structure):

@@ -26,6 +26,7 @@ SOURCES = [
     ("codec_bulk_k2.cu", ["--fmad=false"]),
     ("codec_bulk_k3.cu", ["--fmad=false"]),
     ("decode_attn.cu", []),
+    ("decode_attn_paged.cu", []),
     ("decode_attn_noalloc.cu", []),
     ("fidelity.cu", []),
 ]

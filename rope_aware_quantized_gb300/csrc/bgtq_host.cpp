@@ -6,6 +6,7 @@
 // gain, uniform TQ-MSE values, packed-cache serving path) and the paper
 // review §1 Key Terms / §3 Method & Key Results (TQ-MSE rotates then
 // quantises; the greedy uses the 4^-b distortion rate).
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -495,7 +496,7 @@ static int check_plan(const bgtq_plan* p) {
     return BGTQ_OK;
 }
 
-static int check_cache(const bgtq_plan* p, const bgtq_cache* c) {
+int check_cache(const bgtq_plan* p, const bgtq_cache* c) {
     if (!c || !c->k_codes || !c->k_norm || !c->v_codes || !c->v_norm)
         return set_error(BGTQ_ERR_INVALID_ARG, "cache descriptor or one of its buffers is NULL");
     if (c->capacity <= 0 || (c->capacity & 1)) return set_error(BGTQ_ERR_INVALID_ARG, "capacity must be even and > 0");
@@ -507,6 +508,18 @@ static int check_cache(const bgtq_plan* p, const bgtq_cache* c) {
         return set_error(BGTQ_ERR_INVALID_ARG, "recent must be in [0, capacity]");
     if (c->recent > 0 && (!c->k_recent || (reinterpret_cast<uintptr_t>(c->k_recent) & 15)))
         return set_error(BGTQ_ERR_INVALID_ARG, "k_recent must be a 16-byte aligned buffer when recent > 0");
+    if (c->page_table) {
+        const int64_t P = c->page_tokens;
+        if (P < 16 || P > (1 << 20) || (P & (P - 1)))
+            return set_error(BGTQ_ERR_INVALID_ARG, "page_tokens must be a power of two in [16, 2^20]");
+        if (c->max_pages < 1 || c->n_pages < 1 || c->n_pages > INT32_MAX)
+            return set_error(BGTQ_ERR_INVALID_ARG, "max_pages and n_pages must be >= 1 (n_pages < 2^31)");
+        if (c->capacity != c->max_pages * P)
+            return set_error(BGTQ_ERR_INVALID_ARG, "a paged cache needs capacity == max_pages * page_tokens");
+        if (reinterpret_cast<uintptr_t>(c->page_table) & 3)
+            return set_error(BGTQ_ERR_INVALID_ARG, "page_table must be 4-byte aligned");
+    }
+    if (c->capacity > INT32_MAX) return set_error(BGTQ_ERR_INVALID_ARG, "capacity must be < 2^31");
     (void)p;
     return BGTQ_OK;
 }
@@ -622,9 +635,10 @@ int bgtq_cache_bytes(const bgtq_plan* p, int batch, int64_t capacity, size_t* kb
 
 int bgtq_quantize_append(const bgtq_plan* p, void* stream, const void* k, const void* v, int batch, int t_new,
                          const int32_t* pos_start, const bgtq_cache* c, int32_t* status) {
-    int rc = check_plan(p);
+    // the descriptor first: its checks read no device memory
+    int rc = check_cache(p, c);
     if (rc) return rc;
-    if ((rc = check_cache(p, c))) return rc;
+    if ((rc = check_plan(p))) return rc;
     if (batch < 0 || t_new < 0) return set_error(BGTQ_ERR_INVALID_ARG, "batch and t_new must be >= 0");
     if (batch == 0 || t_new == 0) return BGTQ_OK;
     if (!k || !v || !pos_start) return set_error(BGTQ_ERR_INVALID_ARG, "NULL input pointer");

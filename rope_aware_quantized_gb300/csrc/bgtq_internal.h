@@ -77,6 +77,44 @@ struct DevTables {
     uint32_t* dec_image = nullptr;  // [kImgWords] decode shared-memory image
 };
 
+// Where the records of (sequence b, head h, position pos) live: token slot
+// (b H + h) capacity + pos of a contiguous cache, or (page H + h) P + pos mod P
+// of a paged one (page = page_table[b][pos / P]).  K record, norms: index
+// slot; V pair record of the pair holding pos: index slot / 2 (P and the
+// capacity are even, so a pair never straddles two pages).
+struct CacheMap {
+    const int32_t* page_table;  // [B][max_pages], nullptr: contiguous
+    int64_t cap;                // positions per sequence (capacity = max_pages * P when paged)
+    int64_t max_pages, n_pages;
+    int H, lp;                  // lp = log2 P (paged)
+#ifdef __CUDACC__
+    // -1 when the page_table entry is outside [0, n_pages)
+    __device__ __forceinline__ int64_t slot(int b, int h, int64_t pos) const {
+        if (!page_table) return ((int64_t)b * H + h) * cap + pos;
+        const int32_t pg = page_table[(int64_t)b * max_pages + (pos >> lp)];
+        if (pg < 0 || (int64_t)pg >= n_pages) return -1;
+        return (((int64_t)pg * H + h) << lp) + (pos & ((((int64_t)1) << lp) - 1));
+    }
+#endif
+};
+
+// Host checks of a cache descriptor (buffers, alignment, capacity, the
+// recent-key buffer, paging); sets the thread's error message.
+int check_cache(const bgtq_plan* p, const bgtq_cache* c);
+
+inline CacheMap make_cache_map(const bgtq_cache& c, int H) {
+    CacheMap m;
+    m.page_table = c.page_table;
+    m.cap = c.capacity;
+    m.max_pages = c.page_table ? c.max_pages : 1;
+    m.n_pages = c.page_table ? c.n_pages : 1;
+    m.H = H;
+    m.lp = 0;
+    if (c.page_table)
+        while (((int64_t)1 << m.lp) < c.page_tokens) ++m.lp;
+    return m;
+}
+
 }  // namespace bgtq
 
 struct bgtq_plan {

@@ -95,9 +95,14 @@ __global__ void __launch_bounds__(128) quantize_append_kernel(QParams p) {
             for (int n = 0; n < 2; ++n) {
                 if (!has[n]) continue;
                 const int64_t pos = 2 * (P0 + i + n) + warp;
-                uint32_t* dst = reinterpret_cast<uint32_t*>(p.kc + (unit * p.cap + pos) * (16 * p.bk));
+                const int64_t sl = p.map.slot(b, h, pos);
+                if (sl < 0) {
+                    if (lane == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_PAGE_RANGE);
+                    continue;
+                }
+                uint32_t* dst = reinterpret_cast<uint32_t*>(p.kc + sl * (16 * p.bk));
                 if (lane < krec_words) dst[lane] = rec[warp][n][lane];
-                if (lane == 0) p.kn[unit * p.cap + pos] = rho[n];
+                if (lane == 0) p.kn[sl] = rho[n];
                 if (p.recent > 0 && pos >= end - p.recent) {
                     // fp16 recent-key ring: the key as given, slot pos mod W
                     const uint2 nat = *(reinterpret_cast<const uint2*>(p.k + (unit * p.t_new + (size_t)(pos - ps)) * kD) + lane);
@@ -153,15 +158,17 @@ __global__ void __launch_bounds__(128) quantize_append_kernel(QParams p) {
         int code[2][4];
         float rho[2];
         warp_encode_n<2>(x, el.sg, el.pl, el.is, el.wd, kD, s_thr, code, rho);
+        const int64_t sl0 = p.map.slot(b, h, pos0);  // the pair's page (pos0 even)
+        if (sl0 < 0 && lane == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_PAGE_RANGE);
 #pragma unroll
         for (int par = 0; par < 2; ++par) {
             if (!has[par]) continue;
             pack_v_fields(vrec, vmask, code[par], par, p.bv, lane);
-            if (lane == 0) p.vn[unit * p.cap + pos0 + par] = rho[par];
+            if (lane == 0 && sl0 >= 0) p.vn[sl0 + par] = rho[par];
         }
         __syncwarp();
-        uint32_t* vdst = reinterpret_cast<uint32_t*>(p.vc + (unit * (p.cap / 2) + P) * (32 * p.bv));
-        for (int k = lane; k < vrec_words; k += 32) {
+        uint32_t* vdst = reinterpret_cast<uint32_t*>(p.vc + (sl0 >> 1) * (32 * p.bv));
+        for (int k = lane; k < vrec_words && sl0 >= 0; k += 32) {
             if (has[0] && has[1]) {
                 vdst[k] = vrec[k];
             } else {
@@ -182,7 +189,8 @@ struct DqParams {
     const uint8_t* vc;
     const float* vn;
     int64_t cap, t0, t1;
-    size_t unit;
+    CacheMap map;
+    int b, h;
     const HeadTab* ht;
     const float* cent;
     int bk, bv;
@@ -199,11 +207,13 @@ __global__ void __launch_bounds__(128) dequant_kernel(DqParams p) {
     if (t >= p.t1) return;
     const HeadTab* ht = p.ht;
     const int64_t row = t - p.t0;
+    int64_t sl = p.map.slot(p.b, p.h, t);
+    if (sl < 0) sl = 0;  // page index out of range: unspecified output
     if (p.k_out) {
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(p.kc + (p.unit * p.cap + t) * (16 * p.bk));
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(p.kc + sl * (16 * p.bk));
         if (lane < 4 * p.bk) rec[warp][lane] = src[lane];
         __syncwarp();
-        const float rho = p.kn[p.unit * p.cap + t];
+        const float rho = p.kn[sl];
         const int n_coded = ht->n_coded;
         float y[4];
         int pl[4];
@@ -247,10 +257,10 @@ __global__ void __launch_bounds__(128) dequant_kernel(DqParams p) {
         __syncwarp();
     }
     if (p.v_out) {
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(p.vc + (p.unit * (p.cap / 2) + (t >> 1)) * (32 * p.bv));
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(p.vc + (sl >> 1) * (32 * p.bv));
         for (int i = lane; i < 8 * p.bv; i += 32) rec[warp][i] = src[i];
         __syncwarp();
-        const float rho = p.vn[p.unit * p.cap + t];
+        const float rho = p.vn[sl];
         const int par = (int)(t & 1);
         float y[4];
         int pl[4];
@@ -297,6 +307,7 @@ cudaError_t launch_quantize_append(const bgtq_plan& pl, cudaStream_t s, const vo
     p.vc = static_cast<uint8_t*>(c.v_codes);
     p.vn = c.v_norm;
     p.cap = c.capacity;
+    p.map = make_cache_map(c, pl.H);
     p.heads = pl.dev.heads;
     p.thr = pl.dev.thr;
     p.bk = pl.bk;
@@ -336,7 +347,9 @@ cudaError_t launch_dequant(const bgtq_plan& pl, cudaStream_t s, const bgtq_cache
     p.cap = c.capacity;
     p.t0 = t0;
     p.t1 = t1;
-    p.unit = (size_t)b * pl.H + head;
+    p.map = make_cache_map(c, pl.H);
+    p.b = b;
+    p.h = head;
     p.ht = pl.dev.heads + head;
     p.cent = pl.dev.cent;
     p.bk = pl.bk;

@@ -155,6 +155,8 @@ __global__ void __launch_bounds__(kBulkTok) quantize_append_bulk_kernel(QParams 
     const int64_t pos = (int64_t)(ps & ~1) + (int64_t)blockIdx.x * kBulkTok + tid;
     const bool act = pos >= ps && pos < end;
     const size_t unit = (size_t)b * p.H + h;
+    const int64_t sl = act ? p.map.slot(b, h, pos) : 0;  // record location of token `pos`
+    if (sl < 0 && p.status) atomicOr(p.status, BGTQ_STATUS_PAGE_RANGE);
 
     // ---- key of token `pos`
     if (act) {
@@ -195,10 +197,12 @@ __global__ void __launch_bounds__(kBulkTok) quantize_append_bulk_kernel(QParams 
             rec[wi] |= field << sh;
             if (sh + 2 * w > 32) rec[wi + 1] |= field >> (32 - sh);
         }
-        uint4* dst = reinterpret_cast<uint4*>(p.kc + (unit * p.cap + pos) * (16 * BK));
+        if (sl >= 0) {
+            uint4* dst = reinterpret_cast<uint4*>(p.kc + sl * (16 * BK));
 #pragma unroll
-        for (int i = 0; i < BK; ++i) dst[i] = make_uint4(rec[4 * i], rec[4 * i + 1], rec[4 * i + 2], rec[4 * i + 3]);
-        p.kn[unit * p.cap + pos] = rho;
+            for (int i = 0; i < BK; ++i) dst[i] = make_uint4(rec[4 * i], rec[4 * i + 1], rec[4 * i + 2], rec[4 * i + 3]);
+            p.kn[sl] = rho;
+        }
     }
 
     // ---- value of token `pos`: the thread pair (even, odd) shares a record
@@ -245,14 +249,14 @@ __global__ void __launch_bounds__(kBulkTok) quantize_append_bulk_kernel(QParams 
 #pragma unroll
             for (int i = kW - 1; i >= 0; --i) vw[i] = (vw[i] << BV) | (i ? vw[i - 1] >> (32 - BV) : 0u);
         }
-        p.vn[unit * p.cap + pos] = rho_v;
+        if (sl >= 0) p.vn[sl] = rho_v;
     }
     const bool partner = (pos ^ 1) >= ps && (pos ^ 1) < end;
     uint32_t full[kW];
 #pragma unroll
     for (int i = 0; i < kW; ++i) full[i] = vw[i] | __shfl_xor_sync(0xffffffffu, vw[i], 1);
-    if (!act) return;
-    uint32_t* vdst = reinterpret_cast<uint32_t*>(p.vc + (unit * (p.cap / 2) + (pos >> 1)) * (32 * BV));
+    if (!act || sl < 0) return;
+    uint32_t* vdst = reinterpret_cast<uint32_t*>(p.vc + (sl >> 1) * (32 * BV));
     if (partner) {
         // the pair is complete: the even thread stores the first half, the odd the second
         uint4* d4 = reinterpret_cast<uint4*>(vdst + par * (kW / 2));

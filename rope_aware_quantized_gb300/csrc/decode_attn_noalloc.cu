@@ -63,17 +63,7 @@ extern "C" int bgtq_decode_attn_noalloc(const bgtq_plan* p, void* stream, const 
                                         int out_dtype, float scale, int32_t* status) {
     if (!p) return set_error(BGTQ_ERR_INVALID_ARG, "plan is NULL");
     if (p->flags & BGTQ_PLAN_HOST_ONLY) return set_error(BGTQ_ERR_INVALID_ARG, "plan was built host-only");
-    if (!c || !c->k_codes || !c->k_norm || !c->v_codes || !c->v_norm)
-        return set_error(BGTQ_ERR_INVALID_ARG, "cache descriptor or one of its buffers is NULL");
-    if (c->capacity <= 0 || (c->capacity & 1)) return set_error(BGTQ_ERR_INVALID_ARG, "capacity must be even and > 0");
-    if ((reinterpret_cast<uintptr_t>(c->k_codes) & 15) || (reinterpret_cast<uintptr_t>(c->v_codes) & 15))
-        return set_error(BGTQ_ERR_INVALID_ARG, "k_codes and v_codes must be 16-byte aligned");
-    if ((reinterpret_cast<uintptr_t>(c->k_norm) & 3) || (reinterpret_cast<uintptr_t>(c->v_norm) & 3))
-        return set_error(BGTQ_ERR_INVALID_ARG, "k_norm and v_norm must be 4-byte aligned");
-    if (c->recent < 0 || c->recent > c->capacity)
-        return set_error(BGTQ_ERR_INVALID_ARG, "recent must be in [0, capacity]");
-    if (c->recent > 0 && (!c->k_recent || (reinterpret_cast<uintptr_t>(c->k_recent) & 15)))
-        return set_error(BGTQ_ERR_INVALID_ARG, "k_recent must be a 16-byte aligned buffer when recent > 0");
+    if (int rc = check_cache(p, c)) return rc;
     if (batch < 0 || max_len < 0) return set_error(BGTQ_ERR_INVALID_ARG, "batch and max_len must be >= 0");
     if (batch == 0) return BGTQ_OK;
     if (!q || !seq_lens || !out) return set_error(BGTQ_ERR_INVALID_ARG, "NULL pointer");

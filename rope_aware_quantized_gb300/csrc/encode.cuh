@@ -26,7 +26,8 @@ struct QParams {
     float* kn;
     uint8_t* vc;
     float* vn;
-    int64_t cap;
+    int64_t cap;       // positions per sequence
+    CacheMap map;      // record location of (sequence, head, position)
     const HeadTab* heads;
     const float* thr;
     int bk, bv;

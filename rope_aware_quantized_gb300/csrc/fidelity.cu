@@ -28,6 +28,7 @@ struct MaeParams {
     const uint8_t* kc;  // K records of the cache
     const float* kn;    // key norms of the cache
     int64_t cap, t;
+    CacheMap map;
     int H, G, bk;
     const HeadTab* heads;
     const float* cent;  // [9][256] centroids (fp16-exact values)
@@ -108,9 +109,11 @@ __global__ void __launch_bounds__(kMaeWarps * 32) logit_mae_kernel(MaeParams p) 
     for (int it = 0; it < kMaeTokPerWarp; ++it) {
         const int64_t tok = t0 + it;
         if (tok >= p.t) break;
-        const uint32_t* rsrc = reinterpret_cast<const uint32_t*>(p.kc + (unit * p.cap + tok) * (16 * p.bk));
+        int64_t sl = p.map.slot(b, h, tok);
+        if (sl < 0) sl = 0;  // page index out of range: unspecified result
+        const uint32_t* rsrc = reinterpret_cast<const uint32_t*>(p.kc + sl * (16 * p.bk));
         if (lane < rec_words) s_rec[warp][lane] = rsrc[lane];
-        const float rho = p.kn[unit * p.cap + tok];
+        const float rho = p.kn[sl];
         const uint2 kr = *(reinterpret_cast<const uint2*>(p.k + (unit * p.t + tok) * kD) + lane);
         __syncwarp();
         float y[4];
@@ -165,6 +168,7 @@ cudaError_t launch_logit_mae(const bgtq_plan& pl, cudaStream_t s, const void* q,
     p.kc = static_cast<const uint8_t*>(c.k_codes);
     p.kn = c.k_norm;
     p.cap = c.capacity;
+    p.map = make_cache_map(c, pl.H);
     p.t = t;
     p.H = pl.H;
     p.G = pl.G;

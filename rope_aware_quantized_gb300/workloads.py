@@ -71,17 +71,22 @@ class LayerState:
 
 
 def build_layer(w: Workload, layer: int, device="cuda", keep_host=(), capacity: int | None = None,
-                prefill_chunk: int = 1 << 16, recent: int = 0) -> LayerState:
+                prefill_chunk: int = 1 << 16, recent: int = 0, page_tokens: int = 0) -> LayerState:
     """Calibrate, plan, allocate and prefill one layer.
 
     Each sequence b holds tokens 0 .. len_b - 2 after the prefill; the decode
     step appends token len_b - 1 (the "new" token) and attends over len_b.
     `keep_host` lists (sequence, KV head) pairs whose full fp16 K/V are
     copied back to host memory, for checks against an independent model.
+    page_tokens = P > 0 builds a paged cache whose page table is a seeded
+    random permutation of the pool (no two neighbouring pages adjacent in
+    memory by construction).
     """
     import torch
     lens = w.seq_lens()
     cap = capacity or int(((lens.max() + 1) // 2) * 2)
+    if page_tokens:
+        cap = -(-cap // page_tokens) * page_tokens
     qpos = lens - 1
     bits, energy = [], []
     for h in range(w.n_kv):
@@ -89,7 +94,10 @@ def build_layer(w: Workload, layer: int, device="cuda", keep_host=(), capacity: 
         bits.append(b)
         energy.append(e)
     plan = bgtq_plan_create(np.stack(bits), np.stack(energy), w.group, w.bits_per_key, w.v_bits, plan_seed(w, layer))
-    cache = Cache(plan, w.batch, cap, device, recent=recent)
+    cache = Cache(plan, w.batch, cap, device, recent=recent, page_tokens=page_tokens)
+    if page_tokens:
+        perm = np.random.default_rng([w.seed, layer, 0x9A6E]).permutation(cache.n_pages).astype(np.int32)
+        cache.page_table.copy_(torch.from_numpy(perm.reshape(w.batch, cache.max_pages)).to(device))
     q = torch.empty((w.batch, w.n_q, 128), dtype=torch.float16, device=device)
     new_k = torch.empty((w.batch, w.n_kv, 1, 128), dtype=torch.float16, device=device)
     new_v = torch.empty_like(new_k)
