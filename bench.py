@@ -222,14 +222,14 @@ def traffic_from_profile():
     the current decode kernel source."""
     if not os.path.exists(PROFILE_SUMMARY):
         return None
-    src = os.path.join(ROOT, "rope_aware_quantized_gb300", "csrc", "decode_attn.cu")
+    src = os.path.join(ROOT, "rope_aware_quantized_gb300", "csrc", "decode_kernel.cuh")
     sha = code_digest(src)
     vals = {}
     for line in open(PROFILE_SUMMARY):
         if ":" in line:
             k, v = line.split(":", 1)
             vals[k.strip()] = v.strip()
-    if (vals.get("decode_attn.cu code sha256 prefix", "").split() or [""])[0] != sha:
+    if (vals.get("decode_kernel.cuh code sha256 prefix", "").split() or [""])[0] != sha:
         return None
     try:
         return float(vals["dram bytes per launch"])

@@ -544,15 +544,27 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     const float* vn = p.vn + ubase;
     // token slot of the tile at position T0 (16-token tiles never straddle a
     // page; an out-of-range page index is flagged and page 0 read instead)
+    // (no branch on the page index: the prologue flags bad ones, so the
+    // page-table load can be issued a tile ahead of its use)
     auto tile_slot = [&](int T0) -> int64_t {
         if constexpr (!kPaged) return T0;
-        int64_t sl = p.map.slot(b, h, T0);
-        if (sl < 0) {
-            if (lane == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_PAGE_RANGE);
-            sl = ((int64_t)h << p.map.lp) + (T0 & ((1 << p.map.lp) - 1));
-        }
-        return sl;
+        const int64_t sl = p.map.slot(b, h, T0);
+        return sl >= 0 ? sl : ((int64_t)h << p.map.lp) + (T0 & ((1 << p.map.lp) - 1));
     };
+    // warp w takes tiles T0 = t_begin + 16 w + kStep k; kStages - 1 of them are
+    // being copied while one is processed
+    constexpr int kStep = kWarps * kTile;
+    const int T0w = t_begin + warp * kTile;
+    const int n_tiles = active && T0w < t_end ? (t_end - T0w + kStep - 1) / kStep : 0;
+    // paged: token slots of the first kStages tiles and of the new token,
+    // looked up before the wait (the page table is read like seq_lens)
+    int64_t sl_pre[kStages];
+    int64_t sl_new = 0;
+    if constexpr (kPaged) {
+#pragma unroll
+        for (int k = 0; k < kStages; ++k) sl_pre[k] = k < n_tiles ? tile_slot(T0w + k * kStep) : 0;
+        if (owner) sl_new = p.map.slot(b, h, pos);
+    }
 
     // ---- plan-static set-up, before waiting for the previous kernel: L2
     // prefetch of the token range, the table image, the per-lane recipes
@@ -577,7 +589,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             const int a = (int)max((int64_t)t_begin, (int64_t)pi << lp);
             const int e = (int)min((int64_t)t_end, (int64_t)(pi + 1) << lp);
             const int64_t sl = p.map.slot(b, h, a);
-            if (sl < 0) continue;
+            if (sl < 0) {
+                if (p.status) atomicOr(p.status, BGTQ_STATUS_PAGE_RANGE);
+                continue;
+            }
             prefetch_span(reinterpret_cast<const char*>(kc + sl * (16 * BK)), (size_t)(e - a) * (16 * BK));
             prefetch_span(reinterpret_cast<const char*>(vc + (sl >> 1) * (32 * BV)), (size_t)((e - a + 1) / 2) * (32 * BV));
             prefetch_span(reinterpret_cast<const char*>(kn + sl), (size_t)(e - a) * 4);
@@ -622,7 +637,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     pdl_wait();  // q, the cache and the workspace may belong to the previous kernel
     if (pos_bad && split == 0 && h == 0 && tid == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_APPEND_CAPACITY);
     if (owner) {
-        const int64_t sl = new_token_slot(p, b, h, pos);
+        int64_t sl;
+        if constexpr (kPaged) {
+            sl = sl_new;
+            if (sl < 0 && tid == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_PAGE_RANGE);
+        } else {
+            sl = p.map.slot(b, h, pos);
+        }
         if (sl >= 0) append_new_token<BK, BV>(p, el, unit, sl, pos, s_thr, s_enc, warp, lane);
     }
     float m_ref = -INFINITY, l_run = 0.0f;  // softmax reference (see kLift, kSlack), sum
@@ -812,27 +833,32 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         pv_tile<BV, 15>(acc, pa, tr.vw, vbase, s_tab);
     };
 
-    // warp w takes tiles T0 = t_begin + 16 w + kStep k; kStages - 1 of them are
-    // being copied while one is processed
-    constexpr int kStep = kWarps * kTile;
     using SL = StageLayout<BK, BV>;
-    const int T0w = t_begin + warp * kTile;
-    const int n_tiles = T0w < t_end ? (t_end - T0w + kStep - 1) / kStep : 0;
     uint8_t* st_base = dsmem + kSmemStage + warp * (kStages * SL::kBytes);
     const uint32_t st_addr = (uint32_t)__cvta_generic_to_shared(st_base);
 #pragma unroll
     for (int k = 0; k < kStages - 1; ++k) {
         if (k < n_tiles) {
             const int T0 = T0w + k * kStep;
-            stage_tile<BK, BV>(st_addr + k * SL::kBytes, kc, vc, kn, vn, tile_slot(T0), T0, seq, lane);
+            stage_tile<BK, BV>(st_addr + k * SL::kBytes, kc, vc, kn, vn, kPaged ? sl_pre[k] : tile_slot(T0), T0, seq,
+                               lane);
         }
         cp_async_commit();
     }
+    // paged: the token slot of the next tile to stage, looked up one step early
+    int64_t sl_next = 0;
+    if constexpr (kPaged) sl_next = sl_pre[kStages - 1];
     auto step = [&](int k, auto win) {
         const int kn_ = k + kStages - 1;
         if (kn_ < n_tiles) {
             const int T0 = T0w + kn_ * kStep;
-            stage_tile<BK, BV>(st_addr + (kn_ % kStages) * SL::kBytes, kc, vc, kn, vn, tile_slot(T0), T0, seq, lane);
+            if constexpr (kPaged) {
+                stage_tile<BK, BV>(st_addr + (kn_ % kStages) * SL::kBytes, kc, vc, kn, vn, sl_next, T0, seq, lane);
+                if (kn_ + 1 < n_tiles) sl_next = tile_slot(T0 + kStep);
+            } else {
+                stage_tile<BK, BV>(st_addr + (kn_ % kStages) * SL::kBytes, kc, vc, kn, vn, tile_slot(T0), T0, seq,
+                                   lane);
+            }
         }
         cp_async_commit();
         cp_async_wait<kStages - 1>();
