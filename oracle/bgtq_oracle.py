@@ -21,9 +21,9 @@ distortion rate; Block-GTQ scores each (layer, KV head, block) with a
 label-free energy from calibration data and greedily gives integer bit widths
 by marginal gain under the TQ-MSE 4^-b rate; values use uniform TQ-MSE; the
 packed-cache path attends directly on compressed K/V.  Everything the pages
-leave open (energy formula, codebook, rotation, norm, packing) follows the
-readings listed in DESIGN.md ("Readings of the pages"); each function below
-names the reading it implements.
+leave open (energy formula, codebook, rotation, norm, packing) is settled by a
+numbered reading (R1, R2, ...); each function below names and states the
+reading it implements.
 
 Floating point.  Allocation and codebook design are float64.  The encoder
 and decoder are float32, one IEEE operation at a time in a fixed order
@@ -656,3 +656,33 @@ def keys_with_recent(khat: np.ndarray, k_fp16: np.ndarray, w: int) -> np.ndarray
 def attention_recent(q_fp16, khat, vhat, k_fp16, w: int, scale: float = 1.0 / math.sqrt(D)):
     """Decode attention over the packed cache with an fp16 recent-key buffer of w keys."""
     return attention(q_fp16, keys_with_recent(khat, k_fp16, w), vhat, scale)
+
+
+# =============================================================================
+# Prefill attention fused with quantize (the method's next step before the
+# decode path: attend over the prompt's fp16 tiles while its packed codes are
+# written).  Reading R21: a prefill of T tokens into an empty cache writes the
+# packed records of positions 0 .. T-1 with the encoder of readings R8-R13,
+# unchanged, and returns causal attention over the tokens as given: query row
+# i attends keys 0 .. i with the fp16 keys and values, float64 softmax, the
+# query heads of a KV head sharing its keys (reading R15).
+# =============================================================================
+
+
+def prefill_attention(q_fp16, k_fp16, v_fp16, scale: float = 1.0 / math.sqrt(D), rows: int = 256):
+    """q [G][T][128], k, v [T][128] (fp16) -> [G][T][128] float64:
+    out[g][i] = sum_{j <= i} softmax_j(scale q[g][i] . k[j]) v[j]."""
+    q = np.asarray(q_fp16, dtype=np.float16).astype(np.float64)
+    k = np.asarray(k_fp16, dtype=np.float16).astype(np.float64)
+    v = np.asarray(v_fp16, dtype=np.float16).astype(np.float64)
+    G, T = q.shape[0], q.shape[1]
+    out = np.zeros((G, T, D))
+    for r0 in range(0, T, rows):
+        r1 = min(T, r0 + rows)
+        s = np.einsum("gid,jd->gij", q[:, r0:r1], k[:r1]) * scale
+        causal = np.arange(r1)[None, :] <= np.arange(r0, r1)[:, None]
+        s = np.where(causal[None], s, -np.inf)
+        s = s - s.max(axis=2, keepdims=True)
+        p = np.exp(s)
+        out[:, r0:r1] = np.einsum("gij,jd->gid", p, v[:r1]) / p.sum(axis=2, keepdims=True)
+    return out
