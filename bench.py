@@ -298,6 +298,47 @@ def measure_prefill(w, plan, tokens: int, peaks: dict, stream) -> dict:
             "bytes": "fp16 K and V rows read + packed K/V records and both norms written"}
 
 
+def measure_prefill_attn(w, plan, tokens: int, peaks: dict, stream) -> dict:
+    """The fused prefill (bgtq_prefill_attn: causal attention over the
+    prompt's fp16 K/V plus the packed records of the prompt) on one layer of
+    the workload's shape: `tokens` positions per sequence, fp16 output.
+    Algorithmic work: 4 * 128 flops per (query head, query row, key) pair of
+    the causal triangle (Q K^T and P V)."""
+    import torch
+
+    import rope_aware_quantized_gb300 as bg
+
+    B, H, Hq = w.batch, w.n_kv, w.n_q
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(20261)
+    q = torch.randn((B, Hq, tokens, 128), generator=gen, device="cuda").half()
+    k = torch.randn((B, H, tokens, 128), generator=gen, device="cuda").half()
+    v = torch.randn((B, H, tokens, 128), generator=gen, device="cuda").half()
+    out = torch.empty_like(q)
+    cache = bg.Cache(plan, B, tokens + (tokens & 1))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(6):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            bg.bgtq_prefill_attn(plan, q, k, v, cache, out, status=status)
+            b.record(stream)
+            times.append((a, b))
+    torch.cuda.synchronize()
+    assert status.item() == 0, f"prefill status {status.item()}"
+    ms = statistics.median(a.elapsed_time(b) for a, b in times[2:])
+    flops = 4.0 * 128 * B * Hq * tokens * (tokens + 1) / 2
+    tf = flops / (ms / 1000.0) / 1e12
+    del q, k, v, out, cache
+    return {"tokens": tokens, "batch": B, "query_heads": Hq, "kv_heads": H, "ms_per_launch": ms,
+            "tokens_per_s": B * tokens / (ms / 1000.0), "achieved": tf, "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"], "bound": "tensor",
+            "flops": "4 * 128 per (query head, row, key <= row): causal Q K^T and P V; fp16 mma.sync, fp32 accumulate",
+            "peak_note": "measured dense bf16 (burst); fp16 has the same nominal tensor rate"}
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -421,6 +462,7 @@ def run_gpu(args):
     step_bytes = L * decode_bytes
 
     prefill = measure_prefill(w, layers[0].plan, max_len, peaks, stream)
+    prefill_attn = measure_prefill_attn(w, layers[0].plan, min(max_len, 32768), peaks, stream)
 
     # end to end: pinned host inputs -> device, graph replay, outputs -> host
     hq = torch.empty(q_all.shape, dtype=q_all.dtype, pin_memory=True)
@@ -484,6 +526,7 @@ def run_gpu(args):
             "achieved_step_gbs": step_bytes / (ms / 1000.0) / 1e9,
         }
         line["append_prefill"] = prefill
+        line["prefill_attn"] = prefill_attn
         if cpu:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)

@@ -272,6 +272,34 @@ int bgtq_decode_step(const bgtq_plan* plan, void* stream, const void* q_fp16, co
                      float softmax_scale, void* workspace, size_t ws_bytes, int32_t* dev_status);
 
 /*
+ * bgtq_prefill_attn — prefill of a prompt into an empty cache in one launch:
+ * causal attention over the prompt's own fp16 K/V, and the packed records of
+ * positions 0 .. t-1 written to the cache.
+ * Source: the packed cache is written at prefill and read at decode (review
+ * §1 "Packed-Cache"); fusing the quantizer into attention is named as future
+ * work on the LogQuant page (section "중요성 및 주장").
+ *   q_fp16       device, [batch][H*G][t][128] half, RoPE applied, 16-byte aligned
+ *   k_fp16, v_fp16  device, [batch][H][t][128] half, 16-byte aligned
+ *   t            prompt length, 0 <= t <= capacity
+ *   cache        host pointer to the layer's cache descriptor (contiguous or
+ *                paged; with a recent-key buffer its last W keys are copied too)
+ *   out          device, [batch][H*G][t][128], half (out_dtype 0) or float (1),
+ *                8-byte aligned
+ *   softmax_scale  logit scale, e.g. 1/sqrt(128)
+ *   dev_status   device int32 or NULL
+ * Row i of query head g computes sum_{j <= i} softmax_j(scale q_i . k_j) v_j
+ * with the keys and values as given (fp16 tensor-core products, fp32
+ * accumulation, probabilities rounded to fp16); the records are those
+ * bgtq_quantize_append writes for the same tokens at pos_start = 0, bit for
+ * bit.  Prefill onto a non-empty cache (a later chunk) is not covered.
+ * Errors: INVALID_ARG (pointers, alignment, dtype, scale), CAPACITY (t >
+ * capacity), CUDA.
+ */
+int bgtq_prefill_attn(const bgtq_plan* plan, void* stream, const void* q_fp16, const void* k_fp16,
+                      const void* v_fp16, int batch, int t, const bgtq_cache* cache, void* out, int out_dtype,
+                      float softmax_scale, int32_t* dev_status);
+
+/*
  * bgtq_decode_attn_noalloc — bgtq_decode_attn for callers that cannot
  * allocate device memory (a fixed memory budget, an allocator or pool that
  * must not be bypassed, a host runtime without a device allocator).  The

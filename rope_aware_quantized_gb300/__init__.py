@@ -293,6 +293,30 @@ def bgtq_logit_mae(plan: Plan, q_fp16, k_fp16, cache, t: int, out, softmax_scale
                                 batch, scale, _ptr(out)))
 
 
+def bgtq_prefill_attn(plan: Plan, q_fp16, k_fp16, v_fp16, cache: Cache, out, softmax_scale: float | None = None,
+                      status=None, stream=None):
+    """Prefill of a prompt into an empty cache: causal attention over the prompt's own K/V into
+    `out` and the packed records of positions 0 .. T-1 into `cache`.
+    q: [B][H*G][T][128] float16; k, v: [B][H][T][128] float16; out: like q, float16 or float32."""
+    import torch
+    b, hq, t, d = q_fp16.shape
+    if d != HEAD_DIM or tuple(k_fp16.shape) != (b, plan.n_kv_heads, t, d) or tuple(v_fp16.shape) != tuple(k_fp16.shape):
+        raise ValueError("q must be [B][H*G][T][128], k and v [B][H][T][128]")
+    if tuple(out.shape) != tuple(q_fp16.shape):
+        raise ValueError("out must have the shape of q")
+    if not all(x.is_contiguous() for x in (q_fp16, k_fp16, v_fp16, out)):
+        raise ValueError("q, k, v and out must be contiguous")
+    if out.dtype == torch.float32:
+        out_dtype = 1
+    elif out.dtype == torch.float16:
+        out_dtype = 0
+    else:
+        raise ValueError("out must be float16 or float32")
+    scale = (1.0 / HEAD_DIM ** 0.5) if softmax_scale is None else softmax_scale
+    _check(lib().bgtq_prefill_attn(plan.handle, _stream(stream), _ptr(q_fp16), _ptr(k_fp16), _ptr(v_fp16), b, t,
+                                   C.byref(cache.desc), _ptr(out), out_dtype, scale, _ptr(status)))
+
+
 def bgtq_dequant_debug(plan: Plan, cache: Cache, b: int, head: int, t0: int, t1: int, k_out=None, v_out=None,
                        codec_domain: bool = False, stream=None):
     _check(lib().bgtq_dequant_debug(plan.handle, _stream(stream), C.byref(cache.desc), cache.batch, b, head, t0, t1,

@@ -29,6 +29,7 @@ SOURCES = [
     ("decode_attn_paged.cu", []),
     ("decode_attn_noalloc.cu", []),
     ("fidelity.cu", []),
+    ("prefill_attn.cu", []),
 ]
 
 

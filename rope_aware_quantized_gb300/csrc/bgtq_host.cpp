@@ -704,6 +704,26 @@ int bgtq_decode_step(const bgtq_plan* p, void* stream, const void* q, const void
     return BGTQ_OK;
 }
 
+int bgtq_prefill_attn(const bgtq_plan* p, void* stream, const void* q, const void* k, const void* v, int batch,
+                      int t, const bgtq_cache* c, void* out, int out_dtype, float scale, int32_t* status) {
+    int rc = check_cache(p, c);
+    if (rc) return rc;
+    if ((rc = check_plan(p))) return rc;
+    if (batch < 0 || t < 0) return set_error(BGTQ_ERR_INVALID_ARG, "batch and t must be >= 0");
+    if (t > c->capacity) return set_error(BGTQ_ERR_CAPACITY, "t = %d exceeds the cache capacity", t);
+    if (batch == 0 || t == 0) return BGTQ_OK;
+    if (!q || !k || !v || !out) return set_error(BGTQ_ERR_INVALID_ARG, "NULL pointer");
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15)
+        return set_error(BGTQ_ERR_INVALID_ARG, "q, k and v must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(out) & 7) return set_error(BGTQ_ERR_INVALID_ARG, "out must be 8-byte aligned");
+    if (out_dtype != 0 && out_dtype != 1) return set_error(BGTQ_ERR_INVALID_ARG, "out_dtype must be 0 (half) or 1 (float)");
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return set_error(BGTQ_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
+    if (batch > 65535) return set_error(BGTQ_ERR_UNSUPPORTED, "at most 65535 sequences per call");
+    cudaError_t e = launch_prefill(*p, (cudaStream_t)stream, q, k, v, batch, t, *c, out, out_dtype, scale, status);
+    if (e != cudaSuccess) return set_error(BGTQ_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+    return BGTQ_OK;
+}
+
 int bgtq_logit_mae(const bgtq_plan* p, void* stream, const void* q, const void* k, const bgtq_cache* c, int64_t t,
                    int batch, float scale, float* mae) {
     int rc = check_plan(p);

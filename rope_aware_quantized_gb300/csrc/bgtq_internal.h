@@ -98,6 +98,10 @@ struct CacheMap {
 #endif
 };
 
+cudaError_t launch_prefill(const bgtq_plan& pl, cudaStream_t s, const void* q, const void* k, const void* v,
+                           int batch, int t, const bgtq_cache& c, void* out, int out_dtype, float scale,
+                           int32_t* status);
+
 // Host checks of a cache descriptor (buffers, alignment, capacity, the
 // recent-key buffer, paging); sets the thread's error message.
 int check_cache(const bgtq_plan* p, const bgtq_cache* c);
