@@ -52,6 +52,9 @@ def parse_args():
     ap.add_argument("--eager", action="store_true", help="launch without a CUDA graph (profiling)")
     ap.add_argument("--recent", type=int, default=0,
                     help="keep the last W keys of every sequence in an fp16 recent-key buffer as well")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the fused prefill (bgtq_prefill_attn) of one layer and print its JSON line")
+    ap.add_argument("--prefill-tokens", type=int, default=32768, help="prompt length of the fused-prefill measurement")
     ap.add_argument("--page-tokens", type=int, default=0,
                     help="paged cache: pages of P tokens in a shuffled pool instead of contiguous rows")
     ap.add_argument("--two-call", action="store_true",
@@ -357,6 +360,17 @@ def run_gpu(args):
     lens = w.seq_lens()
     max_len = int(lens.max())
     L, B = (args.layers or w.layers), w.batch
+    if args.prefill_only:
+        bits, energy = zip(*[bg.bgtq_alloc_bits(workloads.calib_keys(w, 0, h), w.bits_per_key) for h in range(w.n_kv)])
+        plan = bg.bgtq_plan_create(np.stack(bits), np.stack(energy), w.group, w.bits_per_key, w.v_bits,
+                                   workloads.plan_seed(w, 0))
+        peaks, _ = load_peaks()
+        r = measure_prefill_attn(w, plan, args.prefill_tokens, peaks, torch.cuda.Stream())
+        if rank == 0:
+            print(json.dumps({"metric": "fused_prefill_tflops", "value": r["achieved"], "unit": "TFLOP/s",
+                              "config": {"workload": w.name, "prompt_tokens": args.prefill_tokens},
+                              "prefill_attn": r}), flush=True)
+        return
 
     # device buffers of all layers' per-step inputs/outputs (views per layer)
     q_all = torch.empty((L, B, w.n_q, 128), dtype=torch.float16, device="cuda")
@@ -462,7 +476,7 @@ def run_gpu(args):
     step_bytes = L * decode_bytes
 
     prefill = measure_prefill(w, layers[0].plan, max_len, peaks, stream)
-    prefill_attn = measure_prefill_attn(w, layers[0].plan, min(max_len, 32768), peaks, stream)
+    prefill_attn = measure_prefill_attn(w, layers[0].plan, min(max_len, args.prefill_tokens), peaks, stream)
 
     # end to end: pinned host inputs -> device, graph replay, outputs -> host
     hq = torch.empty(q_all.shape, dtype=q_all.dtype, pin_memory=True)

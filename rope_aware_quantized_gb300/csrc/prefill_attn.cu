@@ -55,6 +55,11 @@ struct PfParams {
     int32_t* status;
 };
 
+template <bool B>
+struct BoolC {
+    static constexpr bool value = B;
+};
+
 // byte offset of 16-byte chunk c of row r in a swizzled 64 x 256-byte tile
 __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 256 + ((c ^ (r & 7)) << 4)); }
 
@@ -242,7 +247,9 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_kernel(PfParams p) {
 #pragma unroll
     for (int n = 0; n < 16; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
 
-    for (int j = 0; j <= qb; ++j) {
+    // one 64-key tile; kEdge: the diagonal tile (causal mask, keys past T)
+    auto tile = [&](int j, auto edge_tag) {
+        constexpr bool kEdge = decltype(edge_tag)::value;
         const int st = j & 1;
         const uint32_t sK = sK0 + 2 * st * kPfTile, sV = sV0 + 2 * st * kPfTile;
         if (j + 1 <= qb) {
@@ -269,50 +276,51 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_kernel(PfParams p) {
                 mma_f16(s[2 * jj + 1], qa[c], kb[2], kb[3]);
             }
         }
-        // ---- causal mask, scale, online softmax (rows g: e = 0, 1; g + 8: e = 2, 3)
-        const int kbase = j * kPfKeys;
-        const bool edge = j == qb || kbase + kPfKeys > p.T;
+        // ---- online softmax (rows g: e = 0, 1; g + 8: e = 2, 3) in the
+        // log2 domain: the running maxima m are of scale log2(e) s; the scale
+        // is folded into the exponent's fma
+        const float cs = p.scale_log2;
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
         for (int n = 0; n < 8; ++n)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                float x = s[n][e] * p.scale_log2;
-                if (edge) {
-                    const int key = kbase + 8 * n + 2 * t + (e & 1);
+                if (kEdge) {
+                    const int key = j * kPfKeys + 8 * n + 2 * t + (e & 1);
                     const int row = row_g + 8 * (e >> 1);
-                    if (key > row || key >= p.T) x = -INFINITY;
+                    if (key > row || key >= p.T) s[n][e] = -INFINITY;
                 }
-                s[n][e] = x;
-                if (e < 2) mx0 = fmaxf(mx0, x);
-                else mx1 = fmaxf(mx1, x);
+                if (e < 2) mx0 = fmaxf(mx0, s[n][e]);
+                else mx1 = fmaxf(mx1, s[n][e]);
             }
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-        const float a0 = ex2(m0 - n0), a1 = ex2(m1 - n1);  // 0 on the first tile (m = -inf)
-        m0 = n0;
-        m1 = n1;
-        float r0 = 0.0f, r1 = 0.0f;
+        const float n0 = fmaxf(m0, mx0 * cs), n1 = fmaxf(m1, mx1 * cs);
+        if (__any_sync(0xffffffffu, n0 != m0 || n1 != m1)) {
+            // a maximum moved: rescale (exp2(-inf) = 0 on the first tile)
+            const float a0 = ex2(m0 - n0), a1 = ex2(m1 - n1);
+            l0 *= a0;
+            l1 *= a1;
+#pragma unroll
+            for (int n = 0; n < 16; ++n) {
+                acc[n][0] *= a0;
+                acc[n][1] *= a0;
+                acc[n][2] *= a1;
+                acc[n][3] *= a1;
+            }
+            m0 = n0;
+            m1 = n1;
+        }
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
-            s[n][0] = ex2(s[n][0] - n0);
-            s[n][1] = ex2(s[n][1] - n0);
-            s[n][2] = ex2(s[n][2] - n1);
-            s[n][3] = ex2(s[n][3] - n1);
-            r0 += s[n][0] + s[n][1];
-            r1 += s[n][2] + s[n][3];
-        }
-        l0 = l0 * a0 + r0;
-        l1 = l1 * a1 + r1;
-#pragma unroll
-        for (int n = 0; n < 16; ++n) {
-            acc[n][0] *= a0;
-            acc[n][1] *= a0;
-            acc[n][2] *= a1;
-            acc[n][3] *= a1;
+            s[n][0] = ex2(fmaf(s[n][0], cs, -n0));
+            s[n][1] = ex2(fmaf(s[n][1], cs, -n0));
+            s[n][2] = ex2(fmaf(s[n][2], cs, -n1));
+            s[n][3] = ex2(fmaf(s[n][3], cs, -n1));
+            l0 += s[n][0] + s[n][1];
+            l1 += s[n][2] + s[n][3];
         }
         // ---- O += P V (4 k-chunks of 16 keys x 16 n-tiles of 8 dims)
 #pragma unroll
@@ -330,7 +338,9 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_kernel(PfParams p) {
             }
         }
         __syncthreads();  // this stage is refilled by the next iteration
-    }
+    };
+    for (int j = 0; j < qb; ++j) tile(j, BoolC<false>{});
+    tile(qb, BoolC<true>{});
 
     // ---- normalise and store rows row_g, row_g + 8 (dims 8 n + 2 t, + 1)
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
