@@ -198,3 +198,44 @@ def test_paged_full_size_decode_equals_contiguous():
         assert st.item() == 0
         outs.append(out.cpu())
     assert torch.equal(outs[0], outs[1])
+
+
+def test_paged_general_instance_noalloc_and_fidelity():
+    """Explicit widths with wide codes in many slots (the general decode
+    path) on a paged cache with a recent-key buffer: decode (workspace and
+    no-alloc entry points) and the logit-fidelity kernel equal the
+    contiguous cache's results (decode bit for bit)."""
+    H, G, T, P, W = 2, 8, 1500, 64, 100
+    li = synth.layer_inputs(404, 0, H, G, T, 1e5, 1.2)
+    energy = np.stack([bg.bgtq_alloc_bits(li.calib[h], 384)[1] for h in range(H)])
+    bits = np.zeros((H, 64), np.uint8)
+    bits[0, :24] = 8
+    bits[1, 40:] = 8
+    plan = bg.bgtq_plan_create(bits, energy, G, 384, 3, 0xBADC0DE)
+    cap = -(-T // P) * P
+    cont = bg.Cache(plan, 1, cap, recent=W)
+    paged = bg.Cache(plan, 1, cap, recent=W, page_tokens=P, n_pages=cap // P + 2)
+    perm = np.random.default_rng(8).permutation(paged.n_pages)[:cap // P].astype(np.int32)
+    paged.page_table.copy_(dev(perm.reshape(1, -1)))
+    k, v = dev(li.k[None]), dev(li.v[None])
+    for c in (cont, paged):
+        bg.bgtq_quantize_append(plan, k, v, dev(np.array([0], np.int32)), c)
+    q = dev(li.q[None])
+    seq = dev(np.array([T], np.int32))
+    res = []
+    for c in (cont, paged):
+        a, st = decode(plan, c, q, seq, T)
+        assert st == 0
+        out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+        st2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+        bg.bgtq_decode_attn_noalloc(plan, q, c, seq, T, out, status=st2)
+        mae = torch.empty((1, H * G), dtype=torch.float32, device="cuda")
+        bg.bgtq_logit_mae(plan, q, k, c, T, mae)
+        torch.cuda.synchronize()
+        assert st2.item() == 0
+        res.append((a, out.cpu().numpy().astype(np.float64), mae.cpu().numpy()))
+    assert np.array_equal(res[0][0], res[1][0]) and np.array_equal(res[0][1], res[1][1])
+    assert np.array_equal(res[1][0], res[1][1])
+    # the fidelity kernel sums per-block partials with float atomics, whose
+    # order varies from run to run: equal up to that summation order
+    assert np.allclose(res[0][2], res[1][2], rtol=1e-5, atol=0)
