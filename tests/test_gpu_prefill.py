@@ -158,3 +158,41 @@ def test_prefill_rejects_a_prompt_longer_than_the_cache():
     with pytest.raises(bg.BgtqError) as e:
         run(plan, cache, q, li)
     assert e.value.code == -3
+
+
+@pytest.mark.parametrize("W", [0, 48])
+def test_prefill_then_decode_steps(W):
+    """A serving sequence: prefill a prompt (one launch), then two decode
+    steps that append and attend (bgtq_decode_step), with and without an
+    fp16 recent-key buffer; every output against the oracle over the
+    tokens as appended."""
+    H, G, T0, steps = 2, 8, 700, 2
+    T = T0 + steps
+    li, plan, cache, heads = setup(55 + W, H, G, T, recent=W)
+    q_prompt = prompt_queries([type("L", (), {"k": li[0].k[:, :T0]})()], G, T0, 12)
+    k = dev(np.ascontiguousarray(li[0].k[None, :, :T0]))
+    v = dev(np.ascontiguousarray(li[0].v[None, :, :T0]))
+    out = torch.empty(q_prompt.shape, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bg.bgtq_prefill_attn(plan, dev(q_prompt), k, v, cache, out, status=st)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.float64)
+    for h in range(H):
+        want = O.prefill_attention(q_prompt[0][h * G:(h + 1) * G], li[0].k[h][:T0], li[0].v[h][:T0])
+        check_close(got[0][h * G:(h + 1) * G].reshape(-1, 128), want.reshape(-1, 128))
+    ws = torch.zeros(bg.bgtq_decode_attn_workspace(plan, 1, T), dtype=torch.uint8, device="cuda")
+    rng = np.random.default_rng(13)
+    for s in range(steps):
+        pos = T0 + s
+        q = li[0].k[:, rng.integers(0, pos, G)].reshape(H * G, 128)[None]  # earlier keys as queries
+        o = torch.empty((1, H * G, 128), dtype=torch.float32, device="cuda")
+        bg.bgtq_decode_step(plan, dev(q), dev(li[0].k[None, :, pos]), dev(li[0].v[None, :, pos]),
+                            dev(np.array([pos], np.int32)), cache, dev(np.array([pos + 1], np.int32)), T, o, ws,
+                            status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        got = o.cpu().numpy().astype(np.float64)[0]
+        for h, hs in enumerate(heads):
+            e = O.encode_head(hs, li[0].k[h][:pos + 1], li[0].v[h][:pos + 1])
+            want = O.attention_recent(q[0][h * G:(h + 1) * G], e["khat"], e["vhat"], li[0].k[h][:pos + 1], W)
+            check_close(got[h * G:(h + 1) * G], want)
