@@ -98,7 +98,8 @@ typedef struct {
      * that an append writes must not be mapped twice.
      * page_table is read by the decode kernel before it waits for the previous
      * kernel (like seq_lens): it must not be written by a kernel that triggers
-     * its dependents early.  capacity must equal max_pages * page_tokens. */
+     * its dependents early.  capacity must equal max_pages * page_tokens
+     * and be at most 2^21. */
     const int32_t* page_table; /* device, [B][max_pages] */
     int64_t max_pages;         /* entries per row of page_table, >= 1 */
     int64_t page_tokens;       /* P: a power of two, 16 <= P <= 2^20 */

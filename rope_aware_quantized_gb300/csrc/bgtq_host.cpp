@@ -518,6 +518,8 @@ int check_cache(const bgtq_plan* p, const bgtq_cache* c) {
             return set_error(BGTQ_ERR_INVALID_ARG, "a paged cache needs capacity == max_pages * page_tokens");
         if (reinterpret_cast<uintptr_t>(c->page_table) & 3)
             return set_error(BGTQ_ERR_INVALID_ARG, "page_table must be 4-byte aligned");
+        if (c->capacity > (int64_t)1 << 21)
+            return set_error(BGTQ_ERR_INVALID_ARG, "a paged cache holds at most 2^21 positions per sequence");
     }
     if (c->capacity > INT32_MAX) return set_error(BGTQ_ERR_INVALID_ARG, "capacity must be < 2^31");
     (void)p;

@@ -92,6 +92,7 @@ constexpr int kTile = 16;         // tokens per warp iteration; splits start on 
 constexpr int kCluster = 8;       // CTAs per thread-block cluster (consecutive splits of one head)
 constexpr int kMaxClusters = 64;  // clusters per (sequence, head)
 constexpr int64_t kMaxSplitTokens = 4096;  // longest token split of one CTA
+constexpr int kMaxTilesPerWarp = (int)(kMaxSplitTokens / (kWarps * 16));  // 16-token tiles of one warp
 constexpr int kPartStride = 2 + kD;  // m, l, acc[128] per query head
 constexpr uint32_t kPrivByte = 4u * kImgPriv;
 constexpr int kPrivMaxW = 3;
@@ -463,6 +464,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     __shared__ float s_thr[kThrCompact];                 // fused step: encoder thresholds
     __shared__ uint32_t s_enc[3][8 * kPairMaxW];          // fused step: records being assembled
     __shared__ uint2 s_qo[8][32];                         // recent-key buffer: A fragments of q as given
+    __shared__ int64_t s_pslot[kPaged ? kWarps : 1][kPaged ? kMaxTilesPerWarp : 1];  // paged: tile slots
     // after the main loop the table region holds the per-warp partials of
     // the 8 query heads (m, l, acc[128]) that the cluster reads
     // and then the CTA's merged partial of the 8 heads
@@ -556,14 +558,20 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     // being copied while one is processed
     constexpr int kStep = kWarps * kTile;
     const int T0w = t_begin + warp * kTile;
-    const int n_tiles = active && T0w < t_end ? (t_end - T0w + kStep - 1) / kStep : 0;
-    // paged: token slots of the first kStages tiles and of the new token,
-    // looked up before the wait (the page table is read like seq_lens)
-    int64_t sl_pre[kStages];
+    int n_tiles = active && T0w < t_end ? (t_end - T0w + kStep - 1) / kStep : 0;
+    if (kPaged && n_tiles > kMaxTilesPerWarp) {  // excluded by the host's capacity check
+        if (lane == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_SEQLEN_CAPACITY);
+        n_tiles = kMaxTilesPerWarp;
+    }
+    // paged: the token slots of all the warp's tiles (at most kMaxTilesPerWarp:
+    // a paged cache holds at most kMaxSplitTokens * kCluster * kMaxClusters
+    // positions, so a split is at most kMaxSplitTokens long) and of the new
+    // token, looked up before the wait (the page table is read like seq_lens),
+    // so that the main loop only reads a slot from shared memory
     int64_t sl_new = 0;
     if constexpr (kPaged) {
-#pragma unroll
-        for (int k = 0; k < kStages; ++k) sl_pre[k] = k < n_tiles ? tile_slot(T0w + k * kStep) : 0;
+        for (int k = lane; k < n_tiles && k < kMaxTilesPerWarp; k += 32) s_pslot[warp][k] = tile_slot(T0w + k * kStep);
+        __syncwarp();
         if (owner) sl_new = p.map.slot(b, h, pos);
     }
 
@@ -841,25 +849,17 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     for (int k = 0; k < kStages - 1; ++k) {
         if (k < n_tiles) {
             const int T0 = T0w + k * kStep;
-            stage_tile<BK, BV>(st_addr + k * SL::kBytes, kc, vc, kn, vn, kPaged ? sl_pre[k] : tile_slot(T0), T0, seq,
-                               lane);
+            stage_tile<BK, BV>(st_addr + k * SL::kBytes, kc, vc, kn, vn, kPaged ? s_pslot[warp][k] : tile_slot(T0), T0,
+                               seq, lane);
         }
         cp_async_commit();
     }
-    // paged: the token slot of the next tile to stage, looked up one step early
-    int64_t sl_next = 0;
-    if constexpr (kPaged) sl_next = sl_pre[kStages - 1];
     auto step = [&](int k, auto win) {
         const int kn_ = k + kStages - 1;
         if (kn_ < n_tiles) {
             const int T0 = T0w + kn_ * kStep;
-            if constexpr (kPaged) {
-                stage_tile<BK, BV>(st_addr + (kn_ % kStages) * SL::kBytes, kc, vc, kn, vn, sl_next, T0, seq, lane);
-                if (kn_ + 1 < n_tiles) sl_next = tile_slot(T0 + kStep);
-            } else {
-                stage_tile<BK, BV>(st_addr + (kn_ % kStages) * SL::kBytes, kc, vc, kn, vn, tile_slot(T0), T0, seq,
-                                   lane);
-            }
+            stage_tile<BK, BV>(st_addr + (kn_ % kStages) * SL::kBytes, kc, vc, kn, vn,
+                               kPaged ? s_pslot[warp][kn_] : tile_slot(T0), T0, seq, lane);
         }
         cp_async_commit();
         cp_async_wait<kStages - 1>();

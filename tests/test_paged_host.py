@@ -40,6 +40,7 @@ def test_valid_paged_descriptor_passes_the_cache_checks():
     (dict(n_pages=0), "n_pages"),
     (dict(max_pages=0, capacity=64), "max_pages"),
     (dict(page_table=BASE + 2), "4-byte aligned"),
+    (dict(max_pages=(1 << 21) // 64 + 1, capacity=((1 << 21) // 64 + 1) * 64), "at most 2^21"),
 ])
 def test_bad_paged_descriptors_are_rejected(kw, frag):
     rc, msg = append_with(**kw)
