@@ -708,9 +708,11 @@ int bgtq_decode_step(const bgtq_plan* p, void* stream, const void* q, const void
 
 int bgtq_prefill_attn(const bgtq_plan* p, void* stream, const void* q, const void* k, const void* v, int batch,
                       int t, const bgtq_cache* c, void* out, int out_dtype, float scale, int32_t* status) {
+    // the descriptor and the arguments first (none of these checks reads
+    // device memory), the plan's device tables last
+    if (!p) return set_error(BGTQ_ERR_INVALID_ARG, "plan is NULL");
     int rc = check_cache(p, c);
     if (rc) return rc;
-    if ((rc = check_plan(p))) return rc;
     if (batch < 0 || t < 0) return set_error(BGTQ_ERR_INVALID_ARG, "batch and t must be >= 0");
     if (t > c->capacity) return set_error(BGTQ_ERR_CAPACITY, "t = %d exceeds the cache capacity", t);
     if (batch == 0 || t == 0) return BGTQ_OK;
@@ -721,6 +723,7 @@ int bgtq_prefill_attn(const bgtq_plan* p, void* stream, const void* q, const voi
     if (out_dtype != 0 && out_dtype != 1) return set_error(BGTQ_ERR_INVALID_ARG, "out_dtype must be 0 (half) or 1 (float)");
     if (!(scale > 0.0f) || !std::isfinite(scale)) return set_error(BGTQ_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
     if (batch > 65535) return set_error(BGTQ_ERR_UNSUPPORTED, "at most 65535 sequences per call");
+    if ((rc = check_plan(p))) return rc;
     cudaError_t e = launch_prefill(*p, (cudaStream_t)stream, q, k, v, batch, t, *c, out, out_dtype, scale, status);
     if (e != cudaSuccess) return set_error(BGTQ_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
     return BGTQ_OK;
