@@ -194,7 +194,8 @@ int bgtq_plan_get_codebook(const bgtq_plan* plan, int width, const float** centr
                            int* n_levels);
 
 /* Byte sizes of one layer's cache buffers for `batch` sequences of `capacity`
- * tokens (capacity even). */
+ * tokens (capacity even); for a paged cache, of the pools: batch = n_pages,
+ * capacity = page_tokens.  Host only. */
 int bgtq_cache_bytes(const bgtq_plan* plan, int batch, int64_t capacity, size_t* k_codes_bytes,
                      size_t* v_codes_bytes, size_t* norm_bytes);
 
