@@ -60,7 +60,8 @@ def parse_args():
     ap.add_argument("--two-call", action="store_true",
                     help="per layer bgtq_quantize_append + bgtq_decode_attn instead of the fused bgtq_decode_step")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
-    ap.add_argument("--sample-seconds", type=float, default=12.0, help=argparse.SUPPRESS)
+    ap.add_argument("--sample-seconds", type=float, default=10.0, help=argparse.SUPPRESS)
+    ap.add_argument("--sample-procs", type=int, default=1, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -81,7 +82,7 @@ def load_peaks():
 # ----------------------------------------------------------------------------- CPU oracle sample
 
 class OracleSample:
-    """The oracle's decode step on one (layer, head) sample of the workload.
+    """The oracle's decode step on one (layer, KV head) sample of the workload.
 
     One repetition unpacks and dequantises the sample's packed K/V cache,
     runs float64 attention for the head's G queries, and encodes + packs one
@@ -90,40 +91,32 @@ class OracleSample:
 
     TOKENS = 8192
 
-    def __init__(self, workload: str):
+    def __init__(self, workload: str, layer: int = 0, head: int = 0):
         from oracle import bgtq_oracle as O
         from rope_aware_quantized_gb300 import synth, workloads
         self.O = O
         w = workloads.WORKLOADS[workload]
-        self.li = synth.layer_inputs(w.seed, 0, 1, w.group, self.TOKENS, w.rope_base, w.s_ln)
-        self.hs = O.head_state(workloads.calib_keys(w, 0, 0), w.bits_per_key, w.v_bits,
-                               workloads.plan_seed(w, 0), 0)
-        enc = O.encode_head(self.hs, self.li.k[0], self.li.v[0])
+        layer %= w.layers
+        head %= w.n_kv
+        li = synth.layer_inputs(w.seed, layer, w.n_kv, w.group, self.TOKENS, w.rope_base, w.s_ln)
+        self.q = li.q[head * w.group:(head + 1) * w.group]
+        self.k, self.v = li.k[head], li.v[head]
+        self.hs = O.head_state(workloads.calib_keys(w, layer, head), w.bits_per_key, w.v_bits,
+                               workloads.plan_seed(w, layer), head)
+        enc = O.encode_head(self.hs, self.k, self.v)
         self.krec, self.vrec, self.krho, self.vrho = enc["krec"], enc["vrec"], enc["krho"], enc["vrho"]
 
     def rep(self):
-        O, hs, li = self.O, self.hs, self.li
+        O, hs = self.O, self.hs
         kcodes = O.unpack_k(self.krec, hs.kc, hs.bk)
         vcodes = O.unpack_v(self.vrec, hs.bv, self.TOKENS)
         khat = O.dequant(kcodes, self.krho, hs.kc)
         vhat = O.dequant(vcodes, self.vrho, hs.vc)
-        O.attention(li.q, khat, vhat)
-        nk, _ = O.encode(li.k[0][:1], hs.kc)
+        O.attention(self.q, khat, vhat)
+        nk, _ = O.encode(self.k[:1], hs.kc)
         O.pack_k(nk, hs.kc, hs.bk)
-        nv, _ = O.encode(li.v[0][:1], hs.vc)
+        nv, _ = O.encode(self.v[:1], hs.vc)
         O.pack_v(nv, hs.bv)
-
-
-def oracle_sample(workload: str, seconds: float):
-    s = OracleSample(workload)
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        s.rep()
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or reps >= 400:
-            break
-    return {"sec_per_token_head": el / (reps * s.TOKENS), "reps": reps, "tokens": s.TOKENS, "seconds": el}
 
 
 def single_thread_env():
@@ -131,30 +124,151 @@ def single_thread_env():
         os.environ[k] = "1"
 
 
-def cpu_baseline(workload: str, seconds: float):
-    """Run the oracle sample in a single-threaded child process."""
+def host_cpu():
+    """(logical cores, CPU model name) of this host."""
+    model = None
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=20)
+        for line in r.stdout.splitlines():
+            if line.strip().lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model and os.path.exists("/proc/cpuinfo"):
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                model = line.split(":", 1)[1].strip()
+                break
+    return os.cpu_count() or 1, model or "unknown"
+
+
+# Worker state of the all-core oracle pool (spawned processes, one sample each).
+_POOL_SAMPLE = None
+
+
+def _pool_init(workload, counter, barrier):
+    global _POOL_SAMPLE
+    single_thread_env()
+    with counter.get_lock():
+        i = counter.value
+        counter.value += 1
+    from rope_aware_quantized_gb300 import workloads
+    w = workloads.WORKLOADS[workload]
+    _POOL_SAMPLE = OracleSample(workload, i % w.layers, (i // w.layers) % w.n_kv)
+    _POOL_SAMPLE.rep()  # warm
+    if barrier is not None:
+        barrier.wait()
+
+
+def _pool_run(seconds):
+    """Repetitions of this worker's sample for about `seconds`."""
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        _POOL_SAMPLE.rep()
+        reps += 1
+        if time.perf_counter() - t0 >= seconds or reps >= 400:
+            break
+    return reps, time.perf_counter() - t0
+
+
+def _pool_rep(_):
+    t0 = time.perf_counter()
+    _POOL_SAMPLE.rep()
+    return time.perf_counter() - t0
+
+
+def oracle_pool(workload: str, procs: int):
+    """A spawned pool of `procs` single-threaded oracle workers, each holding
+    the sample of a different (layer, KV head) of the workload."""
+    import multiprocessing as mp
+    single_thread_env()
+    ctx = mp.get_context("spawn")
+    counter = ctx.Value("i", 0)
+    barrier = ctx.Barrier(procs)
+    return ctx.Pool(procs, initializer=_pool_init, initargs=(workload, counter, barrier))
+
+
+def oracle_sample(workload: str, seconds: float, procs: int):
+    """Token-heads per second of the oracle's decode work: one process, or
+    `procs` processes in parallel (each on its own sample)."""
+    if procs <= 1:
+        s = OracleSample(workload)
+        s.rep()
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            s.rep()
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= seconds or reps >= 400:
+                break
+        return {"token_heads_per_s": reps * s.TOKENS / el, "reps": reps, "tokens": s.TOKENS, "seconds": el,
+                "procs": 1}
+    pool = oracle_pool(workload, procs)
+    try:
+        res = pool.map(_pool_run, [seconds] * procs, chunksize=1)
+    finally:
+        pool.close()
+        pool.join()
+    reps = sum(r for r, _ in res)
+    wall = max(e for _, e in res)
+    return {"token_heads_per_s": reps * OracleSample.TOKENS / wall, "reps": reps, "tokens": OracleSample.TOKENS,
+            "seconds": wall, "procs": procs}
+
+
+def cpu_baseline(workload: str, seconds: float, procs: int):
+    """Run the oracle sample in a child process (single-threaded numpy; a
+    spawned pool of `procs` workers when procs > 1)."""
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
     env.pop("RANK", None)
     env.pop("WORLD_SIZE", None)
+    env.pop("LOCAL_RANK", None)
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", "--workload", workload,
-                        "--sample-seconds", str(seconds)], capture_output=True, text=True, env=env)
+                        "--sample-seconds", str(seconds), "--sample-procs", str(procs)],
+                       capture_output=True, text=True, env=env)
     if r.returncode != 0:
         raise RuntimeError("oracle sample failed:\n" + r.stderr[-2000:])
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
-def cpu_line_fields(workload: str, sample: dict):
+def step_token_heads(workload: str) -> int:
     from rope_aware_quantized_gb300 import workloads
     w = workloads.WORKLOADS[workload]
-    token_heads = int(w.seq_lens().sum()) * w.n_kv * w.layers
-    step_s = sample["sec_per_token_head"] * token_heads
+    return int(w.seq_lens().sum()) * w.n_kv * w.layers
+
+
+def cpu_line_fields(workload: str, sample: dict):
+    """Tokens/s of a whole decode step extrapolated from the sample rate."""
+    from rope_aware_quantized_gb300 import workloads
+    w = workloads.WORKLOADS[workload]
+    token_heads = step_token_heads(workload)
+    step_s = token_heads / sample["token_heads_per_s"]
     value = w.batch / step_s
-    desc = (f"oracle decode step on one (layer, head) of {sample['tokens']} cached tokens x {sample['reps']} reps "
-            f"({sample['seconds']:.1f} s): unpack + dequantise K/V, float64 attention for {w.group} queries, "
-            f"encode + pack 1 token; scaled to {token_heads} token-heads per step")
+    desc = (f"oracle decode work on {sample['procs']} process(es), each on its own (layer, KV head) sample of "
+            f"{sample['tokens']} cached tokens ({sample['reps']} reps in {sample['seconds']:.1f} s): unpack + "
+            f"dequantise K/V, float64 attention for {w.group} queries, encode + pack 1 token; the measured "
+            f"token-head rate is extrapolated to the step's {token_heads} token-heads")
     return value, step_s, desc
+
+
+def cpu_baseline_block(workload: str, seconds: float):
+    """The line's cpu_baseline: the oracle on all host cores (value) and on
+    one core, both extrapolated from bounded samples."""
+    cores, model = host_cpu()
+    procs = max(1, cores)
+    one = cpu_baseline(workload, seconds, 1)
+    allc = cpu_baseline(workload, seconds, procs) if procs > 1 else one
+    v1, s1, d1 = cpu_line_fields(workload, one)
+    va, sa, da = cpu_line_fields(workload, allc)
+    token_heads = step_token_heads(workload)
+    return {"value": va, "unit": UNIT, "cores": allc["procs"], "kind": "oracle", "sample": da,
+            "extrapolated": True, "scale_factor": token_heads / (allc["procs"] * OracleSample.TOKENS),
+            "ms_per_step": sa * 1000.0, "host_cores": cores, "cpu_model": model,
+            "single_thread": {"value": v1, "unit": UNIT, "cores": 1, "ms_per_step": s1 * 1000.0,
+                              "extrapolated": True, "scale_factor": token_heads / OracleSample.TOKENS,
+                              "sample": d1}}
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -471,9 +585,14 @@ def run_gpu(args):
     if args.recent:  # the fp16 keys of the window are read as well
         decode_bytes += int(np.minimum(lens, args.recent).sum()) * w.n_kv * 256
     peaks, peak_kind = load_peaks()
-    achieved = decode_bytes / (launch_ms / 1000.0) / 1e9
+    iso_achieved = decode_bytes / (launch_ms / 1000.0) / 1e9
     traffic = traffic_from_profile()
     step_bytes = L * decode_bytes
+    # the dominant kernel inside the timed step: every launch of the step is
+    # this kernel (the fused step) or alternates with the 1-token append
+    # (two-call), so its in-step time per launch is at most ms_per_step / L
+    in_step_launch_ms = ms / L
+    achieved = step_bytes / (ms / 1000.0) / 1e9
 
     prefill = measure_prefill(w, layers[0].plan, max_len, peaks, stream)
     prefill_attn = measure_prefill_attn(w, layers[0].plan, min(max_len, args.prefill_tokens), peaks, stream)
@@ -506,9 +625,7 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        s = cpu_baseline(args.workload, args.sample_seconds)
-        v, _, desc = cpu_line_fields(args.workload, s)
-        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
+        cpu = cpu_baseline_block(args.workload, args.sample_seconds)
 
     if rank == 0:
         fp16_bytes = int(lens.sum()) * w.n_kv * 512 * L
@@ -531,7 +648,13 @@ def run_gpu(args):
             },
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                         "kernel": "decode_step" if fused else "decode_attn", "launch_ms": launch_ms, "bytes_per_launch": decode_bytes,
+                         "kernel": "decode_step" if fused else "decode_attn",
+                         "launch_ms_in_step": in_step_launch_ms, "bytes_per_launch": decode_bytes,
+                         "timing": "in-step: step bytes / ms_per_step of the graph-timed step "
+                                   f"({launches_per_step} launches per step, dependent launches overlapping)",
+                         "isolated": {"launch_ms": launch_ms, "achieved": iso_achieved,
+                                      "frac": iso_achieved / peaks["hbm_gbs"],
+                                      "timing": "CUDA events around each launch (breaks the launch overlap)"},
                          "peak_kind": f"{peak_kind} (copy, burst)"},
             "e2e": {"value": replica_throughput(world, B, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "path": "pinned H2D of q/new K/V, graph of the API calls, D2H of out"},
@@ -552,23 +675,34 @@ def run_gpu(args):
 # ----------------------------------------------------------------------------- reference arm (CPU oracle)
 
 def run_reference(args):
+    """The oracle as the reference arm: each step runs one repetition of the
+    oracle's decode work on every host core (one (layer, KV head) sample per
+    process) and is extrapolated to the whole step's token-heads."""
     rank, _, world = env_rank()
     if rank != 0:
         return
     single_thread_env()
     from rope_aware_quantized_gb300 import workloads
     w = workloads.WORKLOADS[args.workload]
-    sample = OracleSample(args.workload)
-    times = []
-    for i in range(args.warmup + args.steps):
-        t0 = time.perf_counter()
-        sample.rep()
-        dt = time.perf_counter() - t0
-        if i >= args.warmup:
-            times.append(dt)
-    per_th = statistics.mean(times) / sample.TOKENS
-    s = {"sec_per_token_head": per_th, "reps": len(times), "tokens": sample.TOKENS, "seconds": sum(times)}
+    cores, model = host_cpu()
+    procs = max(1, cores)
+    pool = oracle_pool(args.workload, procs)
+    try:
+        times = []
+        for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            pool.map(_pool_rep, range(procs), chunksize=1)
+            dt = time.perf_counter() - t0
+            if i >= args.warmup:
+                times.append(dt)
+    finally:
+        pool.close()
+        pool.join()
+    th = procs * OracleSample.TOKENS
+    s = {"token_heads_per_s": th * len(times) / sum(times), "reps": procs * len(times), "tokens": OracleSample.TOKENS,
+         "seconds": sum(times), "procs": procs}
     value, step_s, desc = cpu_line_fields(args.workload, s)
+    token_heads = step_token_heads(args.workload)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_s * 1000.0, "higher_is_better": True, "scaling": "weak",
@@ -576,7 +710,12 @@ def run_reference(args):
         "config": {"workload": w.name, "layers": w.layers, "kv_heads": w.n_kv, "q_heads": w.n_q,
                    "context": int(w.seq_lens().max()), "batch": w.batch,
                    "kv_bits": f"K{w.bits_per_key // 128}V{w.v_bits}"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": procs, "kind": "oracle", "sample": desc,
+                         "extrapolated": True, "scale_factor": token_heads / th, "host_cores": cores,
+                         "cpu_model": model, "measured_ms_per_sample_step": 1000.0 * sum(times) / len(times)},
+        "extrapolated": {"from_token_heads_per_step": th, "to_token_heads_per_step": token_heads,
+                         "note": "each timed step runs the oracle on a bounded sample; ms_per_step and value are "
+                                 "the sample's token-head rate scaled to the full step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -586,7 +725,7 @@ def main():
     args = parse_args()
     if args.oracle_sample:
         single_thread_env()
-        print(json.dumps(oracle_sample(args.workload, args.sample_seconds)), flush=True)
+        print(json.dumps(oracle_sample(args.workload, args.sample_seconds, args.sample_procs)), flush=True)
         return
     if args.impl == "reference":
         run_reference(args)

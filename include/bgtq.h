@@ -310,10 +310,12 @@ int bgtq_prefill_attn(const bgtq_plan* plan, void* stream, const void* q_fp16, c
  *   split-merge scratch is one built-in device array of 2 MiB that every GPU
  *   which loads the library keeps until the process exits.  No call
  *   allocates or frees memory.
- *   The first call on a device looks up that array's address with the device
- *   current; make it before any stream capture.  Every call shares the array
- *   and it keeps the last call's contents (its counters are cleared by each
- *   call), so calls that overlap on the GPU race; order them on one stream.
+ *   Every call looks up that array's address on the current device (a
+ *   host-side lookup, so a reset and re-created context is followed); the
+ *   first call on a device may load the library's device code, so make it
+ *   before any stream capture.  Every call shares the array and it keeps the
+ *   last call's contents (its counters are cleared by each call), so calls
+ *   that overlap on the GPU race; order them on one stream.
  * Errors: as bgtq_decode_attn; WORKSPACE when the problem needs more than the
  * built-in 2 MiB of scratch (then use bgtq_decode_attn with a workspace).
  */

@@ -297,9 +297,7 @@ static void free_dev(bgtq_plan* p) {
     if (p->dev.heads) cudaFree(p->dev.heads);
     if (p->dev.cent) cudaFree(p->dev.cent);
     if (p->dev.thr) cudaFree(p->dev.thr);
-    if (p->dev.pair_lut) cudaFree(p->dev.pair_lut);
-    if (p->dev.single_lut) cudaFree(p->dev.single_lut);
-    if (p->dev.dec_image) cudaFree(p->dev.dec_image);
+    if (p->dev.img_src) cudaFree(p->dev.img_src);
     p->dev = DevTables{};
 }
 
@@ -373,46 +371,76 @@ static int build_head(bgtq_plan* p, int h, const uint8_t* bits, const double* s)
     if (!lane_layout(wd, p->bk, ht.slot_pair, off))
         return set_error(BGTQ_ERR_UNSUPPORTED, "head %d: no balanced lane layout for this allocation", h);
     p->slot_off[h].assign(64, 0);
-    ht.wide_mask = 0;
-    for (int t = 0; t < 4; ++t)
-        for (int sl = 0; sl < 16; ++sl) {
-            int m = ht.slot_pair[t][sl];
-            p->slot_off[h][t * 16 + sl] = off[t][sl];
-            ht.pair_bit[m] = (uint16_t)(32 * p->bk * t + off[t][sl]);
-            ht.slot_w[t][sl] = (uint8_t)wd[m];
-            int sh = (p->bk == 3 && sl >= 8) ? off[t][sl] - 32 : off[t][sl];
-            ht.slot_sh[t][sl] = (uint8_t)std::max(0, sh);
-            if (wd[m] > kPairMaxW) ht.wide_mask |= 1u << sl;
+    ht.max_w = 0;
+    for (int m = 0; m < kNB; ++m) ht.max_w = std::max(ht.max_w, wd[m]);
+    // decode lookup recipes (KSlot): slots 0..7 read the lane slice shifted
+    // left by 7 bits (a field at slice bit o sits at window bit o + 7); slots
+    // 8..15 read the words (1, 2) for bK = 3, else (0, 1) or the single word.
+    // The slots of a lane are sorted by width, the even ranks first, so the
+    // first eight fields end by bit 16 bK + 8 and the last eight start at bit
+    // 16 bK or later: every field fits its window at a shift >= 0.  The table
+    // base of the single tables is set per plan (upload_plan), as it depends
+    // on the widest code of all heads.
+    ht.n_wide = 0;
+    for (int t = 0; t < 4; ++t) {
+        int lead = 0;
+        for (int r = 0; r < 16; ++r) {
+            const int sl = (r & 1) ? 8 + r / 2 : r / 2;  // width order 0, 8, 1, 9, ...
+            if (wd[ht.slot_pair[t][sl]] > kPairTableMaxW) lead = r + 1;
         }
-    // decode lookup recipes: which table copy each (lane t, slot) uses
+        ht.n_wide = std::max(ht.n_wide, lead);
+    }
     for (int t = 0; t < 4; ++t)
         for (int sl = 0; sl < 16; ++sl) {
-            const uint32_t w = ht.slot_w[t][sl], sh = ht.slot_sh[t][sl];
-            uint32_t ex, mask, base, mult;
-            if ((ht.wide_mask >> sl) & 1u) {  // single-entry table, per-token-lane copy (16 B stride)
-                ex = 4;
-                mask = ((1u << w) - 1u) << 4;
-                base = 4u * kImgSingle + ((1u << w) << 4);
-                mult = 2u << 8;
-            } else if (w <= 3 && (sl == 0 || sh >= 7)) {  // per-lane pair table (128 B stride)
-                ex = 7;
-                mask = ((1u << (2 * w)) - 1u) << 7;
-                base = 4u * kImgPriv + ((1u << (2 * w)) << 7);
-                mult = 4u;
-            } else if (w == 4 && (sl == 0 || sh >= 5)) {  // per-token-lane width-4 table (32 B stride)
-                ex = 5;
-                mask = 255u << 5;
-                base = 4u * kImgG4;
-                mult = 4u << 8;
-            } else {  // shared pair table (4 B stride)
-                ex = 2;
-                mask = ((1u << (2 * w)) - 1u) << 2;
-                base = (1u << (2 * w)) << 2;
-                mult = 0;
+            const int m = ht.slot_pair[t][sl];
+            const int w = wd[m];
+            const int o = off[t][sl];
+            p->slot_off[h][t * 16 + sl] = (uint16_t)o;
+            ht.pair_bit[m] = (uint16_t)(32 * p->bk * t + o);
+            KSlot& k = ht.kslot[t][sl];
+            if (p->bk > 3) continue;  // no decode instance reads records of more than 3 words per lane
+            const int sh = sl < 8 ? o : (p->bk == 3 ? o - 39 : o - 7);
+            const int end = sl < 8 ? o + 7 + 2 * w : (p->bk == 3 ? o - 32 : o) + 2 * w;
+            if (sh < 0 || end > 64 || (p->bk == 1 && sl >= 8 && end > 32))
+                return set_error(BGTQ_ERR_UNSUPPORTED, "head %d: K slot (%d, %d) outside its decode window", h, t, sl);
+            if (w <= kPairTableMaxW) {
+                k.sh = (uint32_t)sh;
+                k.mask = ((1u << (2 * w)) - 1u) << 7;
+                k.base = (1u << (2 * w)) << 7;
+                k.wsh = 0;
+            } else if (w <= kLaneTableMaxW) {
+                k.sh = (uint32_t)sh;
+                k.mask = ((1u << w) - 1u) << 7;
+                k.base = (uint32_t)single_base(w) << 7;
+                k.wsh = (uint32_t)w;
+            } else {  // shared table, 4-byte stride: the code at bit 2
+                k.sh = (uint32_t)sh + 5;
+                k.mask = ((1u << w) - 1u) << 2;
+                k.base = kSharedTable;  // | byte offset, set per plan (the region follows the per-lane tables)
+                k.wsh = (uint32_t)w;
             }
-            ht.kmeta[t][sl] = SlotMeta{sl == 0 ? ex : sh - ex, mask, base, mult};
         }
     return BGTQ_OK;
+}
+
+// Decode table source for codes up to width ws: lane_entries(ws) words (the
+// kernel stores 32 copies of each, one per lane), then shared_words(ws) words.
+static void build_image_source(bgtq_plan* p, int ws) {
+    p->img_ws = ws;
+    p->img_src.assign(kImageMaxWords, 0);
+    auto hb = [&](int w, int c) -> uint32_t {
+        const float x = p->cent[w][c];
+        return x == 0.0f ? 0u : (uint32_t)double_to_half_bits(x);
+    };
+    for (int w = 0; w <= kPairTableMaxW; ++w) {
+        const int n = 1 << (2 * w), mask = (1 << w) - 1;
+        for (int f = 0; f < n; ++f) p->img_src[(1 << (2 * w)) + f] = hb(w, f & mask) | (hb(w, f >> w) << 16);
+    }
+    for (int w = kPairTableMaxW + 1; w <= std::min(ws, kLaneTableMaxW); ++w)
+        for (int c = 0; c < (1 << w); ++c) p->img_src[single_base(w) + c] = hb(w, c) | (hb(w, c) << 16);
+    const int le = lane_entries(ws);
+    for (int w = kLaneTableMaxW + 1; w <= ws; ++w)
+        for (int c = 0; c < (1 << w); ++c) p->img_src[le + shared_word(w, ws) + c] = hb(w, c) | (hb(w, c) << 16);
 }
 
 static int build_codebooks(bgtq_plan* p) {
@@ -430,34 +458,6 @@ static int build_codebooks(bgtq_plan* p) {
         for (size_t k = 0; k < c.size(); ++k) p->cent[w].push_back((float)ch[k]);
         for (size_t k = 0; k + 1 < c.size(); ++k) p->thr[w].push_back((float)(0.5 * (ch[k] + ch[k + 1])));
     }
-    p->pair_lut.assign(kPairLutWords, 0);
-    for (int w = 0; w <= kPairMaxW; ++w) {
-        int n = 1 << (2 * w), mask = (1 << w) - 1;
-        for (int f = 0; f < n; ++f) {
-            uint32_t lo = double_to_half_bits(p->cent[w][f & mask]);
-            uint32_t hi = double_to_half_bits(p->cent[w][f >> w]);
-            if (p->cent[w][f & mask] == 0.0f) lo = 0;
-            if (p->cent[w][f >> w] == 0.0f) hi = 0;
-            p->pair_lut[(1 << (2 * w)) + f] = lo | (hi << 16);
-        }
-    }
-    p->single_lut.assign(kSingleLutHalves, 0);
-    for (int w = 0; w <= kWMax; ++w)
-        for (int c = 0; c < (1 << w); ++c)
-            p->single_lut[(1 << w) + c] = p->cent[w][c] == 0.0f ? 0 : double_to_half_bits(p->cent[w][c]);
-    // decode shared-memory image (layout in bgtq_internal.h)
-    p->dec_image.assign(kImgWords, 0);
-    for (int i = 0; i < kPairLutWords; ++i) p->dec_image[i] = p->pair_lut[i];
-    for (int f = 0; f < 256; ++f)
-        for (int g = 0; g < 8; ++g) p->dec_image[kImgG4 + 8 * f + g] = p->pair_lut[256 + f];
-    for (int e = 0; e < 128; ++e)
-        for (int l = 0; l < 32; ++l) p->dec_image[kImgPriv + 32 * e + l] = p->pair_lut[e];
-    for (int e = 0; e < kSingleLutHalves; ++e)
-        for (int g = 0; g < 8; ++g) {
-            const int half = 8 * e + g;
-            uint32_t& wd = p->dec_image[kImgSingle + half / 2];
-            wd |= (uint32_t)p->single_lut[e] << (16 * (half & 1));
-        }
     return BGTQ_OK;
 }
 
@@ -481,9 +481,7 @@ static int upload_plan(bgtq_plan* p) {
     if ((e = upload(&p->dev.heads, p->heads.data(), p->heads.size())) != cudaSuccess ||
         (e = upload(&p->dev.cent, cent.data(), cent.size())) != cudaSuccess ||
         (e = upload(&p->dev.thr, thr.data(), thr.size())) != cudaSuccess ||
-        (e = upload(&p->dev.pair_lut, p->pair_lut.data(), p->pair_lut.size())) != cudaSuccess ||
-        (e = upload(&p->dev.single_lut, p->single_lut.data(), p->single_lut.size())) != cudaSuccess ||
-        (e = upload(&p->dev.dec_image, p->dec_image.data(), p->dec_image.size())) != cudaSuccess) {
+        (e = upload(&p->dev.img_src, p->img_src.data(), p->img_src.size())) != cudaSuccess) {
         free_dev(p);
         return set_error(BGTQ_ERR_CUDA, "plan upload: %s", cudaGetErrorString(e));
     }
@@ -583,6 +581,19 @@ int bgtq_plan_create(bgtq_plan** out, int head_dim, int n_kv_heads, int group, i
     p->slot_off.resize(n_kv_heads);
     int rc = build_codebooks(p);
     for (int h = 0; rc == BGTQ_OK && h < n_kv_heads; ++h) rc = build_head(p, h, block_bits + h * kNB, energy + h * kNB);
+    if (rc == BGTQ_OK) {
+        // decode tables: widest code of all heads (keys) and of the values
+        int ws = p->bv > kPairTableMaxW ? p->bv : 0;
+        for (const HeadTab& ht : p->heads) ws = std::max(ws, ht.max_w);
+        build_image_source(p, ws);
+        for (HeadTab& ht : p->heads)
+            for (int t = 0; t < 4; ++t)
+                for (int sl = 0; sl < 16; ++sl) {
+                    KSlot& k = ht.kslot[t][sl];
+                    if (k.base & kSharedTable)
+                        k.base = kSharedTable | (uint32_t)(lane_entries(ws) * 128 + 4 * shared_word((int)k.wsh, ws));
+                }
+    }
     if (rc == BGTQ_OK && !(flags & BGTQ_PLAN_HOST_ONLY)) rc = upload_plan(p);
     if (rc != BGTQ_OK) {
         delete p;

@@ -15,66 +15,71 @@ namespace bgtq {
 constexpr int kD = 128;      // head dim
 constexpr int kNB = 64;      // RoPE 2-D blocks per key
 constexpr int kWMax = 8;     // widest code
-constexpr int kPairMaxW = 5; // widest code decoded through the pair table
+constexpr int kPairMaxW = 5; // widest value code of a plan
 
-// Pair table: entry (4^w + f) holds half2(c_w[f & (2^w-1)], c_w[f >> w]) for
-// w = 0..kPairMaxW, so a pre-shifted field f<<2 is OR-ed with (4^w)<<2.
-constexpr int kPairLutWords = 1 << (2 * kPairMaxW + 1);
-// Single table: entry (2^w + c) holds c_w[c] (fp16 bits) for w = 0..8.
-constexpr int kSingleLutHalves = 1 << (kWMax + 1);
+// Decode lookup tables in shared memory.  Tables of widths up to 6 hold one
+// copy of every entry per lane (entry e of lane L is word 32 e + L), so the 32
+// lookups of a warp instruction fall on 32 distinct banks whatever the codes:
+//   entries [0, 128): pair tables of widths 0..3; entry 4^w + f holds the fp16
+//     pair (c_w[f mod 2^w], c_w[f >> w]) (entry 0 is zero)
+//   entries single_base(w) + c, widths 4..6: c_w[c] in both halves; every
+//     base is a multiple of 2^w, so an entry address is (c << 7) | (base << 7) | 4 L.
+// The rare widths 7 and 8 have one shared copy after the per-lane region
+// (word shared_word(w) + c, both halves), looked up with a 4-byte stride.
+constexpr int kPairEntries = 128;
+constexpr int kPairTableMaxW = 3;   // widths decoded as pairs (one lookup per two codes)
+constexpr int kLaneTableMaxW = 6;   // widest code with per-lane copies
+__host__ __device__ constexpr int single_base(int w) { return w == 4 ? 128 : w == 5 ? 160 : 192; }
+// per-lane entries for codes up to width ws
+__host__ __device__ constexpr int lane_entries(int ws) { return ws <= 3 ? 128 : ws == 4 ? 144 : ws == 5 ? 192 : 256; }
+// shared words for codes up to width ws (width 8 at word 0, width 7 after it)
+__host__ __device__ constexpr int shared_words(int ws) { return ws <= 6 ? 0 : ws == 7 ? 128 : 384; }
+__host__ __device__ constexpr int shared_word(int w, int ws) { return w == 8 ? 0 : (ws >= 8 ? 256 : 0); }
+constexpr int kImageMaxWords = 256 + 384;  // lane_entries(8) + shared_words(8): words of the compact source
+// bytes of the table region for codes up to width ws
+__host__ __device__ constexpr int image_bytes(int ws) { return lane_entries(ws) * 128 + shared_words(ws) * 4; }
 
-// Shared-memory image of the decode tables (32-bit words), copied verbatim
-// by every decode CTA.  Arranged so that the lanes of a warp rarely collide
-// on a bank:
-//   [0, 2048)       pair tables of widths 0..5, shared by all lanes (entry 4^w + f)
-//   [2048, 4096)    8 copies of the width-4 pair table, one per token lane g
-//                   (entry 256 + f of copy g at 2048 + 8 f + g)
-//   [4096, 8192)    per-lane copies of the pair tables of widths 0..3
-//                   (entry e of lane L at 4096 + 32 e + L)
-//   [8192, 10240)   8 copies of the single-entry table by token lane g, as
-//                   fp16 halves (entry 2^w + c of copy g at half 8 (2^w + c) + g)
-constexpr int kImgG4 = 2048;
-constexpr int kImgPriv = 4096;
-constexpr int kImgSingle = 8192;
-constexpr int kImgWords = 10240;
-
-// How decode lane (g, t) extracts and looks up one K slot: the 64-bit window
-// is shifted right by `sh` (slot 0: its word is shifted left by `sh`), masked
-// with `mask` and OR-ed with base + (mult & 255) * lane + (mult >> 8) * g.
-struct SlotMeta {
-    uint32_t sh, mask, base, mult;
+// Lookup recipe of K slot (lane t, slot s): the slot's 64-bit window (slots
+// 0..7: the lane slice shifted left by 7 bits; slots 8..15: the slice's upper
+// two words, or its two words, or its one word) shifted right by `sh` puts
+// the slot's first code at bit 7 (per-lane tables) or bit 2 (shared tables);
+// `mask` keeps the field (pair table: both codes, 2w bits; single table: the
+// first code, w bits) and `base` is the table's byte base, to which the lane
+// adds 4 L unless bit 31 (kSharedTable) is set.  Single-table slots (w >= 4)
+// look up the second code w bits higher (wsh = w); pair-table slots have
+// wsh = 0.
+struct KSlot {
+    uint32_t sh, mask, base, wsh;
 };
+constexpr uint32_t kSharedTable = 0x80000000u;
 
 // Per-head device tables.  All arrays are in codec order unless noted.
 struct HeadTab {
     int32_t n_coded;
-    uint32_t wide_mask;       // decode: slots decoded through the single table
-    int32_t pad[2];
+    int32_t n_wide;           // decode: leading slots (in width order 0, 8, 1, 9, ...) that may hold w >= 4
+    int32_t max_w;            // widest key code
+    int32_t pad;
     uint8_t perm[kD];         // codec index -> original dim
     uint8_t width[kD];        // code width per codec index (0 past n_coded)
     uint8_t plog2[kD];        // log2 of the rotation piece size (0 past n_coded)
     uint8_t slot_pair[4][16]; // decode lane layout: codec pair per (lane, slot)
-    uint8_t slot_w[4][16];    // width of that pair
-    uint8_t slot_sh[4][16];   // field shift inside the slot's 64-bit window
     uint16_t pair_bit[kNB];   // absolute bit position of codec pair m in the K record
     float whiten[kD];
     float dewhiten[kD];
     float inv_sqrt[kD];
     float sign_k[kD];
     float sign_v[kD];
-    SlotMeta kmeta[4][16];    // decode: lookup recipe of (lane t, slot)
+    KSlot kslot[4][16];       // decode: lookup recipe of (lane t, slot)
 };
 
-static_assert(offsetof(HeadTab, kmeta) % 16 == 0 && sizeof(HeadTab) % 16 == 0,
+static_assert(offsetof(HeadTab, kslot) % 16 == 0 && sizeof(HeadTab) % 16 == 0,
               "decode loads the lookup recipes with 16-byte loads");
 
 struct DevTables {
     HeadTab* heads = nullptr;     // [H]
     float* cent = nullptr;        // [9][256] centroids (fp16-exact floats)
     float* thr = nullptr;         // [9][256] thresholds (first 2^w - 1 used)
-    uint32_t* pair_lut = nullptr; // [kPairLutWords]
-    uint16_t* single_lut = nullptr; // [kSingleLutHalves]
-    uint32_t* dec_image = nullptr;  // [kImgWords] decode shared-memory image
+    uint32_t* img_src = nullptr;  // [kImageMaxWords] decode tables: per-lane entries, then shared words
 };
 
 // Where the records of (sequence b, head h, position pos) live: token slot
@@ -128,9 +133,8 @@ struct bgtq_plan {
     std::vector<bgtq::HeadTab> heads;
     std::vector<float> cent[bgtq::kWMax + 1];
     std::vector<float> thr[bgtq::kWMax + 1];
-    std::vector<uint32_t> pair_lut;
-    std::vector<uint16_t> single_lut;
-    std::vector<uint32_t> dec_image;
+    std::vector<uint32_t> img_src;  // decode table entries (see single_base)
+    int img_ws = 0;                 // widest code the decode tables cover
     // inspection copies (bgtq_plan_get_head)
     std::vector<std::vector<int8_t>> sign_k8, sign_v8;
     std::vector<std::vector<uint8_t>> piece;
@@ -154,6 +158,7 @@ cudaError_t launch_logit_mae(const bgtq_plan& p, cudaStream_t s, const void* q, 
 struct SplitPlan {
     int n_split = 1;
     int tokens_per_split = 64;
+    int slack = 0;  // the newest range (split 0) holds about this many tokens fewer
 };
 SplitPlan decode_split(const bgtq_plan& p, int batch, int64_t max_len);
 size_t decode_workspace_bytes(const bgtq_plan& p, int batch, const SplitPlan& sp);

@@ -9,6 +9,7 @@
 #include <cmath>
 #include <map>
 #include <mutex>
+#include <tuple>
 
 #include "decode_kernel.cuh"
 
@@ -19,48 +20,58 @@ namespace {
 // clusters (cluster placement can leave SMs unusable, so this is at most
 // the SM count times the blocks per SM).
 template <int BK, int BV>
-int resident_ctas() {
+int resident_ctas(int ws) {
     if (ensure_smem_attr<BK, BV, false>() != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = launch_config<BK, BV>(dim3(kCluster, 1, 1), nullptr, attr);
+    cudaLaunchConfig_t cfg = launch_config<BK, BV>(dim3(kCluster, 1, 1), nullptr, ws, attr);
     cfg.numAttrs = 1;  // occupancy: the cluster shape only
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, decode_kernel<BK, BV, 2, false>, &cfg) != cudaSuccess || clusters <= 0) {
         cudaGetLastError();
         return 0;
     }
-    return clusters * kCluster;
+    // never more than the SMs hold block by block (registers, shared memory)
+    int per_sm = 0, dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<BK, BV, 2, false>, kWarps * 32,
+                                                      cfg.dynamicSmemBytes) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    const int cap = per_sm * sms / kCluster * kCluster;
+    return std::min(clusters * kCluster, cap);
 }
 
-int resident_ctas_for(int bk, int bv) {
+int resident_ctas_for(int bk, int bv, int ws) {
     static std::mutex mu;
-    static std::map<std::pair<int, int>, int> cache;
+    static std::map<std::tuple<int, int, int>, int> cache;
     int dev = 0;
     cudaGetDevice(&dev);
     const int key = bk * 10 + bv;
     std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find({dev, key});
+    auto it = cache.find({dev, key, ws});
     if (it != cache.end()) return it->second;
     int n = 0;
     switch (key) {
-        case 11: n = resident_ctas<1, 1>(); break;
-        case 12: n = resident_ctas<1, 2>(); break;
-        case 13: n = resident_ctas<1, 3>(); break;
-        case 14: n = resident_ctas<1, 4>(); break;
-        case 21: n = resident_ctas<2, 1>(); break;
-        case 22: n = resident_ctas<2, 2>(); break;
-        case 23: n = resident_ctas<2, 3>(); break;
-        case 24: n = resident_ctas<2, 4>(); break;
-        case 31: n = resident_ctas<3, 1>(); break;
-        case 32: n = resident_ctas<3, 2>(); break;
-        case 33: n = resident_ctas<3, 3>(); break;
-        case 34: n = resident_ctas<3, 4>(); break;
+        case 11: n = resident_ctas<1, 1>(ws); break;
+        case 12: n = resident_ctas<1, 2>(ws); break;
+        case 13: n = resident_ctas<1, 3>(ws); break;
+        case 14: n = resident_ctas<1, 4>(ws); break;
+        case 21: n = resident_ctas<2, 1>(ws); break;
+        case 22: n = resident_ctas<2, 2>(ws); break;
+        case 23: n = resident_ctas<2, 3>(ws); break;
+        case 24: n = resident_ctas<2, 4>(ws); break;
+        case 31: n = resident_ctas<3, 1>(ws); break;
+        case 32: n = resident_ctas<3, 2>(ws); break;
+        case 33: n = resident_ctas<3, 3>(ws); break;
+        case 34: n = resident_ctas<3, 4>(ws); break;
         default: n = 0;
     }
-    cache[{dev, key}] = n;
+    cache[{dev, key, ws}] = n;
     return n;
 }
 
@@ -73,7 +84,8 @@ SplitPlan decode_split(const bgtq_plan& p, int batch, int64_t max_len) {
     SplitPlan sp;
     const int64_t units = std::max<int64_t>(1, (int64_t)batch * p.H);
     const int64_t len = std::max<int64_t>(max_len, 1);
-    int64_t slots = (p.bk >= 1 && p.bk <= 3 && p.bv >= 1 && p.bv <= 4) ? resident_ctas_for(p.bk, p.bv) : 0;
+    int64_t slots = (p.bk >= 1 && p.bk <= 3 && p.bv >= 1 && p.bv <= 4)
+                        ? resident_ctas_for(p.bk, p.bv, p.img_ws) : 0;
     if (slots <= 0) slots = std::max(1, p.num_sms);
     // Leave one cluster's room for a kernel that programmatic dependent
     // launch starts early next to this one, so that every cluster of this
@@ -90,10 +102,29 @@ SplitPlan decode_split(const bgtq_plan& p, int batch, int64_t max_len) {
     ns = std::min<int64_t>(ns, (int64_t)kCluster * kMaxClusters);
     if (len >= kStepTok * kCluster) ns = std::max<int64_t>(ns, kCluster);
     ns = std::max<int64_t>(ns, 1);
-    int64_t tps = (len + ns - 1) / ns;
-    tps = (tps + kStepTok - 1) / kStepTok * kStepTok;
-    const int64_t n = (len + tps - 1) / tps;
+    // The newest range (split 0) is shorter by `slack` tokens: in a fused
+    // decode step its CTA first appends the new token (a few microseconds of
+    // encoding).  The ranges are the same with and without the append, so
+    // both paths merge identical partials.  Ranges are whole 16-token tiles.
+    int64_t slack = 0, tps = 0;
+    for (;; ++ns) {
+        slack = std::min<int64_t>(256, (len + ns - 1) / ns / 4) / kTile * kTile;
+        tps = (len + slack + ns - 1) / ns;
+        tps = std::max<int64_t>((tps + kTile - 1) / kTile * kTile, kStepTok);
+        if (tps <= kMaxSplitTokens) break;
+        if (ns >= (int64_t)kCluster * kMaxClusters) {  // the longest sequences: no slack
+            slack = 0;
+            tps = std::max<int64_t>(((len + ns - 1) / ns + kTile - 1) / kTile * kTile, kStepTok);
+            break;
+        }
+    }
+    // splits the kernel makes active for a sequence of len tokens (at most
+    // that for shorter ones): split 0 holds [a0, len), a0 = len - tps + slack
+    // rounded up to a tile
+    const int64_t a0 = std::max<int64_t>(0, (len - tps + slack + kTile - 1) / kTile * kTile);
+    const int64_t n = 1 + (a0 + tps - 1) / tps;
     sp.tokens_per_split = (int)tps;
+    sp.slack = (int)slack;
     sp.n_split = (int)((n + kCluster - 1) / kCluster * kCluster);
     return sp;
 }
@@ -127,15 +158,18 @@ cudaError_t launch_decode(const bgtq_plan& pl, cudaStream_t s, const void* q, co
     p.count = static_cast<uint32_t*>(ws);
     p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + counters);
     p.heads = pl.dev.heads;
-    p.pair_lut = pl.dev.pair_lut;
-    p.single_lut = pl.dev.single_lut;
-    p.dec_image = pl.dev.dec_image;
+    p.img_src = pl.dev.img_src;
+    p.img_lane = lane_entries(pl.img_ws);
+    p.img_shared = shared_words(pl.img_ws);
+    p.img_ws = pl.img_ws;
+    p.img_bytes = 0;  // set at launch
     p.scale_log2 = scale * 1.4426950408889634f;
     p.v_inv_sqrt = (float)(1.0 / std::sqrt((double)kD));
     p.H = pl.H;
     p.G = pl.G;
     p.n_split = sp.n_split;
     p.tps = sp.tokens_per_split;
+    p.slack = sp.slack;
     p.status = status;
     p.k_new = static_cast<const __half*>(k_new);
     p.v_new = static_cast<const __half*>(v_new);
@@ -144,11 +178,10 @@ cudaError_t launch_decode(const bgtq_plan& pl, cudaStream_t s, const void* q, co
     p.k_recent = static_cast<__half*>(c.k_recent);
     p.recent = c.recent;
     dim3 grid((unsigned)sp.n_split, (unsigned)pl.H, (unsigned)batch);
-    // the fast instance checks only slots 0 and 8 (each lane's two widest
-    // pairs) for codes wider than the pair tables; the general instance
-    // checks every slot
+    // the fast instances decode codes of width >= 4 only in each lane's
+    // kFastWide widest slots; the general instance in any slot
     bool any_wide = false;
-    for (const HeadTab& ht : pl.heads) any_wide |= (ht.wide_mask & ~((1u << 0) | (1u << 8))) != 0;
+    for (const HeadTab& ht : pl.heads) any_wide |= ht.n_wide > kFastWide;
     const int kind = any_wide ? 2 : (c.recent > 0 ? 1 : 0);
     if (c.page_table) return launch_decode_paged(p, grid, s, kind, pl.bk, pl.bv);
     const int key = pl.bk * 10 + pl.bv;

@@ -11,16 +11,17 @@
 // process exits.
 //
 // Rules for callers:
-//   - The first call on a device looks up the array's device address (with
-//     that device current) and caches it; make that first call before any
-//     stream capture.
+//   - Every call looks up the array's device address on the current device
+//     (cudaGetSymbolAddress, a host-side lookup, not a stream operation), so
+//     a context that was reset and re-created gets the array's new address.
+//     The first call on a device may load the library's device code into the
+//     context; make that first call before any stream capture.
 //   - All calls share the array and it keeps the last call's contents, so
 //     calls that overlap on the GPU (different streams, no ordering) race and
 //     give wrong results.  Calls ordered on one stream are fine.
 //   - Problems whose merge scratch would exceed kScratchBytes are rejected
 //     with BGTQ_ERR_WORKSPACE; use bgtq_decode_attn with a workspace instead.
 #include <cmath>
-#include <mutex>
 
 #include "bgtq_internal.h"
 
@@ -28,28 +29,22 @@ namespace bgtq {
 namespace {
 
 constexpr size_t kScratchBytes = (size_t)2 << 20;  // 2 MiB
-constexpr int kMaxDevices = 64;
-
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
-std::mutex g_scratch_mutex;
-void* g_scratch_ptr[kMaxDevices] = {nullptr};
-
-// Device address of g_decode_scratch on the current device (looked up once).
+// Device address of g_decode_scratch in the current device's context.  Looked
+// up on every call rather than cached per device ordinal: after
+// cudaDeviceReset (or a released primary context) the module is loaded again
+// and the array may live at another address.
 int scratch_address(void** out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return set_error(BGTQ_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxDevices) return set_error(BGTQ_ERR_UNSUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void* ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
-        if (e != cudaSuccess || !ptr)
-            return set_error(BGTQ_ERR_CUDA, "cudaGetSymbolAddress(decode scratch): %s", cudaGetErrorString(e));
-        g_scratch_ptr[dev] = ptr;
-    }
-    *out = g_scratch_ptr[dev];
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
+    if (e != cudaSuccess || !ptr)
+        return set_error(BGTQ_ERR_CUDA, "cudaGetSymbolAddress(decode scratch) on device %d: %s", dev,
+                         cudaGetErrorString(e));
+    *out = ptr;
     return BGTQ_OK;
 }
 

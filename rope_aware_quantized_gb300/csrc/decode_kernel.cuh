@@ -9,9 +9,9 @@
 //
 // Per CTA: one (sequence, KV head, token split), 4 warps; thread-block
 // clusters of 8 consecutive splits.  Before waiting for the previous kernel
-// (programmatic dependent launch) a CTA prefetches its token range into L2,
-// copies the plan's table image into shared memory and loads its per-lane
-// lookup recipes.  After the wait: the fused step's owning CTA quantize-
+// (programmatic dependent launch) a CTA builds the lookup tables in shared
+// memory (one copy per lane) and loads its per-lane lookup recipes.  After
+// the wait: the fused step's owning CTA quantize-
 // appends the new token; the G query heads are rotated once into the key
 // codec domain (de-whitening, signs, blockwise Hadamard, 1/sqrt(piece),
 // softmax scale and log2 e folded in), scaled per head by a power of two into
@@ -20,12 +20,15 @@
 // 16-token tile, tiles staged in shared memory by cp.async:
 //   S^T = Q_hilo . K_hat^T     8 k-chunks x 2 token n-tiles of m16n8k16 mma;
 //                              K_hat fragments come from a 64-bit window of
-//                              the lane's K record slice, one shift + mask +
-//                              one shared-memory pair-table lookup per 2 coords
+//                              the lane's K record slice: one shift + mask and
+//                              one lookup in the lane's own copy of a pair
+//                              table per 2 coords (codes of 4+ bits: one
+//                              lookup per code in a single-code table)
 //   logits = (hi + lo rows) * rho_K * scale, online softmax per head (exp2)
-//   O_hilo += P_hilo . V_hat   16 dim n-tiles of m16n8k16 mma; P' = p*rho_V
-//                              split hi + lo into the A rows; V_hat fragments
-//                              come straight from the token-pair V records
+//   O^T += V_hat^T . P'        8 dim m-tiles of m16n8k16 mma, twice (P' =
+//                              p*rho_V split hi + lo into two B operands);
+//                              V_hat fragments come straight from the
+//                              token-pair V records through the pair table
 // Epilogue: each warp leaves its partial (m, l, acc) in shared memory; CTA
 // rank r of the cluster reduces query head r over the cluster's 32 warp
 // partials through distributed shared memory and writes one cluster partial
@@ -60,12 +63,14 @@ struct DecodeParams {
     float* part;
     uint32_t* count;
     const HeadTab* heads;
-    const uint32_t* pair_lut;
-    const uint16_t* single_lut;
-    const uint32_t* dec_image;
+    const uint32_t* img_src;  // lookup tables: img_lane per-lane entries, then img_shared shared words
+    int img_lane, img_shared;
+    int img_ws;               // widest code the tables cover
+    int img_bytes;            // bytes of the table region of the dynamic shared memory
     float scale_log2;
     float v_inv_sqrt;
     int H, G, n_split, tps;
+    int slack;  // the newest token range is shorter by about this many tokens (multiple of 16)
     int32_t* status;
     // fused step: one new token per (sequence, KV head) quantize-appended at
     // pos_new[b] before attention (k_new == nullptr: attention only)
@@ -94,8 +99,9 @@ constexpr int kMaxClusters = 64;  // clusters per (sequence, head)
 constexpr int64_t kMaxSplitTokens = 4096;  // longest token split of one CTA
 constexpr int kMaxTilesPerWarp = (int)(kMaxSplitTokens / (kWarps * 16));  // 16-token tiles of one warp
 constexpr int kPartStride = 2 + kD;  // m, l, acc[128] per query head
-constexpr uint32_t kPrivByte = 4u * kImgPriv;
-constexpr int kPrivMaxW = 3;
+// leading slots (width order 0, 8, 1, 9, ...) that may hold codes of width >= 4
+// in the fast instances; the general instance treats every slot so
+constexpr int kFastWide = 8;
 // Softmax reference (log2 domain): set kLift above the largest logit when it
 // is moved, moved again only when a logit passes it by more than kSlack.  The
 // weights p then stay in (0, 2^kSlack] and the largest is >= 2^-kLift after a
@@ -128,41 +134,6 @@ __device__ __forceinline__ unsigned ticket_acq_rel(unsigned* ptr) {
     return old;
 }
 
-// One thread's L2 prefetch of [base, base + bytes), rounded inward to
-// 16-byte boundaries, in 16 KB pieces.
-__device__ __forceinline__ void prefetch_span(const char* base, size_t bytes);
-
-// Bulk prefetch of [ptr, ptr + bytes) into L2 (16-byte aligned, multiple of 16).
-__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(ptr), "r"(bytes) : "memory");
-}
-
-// Prefetch the 16-byte-aligned part of [base, base + bytes) in 16 KB pieces
-// spread over the CTA's threads (the bulk prefetch needs 16-byte aligned
-// addresses and sizes, so the range is shrunk to the aligned interior).
-__device__ __forceinline__ void prefetch_range(const char* base, size_t bytes, int tid) {
-    constexpr size_t kChunk = 16384;
-    const uintptr_t a0 = (reinterpret_cast<uintptr_t>(base) + 15) & ~(uintptr_t)15;
-    const uintptr_t a1 = (reinterpret_cast<uintptr_t>(base) + bytes) & ~(uintptr_t)15;
-    if (a1 <= a0) return;
-    const size_t total = a1 - a0;
-    const size_t n = (total + kChunk - 1) / kChunk;
-    for (size_t i = tid; i < n; i += kWarps * 32) {
-        const size_t off = i * kChunk;
-        const size_t len = total - off < kChunk ? total - off : kChunk;
-        prefetch_l2(reinterpret_cast<const void*>(a0 + off), (uint32_t)len);
-    }
-}
-
-__device__ __forceinline__ void prefetch_span(const char* base, size_t bytes) {
-    const uintptr_t a0 = (reinterpret_cast<uintptr_t>(base) + 15) & ~(uintptr_t)15;
-    const uintptr_t a1 = (reinterpret_cast<uintptr_t>(base) + bytes) & ~(uintptr_t)15;
-    for (uintptr_t a = a0; a < a1; a += 16384) {
-        const uintptr_t len = a1 - a < 16384 ? a1 - a : 16384;
-        prefetch_l2(reinterpret_cast<const void*>(a), (uint32_t)len);
-    }
-}
-
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
 // hi = fp16(x), lo = fp16(x - hi) for a pair of values
@@ -171,11 +142,6 @@ __device__ __forceinline__ void split_hilo(float x0, float x1, uint32_t& hi, uin
     const float2 hf = __half22float2(h);
     hi = h2_bits(h);
     lo = h2_bits(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
-}
-
-template <int BK>
-__device__ __forceinline__ uint32_t kword(const uint32_t (&kw)[BK], int i) {
-    return i < BK ? kw[i < BK ? i : 0] : 0u;
 }
 
 __device__ __forceinline__ uint32_t lds32(const uint32_t* tab, uint32_t byte) {
@@ -188,78 +154,96 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// Decoded fp16 pair of K slot S (compile-time) of the lane's record slice.
-// (sh, mask, base) select the field and the table: the field is shifted so
-// that it lands pre-multiplied by the entry stride of its table (shared
-// tables: 4 bytes; per-token-lane copies: 32 bytes; per-lane copies: 128
-// bytes), masked and OR-ed with the copy's byte base.  Slots flagged in
-// `wide` use the single-entry table (two lookups, 16-byte entry stride).
-template <int BK, int S, bool kCheckWide>
-__device__ __forceinline__ uint32_t k_pair(const uint32_t (&kw)[BK], uint32_t sh, uint32_t mask, uint32_t base,
-                                           uint32_t wide, const uint32_t* s_tab, const uint16_t* s_single) {
-    constexpr bool kUpper = (BK == 3 && S >= 8);
-    static_assert(BK >= 1 && BK <= 3, "K record slices of 1..3 words");
-    const uint32_t lo = kUpper ? kword(kw, 1) : kword(kw, 0);
-    const uint32_t hi = kUpper ? kword(kw, 2) : kword(kw, 1);
-    const uint64_t win = ((uint64_t)hi << 32) | lo;
-    // slot 0 starts at bit 0: its field is shifted left (by sh) instead
-    if (!kCheckWide || !((wide >> S) & 1u)) {
-        const uint32_t x = S == 0 ? (kword(kw, 0) << sh) : (uint32_t)(win >> sh);
-        return lds32(s_tab, (x & mask) | base);
-    }
-    const uint32_t x = S == 0 ? (kword(kw, 0) << sh) : (uint32_t)(win >> sh);
-    const uint32_t w = __popc(mask);
-    const uint32_t a0 = (x & mask) | base;
-    const uint32_t a1 = ((x >> w) & mask) | base;
-    const uint32_t h0 = *reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(s_single) + a0);
-    const uint32_t h1 = *reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(s_single) + a1);
-    return h0 | (h1 << 16);
+// 64-bit windows of one token's K lane slice (BK words): slots 0..7 read the
+// slice shifted left by 7 bits, slots 8..15 its upper words (see KSlot).
+template <int BK>
+__device__ __forceinline__ uint64_t kwin_lo(const uint32_t (&kw)[BK]) {
+    if constexpr (BK >= 2) return ((((uint64_t)kw[1]) << 32) | kw[0]) << 7;
+    else return ((uint64_t)kw[0]) << 7;
+}
+template <int BK>
+__device__ __forceinline__ uint64_t kwin_hi(const uint32_t (&kw)[BK]) {
+    if constexpr (BK == 3) return (((uint64_t)kw[2]) << 32) | kw[1];
+    else if constexpr (BK == 2) return (((uint64_t)kw[1]) << 32) | kw[0];
+    else return (uint64_t)kw[0];
 }
 
-// Decoded fp16 pair (even token, odd token) of V codec dim 16*g + ND from the
-// lane-group's BV words of a token-pair record (compile-time bit position).
-template <int BV, int ND>
-__device__ __forceinline__ uint32_t v_pair(const uint32_t (&vw)[BV], uint32_t vbase, const uint32_t* s_tab) {
+// Decoded fp16 pair of one K slot: one lookup in the lane's copy of a pair
+// table or, for slots whose codes may be 4 bits or wider (kMayWide), a second
+// lookup of the second code in the single table.  A pair-table slot has
+// wsh = 0: its second lookup repeats the first and the byte permutation
+// keeps that word whole; a single-table entry holds its value in both halves,
+// so the permutation joins the first code's low half to the second's high.
+template <bool kMayWide>
+__device__ __forceinline__ uint32_t k_lookup(uint64_t win, uint32_t sh, uint32_t mask, uint32_t base, uint32_t wsh,
+                                             const uint32_t* s_tab) {
+    const uint32_t x = (uint32_t)(win >> sh);
+    const uint32_t v0 = lds32(s_tab, (x & mask) | base);
+    if constexpr (!kMayWide) return v0;
+    const uint32_t v1 = lds32(s_tab, ((x >> wsh) & mask) | base);
+    return __byte_perm(v0, v1, 0x7610);
+}
+
+// Rank of slot S in the lane's width order (slots 0, 8, 1, 9, ...).
+template <int S>
+__host__ __device__ constexpr int slot_rank() { return S < 8 ? 2 * S : 2 * (S - 8) + 1; }
+
+// Decoded fp16 pair (even token, odd token) of V codec dim 16 g + J from the
+// lane group's BV words of a token-pair record (compile-time bit position):
+// the field is brought to bit 7 and looked up in the lane's pair table
+// (BV <= 3), or its two codes in the width-4 single table (BV = 4).
+template <int BV, int J>
+__device__ __forceinline__ uint32_t v_field(const uint32_t (&vw)[BV], uint32_t vbase, const uint32_t* s_tab) {
     constexpr int FB = 2 * BV;
-    constexpr int O = FB * ND;
+    constexpr int O = FB * J;
     constexpr int WI = O >> 5, SH = O & 31;
-    constexpr int PS = BV <= kPrivMaxW ? 7 : 2;  // entry stride 128 B (per-lane) or 4 B (shared)
-    constexpr uint32_t MASK = ((1u << FB) - 1u) << PS;
     uint32_t x;
     if constexpr (SH + FB <= 32) {
-        if constexpr (SH >= PS)
-            x = vw[WI] >> (SH - PS);
+        if constexpr (SH >= 7)
+            x = vw[WI] >> (SH - 7);
         else
-            x = vw[WI] << (PS - SH);
+            x = vw[WI] << (7 - SH);
     } else {
-        x = __funnelshift_r(vw[WI], vw[WI + 1 < BV ? WI + 1 : WI], SH - PS);
+        x = __funnelshift_r(vw[WI], vw[WI + 1 < BV ? WI + 1 : WI], SH - 7);
     }
-    return lds32(s_tab, (x & MASK) | vbase);
+    if constexpr (BV <= kPairTableMaxW) {
+        constexpr uint32_t MASK = ((1u << FB) - 1u) << 7;
+        return lds32(s_tab, (x & MASK) | vbase);
+    } else {
+        constexpr uint32_t MASK = ((1u << BV) - 1u) << 7;
+        const uint32_t v0 = lds32(s_tab, (x & MASK) | vbase);
+        const uint32_t v1 = lds32(s_tab, ((x >> BV) & MASK) | vbase);
+        return __byte_perm(v0, v1, 0x7610);
+    }
 }
 
-template <int BK, int C, bool kAnyWide>
-__device__ __forceinline__ void s_chunk(float (&sacc)[2][4], const uint32_t (&qa)[8][4], const uint32_t (&kw)[2][BK],
-                                        const uint32_t (&ksh)[16], const uint32_t (&kmask)[16],
-                                        const uint32_t (&kbase)[16], uint32_t wide, const uint32_t* s_tab,
-                                        const uint16_t* s_single) {
-    constexpr bool kW0 = kAnyWide || (2 * C == 0) || (2 * C == 8);
-    constexpr bool kW1 = kAnyWide;
+// S^T += Q_hilo . K_hat^T for k-chunk C (slots 2C, 2C+1) of both 8-token
+// groups of the tile.
+template <int NW, int C>
+__device__ __forceinline__ void s_chunk(float (&sacc)[2][4], const uint32_t (&qa)[8][4], const uint64_t (&wl)[2],
+                                        const uint64_t (&wh)[2], const uint32_t (&ksh)[16], const uint32_t (&kmask)[16],
+                                        const uint32_t (&kbase)[16], const uint32_t (&kwsh)[16], const uint32_t* s_tab) {
+    constexpr int S0 = 2 * C, S1 = 2 * C + 1;
+    constexpr bool W0 = slot_rank<S0>() < NW, W1 = slot_rank<S1>() < NW;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-        const uint32_t b0 =
-            k_pair<BK, 2 * C, kW0>(kw[nt], ksh[2 * C], kmask[2 * C], kbase[2 * C], wide, s_tab, s_single);
-        const uint32_t b1 = k_pair<BK, 2 * C + 1, kW1>(kw[nt], ksh[2 * C + 1], kmask[2 * C + 1], kbase[2 * C + 1],
-                                                       wide, s_tab, s_single);
+        const uint64_t win = C < 4 ? wl[nt] : wh[nt];
+        const uint32_t b0 = k_lookup<W0>(win, ksh[S0], kmask[S0], kbase[S0], kwsh[S0], s_tab);
+        const uint32_t b1 = k_lookup<W1>(win, ksh[S1], kmask[S1], kbase[S1], kwsh[S1], s_tab);
         mma16816(sacc[nt], qa[C], b0, b1);
     }
 }
 
-template <int BV, int ND>
-__device__ __forceinline__ void pv_tile(float (&acc)[16][4], const uint32_t (&pa)[4], const uint32_t (&vw)[2][BV],
-                                        uint32_t vbase, const uint32_t* s_tab) {
-    const uint32_t b0 = v_pair<BV, ND>(vw[0], vbase, s_tab);
-    const uint32_t b1 = v_pair<BV, ND>(vw[1], vbase, s_tab);
-    mma16816(acc[ND], pa, b0, b1);
+// O^T += V_hat^T . P' for dim tile MT (codec dims 16 g + 2 MT and + 1 of the
+// lane groups g = 0..7): A = the decoded value pairs of token pairs t and
+// t + 4, B = the weights P' of the 16 tokens split hi + lo (two mma).
+template <int BV, int MT>
+__device__ __forceinline__ void pv_mtile(float (&acc)[8][4], const uint32_t (&pb)[2][2], const uint32_t (&vw)[2][BV],
+                                         uint32_t vbase, const uint32_t* s_tab) {
+    const uint32_t a[4] = {v_field<BV, 2 * MT>(vw[0], vbase, s_tab), v_field<BV, 2 * MT + 1>(vw[0], vbase, s_tab),
+                           v_field<BV, 2 * MT>(vw[1], vbase, s_tab), v_field<BV, 2 * MT + 1>(vw[1], vbase, s_tab)};
+    mma16816(acc[MT], a, pb[0][0], pb[0][1]);
+    mma16816(acc[MT], a, pb[1][0], pb[1][1]);
 }
 
 // Blockwise Hadamard butterflies over the warp's 128 slots (lane L holds
@@ -301,15 +285,26 @@ struct StageLayout {
     static_assert(kK % 16 == 0 && kV % 16 == 0, "16-byte copies");
 };
 
-// Dynamic shared memory of decode_kernel<BK, BV>: the table image, the
-// rotated queries, then kStages staged tiles per warp.
-constexpr int kSmemTab = 0;
-constexpr int kSmemQ = kImgWords * 4;
-constexpr int kSmemStage = kSmemQ + 8 * kD * 4;
-template <int BK, int BV>
-constexpr int decode_smem_bytes() {
-    return kSmemStage + kWarps * kStages * StageLayout<BK, BV>::kBytes;
+// Dynamic shared memory of decode_kernel<BK, BV>: the lookup tables (img_bytes
+// of them, at least the size of the per-warp and per-CTA partials that
+// reuse the region after the main loop), then kStages staged tiles per warp.
+// The rotated queries live at the start of the staging region until the
+// first tiles are staged.
+constexpr int kPartBytes = (kWarps + 1) * 8 * kPartStride * 4;
+inline int decode_table_bytes(int ws) {
+    const int b = (image_bytes(ws) + 127) / 128 * 128;
+    return b > kPartBytes ? b : (kPartBytes + 127) / 128 * 128;
 }
+template <int BK, int BV>
+constexpr int decode_stage_bytes() {
+    return kWarps * kStages * StageLayout<BK, BV>::kBytes;
+}
+template <int BK, int BV>
+int decode_smem_bytes(int ws) {
+    return decode_table_bytes(ws) + decode_stage_bytes<BK, BV>();
+}
+static_assert(kWarps * kStages * StageLayout<1, 1>::kBytes >= 8 * kD * 4, "the rotated queries fit the staging region");
+static_assert(kWarps * kStages * StageLayout<1, 1>::kBytes >= kImageMaxWords * 4, "the table source fits the staging region");
 
 // 16-byte (or, for the norms, 4-byte) asynchronous copy global -> shared;
 // `valid` false copies nothing and zero-fills.
@@ -453,12 +448,12 @@ struct BoolTag {
 // so that the instances without them carry none of their code.
 template <int BK, int BV, int kKind, bool kPaged>
 __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) {
-    constexpr bool kAnyWide = kKind == 2;
+    constexpr int NW = kKind == 2 ? 16 : kFastWide;  // leading slots that may hold codes of width >= 4
     constexpr bool kWinPath = kKind >= 1;
     extern __shared__ __align__(16) uint8_t dsmem[];
-    uint32_t* s_tab = reinterpret_cast<uint32_t*>(dsmem + kSmemTab);
-    const uint16_t* s_single = reinterpret_cast<const uint16_t*>(s_tab);
-    float (*s_q)[kD] = reinterpret_cast<float (*)[kD]>(dsmem + kSmemQ);
+    uint32_t* s_tab = reinterpret_cast<uint32_t*>(dsmem);
+    uint8_t* s_stage = dsmem + p.img_bytes;
+    float (*s_q)[kD] = reinterpret_cast<float (*)[kD]>(s_stage);
     __shared__ float s_qunscale[8];
     __shared__ int s_last;
     __shared__ float s_thr[kThrCompact];                 // fused step: encoder thresholds
@@ -470,7 +465,6 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     // and then the CTA's merged partial of the 8 heads
     float (*s_wp)[8][kPartStride] = reinterpret_cast<float (*)[8][kPartStride]>(s_tab);
     float (*s_cp)[kPartStride] = reinterpret_cast<float (*)[kPartStride]>(s_tab + kWarps * 8 * kPartStride);
-    static_assert((kWarps + 1) * 8 * kPartStride <= kImgWords, "partials fit in the table region");
 
     // The next kernel may launch right away; everything this kernel reads
     // that an earlier kernel may still be writing (q, the cache, the
@@ -487,13 +481,16 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         if (tid == 0 && split == 0 && h == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_SEQLEN_CAPACITY);
         seq = seq < 0 ? 0 : (int)p.cap;
     }
-    const int n_active = (seq + p.tps - 1) / p.tps;
+    // Token ranges, newest first: split 0 attends [a0, seq) with a0 the
+    // multiple of 16 at or above seq - (tps - slack), split s >= 1 the tps
+    // tokens [a0 - s tps, a0 - (s - 1) tps) (the oldest one clipped at 0).
+    // CTAs start in split order, so the newest tokens, and in a fused step
+    // the append, go to the CTA that starts first, and its range is shorter
+    // by about `slack` tokens to make up for the append.
+    const int a0 = max(0, (seq - p.tps + p.slack + 15) & ~15);
+    const int n_active = 1 + (a0 + p.tps - 1) / p.tps;
     const int n_clusters = (n_active + kCluster - 1) / kCluster;
     const int cid = split / kCluster;
-    // Split s < n_active attends token range n_active - 1 - s (tokens
-    // tps r .. tps (r + 1) - 1 of range r).  CTAs start in split order, so
-    // the newest tokens, and in a fused step the append, go to the CTA that
-    // starts first.
     // Fused step: the CTA whose token range holds the new position appends
     // the new token before attending (split 0 when the position is not
     // attended).  pos_new is read before the wait, like seq_lens.
@@ -503,7 +500,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     if (p.k_new) {
         pos = p.pos_new[b];
         pos_bad = pos < 0 || (int64_t)pos + 1 > p.cap;
-        owner = !pos_bad && split == (pos < seq ? n_active - 1 - pos / p.tps : 0);
+        owner = !pos_bad && split == (pos < seq && pos < a0 ? 1 + (a0 - 1 - pos) / p.tps : 0);
         if (owner) {
             stage_thresholds(s_thr, p.thr, tid, kWarps * 32);
             if (warp < 2) enc_lane_load(el, p.heads + h, warp == 0, BV, p.v_inv_sqrt, lane);
@@ -534,8 +531,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     const int crank = (int)cluster.block_rank();
     const bool active = split < n_active;
     const HeadTab* ht = p.heads + h;
-    const int t_begin = active ? (n_active - 1 - split) * p.tps : seq;
-    const int t_end = min(t_begin + p.tps, seq);
+    const int t_begin = !active ? seq : split == 0 ? a0 : max(0, a0 - split * p.tps);
+    const int t_end = !active ? seq : split == 0 ? seq : a0 - (split - 1) * p.tps;
     const int wstart = p.recent > 0 ? max(0, seq - (int)p.recent) : seq;  // first position of the fp16 keys
     // record bases: the (sequence, head) row of a contiguous cache (token
     // slot = position), the pools of a paged one (token slot per tile)
@@ -575,49 +572,55 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         if (owner) sl_new = p.map.slot(b, h, pos);
     }
 
-    // ---- plan-static set-up, before waiting for the previous kernel: L2
-    // prefetch of the token range, the table image, the per-lane recipes
+    // ---- plan-static set-up, before waiting for the previous kernel: the
+    // lookup tables, the per-lane recipes
     const int n_coded = ht->n_coded;
     int q_pl[4], q_src[4];
     float q_f[4], q_sc[4];
-    uint32_t ksh[16], kmask[16], kbase[16];
+    uint32_t ksh[16], kmask[16], kbase[16], kwsh[16];
     uint32_t slot_pairs[4];
-    if (active && !paged) {
-        prefetch_range(reinterpret_cast<const char*>(kc + (size_t)t_begin * (16 * BK)),
-                       (size_t)(t_end - t_begin) * (16 * BK), tid);
-        prefetch_range(reinterpret_cast<const char*>(vc + (size_t)(t_begin / 2) * (32 * BV)),
-                       (size_t)((t_end - t_begin + 1) / 2) * (32 * BV), tid);
-        prefetch_range(reinterpret_cast<const char*>(kn + t_begin), (size_t)(t_end - t_begin) * 4, tid);
-        prefetch_range(reinterpret_cast<const char*>(vn + t_begin), (size_t)(t_end - t_begin) * 4, tid);
-    } else if (kPaged && active) {
-        // paged: thread i prefetches the part of page i of the range (the
-        // page table is read before the wait, like seq_lens)
+    // (no L2 prefetch of the token range before the wait: under programmatic
+    // dependent launch it competes with the previous kernel's own reads)
+    if (kPaged && active) {
+        // paged: thread i checks the page-table entry of page i of the range
+        // (the page table is read before the wait, like seq_lens); the main
+        // loop reads page 0 in place of a bad one
         const int lp = p.map.lp;
         const int pg0 = t_begin >> lp, pg1 = (t_end - 1) >> lp;
         for (int pi = pg0 + tid; pi <= pg1; pi += kWarps * 32) {
             const int a = (int)max((int64_t)t_begin, (int64_t)pi << lp);
-            const int e = (int)min((int64_t)t_end, (int64_t)(pi + 1) << lp);
-            const int64_t sl = p.map.slot(b, h, a);
-            if (sl < 0) {
-                if (p.status) atomicOr(p.status, BGTQ_STATUS_PAGE_RANGE);
-                continue;
-            }
-            prefetch_span(reinterpret_cast<const char*>(kc + sl * (16 * BK)), (size_t)(e - a) * (16 * BK));
-            prefetch_span(reinterpret_cast<const char*>(vc + (sl >> 1) * (32 * BV)), (size_t)((e - a + 1) / 2) * (32 * BV));
-            prefetch_span(reinterpret_cast<const char*>(kn + sl), (size_t)(e - a) * 4);
-            prefetch_span(reinterpret_cast<const char*>(vn + sl), (size_t)(e - a) * 4);
+            if (p.map.slot(b, h, a) < 0 && p.status) atomicOr(p.status, BGTQ_STATUS_PAGE_RANGE);
         }
     }
     if (active) {
-        // the table image: independent 16-byte loads, then the stores
-        constexpr int kPer = kImgWords / 4 / (kWarps * 32);
-        static_assert(kImgWords % (4 * kWarps * 32) == 0, "image size");
-        uint4 img[kPer];
-        const uint4* src = reinterpret_cast<const uint4*>(p.dec_image);
+        // the lookup tables: the compact source into the (not yet used)
+        // staging region with independent loads, then 32 copies (one per lane)
+        // of every per-lane entry, entry e of lane L at word 32 e + L (a
+        // 16-byte store covers 4 lanes), and one copy of the shared words
+        {
+            uint32_t* src = reinterpret_cast<uint32_t*>(s_stage);
+            const int nw = p.img_lane + p.img_shared;
+            constexpr int kPerThread = (kImageMaxWords + kWarps * 32 - 1) / (kWarps * 32);
+            uint32_t v[kPerThread];
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) img[i] = __ldg(src + tid + i * kWarps * 32);
+            for (int u = 0; u < kPerThread; ++u) {
+                const int e = tid + u * kWarps * 32;
+                v[u] = e < nw ? __ldg(p.img_src + e) : 0u;
+            }
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) reinterpret_cast<uint4*>(s_tab)[tid + i * kWarps * 32] = img[i];
+            for (int u = 0; u < kPerThread; ++u) {
+                const int e = tid + u * kWarps * 32;
+                if (e < nw) src[e] = v[u];
+            }
+            __syncthreads();
+            uint4* dst = reinterpret_cast<uint4*>(s_tab);
+            for (int i = tid; i < p.img_lane * 8; i += kWarps * 32) {
+                const uint32_t x = src[i >> 3];
+                dst[i] = make_uint4(x, x, x, x);
+            }
+            for (int i = tid; i < p.img_shared; i += kWarps * 32) s_tab[32 * p.img_lane + i] = src[p.img_lane + i];
+            __syncthreads();  // the source is read before the staging region is reused
+        }
         // query rotation recipe of the lane's codec coordinates 4L..4L+3
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -628,13 +631,15 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             q_f[i] = coded ? ht->sign_k[j] * ht->dewhiten[j] : 0.0f;
             q_sc[i] = coded ? ht->inv_sqrt[j] * p.scale_log2 : 0.0f;
         }
-        // K slot lookup recipes and codec pairs of the lane's slots
+        // K slot lookup recipes (the lane's table copy: + 4 L) and codec
+        // pairs of the lane's slots
 #pragma unroll
         for (int s = 0; s < 16; ++s) {
-            const uint4 m = __ldg(reinterpret_cast<const uint4*>(&ht->kmeta[t][s]));
+            const uint4 m = __ldg(reinterpret_cast<const uint4*>(&ht->kslot[t][s]));
             ksh[s] = m.x;
             kmask[s] = m.y;
-            kbase[s] = m.z + (m.w & 255u) * lane + (m.w >> 8) * g;
+            kbase[s] = (m.z & kSharedTable) ? (m.z & ~kSharedTable) : (m.z | (4u * lane));
+            kwsh[s] = m.w;
         }
         const uint4 sp = __ldg(reinterpret_cast<const uint4*>(&ht->slot_pair[t][0]));
         slot_pairs[0] = sp.x;
@@ -656,9 +661,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         if (sl >= 0) append_new_token<BK, BV>(p, el, unit, sl, pos, s_thr, s_enc, warp, lane);
     }
     float m_ref = -INFINITY, l_run = 0.0f;  // softmax reference (see kLift, kSlack), sum
-    float acc[16][4];
+    // O^T accumulator: acc[mt][e] = query head 2t + e, codec dim 16 g + 2 mt;
+    // acc[mt][2 + e] = the same head, dim 16 g + 2 mt + 1
+    float acc[8][4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
     if (active) {
     // ---- query heads into the key codec domain: warp w rotates heads
     // kHPW w .. kHPW w + kHPW - 1, lane L holding codec coordinates 4L..4L+3
@@ -723,8 +730,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         split_hilo(v0 ? x0 : 0.0f, v0 ? x1 : 0.0f, qa[c][0], qa[c][1]);
         split_hilo(v1 ? y0 : 0.0f, v1 ? y1 : 0.0f, qa[c][2], qa[c][3]);
     }
-    const uint32_t wide = ht->wide_mask;
-    const uint32_t vbase = BV <= kPrivMaxW ? kPrivByte + 4u * lane + ((1u << (2 * BV)) << 7) : (1u << (2 * BV)) << 2;
+    // value tables: the lane's copy of the width-BV pair table, or of the
+    // width-4 single table
+    const uint32_t vbase = (BV <= kPairTableMaxW ? (1u << (2 * BV)) << 7 : (uint32_t)single_base(4) << 7) | (4u * lane);
+    __syncthreads();  // every warp has its query fragments: the staging region may be filled
 
     // ---- main loop: 16-token tiles, operands of the next tile loaded while
     // the current one is decoded (ping-pong register buffers).  kWin: the
@@ -750,18 +759,20 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
                 }
             }
         };
-        if constexpr (kWin && !kAnyWide) load_kb();
+        if constexpr (kWin && NW != 16) load_kb();
         float sacc[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.0f;
-        s_chunk<BK, 0, kAnyWide>(sacc, qa, tr.kw, ksh, kmask, kbase, wide, s_tab, s_single);
-        s_chunk<BK, 1, kAnyWide>(sacc, qa, tr.kw, ksh, kmask, kbase, wide, s_tab, s_single);
-        s_chunk<BK, 2, kAnyWide>(sacc, qa, tr.kw, ksh, kmask, kbase, wide, s_tab, s_single);
-        s_chunk<BK, 3, kAnyWide>(sacc, qa, tr.kw, ksh, kmask, kbase, wide, s_tab, s_single);
-        s_chunk<BK, 4, kAnyWide>(sacc, qa, tr.kw, ksh, kmask, kbase, wide, s_tab, s_single);
-        s_chunk<BK, 5, kAnyWide>(sacc, qa, tr.kw, ksh, kmask, kbase, wide, s_tab, s_single);
-        s_chunk<BK, 6, kAnyWide>(sacc, qa, tr.kw, ksh, kmask, kbase, wide, s_tab, s_single);
-        s_chunk<BK, 7, kAnyWide>(sacc, qa, tr.kw, ksh, kmask, kbase, wide, s_tab, s_single);
+        const uint64_t wl[2] = {kwin_lo<BK>(tr.kw[0]), kwin_lo<BK>(tr.kw[1])};
+        const uint64_t wh[2] = {kwin_hi<BK>(tr.kw[0]), kwin_hi<BK>(tr.kw[1])};
+        s_chunk<NW, 0>(sacc, qa, wl, wh, ksh, kmask, kbase, kwsh, s_tab);
+        s_chunk<NW, 1>(sacc, qa, wl, wh, ksh, kmask, kbase, kwsh, s_tab);
+        s_chunk<NW, 2>(sacc, qa, wl, wh, ksh, kmask, kbase, kwsh, s_tab);
+        s_chunk<NW, 3>(sacc, qa, wl, wh, ksh, kmask, kbase, kwsh, s_tab);
+        s_chunk<NW, 4>(sacc, qa, wl, wh, ksh, kmask, kbase, kwsh, s_tab);
+        s_chunk<NW, 5>(sacc, qa, wl, wh, ksh, kmask, kbase, kwsh, s_tab);
+        s_chunk<NW, 6>(sacc, qa, wl, wh, ksh, kmask, kbase, kwsh, s_tab);
+        s_chunk<NW, 7>(sacc, qa, wl, wh, ksh, kmask, kbase, kwsh, s_tab);
         // logits (log2 domain) of head g for tokens T0 + 8 nt + 2 t + e
         float lg[2][2];
 #pragma unroll
@@ -776,7 +787,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             // the tokens of the tile inside the fp16 recent-key buffer take
             // their logits from their exact keys (q as given . k, on the
             // tensor cores)
-            if constexpr (kAnyWide) load_kb();
+            if constexpr (NW == 16) load_kb();
             float s16[2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) s16[nt][0] = s16[nt][1] = s16[nt][2] = s16[nt][3] = 0.0f;
@@ -804,12 +815,16 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             const float ref = mx > m_ref + kSlack ? mx + kLift : m_ref;
             const float alpha = fast_exp2(m_ref - ref);
             l_run *= alpha;
+            // the accumulator of lane (g, t) holds query heads 2t and 2t + 1:
+            // their factors come from the lanes of those heads
+            const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
+            const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                acc[i][0] *= alpha;
-                acc[i][1] *= alpha;
-                acc[i][2] *= alpha;
-                acc[i][3] *= alpha;
+            for (int i = 0; i < 8; ++i) {
+                acc[i][0] *= a0;
+                acc[i][1] *= a1;
+                acc[i][2] *= a0;
+                acc[i][3] *= a1;
             }
             m_ref = ref;
         }
@@ -821,29 +836,23 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
                 pr[nt][e] = fast_exp2(lg[nt][e] - m_ref);
                 l_run += pr[nt][e];
             }
-        uint32_t pa[4];
-        split_hilo(pr[0][0] * tr.rv[0][0], pr[0][1] * tr.rv[0][1], pa[0], pa[1]);
-        split_hilo(pr[1][0] * tr.rv[1][0], pr[1][1] * tr.rv[1][1], pa[2], pa[3]);
-        pv_tile<BV, 0>(acc, pa, tr.vw, vbase, s_tab);
-        pv_tile<BV, 1>(acc, pa, tr.vw, vbase, s_tab);
-        pv_tile<BV, 2>(acc, pa, tr.vw, vbase, s_tab);
-        pv_tile<BV, 3>(acc, pa, tr.vw, vbase, s_tab);
-        pv_tile<BV, 4>(acc, pa, tr.vw, vbase, s_tab);
-        pv_tile<BV, 5>(acc, pa, tr.vw, vbase, s_tab);
-        pv_tile<BV, 6>(acc, pa, tr.vw, vbase, s_tab);
-        pv_tile<BV, 7>(acc, pa, tr.vw, vbase, s_tab);
-        pv_tile<BV, 8>(acc, pa, tr.vw, vbase, s_tab);
-        pv_tile<BV, 9>(acc, pa, tr.vw, vbase, s_tab);
-        pv_tile<BV, 10>(acc, pa, tr.vw, vbase, s_tab);
-        pv_tile<BV, 11>(acc, pa, tr.vw, vbase, s_tab);
-        pv_tile<BV, 12>(acc, pa, tr.vw, vbase, s_tab);
-        pv_tile<BV, 13>(acc, pa, tr.vw, vbase, s_tab);
-        pv_tile<BV, 14>(acc, pa, tr.vw, vbase, s_tab);
-        pv_tile<BV, 15>(acc, pa, tr.vw, vbase, s_tab);
+        // P' = p * rho_V of head g for tokens 2t, 2t+1 (b0) and 8+2t, 9+2t
+        // (b1): the B fragment of the P.V product, split hi + lo
+        uint32_t pb[2][2];
+        split_hilo(pr[0][0] * tr.rv[0][0], pr[0][1] * tr.rv[0][1], pb[0][0], pb[1][0]);
+        split_hilo(pr[1][0] * tr.rv[1][0], pr[1][1] * tr.rv[1][1], pb[0][1], pb[1][1]);
+        pv_mtile<BV, 0>(acc, pb, tr.vw, vbase, s_tab);
+        pv_mtile<BV, 1>(acc, pb, tr.vw, vbase, s_tab);
+        pv_mtile<BV, 2>(acc, pb, tr.vw, vbase, s_tab);
+        pv_mtile<BV, 3>(acc, pb, tr.vw, vbase, s_tab);
+        pv_mtile<BV, 4>(acc, pb, tr.vw, vbase, s_tab);
+        pv_mtile<BV, 5>(acc, pb, tr.vw, vbase, s_tab);
+        pv_mtile<BV, 6>(acc, pb, tr.vw, vbase, s_tab);
+        pv_mtile<BV, 7>(acc, pb, tr.vw, vbase, s_tab);
     };
 
     using SL = StageLayout<BK, BV>;
-    uint8_t* st_base = dsmem + kSmemStage + warp * (kStages * SL::kBytes);
+    uint8_t* st_base = s_stage + warp * (kStages * SL::kBytes);
     const uint32_t st_addr = (uint32_t)__cvta_generic_to_shared(st_base);
 #pragma unroll
     for (int k = 0; k < kStages - 1; ++k) {
@@ -891,10 +900,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         s_wp[warp][g][1] = l_run;
     }
 #pragma unroll
-    for (int nd = 0; nd < 16; ++nd) {
-        s_wp[warp][g][2 + 16 * (2 * t) + nd] = acc[nd][0] + acc[nd][2];
-        s_wp[warp][g][2 + 16 * (2 * t + 1) + nd] = acc[nd][1] + acc[nd][3];
-    }
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            s_wp[warp][2 * t + e][2 + 16 * g + 2 * mt] = acc[mt][e];
+            s_wp[warp][2 * t + e][2 + 16 * g + 2 * mt + 1] = acc[mt][2 + e];
+        }
 
     // ---- CTA merge: thread tid merges query head tid / 16, dims
     // 8 (tid % 16) .. + 7, over the 4 warps -> s_cp
@@ -987,45 +998,71 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             const unsigned prev = ticket_acq_rel(p.count + unit * G + r);
             s_last = (prev == (unsigned)(n_clusters - 1)) ? 1 : 0;
         }
-        __syncthreads();  // thread 0's acquire is ordered before warp 0's loads below
-        if (!s_last || warp != 0) continue;
-        // ---- last cluster partial of query head r: warp 0 merges all of
-        // them (lane holds dims lane + 32 i), kBatch partials per batch of
-        // independent loads, online rescaling between batches
-        constexpr int kBatch = 16;
+        __syncthreads();  // thread 0's acquire is ordered before the loads below
+        if (!s_last) continue;
+        // ---- last cluster partial of query head r: warp w merges the
+        // partials of clusters w, w + kWarps, ... (one batch of independent
+        // loads; lane holds dims lane + 32 i) into the free per-warp region,
+        // then warp 0 merges the kWarps results
+        constexpr int kPerWarp = (kMaxClusters + kWarps - 1) / kWarps;
         float M = -INFINITY, L = 0.0f, O[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int c0 = 0; c0 < n_clusters; c0 += kBatch) {
-            float mc[kBatch], lc[kBatch], oc[kBatch][4];
+        float sgn[4];  // value rotation signs of the lane's output dims, fetched with the partials
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                const int c = c0 + j;
-                mc[j] = -INFINITY;
-                lc[j] = 0.0f;
-                oc[j][0] = oc[j][1] = oc[j][2] = oc[j][3] = 0.0f;
+        for (int i = 0; i < 4; ++i) sgn[i] = warp == 0 ? __ldg(&ht->sign_v[lane + 32 * i]) * p.v_inv_sqrt : 0.0f;
+        {
+            float mc[kPerWarp], lc[kPerWarp], oc[kPerWarp][4];
+#pragma unroll
+            for (int jj = 0; jj < kPerWarp; ++jj) {
+                const int c = warp + kWarps * jj;
+                mc[jj] = -INFINITY;
+                lc[jj] = 0.0f;
+                oc[jj][0] = oc[jj][1] = oc[jj][2] = oc[jj][3] = 0.0f;
                 if (c < n_clusters) {
                     const float* src = cpart_base + ((size_t)c * G + r) * kPartStride;
-                    mc[j] = __ldcg(src);
-                    lc[j] = __ldcg(src + 1);
+                    mc[jj] = __ldcg(src);
+                    lc[jj] = __ldcg(src + 1);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) oc[j][i] = __ldcg(src + 2 + lane + 32 * i);
+                    for (int i = 0; i < 4; ++i) oc[jj][i] = __ldcg(src + 2 + lane + 32 * i);
                 }
             }
-            float Mn = M;
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) Mn = fmaxf(Mn, mc[j]);
-            const float a = M == -INFINITY ? 0.0f : exp2f(M - Mn);
-            L *= a;
+            for (int jj = 0; jj < kPerWarp; ++jj) M = fmaxf(M, mc[jj]);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) O[i] *= a;
+            for (int jj = 0; jj < kPerWarp; ++jj) {
+                const float f = mc[jj] == -INFINITY ? 0.0f : exp2f(mc[jj] - M);
+                L += lc[jj] * f;
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                const float f = mc[j] == -INFINITY ? 0.0f : exp2f(mc[j] - Mn);
-                L += lc[j] * f;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) O[i] += oc[j][i] * f;
+                for (int i = 0; i < 4; ++i) O[i] += oc[jj][i] * f;
             }
-            M = Mn;
         }
+        float* sw = &s_wp[warp][0][0];
+        if (lane == 0) {
+            sw[0] = M;
+            sw[1] = L;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sw[2 + lane + 32 * i] = O[i];
+        __syncthreads();
+        if (warp == 0) {
+            float mw[kWarps];
+            float Mt = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                mw[w] = s_wp[w][0][0];
+                Mt = fmaxf(Mt, mw[w]);
+            }
+            L = 0.0f;
+            O[0] = O[1] = O[2] = O[3] = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float f = mw[w] == -INFINITY ? 0.0f : exp2f(mw[w] - Mt);
+                L += s_wp[w][0][1] * f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) O[i] += s_wp[w][0][2 + lane + 32 * i] * f;
+            }
+        }
+        __syncthreads();  // the per-warp region is read before a next head reuses it
+        if (warp != 0) continue;
         // inverse value rotation (Hadamard-128, 1/sqrt(128), signs): stages
         // 1..16 by shuffles, 32 and 64 between the lane's four dims
         float v[4];
@@ -1049,7 +1086,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int d = lane + 32 * i;
-            const float val = v[i] * p.v_inv_sqrt * ht->sign_v[d];
+            const float val = v[i] * sgn[i];
             const size_t o = ((size_t)b * p.H * G + (size_t)h * G + r) * kD + d;
             if (p.out_dtype) static_cast<float*>(p.out)[o] = val;
             else static_cast<__half*>(p.out)[o] = __float2half_rn(val);
@@ -1060,7 +1097,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
 }
 
 // The dynamic shared memory of the three instances of decode_kernel<BK, BV>
-// of one paging mode is raised above the 48 KB default once per device.
+// of one paging mode is raised above the 48 KB default once per device, to
+// the size with the largest lookup tables.
 template <int BK, int BV, bool kPaged>
 cudaError_t ensure_smem_attr() {
     static std::mutex mu;
@@ -1070,24 +1108,22 @@ cudaError_t ensure_smem_attr() {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (done[dev]) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<BK, BV, 0, kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         decode_smem_bytes<BK, BV>());
+    const int bytes = decode_smem_bytes<BK, BV>(kWMax);
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<BK, BV, 0, kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(decode_kernel<BK, BV, 1, kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 decode_smem_bytes<BK, BV>());
+        e = cudaFuncSetAttribute(decode_kernel<BK, BV, 1, kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(decode_kernel<BK, BV, 2, kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 decode_smem_bytes<BK, BV>());
+        e = cudaFuncSetAttribute(decode_kernel<BK, BV, 2, kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess) done[dev] = true;
     return e;
 }
 
 template <int BK, int BV>
-cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t s, cudaLaunchAttribute* attr /*[2]*/) {
+cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t s, int ws, cudaLaunchAttribute* attr /*[2]*/) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kWarps * 32, 1, 1);
-    cfg.dynamicSmemBytes = decode_smem_bytes<BK, BV>();
+    cfg.dynamicSmemBytes = decode_smem_bytes<BK, BV>(ws);
     cfg.stream = s;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kCluster;
@@ -1101,11 +1137,13 @@ cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t s, cudaLaunchAttribute*
 }
 
 template <int BK, int BV, bool kPaged>
-cudaError_t launch_t(const DecodeParams& p, dim3 grid, cudaStream_t s, int kind) {
+cudaError_t launch_t(DecodeParams p, dim3 grid, cudaStream_t s, int kind) {
     cudaError_t e = ensure_smem_attr<BK, BV, kPaged>();
     if (e != cudaSuccess) return e;
+    const int ws = p.img_ws;
+    p.img_bytes = decode_table_bytes(ws);
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = launch_config<BK, BV>(grid, s, attr);
+    cudaLaunchConfig_t cfg = launch_config<BK, BV>(grid, s, ws, attr);
     if (kind == 2) return cudaLaunchKernelEx(&cfg, decode_kernel<BK, BV, 2, kPaged>, p);
     if (kind == 1) return cudaLaunchKernelEx(&cfg, decode_kernel<BK, BV, 1, kPaged>, p);
     return cudaLaunchKernelEx(&cfg, decode_kernel<BK, BV, 0, kPaged>, p);

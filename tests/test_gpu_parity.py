@@ -216,7 +216,9 @@ def test_decode_extreme_query_magnitudes(qmul):
 def test_decode_value_magnitudes(vmul):
     """P' = p * rho_V enters the tensor cores as fp16 hi + lo: value norms two
     decades below and above unit scale must stay accurate (no fp16
-    subnormals or overflow in the weights)."""
+    subnormals or overflow in the weights).  The bound is the stated
+    absolute one even for values scaled by 100: the hi + lo weights carry
+    about fp32 precision, so only float32 rounding is left."""
     H, G, T = 2, 8, 2000
     li, plan, cache, heads = build(321, H, G, T, 384, 3, s_ln=1.2)
     li = [synth.LayerInputs(li[0].k, (li[0].v.astype(np.float64) * vmul).astype(np.float16), li[0].q,
@@ -229,7 +231,7 @@ def test_decode_value_magnitudes(vmul):
         want = oracle_out(heads, li[0], q, T, G)
         err = np.abs(got[0] - want)
         rel = np.linalg.norm(got[0] - want) / np.linalg.norm(want)
-        assert err.max() <= MAX_ABS * max(1.0, vmul), f"max abs {err.max():.3e}"
+        assert err.max() <= MAX_ABS, f"max abs {err.max():.3e}"
         assert rel <= REL_L2, f"rel l2 {rel:.3e}"
 
 
