@@ -33,27 +33,33 @@ namespace {
 constexpr int kBulkTok = 128;
 // Per-thread column of 129 words in dynamic shared memory (the odd stride
 // keeps the threads of a warp on distinct banks): first the fp16 key row,
-// then the rotated coordinates that the code loops read back.
+// then the rotated coordinates that the code loops read back.  The quotients
+// u = y / rho use the token's reciprocal of rho (see quot), and the code
+// searches run at the width of each rotation piece.
 constexpr int kColWords = 129;
 constexpr int kBulkDynSmem = kBulkTok * kColWords * 4;
 
-// Code of coordinate y at width w: the number of width-w thresholds <= y / rho
-// (binary search over the sorted thresholds; the steps wider than the width
-// are skipped by a uniform predicate, so the loop has a fixed trip count).
-__device__ __forceinline__ uint32_t bulk_code(float y, float rho, int w, const float* s_thr) {
-    const float u = rho > 0.0f ? __fdiv_rn(y, rho) : 0.0f;
-    const float* tb = s_thr + (1 << w) - 1;
-    int c = 0;
-#pragma unroll
-    for (int k = kWMax - 1; k >= 0; --k)
-        if (k < w && tb[c + (1 << k) - 1] <= u) c += 1 << k;
-    return (uint32_t)c;
+// The quotient y / rho correctly rounded, as __fdiv_rn gives it, from the
+// correctly rounded reciprocal r = 1/rho (r = 0 when rho = 0, which makes the
+// quotient 0 as the encoder requires): two Newton-Raphson corrections in
+// Markstein's form, q' = q + r (y - q rho), each remainder exact by FMA; with
+// r correctly rounded the last correction rounds to the correctly rounded
+// quotient (P. Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Develop. 34(1), 1990).  The
+// encoder's quotients lie in [-sqrt(128), sqrt(128)] and come from fp16 data,
+// far from under- and overflow.
+__device__ __forceinline__ float quot(float y, float rho, float r) {
+    const float q0 = __fmul_rn(y, r);
+    const float e0 = __fmaf_rn(-q0, rho, y);
+    const float q1 = __fmaf_rn(e0, r, q0);
+    const float e1 = __fmaf_rn(-q1, rho, y);
+    return __fmaf_rn(e1, r, q1);
 }
 
+// Code of quotient u at width W: the number of width-W thresholds <= u, by
+// binary search over the sorted thresholds tb (= s_thr + 2^W - 1).
 template <int W>
-__device__ __forceinline__ uint32_t bulk_code_w(float y, float rho, const float* s_thr) {
-    const float u = rho > 0.0f ? __fdiv_rn(y, rho) : 0.0f;
-    const float* tb = s_thr + (1 << W) - 1;
+__device__ __forceinline__ uint32_t code_w(float u, const float* tb) {
     int c = 0;
 #pragma unroll
     for (int k = W - 1; k >= 0; --k)
@@ -61,27 +67,45 @@ __device__ __forceinline__ uint32_t bulk_code_w(float y, float rho, const float*
     return (uint32_t)c;
 }
 
-// Rotation pieces of one token held by one thread (stage h applies to the
-// coordinates [0, end[h]); kFull: one piece of 128), the 1/sqrt(piece)
-// scaling and the norm tree; returns rho = sqrt(sum y^2 / n).
-// Butterfly stage H over the first e coordinates (e a multiple of 2H);
-// pairs outside keep their values (selected, not branched, so z stays in
-// registers).
+// Butterfly stage H over the first e coordinates (e a multiple of 2H).  Small
+// stages keep the pairs past e by selection (nearly every block is active);
+// large ones skip inactive blocks by a branch that is uniform across the block.
 template <int H, bool kFull>
 __device__ __forceinline__ void bulk_stage(float (&z)[kD], int e) {
 #pragma unroll
     for (int blk = 0; blk < kD; blk += 2 * H) {
-        const bool act = kFull || blk < e;
+        if constexpr (kFull) {
 #pragma unroll
-        for (int i = 0; i < H; ++i) {
-            const float a0 = z[blk + i], a1 = z[blk + i + H];
-            const float s0 = __fadd_rn(a0, a1), s1 = __fsub_rn(a0, a1);
-            z[blk + i] = act ? s0 : a0;
-            z[blk + i + H] = act ? s1 : a1;
+            for (int i = 0; i < H; ++i) {
+                const float a0 = z[blk + i], a1 = z[blk + i + H];
+                z[blk + i] = __fadd_rn(a0, a1);
+                z[blk + i + H] = __fsub_rn(a0, a1);
+            }
+        } else if constexpr (H < 8) {
+            const bool act = blk < e;
+#pragma unroll
+            for (int i = 0; i < H; ++i) {
+                const float a0 = z[blk + i], a1 = z[blk + i + H];
+                const float s0 = __fadd_rn(a0, a1), s1 = __fsub_rn(a0, a1);
+                z[blk + i] = act ? s0 : a0;
+                z[blk + i + H] = act ? s1 : a1;
+            }
+        } else {
+            if (blk < e) {
+#pragma unroll
+                for (int i = 0; i < H; ++i) {
+                    const float a0 = z[blk + i], a1 = z[blk + i + H];
+                    z[blk + i] = __fadd_rn(a0, a1);
+                    z[blk + i + H] = __fsub_rn(a0, a1);
+                }
+            }
         }
     }
 }
 
+// Rotation pieces of one token held by one thread (stage h applies to the
+// coordinates [0, end[h]); kFull: one piece of 128), the 1/sqrt(piece)
+// scaling and the norm tree; returns rho = sqrt(sum y^2 / n).
 template <bool kFull>
 __device__ __forceinline__ float bulk_rotate_norm(float (&z)[kD], int n, const int* s_end, const float* s_is,
                                                   float v_inv_sqrt) {
@@ -107,14 +131,40 @@ __device__ __forceinline__ float bulk_rotate_norm(float (&z)[kD], int n, const i
     return __fsqrt_rn(__fdiv_rn(part[0], (float)n));
 }
 
+// Codes and packing of the key pairs of one rotation piece (codec coordinates
+// [j0, j0 + n), all of width W) into the thread's record: four pairs at a time
+// so that their threshold searches overlap.
+template <int W>
+__device__ __forceinline__ void bulk_key_piece(const float* col, int j0, int n, float rho, float r, const float* s_thr,
+                                               const uint16_t* s_pbit, uint32_t* rec) {
+    const float* tb = s_thr + (1 << W) - 1;
+    const int m1 = (j0 + n) >> 1;
+    for (int m0 = j0 >> 1; m0 < m1; m0 += 4) {
+        uint32_t f[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int m = min(m0 + q, m1 - 1);
+            f[q] = code_w<W>(quot(col[2 * m], rho, r), tb) | (code_w<W>(quot(col[2 * m + 1], rho, r), tb) << W);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (m0 + q >= m1) break;
+            const int bit = s_pbit[m0 + q];
+            const int wi = bit >> 5, sh = bit & 31;
+            rec[wi] |= f[q] << sh;
+            if (sh + 2 * W > 32) rec[wi + 1] |= f[q] >> (32 - sh);
+        }
+    }
+}
+
 template <int BK, int BV>
 __global__ void __launch_bounds__(kBulkTok) quantize_append_bulk_kernel(QParams p) {
     __shared__ float s_thr[kThrCompact];
-    __shared__ float s_ws[kD];   // whitening x sign (keys; 0 past n_coded)
+    __shared__ float2 s_pw[kD];  // keys: (whitening x sign, source dim) per codec coordinate (0 past n_coded)
     __shared__ float s_is[kD];   // 1/sqrt(piece) (keys)
     __shared__ float s_sv[kD];   // value signs
-    __shared__ uint8_t s_perm[kD];
     __shared__ uint8_t s_width[kD];
+    __shared__ uint8_t s_plog2[kD];
     __shared__ uint16_t s_pbit[kNB];
     __shared__ int s_end[7];
     __shared__ uint32_t s_rec[kBulkTok * (4 * BK + 1)];
@@ -131,11 +181,11 @@ __global__ void __launch_bounds__(kBulkTok) quantize_append_bulk_kernel(QParams 
     {
         const int j = tid;
         const bool coded = j < nc;
-        s_ws[j] = coded ? __fmul_rn(ht->whiten[j], ht->sign_k[j]) : 0.0f;
+        s_pw[j] = make_float2(coded ? __fmul_rn(ht->whiten[j], ht->sign_k[j]) : 0.0f, __int_as_float((int)ht->perm[j]));
         s_is[j] = ht->inv_sqrt[j];
         s_sv[j] = ht->sign_v[j];
-        s_perm[j] = ht->perm[j];
         s_width[j] = coded ? ht->width[j] : 0;
+        s_plog2[j] = coded ? ht->plog2[j] : 0;
         if (j < kNB) s_pbit[j] = ht->pair_bit[j];
         if (j < 7) {
             int e = 0;
@@ -157,11 +207,11 @@ __global__ void __launch_bounds__(kBulkTok) quantize_append_bulk_kernel(QParams 
     const size_t unit = (size_t)b * p.H + h;
     const int64_t sl = act ? p.map.slot(b, h, pos) : 0;  // record location of token `pos`
     if (sl < 0 && p.status) atomicOr(p.status, BGTQ_STATUS_PAGE_RANGE);
+    float* col = s_col + tid * kColWords;
 
     // ---- key of token `pos`
     if (act) {
         const uint4* src = reinterpret_cast<const uint4*>(p.k + (unit * p.t_new + (size_t)(pos - ps)) * kD);
-        float* col = s_col + tid * kColWords;
         uint32_t* row = reinterpret_cast<uint32_t*>(col);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -180,22 +230,33 @@ __global__ void __launch_bounds__(kBulkTok) quantize_append_bulk_kernel(QParams 
         const __half* rowh = reinterpret_cast<const __half*>(row);
         float z[kD];
 #pragma unroll
-        for (int j = 0; j < kD; ++j) z[j] = j < nc ? __fmul_rn(__half2float(rowh[s_perm[j]]), s_ws[j]) : 0.0f;
+        for (int j = 0; j < kD; ++j) {
+            const float2 pw = s_pw[j];
+            z[j] = __fmul_rn(__half2float(rowh[__float_as_int(pw.y)]), pw.x);
+        }
         const float rho = bulk_rotate_norm<false>(z, nc, s_end, s_is, p.v_inv_sqrt);
+        const float r = rho > 0.0f ? __frcp_rn(rho) : 0.0f;
+        // the rotated coordinates go back to the column (the row is no longer
+        // needed): the code loops below index them at run time
 #pragma unroll
         for (int j = 0; j < kD; ++j) col[j] = z[j];
         uint32_t* rec = s_rec + tid * (4 * BK + 1);
 #pragma unroll
         for (int i = 0; i < 4 * BK; ++i) rec[i] = 0;
-        // codes and packing as a rolled loop over the codec pairs (small code)
-#pragma unroll 2
-        for (int m = 0; 2 * m < nc; ++m) {
-            const int w = s_width[2 * m];
-            const uint32_t field = bulk_code(col[2 * m], rho, w, s_thr) | (bulk_code(col[2 * m + 1], rho, w, s_thr) << w);
-            const int bit = s_pbit[m];
-            const int wi = bit >> 5, sh = bit & 31;
-            rec[wi] |= field << sh;
-            if (sh + 2 * w > 32) rec[wi + 1] |= field >> (32 - sh);
+        // rotation pieces in codec order, each of one width (uniform loop)
+        for (int j = 0; j < nc;) {
+            const int w = s_width[j], n = 1 << s_plog2[j];
+            switch (w) {
+                case 1: bulk_key_piece<1>(col, j, n, rho, r, s_thr, s_pbit, rec); break;
+                case 2: bulk_key_piece<2>(col, j, n, rho, r, s_thr, s_pbit, rec); break;
+                case 3: bulk_key_piece<3>(col, j, n, rho, r, s_thr, s_pbit, rec); break;
+                case 4: bulk_key_piece<4>(col, j, n, rho, r, s_thr, s_pbit, rec); break;
+                case 5: bulk_key_piece<5>(col, j, n, rho, r, s_thr, s_pbit, rec); break;
+                case 6: bulk_key_piece<6>(col, j, n, rho, r, s_thr, s_pbit, rec); break;
+                case 7: bulk_key_piece<7>(col, j, n, rho, r, s_thr, s_pbit, rec); break;
+                default: bulk_key_piece<8>(col, j, n, rho, r, s_thr, s_pbit, rec); break;
+            }
+            j += n;
         }
         if (sl >= 0) {
             uint4* dst = reinterpret_cast<uint4*>(p.kc + sl * (16 * BK));
@@ -228,20 +289,27 @@ __global__ void __launch_bounds__(kBulkTok) quantize_append_bulk_kernel(QParams 
             }
         }
         rho_v = bulk_rotate_norm<true>(z, kD, s_end, s_is, p.v_inv_sqrt);
-        float* col = s_col + tid * kColWords;
+        const float r = rho_v > 0.0f ? __frcp_rn(rho_v) : 0.0f;
 #pragma unroll
         for (int j = 0; j < kD; ++j) col[j] = z[j];
-        // fields as for an even token (code at bit 2 BV j), shifted up by BV
-        // for an odd one; codes by a rolled loop into a shared-memory record
+        // fields as for an even token (code of dim j at bit 2 BV j), shifted up
+        // by BV for an odd one; 16 dims (BV words of the record) at a time
+        const float* tb = s_thr + (1 << BV) - 1;
         uint32_t* vr = s_vrec + tid * (8 * BV + 1);
+#pragma unroll 1
+        for (int g = 0; g < 8; ++g) {
+            uint32_t wds[BV];
 #pragma unroll
-        for (int i = 0; i < kW; ++i) vr[i] = 0;
-#pragma unroll 4
-        for (int j = 0; j < kD; ++j) {
-            const uint32_t c = bulk_code_w<BV>(col[j], rho_v, s_thr);
-            const int bit = 2 * BV * j;
-            vr[bit >> 5] |= c << (bit & 31);
-            if ((bit & 31) + BV > 32) vr[(bit >> 5) + 1] |= c >> (32 - (bit & 31));
+            for (int i = 0; i < BV; ++i) wds[i] = 0;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t c = code_w<BV>(quot(col[16 * g + i], rho_v, r), tb);
+                const int bit = 2 * BV * i;  // compile-time after unrolling
+                wds[bit >> 5] |= c << (bit & 31);
+                if ((bit & 31) + BV > 32) wds[(bit >> 5) + 1] |= c >> (32 - (bit & 31));
+            }
+#pragma unroll
+            for (int i = 0; i < BV; ++i) vr[BV * g + i] = wds[i];
         }
 #pragma unroll
         for (int i = 0; i < kW; ++i) vw[i] = vr[i];
