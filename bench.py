@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--prefill-tokens", type=int, default=32768, help="prompt length of the fused-prefill measurement")
     ap.add_argument("--page-tokens", type=int, default=0,
                     help="paged cache: pages of P tokens in a shuffled pool instead of contiguous rows")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the measurements of the other workloads (profiling runs)")
     ap.add_argument("--two-call", action="store_true",
                     help="per layer bgtq_quantize_append + bgtq_decode_attn instead of the fused bgtq_decode_step")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
@@ -375,6 +377,117 @@ def replica_throughput(world: int, batch: int, ms_per_step: float) -> float:
 
 # ----------------------------------------------------------------------------- GPU arm
 
+L2_BYTES = 129 * 2 ** 20  # GB300 L2
+
+
+def decode_workload(wname: str, peaks: dict, stream, steps: int, warmup: int) -> dict:
+    """Graph-timed fused decode steps (bgtq_decode_step per layer) of a named
+    workload other than the headline one.  A workload whose step reads less
+    than 4x L2 is run over enough replicas of its cache (separate buffers of
+    the same content) that consecutive steps never find their bytes in L2;
+    the graph then holds one step per replica."""
+    import torch
+
+    import rope_aware_quantized_gb300 as bg
+    from rope_aware_quantized_gb300 import workloads
+
+    w = workloads.WORKLOADS[wname]
+    lens = w.seq_lens()
+    max_len = int(lens.max())
+    bpth = w.packed_bytes_per_token_head()
+    layer_bytes = int(lens.sum()) * w.n_kv * bpth
+    step_layers = w.layers
+    replicas = 1
+    if layer_bytes * w.layers < 4 * L2_BYTES:
+        replicas = -(-4 * L2_BYTES // (layer_bytes * w.layers))
+    layers = [workloads.build_layer(w, l % w.layers) for l in range(w.layers * replicas)]
+    ws = torch.zeros(bg.bgtq_decode_attn_workspace(layers[0].plan, w.batch, max_len), dtype=torch.uint8, device="cuda")
+    outs = [torch.empty((w.batch, w.n_q, 128), dtype=torch.float16, device="cuda") for _ in layers]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def run_all():
+        for ls, o in zip(layers, outs):
+            bg.bgtq_decode_step(ls.plan, ls.q, ls.new_k[:, :, 0], ls.new_v[:, :, 0], ls.pos_new, ls.cache, ls.seq_lens,
+                                max_len, o, ws, status=status)
+
+    with torch.cuda.stream(stream):
+        run_all()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        run_all()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    assert status.item() == 0, f"device status {status.item()}"
+    ms = e0.elapsed_time(e1) / steps / replicas  # one decode step of the whole workload
+    step_bytes = step_layers * (layer_bytes + w.batch * w.n_q * 128 * 2 * 2
+                                + w.batch * w.n_kv * (2 * 256 + 16 * (w.bits_per_key // 128) + 16 * w.v_bits + 8))
+    gbs = step_bytes / (ms / 1000.0) / 1e9
+    r = {"tokens_per_s": w.batch / (ms / 1000.0), "ms_per_step": ms, "layers": w.layers, "batch": w.batch,
+         "kv_heads": w.n_kv, "q_heads": w.n_q, "context_max": max_len, "context_mean": float(lens.mean()),
+         "kv_bits": f"K{w.bits_per_key // 128}V{w.v_bits}", "packed_bytes_per_step": step_bytes,
+         "fp16_kv_bytes_per_step": int(lens.sum()) * w.n_kv * 512 * w.layers,
+         "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "bound": "hbm",
+         "steps": steps, "warmup": warmup,
+         "timing": "CUDA graph of per-layer bgtq_decode_step calls, events on the launching stream",
+         "l2": (f"{replicas} cache replicas cycled ({replicas * layer_bytes * w.layers / 1e6:.0f} MB > 4x L2)"
+                if replicas > 1 else "inputs larger than L2, no flush")}
+    del layers, outs, ws
+    torch.cuda.empty_cache()
+    return r
+
+
+def ragged_prefill(wname: str, peaks: dict, stream) -> dict:
+    """The ragged workload's prefill pass: every sequence's full context of
+    fp16 K and V rows (batch x KV heads x context tokens) encoded into an
+    empty packed cache by one bgtq_quantize_append call."""
+    import torch
+
+    import rope_aware_quantized_gb300 as bg
+    from rope_aware_quantized_gb300 import workloads
+
+    w = workloads.WORKLOADS[wname]
+    B, H, T = w.batch, w.n_kv, w.context
+    plan = workloads.build_plan(w, 0)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(20262)
+    k = torch.randn((B, H, T, 128), generator=gen, device="cuda").half()
+    v = torch.randn((B, H, T, 128), generator=gen, device="cuda").half()
+    cache = bg.Cache(plan, B, T)
+    pos = torch.zeros(B, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    times = []
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            bg.bgtq_quantize_append(plan, k, v, pos, cache, status=status)
+            b.record(stream)
+            times.append((a, b))
+    torch.cuda.synchronize()
+    assert status.item() == 0, f"append status {status.item()}"
+    ms = statistics.median(a.elapsed_time(b) for a, b in times[2:])
+    rows = B * H * T
+    nbytes = rows * 128 * 2 * 2 + rows * (16 * (w.bits_per_key // 128) + 16 * w.v_bits + 8)
+    gbs = nbytes / (ms / 1000.0) / 1e9
+    del k, v, cache
+    torch.cuda.empty_cache()
+    return {"tokens": B * T, "batch": B, "kv_heads": H, "tokens_per_sequence": T, "ms_per_launch": ms,
+            "tokens_per_s": B * T / (ms / 1000.0), "bytes_per_launch": nbytes, "achieved": gbs, "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "bound": "hbm",
+            "bytes": "fp16 K and V rows read + packed K/V records and both norms written"}
+
+
 def measure_prefill(w, plan, tokens: int, peaks: dict, stream) -> dict:
     """The quantize-append kernel alone on a prefill: `tokens` fp16 K/V rows
     per (sequence, KV head) of one layer encoded into an empty packed cache in
@@ -623,6 +736,18 @@ def run_gpu(args):
     e2e_ms = max_over_ranks(x0.elapsed_time(x1) / args.steps, dist, "cuda")
     assert status.item() == 0, f"device status {status.item()}"
 
+    # the other workloads of the path, each in its own measurement (rank 0 of
+    # a single-GPU run; the headline workload's buffers are released first)
+    others = {}
+    if rank == 0 and world == 1 and not args.headline_only and args.workload == "qwen3b_36l_128k" and not args.layers:
+        del graph, layers, q_all, nk_all, nv_all, out_all, nk_tok, nv_tok, hq, hk, hv, ho
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        k_other, w_other = max(5, args.steps // 2), max(3, args.warmup)
+        for name in ("qwen3b_36l_512k", "llama8b_ragged_b32", "llama8b_layer", "tiny"):
+            others[name] = decode_workload(name, peaks, stream, k_other, w_other)
+        others["llama8b_ragged_b32"]["prefill"] = ragged_prefill("llama8b_ragged_b32", peaks, stream)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_block(args.workload, args.sample_seconds)
@@ -664,6 +789,8 @@ def run_gpu(args):
         }
         line["append_prefill"] = prefill
         line["prefill_attn"] = prefill_attn
+        if others:
+            line["workloads"] = others
         if cpu:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)

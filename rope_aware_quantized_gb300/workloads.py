@@ -88,12 +88,7 @@ def build_layer(w: Workload, layer: int, device="cuda", keep_host=(), capacity: 
     if page_tokens:
         cap = -(-cap // page_tokens) * page_tokens
     qpos = lens - 1
-    bits, energy = [], []
-    for h in range(w.n_kv):
-        b, e = bgtq_alloc_bits(calib_keys(w, layer, h), w.bits_per_key, 8, 0)
-        bits.append(b)
-        energy.append(e)
-    plan = bgtq_plan_create(np.stack(bits), np.stack(energy), w.group, w.bits_per_key, w.v_bits, plan_seed(w, layer))
+    plan = build_plan(w, layer)
     cache = Cache(plan, w.batch, cap, device, recent=recent, page_tokens=page_tokens)
     if page_tokens:
         perm = np.random.default_rng([w.seed, layer, 0x9A6E]).permutation(cache.n_pages).astype(np.int32)
@@ -135,6 +130,17 @@ def build_layer(w: Workload, layer: int, device="cuda", keep_host=(), capacity: 
     pos_new = torch.tensor(lens - 1, dtype=torch.int32, device=device)
     torch.cuda.synchronize()
     return LayerState(plan, cache, q, new_k, new_v, seq_lens, pos_new, host)
+
+
+def build_plan(w: Workload, layer: int) -> Plan:
+    """Block-GTQ allocation of every KV head of (workload, layer) from its
+    calibration keys, and the layer's plan."""
+    bits, energy = [], []
+    for h in range(w.n_kv):
+        b, e = bgtq_alloc_bits(calib_keys(w, layer, h), w.bits_per_key, 8, 0)
+        bits.append(b)
+        energy.append(e)
+    return bgtq_plan_create(np.stack(bits), np.stack(energy), w.group, w.bits_per_key, w.v_bits, plan_seed(w, layer))
 
 
 def plan_seed(w: Workload, layer: int) -> int:
