@@ -287,10 +287,11 @@ struct StageLayout {
 
 // Dynamic shared memory of decode_kernel<BK, BV>: the lookup tables (img_bytes
 // of them, at least the size of the per-warp and per-CTA partials that
-// reuse the region after the main loop), then kStages staged tiles per warp.
-// The rotated queries live at the start of the staging region until the
-// first tiles are staged.
+// reuse the region after the main loop), the rotated queries, then kStages
+// staged tiles per warp (whose region also holds the tables' compact source
+// during the set-up).
 constexpr int kPartBytes = (kWarps + 1) * 8 * kPartStride * 4;
+constexpr int kQBytes = 8 * kD * 4;  // rotated queries
 inline int decode_table_bytes(int ws) {
     const int b = (image_bytes(ws) + 127) / 128 * 128;
     return b > kPartBytes ? b : (kPartBytes + 127) / 128 * 128;
@@ -301,9 +302,8 @@ constexpr int decode_stage_bytes() {
 }
 template <int BK, int BV>
 int decode_smem_bytes(int ws) {
-    return decode_table_bytes(ws) + decode_stage_bytes<BK, BV>();
+    return decode_table_bytes(ws) + kQBytes + decode_stage_bytes<BK, BV>();
 }
-static_assert(kWarps * kStages * StageLayout<1, 1>::kBytes >= 8 * kD * 4, "the rotated queries fit the staging region");
 static_assert(kWarps * kStages * StageLayout<1, 1>::kBytes >= kImageMaxWords * 4, "the table source fits the staging region");
 
 // 16-byte (or, for the norms, 4-byte) asynchronous copy global -> shared;
@@ -452,8 +452,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     constexpr bool kWinPath = kKind >= 1;
     extern __shared__ __align__(16) uint8_t dsmem[];
     uint32_t* s_tab = reinterpret_cast<uint32_t*>(dsmem);
-    uint8_t* s_stage = dsmem + p.img_bytes;
-    float (*s_q)[kD] = reinterpret_cast<float (*)[kD]>(s_stage);
+    float (*s_q)[kD] = reinterpret_cast<float (*)[kD]>(dsmem + p.img_bytes);
+    uint8_t* s_stage = dsmem + p.img_bytes + kQBytes;
     __shared__ float s_qunscale[8];
     __shared__ int s_last;
     __shared__ float s_thr[kThrCompact];                 // fused step: encoder thresholds
@@ -593,35 +593,15 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         }
     }
     if (active) {
-        // the lookup tables: the compact source into the (not yet used)
-        // staging region with independent loads, then 32 copies (one per lane)
-        // of every per-lane entry, entry e of lane L at word 32 e + L (a
-        // 16-byte store covers 4 lanes), and one copy of the shared words
-        {
-            uint32_t* src = reinterpret_cast<uint32_t*>(s_stage);
-            const int nw = p.img_lane + p.img_shared;
-            constexpr int kPerThread = (kImageMaxWords + kWarps * 32 - 1) / (kWarps * 32);
-            uint32_t v[kPerThread];
+        // every plan-static load of the set-up is issued at once, so that they
+        // share one round trip: the K slot lookup recipes (the lane's table
+        // copy: + 4 L) and codec pairs of the lane's slots, the query rotation
+        // recipe of the lane's codec coordinates 4L..4L+3, and the compact
+        // source of the lookup tables
+        uint4 km[16];
 #pragma unroll
-            for (int u = 0; u < kPerThread; ++u) {
-                const int e = tid + u * kWarps * 32;
-                v[u] = e < nw ? __ldg(p.img_src + e) : 0u;
-            }
-#pragma unroll
-            for (int u = 0; u < kPerThread; ++u) {
-                const int e = tid + u * kWarps * 32;
-                if (e < nw) src[e] = v[u];
-            }
-            __syncthreads();
-            uint4* dst = reinterpret_cast<uint4*>(s_tab);
-            for (int i = tid; i < p.img_lane * 8; i += kWarps * 32) {
-                const uint32_t x = src[i >> 3];
-                dst[i] = make_uint4(x, x, x, x);
-            }
-            for (int i = tid; i < p.img_shared; i += kWarps * 32) s_tab[32 * p.img_lane + i] = src[p.img_lane + i];
-            __syncthreads();  // the source is read before the staging region is reused
-        }
-        // query rotation recipe of the lane's codec coordinates 4L..4L+3
+        for (int s = 0; s < 16; ++s) km[s] = __ldg(reinterpret_cast<const uint4*>(&ht->kslot[t][s]));
+        const uint4 sp = __ldg(reinterpret_cast<const uint4*>(&ht->slot_pair[t][0]));
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int j = 4 * lane + i;
@@ -631,21 +611,43 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             q_f[i] = coded ? ht->sign_k[j] * ht->dewhiten[j] : 0.0f;
             q_sc[i] = coded ? ht->inv_sqrt[j] * p.scale_log2 : 0.0f;
         }
-        // K slot lookup recipes (the lane's table copy: + 4 L) and codec
-        // pairs of the lane's slots
+        uint32_t* src = reinterpret_cast<uint32_t*>(s_stage);
+        const int nw = p.img_lane + p.img_shared;
+        constexpr int kPerThread = (kImageMaxWords + kWarps * 32 - 1) / (kWarps * 32);
+        uint32_t v[kPerThread];
+#pragma unroll
+        for (int u = 0; u < kPerThread; ++u) {
+            const int e = tid + u * kWarps * 32;
+            v[u] = e < nw ? __ldg(p.img_src + e) : 0u;
+        }
 #pragma unroll
         for (int s = 0; s < 16; ++s) {
-            const uint4 m = __ldg(reinterpret_cast<const uint4*>(&ht->kslot[t][s]));
-            ksh[s] = m.x;
-            kmask[s] = m.y;
-            kbase[s] = (m.z & kSharedTable) ? (m.z & ~kSharedTable) : (m.z | (4u * lane));
-            kwsh[s] = m.w;
+            ksh[s] = km[s].x;
+            kmask[s] = km[s].y;
+            kbase[s] = (km[s].z & kSharedTable) ? (km[s].z & ~kSharedTable) : (km[s].z | (4u * lane));
+            kwsh[s] = km[s].w;
         }
-        const uint4 sp = __ldg(reinterpret_cast<const uint4*>(&ht->slot_pair[t][0]));
         slot_pairs[0] = sp.x;
         slot_pairs[1] = sp.y;
         slot_pairs[2] = sp.z;
         slot_pairs[3] = sp.w;
+        // the lookup tables: the compact source into the (not yet used)
+        // staging region, then 32 copies (one per lane) of every per-lane
+        // entry, entry e of lane L at word 32 e + L (a 16-byte store covers 4
+        // lanes), and one copy of the shared words
+#pragma unroll
+        for (int u = 0; u < kPerThread; ++u) {
+            const int e = tid + u * kWarps * 32;
+            if (e < nw) src[e] = v[u];
+        }
+        __syncthreads();
+        uint4* dst = reinterpret_cast<uint4*>(s_tab);
+        for (int i = tid; i < p.img_lane * 8; i += kWarps * 32) {
+            const uint32_t x = src[i >> 3];
+            dst[i] = make_uint4(x, x, x, x);
+        }
+        for (int i = tid; i < p.img_shared; i += kWarps * 32) s_tab[32 * p.img_lane + i] = src[p.img_lane + i];
+        __syncthreads();  // the source is read before the staging region is reused
     }
 
     pdl_wait();  // q, the cache and the workspace may belong to the previous kernel
@@ -659,6 +661,23 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             sl = p.map.slot(b, h, pos);
         }
         if (sl >= 0) append_new_token<BK, BV>(p, el, unit, sl, pos, s_thr, s_enc, warp, lane);
+        __syncthreads();  // the new token's records are written before any warp stages them
+    }
+    // the first kStages - 1 tiles of every warp are copied while the queries
+    // are rotated
+    using SL = StageLayout<BK, BV>;
+    uint8_t* st_base = s_stage + warp * (kStages * SL::kBytes);
+    const uint32_t st_addr = (uint32_t)__cvta_generic_to_shared(st_base);
+    if (active) {
+#pragma unroll
+        for (int k = 0; k < kStages - 1; ++k) {
+            if (k < n_tiles) {
+                const int T0 = T0w + k * kStep;
+                stage_tile<BK, BV>(st_addr + k * SL::kBytes, kc, vc, kn, vn, kPaged ? s_pslot[warp][k] : tile_slot(T0),
+                                   T0, seq, lane);
+            }
+            cp_async_commit();
+        }
     }
     float m_ref = -INFINITY, l_run = 0.0f;  // softmax reference (see kLift, kSlack), sum
     // O^T accumulator: acc[mt][e] = query head 2t + e, codec dim 16 g + 2 mt;
@@ -733,7 +752,6 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     // value tables: the lane's copy of the width-BV pair table, or of the
     // width-4 single table
     const uint32_t vbase = (BV <= kPairTableMaxW ? (1u << (2 * BV)) << 7 : (uint32_t)single_base(4) << 7) | (4u * lane);
-    __syncthreads();  // every warp has its query fragments: the staging region may be filled
 
     // ---- main loop: 16-token tiles, operands of the next tile loaded while
     // the current one is decoded (ping-pong register buffers).  kWin: the
@@ -851,18 +869,6 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         pv_mtile<BV, 7>(acc, pb, tr.vw, vbase, s_tab);
     };
 
-    using SL = StageLayout<BK, BV>;
-    uint8_t* st_base = s_stage + warp * (kStages * SL::kBytes);
-    const uint32_t st_addr = (uint32_t)__cvta_generic_to_shared(st_base);
-#pragma unroll
-    for (int k = 0; k < kStages - 1; ++k) {
-        if (k < n_tiles) {
-            const int T0 = T0w + k * kStep;
-            stage_tile<BK, BV>(st_addr + k * SL::kBytes, kc, vc, kn, vn, kPaged ? s_pslot[warp][k] : tile_slot(T0), T0,
-                               seq, lane);
-        }
-        cp_async_commit();
-    }
     auto step = [&](int k, auto win) {
         const int kn_ = k + kStages - 1;
         if (kn_ < n_tiles) {
