@@ -188,6 +188,26 @@ typedef struct {
 
 int bgtq_plan_get_head(const bgtq_plan* plan, int head, bgtq_head_tables* out);
 
+/*
+ * bgtq_plan_save / bgtq_plan_load — a plan as bytes (to keep a calibration
+ * with a model, or to build it on another host).  The paper has no
+ * counterpart; a plan is a deterministic function of its inputs (the
+ * Block-GTQ widths and energies of every head, the group, budgets, seed and
+ * RoPE layout), so those are what is stored, in a versioned, checksummed,
+ * little-endian record; loading runs bgtq_plan_create on them and rebuilds
+ * every table bit for bit.
+ *   bgtq_plan_save: buf host (NULL: only *bytes is set), capacity its size;
+ *                   *bytes = the record's size.  INVALID_ARG if capacity is
+ *                   too small.
+ *   bgtq_plan_load: buf/bytes a record from bgtq_plan_save; flags as for
+ *                   bgtq_plan_create (BGTQ_PLAN_HOST_ONLY: no device tables).
+ *                   INVALID_ARG for a foreign, truncated or corrupted record
+ *                   (magic, size, checksum), UNSUPPORTED for another format
+ *                   version, and bgtq_plan_create's errors.
+ */
+int bgtq_plan_save(const bgtq_plan* plan, void* buf, size_t capacity, size_t* bytes);
+int bgtq_plan_load(bgtq_plan** out, const void* buf, size_t bytes, int flags);
+
 /* Codebook of one width (0..8): 2^width fp16-exact centroids as floats and
  * 2^width - 1 float thresholds (host pointers owned by the plan). */
 int bgtq_plan_get_codebook(const bgtq_plan* plan, int width, const float** centroids, const float** thresholds,

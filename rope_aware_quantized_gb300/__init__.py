@@ -131,6 +131,25 @@ def bgtq_plan_create(block_bits, energy, group: int, bits_per_key: int, v_bits: 
     return Plan(h.value, bb.shape[0], group, bits_per_key, v_bits)
 
 
+def bgtq_plan_save(plan: Plan) -> bytes:
+    """The plan as a versioned, checksummed byte record (its defining inputs)."""
+    n = C.c_size_t()
+    _check(lib().bgtq_plan_save(plan.handle, None, 0, C.byref(n)))
+    buf = C.create_string_buffer(n.value)
+    _check(lib().bgtq_plan_save(plan.handle, buf, n.value, C.byref(n)))
+    return buf.raw[:n.value]
+
+
+def bgtq_plan_load(data: bytes, host_only: bool = False) -> Plan:
+    """A plan rebuilt from a bgtq_plan_save record."""
+    data = bytes(data)
+    h = C.c_void_p()
+    _check(lib().bgtq_plan_load(C.byref(h), data, len(data), BGTQ_PLAN_HOST_ONLY if host_only else 0))
+    # the record's header holds the shape: read it back the same way the library does
+    H, G, bpk, bv = (int.from_bytes(data[12 + 4 * i:16 + 4 * i], "little") for i in range(4))
+    return Plan(h.value, H, G, bpk, bv)
+
+
 def bgtq_cache_bytes(plan: Plan, batch: int, capacity: int):
     kb, vb, nb = C.c_size_t(), C.c_size_t(), C.c_size_t()
     _check(lib().bgtq_cache_bytes(plan.handle, batch, capacity, C.byref(kb), C.byref(vb), C.byref(nb)))

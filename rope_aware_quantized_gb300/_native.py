@@ -34,6 +34,8 @@ EXPORTS = {
     "bgtq_plan_create": (C.c_int, [C.POINTER(C.c_void_p), C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
                                    C.c_void_p, C.c_void_p, C.c_uint64, C.c_int, C.c_int]),
     "bgtq_plan_destroy": (C.c_int, [C.c_void_p]),
+    "bgtq_plan_save": (C.c_int, [C.c_void_p, C.c_void_p, C.c_size_t, C.POINTER(C.c_size_t)]),
+    "bgtq_plan_load": (C.c_int, [C.POINTER(C.c_void_p), C.c_void_p, C.c_size_t, C.c_int]),
     "bgtq_plan_get_head": (C.c_int, [C.c_void_p, C.c_int, C.POINTER(BgtqHeadTables)]),
     "bgtq_plan_get_codebook": (C.c_int, [C.c_void_p, C.c_int, C.POINTER(C.POINTER(C.c_float)),
                                          C.POINTER(C.POINTER(C.c_float)), C.POINTER(C.c_int)]),

@@ -574,6 +574,8 @@ int bgtq_plan_create(bgtq_plan** out, int head_dim, int n_kv_heads, int group, i
     p->rope_layout = rope_layout;
     p->seed = seed;
     p->flags = flags;
+    p->in_bits.assign(block_bits, block_bits + (size_t)n_kv_heads * kNB);
+    p->in_energy.assign(energy, energy + (size_t)n_kv_heads * kNB);
     p->heads.resize(n_kv_heads);
     p->sign_k8.resize(n_kv_heads);
     p->sign_v8.resize(n_kv_heads);
@@ -601,6 +603,99 @@ int bgtq_plan_create(bgtq_plan** out, int head_dim, int n_kv_heads, int group, i
     }
     *out = p;
     return BGTQ_OK;
+}
+
+// ---- plan serialization: the defining inputs, versioned and checksummed
+// (every table is a deterministic function of them).  Little-endian:
+//   "BGTQPLAN" | u32 version | u32 H, G, bits_per_key, v_bits, rope_layout |
+//   u64 seed | u8 widths[H][64] | f64 energies[H][64] | u64 FNV-1a of all
+//   preceding bytes
+
+}  // extern "C"
+
+namespace {
+
+constexpr char kPlanMagic[8] = {'B', 'G', 'T', 'Q', 'P', 'L', 'A', 'N'};
+constexpr uint32_t kPlanVersion = 1;
+constexpr size_t kPlanHeader = 8 + 4 + 5 * 4 + 8;
+
+uint64_t fnv1a(const uint8_t* d, size_t n) {
+    uint64_t h = 1469598103934665603ull;
+    for (size_t i = 0; i < n; ++i) {
+        h ^= d[i];
+        h *= 1099511628211ull;
+    }
+    return h;
+}
+
+void put_le(uint8_t*& o, uint64_t v, int nbytes) {
+    for (int i = 0; i < nbytes; ++i) *o++ = (uint8_t)(v >> (8 * i));
+}
+
+uint64_t get_le(const uint8_t*& i, int nbytes) {
+    uint64_t v = 0;
+    for (int k = 0; k < nbytes; ++k) v |= (uint64_t)(*i++) << (8 * k);
+    return v;
+}
+
+}  // namespace
+
+extern "C" {
+
+int bgtq_plan_save(const bgtq_plan* p, void* buf, size_t capacity, size_t* bytes) {
+    if (!p || !bytes) return set_error(BGTQ_ERR_INVALID_ARG, "NULL pointer");
+    const size_t n = kPlanHeader + (size_t)p->H * kNB * (1 + 8) + 8;
+    *bytes = n;
+    if (!buf) return BGTQ_OK;
+    if (capacity < n) return set_error(BGTQ_ERR_INVALID_ARG, "buffer holds %zu bytes, the plan needs %zu", capacity, n);
+    uint8_t* o = static_cast<uint8_t*>(buf);
+    std::memcpy(o, kPlanMagic, 8);
+    o += 8;
+    put_le(o, kPlanVersion, 4);
+    put_le(o, (uint32_t)p->H, 4);
+    put_le(o, (uint32_t)p->G, 4);
+    put_le(o, (uint32_t)p->bits_per_key, 4);
+    put_le(o, (uint32_t)p->bv, 4);
+    put_le(o, (uint32_t)p->rope_layout, 4);
+    put_le(o, p->seed, 8);
+    for (uint8_t b : p->in_bits) *o++ = b;
+    for (double e : p->in_energy) {
+        uint64_t u;
+        std::memcpy(&u, &e, 8);
+        put_le(o, u, 8);
+    }
+    const uint64_t h = fnv1a(static_cast<const uint8_t*>(buf), (size_t)(o - static_cast<uint8_t*>(buf)));
+    put_le(o, h, 8);
+    return BGTQ_OK;
+}
+
+int bgtq_plan_load(bgtq_plan** out, const void* buf, size_t bytes, int flags) {
+    if (!out || !buf) return set_error(BGTQ_ERR_INVALID_ARG, "NULL pointer");
+    *out = nullptr;
+    const uint8_t* b = static_cast<const uint8_t*>(buf);
+    if (bytes < kPlanHeader + 8 || std::memcmp(b, kPlanMagic, 8) != 0)
+        return set_error(BGTQ_ERR_INVALID_ARG, "not a serialized Block-GTQ plan");
+    const uint8_t* i = b + 8;
+    const uint32_t version = (uint32_t)get_le(i, 4);
+    if (version != kPlanVersion)
+        return set_error(BGTQ_ERR_UNSUPPORTED, "plan format version %u (this library reads version %u)", version,
+                         kPlanVersion);
+    const int H = (int)get_le(i, 4), G = (int)get_le(i, 4), bpk = (int)get_le(i, 4), bv = (int)get_le(i, 4);
+    const int layout = (int)get_le(i, 4);
+    const uint64_t seed = get_le(i, 8);
+    if (H < 1 || H > 4096) return set_error(BGTQ_ERR_INVALID_ARG, "serialized plan: head count %d out of range", H);
+    const size_t n = kPlanHeader + (size_t)H * kNB * (1 + 8) + 8;
+    if (bytes < n) return set_error(BGTQ_ERR_INVALID_ARG, "serialized plan truncated (%zu of %zu bytes)", bytes, n);
+    const uint8_t* ce = b + n - 8;
+    if (get_le(ce, 8) != fnv1a(b, n - 8)) return set_error(BGTQ_ERR_INVALID_ARG, "serialized plan: checksum mismatch");
+    std::vector<uint8_t> bits(i, i + (size_t)H * kNB);
+    i += (size_t)H * kNB;
+    std::vector<double> energy((size_t)H * kNB);
+    for (double& e : energy) {
+        const uint64_t u = get_le(i, 8);
+        std::memcpy(&e, &u, 8);
+    }
+    return bgtq_plan_create(out, kD, H, G, bpk, bv, bits.data(), energy.data(), seed, layout, flags);
 }
 
 int bgtq_plan_destroy(bgtq_plan* p) {

@@ -133,6 +133,8 @@ struct bgtq_plan {
     std::vector<bgtq::HeadTab> heads;
     std::vector<float> cent[bgtq::kWMax + 1];
     std::vector<float> thr[bgtq::kWMax + 1];
+    std::vector<uint8_t> in_bits;   // the plan's defining inputs, kept for bgtq_plan_save:
+    std::vector<double> in_energy;  // block widths and energies [H][64]
     std::vector<uint32_t> img_src;  // decode table entries (see single_base)
     int img_ws = 0;                 // widest code the decode tables cover
     // inspection copies (bgtq_plan_get_head)
