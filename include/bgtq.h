@@ -68,6 +68,9 @@ extern "C" {
 #define BGTQ_STATUS_SEQLEN_CAPACITY 2 /* seq_len > capacity or < 0: clamped */
 #define BGTQ_STATUS_PAGE_RANGE 4      /* a page_table entry outside [0, n_pages) was met: writes to that
                                          page skipped, reads use page 0 (output unspecified) */
+#define BGTQ_STATUS_TIMEOUT 8         /* a wait inside a pipelined kernel gave up after 2 s: that launch
+                                         skipped the rest of its work (output unspecified); never expected,
+                                         reported instead of hanging the GPU */
 
 /* plan flags */
 #define BGTQ_PLAN_HOST_ONLY 1 /* build the tables on the host only (inspection, no GPU needed) */
@@ -306,7 +309,7 @@ int bgtq_decode_step(const bgtq_plan* plan, void* stream, const void* q_fp16, co
  *   cache        host pointer to the layer's cache descriptor (contiguous or
  *                paged; with a recent-key buffer its last W keys are copied too)
  *   out          device, [batch][H*G][t][128], half (out_dtype 0) or float (1),
- *                8-byte aligned
+ *                16-byte aligned
  *   softmax_scale  logit scale, e.g. 1/sqrt(128)
  *   dev_status   device int32 or NULL
  * Row i of query head g computes sum_{j <= i} softmax_j(scale q_i . k_j) v_j

@@ -825,10 +825,12 @@ int bgtq_prefill_attn(const bgtq_plan* p, void* stream, const void* q, const voi
     if (!q || !k || !v || !out) return set_error(BGTQ_ERR_INVALID_ARG, "NULL pointer");
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15)
         return set_error(BGTQ_ERR_INVALID_ARG, "q, k and v must be 16-byte aligned");
-    if (reinterpret_cast<uintptr_t>(out) & 7) return set_error(BGTQ_ERR_INVALID_ARG, "out must be 8-byte aligned");
+    if (reinterpret_cast<uintptr_t>(out) & 15) return set_error(BGTQ_ERR_INVALID_ARG, "out must be 16-byte aligned");
     if (out_dtype != 0 && out_dtype != 1) return set_error(BGTQ_ERR_INVALID_ARG, "out_dtype must be 0 (half) or 1 (float)");
     if (!(scale > 0.0f) || !std::isfinite(scale)) return set_error(BGTQ_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
     if (batch > 65535) return set_error(BGTQ_ERR_UNSUPPORTED, "at most 65535 sequences per call");
+    if ((uint64_t)batch * p->H * p->G * (uint64_t)t + 128 >= (1ull << 31))
+        return set_error(BGTQ_ERR_UNSUPPORTED, "batch * query heads * t must stay below 2^31 - 128");
     if ((rc = check_plan(p))) return rc;
     cudaError_t e = launch_prefill(*p, (cudaStream_t)stream, q, k, v, batch, t, *c, out, out_dtype, scale, status);
     if (e != cudaSuccess) return set_error(BGTQ_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));

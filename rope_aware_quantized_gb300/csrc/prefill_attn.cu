@@ -1,5 +1,7 @@
-// Fused prefill: causal attention over the prompt's fp16 K/V on the tensor
-// cores and, in the same launch, the packed K/V records of the prompt.
+// Fused prefill: causal attention over the prompt's fp16 K/V on the
+// fifth-generation tensor cores (tcgen05 MMAs with accumulators in tensor
+// memory, tiles copied by TMA) and, in the same launch, the packed K/V
+// records of the prompt.
 //
 // Method: "RoPE-Aware Bit Allocation for KV-Cache Quantization" — the packed
 // cache (review §1 "Packed-Cache") is written when the prompt is prefilled
@@ -7,16 +9,33 @@
 // as given.  Fusing the quantizer into an attention operator is named as
 // future work on the LogQuant page (section "중요성 및 주장").
 //
-// Grid (query blocks of 64 rows, heaviest first; query heads; sequences),
-// 4 warps of 16 query rows.  K and V tiles of 64 keys are staged in shared
-// memory by cp.async, two stages, 16-byte chunks XOR-swizzled by row so the
-// ldmatrix reads hit 8 distinct bank groups.  S = Q K^T and O += P V are
-// m16n8k16 fp16 mma with fp32 accumulation (P rounded to fp16); the softmax
-// is online, in the log2 domain.  The CTA of the first query head of each KV
-// head also encodes the keys and values of its own 64 positions, before it
-// attends, with the warp encoder steps of the append kernel (the records are
-// bit-identical to an append of the same tokens).
+// One CTA takes 128 query rows of two query heads that share a KV head, so
+// that both attend the same K/V tiles; 10 warps:
+//   warps 0-3, 4-7  softmax warpgroups: thread i of warpgroup g owns row i of
+//                   query head g, which is lane i of tensor memory
+//   warp 8          issues the MMAs (one thread) and owns the tensor memory
+//   warp 9          issues the TMA copies (one thread)
+// Tensor memory, 512 columns of fp32: S_g = Q_g K^T at columns 128 g, the
+// output accumulator O_g at 256 + 128 g.  The softmax writes P_g (fp16, two
+// per column) over the first 64 columns of S_g and O_g += P_g V reads its A
+// operand from there.  Shared memory holds Q_0, Q_1 and two stages of K and
+// V tiles (128 x 128 fp16 each), each tile two 64-column TMA boxes with the
+// 128-byte swizzle that the MMA descriptors name: Q and K are K-major
+// operands, V the MN-major B operand of P V.  MMA order for key tile j:
+// PV_0(j), S_0(j+1), PV_1(j), S_1(j+1); warpgroup 0's softmax of a tile runs
+// while the tensor cores serve warpgroup 1 and the other way round.  The
+// softmax is online in the log2 domain; a row's running maximum is raised
+// (and its O rescaled in tensor memory) only when a tile's maximum exceeds
+// it by more than kHeadroom, so a probability never exceeds 2^kHeadroom.
+// The CTAs of the first pair of query heads of each KV head also encode the
+// keys and values of their 128 positions, with the warp encoder steps of the
+// append kernel (records bit-identical to an append of the same tokens).
+// Every wait is bounded: after kWaitNs it sets BGTQ_STATUS_TIMEOUT, the CTA
+// skips the rest of its work, lets its copies and MMAs land and frees its
+// tensor memory.
+#include <cuda.h>
 #include <cuda_fp16.h>
+#include <cuda_runtime.h>
 
 #include <cmath>
 #include <mutex>
@@ -26,11 +45,34 @@
 namespace bgtq {
 namespace {
 
-constexpr int kPfWarps = 4;
-constexpr int kPfRows = 64;                 // query rows per CTA (16 per warp)
-constexpr int kPfKeys = 64;                 // keys per tile
-constexpr int kPfTile = kPfKeys * kD * 2;   // bytes of a 64 x 128 fp16 tile
-constexpr int kPfSmem = 5 * kPfTile;        // Q, then K and V of two stages
+constexpr int kTcRows = 128;                      // query rows per warpgroup (tensor-memory lanes)
+constexpr int kTcKeys = 128;                      // keys per tile
+constexpr int kTcThreads = 320;                   // two softmax warpgroups, the MMA warp, the TMA warp
+constexpr int kEncWarps = 8;                      // warps that encode the block's records
+constexpr uint32_t kTcTile = kTcRows * kD * 2;    // one 128 x 128 fp16 tile: 32 KB
+constexpr uint32_t kTcBox = kTcTile / 2;          // one 64-column box of it (128 rows x 128 B)
+constexpr uint32_t kOffQ = 0;                     // Q_g at + g kTcTile
+constexpr uint32_t kOffK = 2 * kTcTile;           // K stage s at + s kTcTile
+constexpr uint32_t kOffV = 4 * kTcTile;           // V stage s at + s kTcTile
+constexpr uint32_t kTcSmem = 6 * kTcTile + 1024;  // + room to align the base to 1 KB
+constexpr uint32_t kTmemCols = 512;
+constexpr float kHeadroom = 8.0f;
+constexpr unsigned long long kWaitNs = 2000000000ull;
+
+// mbarriers: tile copies landed (Q, K/V per stage), stages free again,
+// S_g computed, P_g written, O_g final, every MMA done
+enum {
+    kBarQ = 0,
+    kBarKFull = 1,
+    kBarVFull = 3,
+    kBarKEmpty = 5,
+    kBarVEmpty = 7,
+    kBarS = 9,
+    kBarP = 11,
+    kBarO = 13,
+    kBarDrain = 15,
+    kNumBars = 16
+};
 
 struct PfParams {
     const __half* q;  // [B][H*G][T][128]
@@ -55,40 +97,156 @@ struct PfParams {
     int32_t* status;
 };
 
-template <bool B>
-struct BoolC {
-    static constexpr bool value = B;
-};
+// ---- descriptors (PTX ISA, tcgen05 "Matrix Descriptors" and "Instruction
+// descriptor" tables)
 
-// byte offset of 16-byte chunk c of row r in a swizzled 64 x 256-byte tile
-__device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 256 + ((c ^ (r & 7)) << 4)); }
-
-__device__ __forceinline__ void cp16z(uint32_t dst, const void* src, bool ok) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(ok ? 16 : 0) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+// Shared-memory matrix descriptor: start address, leading and stride byte
+// offsets (each >> 4 in 14 bits at bits 0, 16 and 32), the fixed 0b001 at
+// bits 46-48, base offset 0 (bits 49-51; every pattern starts 1 KB aligned)
+// and the 128-byte swizzle (2) in bits 61-63.
+__host__ __device__ constexpr uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-__device__ __forceinline__ void ldsm4(uint32_t a, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(a));
+// Instruction descriptor of kind::f16: dense, fp32 D (bits 4-5 = 1), fp16 A
+// and B (bits 7-9, 10-12 = 0), no negation, A K-major (bit 15 = 0), B K-major
+// (0) or MN-major (1) in bit 16, N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t instr_desc(int m, int n, int b_mn_major) {
+    return (1u << 4) | ((uint32_t)b_mn_major << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
-__device__ __forceinline__ void ldsm4t(uint32_t a, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(a));
+
+// The descriptors the kernel builds, decoded field by field against the
+// layout above for the extreme addresses it can use (a 1 KB-aligned base
+// anywhere in the 227 KB a CTA can address).
+bool descriptors_valid() {
+    const uint32_t idS = instr_desc(kTcRows, kTcKeys, 0), idO = instr_desc(kTcRows, kD, 1);
+    for (uint32_t id : {idS, idO}) {
+        const uint32_t n = ((id >> 17) & 0x3Fu) << 3, m = ((id >> 24) & 0x1Fu) << 4;
+        if (m != 128 || n % 16 != 0 || n < 16 || n > 256) return false;       // M = 128: N in 16..256, step 16
+        if (((id >> 4) & 3u) != 1u || ((id >> 7) & 0x3Fu) != 0u) return false;  // fp32 D; fp16 A and B
+        if (((id >> 13) & 7u) != 0u || (id & 0xFu) != 0u) return false;        // no negation, A K-major, dense
+    }
+    if (((idS >> 16) & 1u) != 0u || ((idO >> 16) & 1u) != 1u) return false;
+    constexpr uint32_t kMaxSmem = 227u * 1024u;
+    for (uint32_t base = 0; base + kTcSmem <= kMaxSmem + 1024; base += 1024) {
+        // S operands (K-major: LBO unused, SBO = 8 rows of 128 B), steps of 16 in K
+        for (int k = 0; k < kD / 16; ++k) {
+            const uint32_t off = (uint32_t)(k >> 2) * kTcBox + (uint32_t)(k & 3) * 32;
+            for (uint32_t a : {base + kOffQ + kTcTile + off, base + kOffK + kTcTile + off}) {
+                const uint64_t d = smem_desc(a, 16, 1024);
+                if (((d & 0x3FFFu) << 4) != a || (((d >> 32) & 0x3FFFu) << 4) != 1024u) return false;
+                if (((d >> 46) & 7u) != 1u || ((d >> 49) & 7u) != 0u || (d >> 61) != 2u) return false;
+            }
+            // V (MN-major: LBO = the 64-column box stride, SBO = 8 keys of 128 B), steps of 16 keys
+            const uint32_t av = base + kOffV + kTcTile + (uint32_t)k * 2048;
+            const uint64_t d = smem_desc(av, kTcBox, 1024);
+            if (((d & 0x3FFFu) << 4) != av || (((d >> 16) & 0x3FFFu) << 4) != kTcBox) return false;
+            if ((((d >> 32) & 0x3FFFu) << 4) != 1024u || (d >> 61) != 2u) return false;
+        }
+    }
+    return true;
 }
-// (not volatile: a pure register operation the compiler may schedule freely)
-__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+
+// ---- device helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* ptr) { return (uint32_t)__cvta_generic_to_shared(ptr); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase of parity `parity` of an mbarrier, for kWaitNs at most
+// and not at all once another thread of the CTA gave up (`check_abort`).
+// Giving up sets the status bit and the CTA's abort flag.
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* status,
+                          bool check_abort = true) {
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_try(bar, parity)) return true;
+        if (check_abort && *abort_flag) return false;
+        if (global_ns() - t0 > kWaitNs) {
+            *abort_flag = 1;
+            if (status) atomicOr(status, BGTQ_STATUS_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+// A operand from tensor memory
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(
+            d),
+        "r"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+// the mbarrier arrives once every MMA this thread issued so far has completed
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 32 consecutive fp32 columns of the warp's 32 lanes
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t* r = reinterpret_cast<uint32_t*>(v);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -99,28 +257,18 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Copy rows [0, 64) of a row-major [.][128] fp16 matrix starting at `src`
-// into the swizzled tile at `dst`; rows >= valid are zero-filled.
-__device__ __forceinline__ void stage_rows(uint32_t dst, const __half* src, int valid, int tid) {
-#pragma unroll
-    for (int i = tid; i < kPfKeys * 16; i += kPfWarps * 32) {
-        const int r = i >> 4, c = i & 15;
-        const bool ok = r < valid;
-        cp16z(dst + swz(r, c), ok ? src + (size_t)r * kD + 8 * c : src, ok);
-    }
-}
-
 // Encode the keys and values of positions [p0, p0 + n) of (b, h): warp w
-// takes the token pairs w, w + 4, ...; the steps are the append kernel's.
+// takes the token pairs w, w + n_warps, ...; the steps are the append
+// kernel's.
 __device__ void encode_block(const PfParams& p, int b, int h, int p0, int n, const float* s_thr,
-                             uint32_t (*s_rec)[8 * kPairMaxW], uint32_t* s_vmask, int warp, int lane) {
+                             uint32_t (*s_rec)[8 * kPairMaxW], uint32_t* s_vmask, int warp, int lane, int n_warps) {
     const HeadTab* ht = p.heads + h;
     EncLane ek, ev;
     enc_lane_load(ek, ht, true, p.bv, p.v_inv_sqrt, lane);
     enc_lane_load(ev, ht, false, p.bv, p.v_inv_sqrt, lane);
     const size_t row0 = ((size_t)b * p.H + h) * p.T;
     const size_t unit = (size_t)b * p.H + h;
-    for (int pi = warp; 2 * pi < n; pi += kPfWarps) {
+    for (int pi = warp; 2 * pi < n; pi += n_warps) {
         const int pos0 = p0 + 2 * pi;
         const bool has[2] = {true, 2 * pi + 1 < n};
         // ---- keys of the pair
@@ -204,169 +352,297 @@ __device__ void encode_block(const PfParams& p, int b, int h, int p0, int n, con
     }
 }
 
-__global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_kernel(PfParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ float s_thr[kThrCompact];
-    __shared__ uint32_t s_rec[kPfWarps][3][8 * kPairMaxW];
-    __shared__ uint32_t s_vmask[kPfWarps][8 * kPairMaxW];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-    const int nqb = (p.T + kPfRows - 1) / kPfRows;
-    const int qb = nqb - 1 - (int)blockIdx.x;
-    const int hq = blockIdx.y, b = blockIdx.z;
-    const int h = hq / p.G;
-    const int q0 = qb * kPfRows;
-    const __half* qsrc = p.q + (((size_t)b * p.H * p.G + hq) * p.T + q0) * kD;
-    const __half* ksrc = p.k + ((size_t)b * p.H + h) * p.T * kD;
-    const __half* vsrc = p.v + ((size_t)b * p.H + h) * p.T * kD;
-    const uint32_t sQ = (uint32_t)__cvta_generic_to_shared(smem);
-    const uint32_t sK0 = sQ + kPfTile, sV0 = sQ + 2 * kPfTile;  // stage s: + 2 s kPfTile
-
-    // the query block and the first K/V tile
-    stage_rows(sQ, qsrc, min(kPfRows, p.T - q0), tid);
-    stage_rows(sK0, ksrc, min(kPfKeys, p.T), tid);
-    stage_rows(sV0, vsrc, min(kPfKeys, p.T), tid);
-    cp_commit();
-    // the first query head of each KV head encodes its block's keys and values
-    if (hq % p.G == 0) {
-        stage_thresholds(s_thr, p.thr, tid, kPfWarps * 32);
-        __syncthreads();
-        encode_block(p, b, h, q0, min(kPfRows, p.T - q0), s_thr, s_rec[warp], s_vmask[warp], warp, lane);
+// Softmax warpgroup g: the online softmax of row r of query head hq0 + g
+// over key tiles 0 .. nkt-1, then the normalised output row.
+__device__ __forceinline__ void softmax_rows(const PfParams& p, uint32_t tmem, int g, int b, int hq, int q0, int nkt,
+                                             uint32_t bar_s, uint32_t bar_p, uint32_t bar_o, volatile int* abort_flag,
+                                             int warp, int lane) {
+    const int r = 32 * (warp & 3) + lane;  // row of the block = tensor-memory lane
+    const int row = q0 + r;
+    const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t tS = tmem + lanes + 128u * g, tO = tmem + lanes + 256u + 128u * g;
+    const float c = p.scale_log2;
+    float m = 0.0f, l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < nkt; ++j) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_s, j & 1, abort_flag, p.status))) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        float s[kTcKeys];
+#pragma unroll
+        for (int q = 0; q < kTcKeys / 32; ++q) tmem_ld32(tS + 32 * q, s + 32 * q);
+        tmem_wait_ld();
+        if (j == nkt - 1) {  // the diagonal tile: keys after the row, and past the prompt
+            const int lim = min(row, p.T - 1) - j * kTcKeys;
+#pragma unroll
+            for (int k = 0; k < kTcKeys; ++k)
+                if (k > lim) s[k] = -INFINITY;
+        }
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+        for (int k = 8; k < kTcKeys; ++k) mx[k & 7] = fmaxf(mx[k & 7], s[k]);
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * c;
+        float f = 1.0f;
+        bool raise = false;
+        if (j == 0) {
+            m = mt;  // key 0 is before every row: finite
+        } else if (mt > m + kHeadroom) {
+            f = ex2(m - mt);
+            m = mt;
+            l *= f;
+            raise = true;
+        }
+        if (__any_sync(0xffffffffu, raise)) {
+            // the row's O so far is in tensor memory; PV of tile j-1 has
+            // completed (S of tile j was issued after it)
+#pragma unroll 1
+            for (int q = 0; q < kD / 32; ++q) {
+                float o[32];
+                tmem_ld32(tO + 32 * q, o);
+                tmem_wait_ld();
+                uint32_t w[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(o[i] * f);
+                tmem_st32(tO + 32 * q, w);
+            }
+        }
+        uint32_t pk[kTcKeys / 2];
+        float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int i = 0; i < kTcKeys / 2; ++i) {
+            const float p0 = ex2(fmaf(s[2 * i], c, -m)), p1 = ex2(fmaf(s[2 * i + 1], c, -m));
+            ls[i & 3] += p0 + p1;
+            pk[i] = pack_h2(p0, p1);
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        // P over the first 64 columns of S (already read)
+        tmem_st32(tS, pk);
+        tmem_st32(tS + 32, pk + 32);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar_p);
     }
-    cp_wait<0>();
-    __syncthreads();
-
-    // query fragments of the warp's 16 rows (8 k-chunks of 16 dims)
-    uint32_t qa[8][4];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const int r = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;
-        ldsm4(sQ + swz(r, 2 * c + (lane >> 4)), qa[c]);
-    }
-    const int row_g = q0 + 16 * warp + g;  // rows row_g and row_g + 8
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-    float acc[16][4];
-#pragma unroll
-    for (int n = 0; n < 16; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
-
-    // one 64-key tile; kEdge: the diagonal tile (causal mask, keys past T)
-    auto tile = [&](int j, auto edge_tag) {
-        constexpr bool kEdge = decltype(edge_tag)::value;
-        const int st = j & 1;
-        const uint32_t sK = sK0 + 2 * st * kPfTile, sV = sV0 + 2 * st * kPfTile;
-        if (j + 1 <= qb) {
-            const uint32_t nK = sK0 + 2 * (st ^ 1) * kPfTile, nV = sV0 + 2 * (st ^ 1) * kPfTile;
-            const int k0 = (j + 1) * kPfKeys;
-            stage_rows(nK, ksrc + (size_t)k0 * kD, min(kPfKeys, p.T - k0), tid);
-            stage_rows(nV, vsrc + (size_t)k0 * kD, min(kPfKeys, p.T - k0), tid);
-        }
-        cp_commit();
-        cp_wait<1>();
-        __syncthreads();
-        // ---- S = Q K^T for the warp's 16 rows x 64 keys
-        float s[8][4];
-#pragma unroll
-        for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.0f;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                uint32_t kb[4];
-                const int key = 16 * jj + (lane & 7) + (lane >> 4) * 8;
-                ldsm4(sK + swz(key, 2 * c + ((lane >> 3) & 1)), kb);
-                mma_f16(s[2 * jj], qa[c], kb[0], kb[1]);
-                mma_f16(s[2 * jj + 1], qa[c], kb[2], kb[3]);
-            }
-        }
-        // ---- online softmax (rows g: e = 0, 1; g + 8: e = 2, 3) in the
-        // log2 domain: the running maxima m are of scale log2(e) s; the scale
-        // is folded into the exponent's fma
-        const float cs = p.scale_log2;
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int n = 0; n < 8; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if (kEdge) {
-                    const int key = j * kPfKeys + 8 * n + 2 * t + (e & 1);
-                    const int row = row_g + 8 * (e >> 1);
-                    if (key > row || key >= p.T) s[n][e] = -INFINITY;
-                }
-                if (e < 2) mx0 = fmaxf(mx0, s[n][e]);
-                else mx1 = fmaxf(mx1, s[n][e]);
-            }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float n0 = fmaxf(m0, mx0 * cs), n1 = fmaxf(m1, mx1 * cs);
-        if (__any_sync(0xffffffffu, n0 != m0 || n1 != m1)) {
-            // a maximum moved: rescale (exp2(-inf) = 0 on the first tile)
-            const float a0 = ex2(m0 - n0), a1 = ex2(m1 - n1);
-            l0 *= a0;
-            l1 *= a1;
-#pragma unroll
-            for (int n = 0; n < 16; ++n) {
-                acc[n][0] *= a0;
-                acc[n][1] *= a0;
-                acc[n][2] *= a1;
-                acc[n][3] *= a1;
-            }
-            m0 = n0;
-            m1 = n1;
-        }
-#pragma unroll
-        for (int n = 0; n < 8; ++n) {
-            s[n][0] = ex2(fmaf(s[n][0], cs, -n0));
-            s[n][1] = ex2(fmaf(s[n][1], cs, -n0));
-            s[n][2] = ex2(fmaf(s[n][2], cs, -n1));
-            s[n][3] = ex2(fmaf(s[n][3], cs, -n1));
-            l0 += s[n][0] + s[n][1];
-            l1 += s[n][2] + s[n][3];
-        }
-        // ---- O += P V (4 k-chunks of 16 keys x 16 n-tiles of 8 dims)
-#pragma unroll
-        for (int kc = 0; kc < 4; ++kc) {
-            const uint32_t pa[4] = {pack_h2(s[2 * kc][0], s[2 * kc][1]), pack_h2(s[2 * kc][2], s[2 * kc][3]),
-                                    pack_h2(s[2 * kc + 1][0], s[2 * kc + 1][1]),
-                                    pack_h2(s[2 * kc + 1][2], s[2 * kc + 1][3])};
-            const int key = 16 * kc + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-            for (int n2 = 0; n2 < 8; ++n2) {
-                uint32_t vb[4];
-                ldsm4t(sV + swz(key, 2 * n2 + (lane >> 4)), vb);
-                mma_f16(acc[2 * n2], pa, vb[0], vb[1]);
-                mma_f16(acc[2 * n2 + 1], pa, vb[2], vb[3]);
-            }
-        }
-        __syncthreads();  // this stage is refilled by the next iteration
-    };
-    for (int j = 0; j < qb; ++j) tile(j, BoolC<false>{});
-    tile(qb, BoolC<true>{});
-
-    // ---- normalise and store rows row_g, row_g + 8 (dims 8 n + 2 t, + 1)
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    const float i0 = 1.0f / l0, i1 = 1.0f / l1;
-    const size_t orow0 = ((size_t)b * p.H * p.G + hq) * p.T;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int row = row_g + 8 * half;
+    if (!ok || !__all_sync(0xffffffffu, mbar_wait(bar_o, 0, abort_flag, p.status))) return;
+    tc_fence_after();
+    const float inv = 1.0f / l;
+    const size_t o0 = ((size_t)((size_t)b * p.H * p.G + hq) * p.T + row) * kD;
+#pragma unroll 1
+    for (int q = 0; q < kD / 32; ++q) {
+        float o[32];
+        tmem_ld32(tO + 32 * q, o);
+        tmem_wait_ld();
         if (row >= p.T) continue;
-        const float inv = half ? i1 : i0;
-        const size_t o = (orow0 + row) * kD;
+        if (p.out_dtype) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + o0 + 32 * q);
 #pragma unroll
-        for (int n = 0; n < 16; ++n) {
-            const float x0 = acc[n][2 * half] * inv, x1 = acc[n][2 * half + 1] * inv;
-            const int d = 8 * n + 2 * t;
-            if (p.out_dtype) {
-                *reinterpret_cast<float2*>(static_cast<float*>(p.out) + o + d) = make_float2(x0, x1);
-            } else {
-                *reinterpret_cast<__half2*>(static_cast<__half*>(p.out) + o + d) = __floats2half2_rn(x0, x1);
-            }
+            for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+        } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(p.out) + o0 + 32 * q);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(pack_h2(o[8 * i] * inv, o[8 * i + 1] * inv), pack_h2(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
+                                    pack_h2(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
+                                    pack_h2(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
         }
     }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, PfParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t s_bar[kNumBars];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+    __shared__ float s_thr[kThrCompact];
+    __shared__ uint32_t s_rec[kEncWarps][3][8 * kPairMaxW];
+    __shared__ uint32_t s_vmask[kEncWarps][8 * kPairMaxW];
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int npair = (p.G + 1) >> 1;
+    const int pair = (int)blockIdx.x % npair;
+    const int h = (int)(blockIdx.x / npair) % p.H;
+    const int b = (int)blockIdx.x / (npair * p.H);
+    const int nqb = (p.T + kTcRows - 1) / kTcRows;
+    const int qb = nqb - 1 - (int)blockIdx.y;  // heaviest query blocks first
+    const int q0 = qb * kTcRows;
+    const int hq0 = h * p.G + 2 * pair;
+    const int ng = 2 * pair + 1 < p.G ? 2 : 1;  // query heads of this CTA
+    const int nkt = qb + 1;                     // key tiles; tile qb holds the diagonal
+    const uint32_t bar0 = smem_u32(&s_bar[0]);
+    volatile int* abort_flag = &s_abort;
+#define BAR(i) (bar0 + 8u * (uint32_t)(i))
+
+    if (tid == 0) {
+        s_abort = 0;
+        for (int i = 0; i < kNumBars; ++i) mbar_init(BAR(i), (i == kBarP || i == kBarP + 1) ? kTcRows : 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 8) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    if (warp == 9) {
+        // ---- TMA: Q of the CTA's heads, then K and V tiles through two stages
+        if (lane == 0) {
+            int used[2] = {0, 0};
+            const int qrow = ((b * p.H * p.G) + hq0) * p.T + q0;
+            mbar_expect_tx(BAR(kBarQ), ng * kTcTile);
+            for (int g = 0; g < ng; ++g)
+                for (int x = 0; x < 2; ++x)
+                    tma_load_2d(sbase + kOffQ + g * kTcTile + x * kTcBox, &tq, 64 * x, qrow + g * p.T, BAR(kBarQ));
+            const int krow = (b * p.H + h) * p.T;
+            for (int j = 0; j < nkt; ++j) {
+                const int s = j & 1;
+                const uint32_t par = (uint32_t)((j >> 1) - 1) & 1u;
+                if (j >= 2 && !mbar_wait(BAR(kBarKEmpty + s), par, abort_flag, p.status)) break;
+                mbar_expect_tx(BAR(kBarKFull + s), kTcTile);
+                for (int x = 0; x < 2; ++x)
+                    tma_load_2d(sbase + kOffK + s * kTcTile + x * kTcBox, &tk, 64 * x, krow + j * kTcKeys, BAR(kBarKFull + s));
+                if (j >= 2 && !mbar_wait(BAR(kBarVEmpty + s), par, abort_flag, p.status)) {
+                    used[s] = 2 * j + 1;  // K of tile j in flight, V not
+                    break;
+                }
+                mbar_expect_tx(BAR(kBarVFull + s), kTcTile);
+                for (int x = 0; x < 2; ++x)
+                    tma_load_2d(sbase + kOffV + s * kTcTile + x * kTcBox, &tv, 64 * x, krow + j * kTcKeys, BAR(kBarVFull + s));
+                used[s] = 2 * j + 2;
+            }
+            // every copy issued has landed before the CTA ends (normally at
+            // once: the MMA thread waited for them)
+            mbar_wait(BAR(kBarQ), 0, abort_flag, p.status, false);
+            for (int s = 0; s < 2; ++s) {
+                if (used[s] == 0) continue;
+                const int jl = (used[s] - 1) >> 1;  // last tile on this stage
+                const uint32_t par = (uint32_t)(jl >> 1) & 1u;
+                mbar_wait(BAR(kBarKFull + s), par, abort_flag, p.status, false);
+                if (used[s] & 1) {  // its V was not issued: the previous use's V
+                    if (jl >= 2) mbar_wait(BAR(kBarVFull + s), par ^ 1u, abort_flag, p.status, false);
+                } else {
+                    mbar_wait(BAR(kBarVFull + s), par, abort_flag, p.status, false);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 8) {
+        // ---- MMA issue
+        if (lane == 0) {
+            constexpr uint32_t idS = instr_desc(kTcRows, kTcKeys, 0);
+            constexpr uint32_t idO = instr_desc(kTcRows, kD, 1);
+            auto issue_s = [&](int g, int j) {
+                const uint32_t qa = sbase + kOffQ + g * kTcTile, ka = sbase + kOffK + (j & 1) * kTcTile;
+#pragma unroll
+                for (int k = 0; k < kD / 16; ++k) {
+                    const uint32_t off = (uint32_t)(k >> 2) * kTcBox + (uint32_t)(k & 3) * 32;
+                    mma_ss(tmem + 128u * g, smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), idS, k > 0);
+                }
+                mma_commit(BAR(kBarS + g));
+            };
+            auto issue_pv = [&](int g, int j) {
+                const uint32_t va = sbase + kOffV + (j & 1) * kTcTile;
+#pragma unroll
+                for (int k = 0; k < kTcKeys / 16; ++k)
+                    mma_ts(tmem + 256u + 128u * g, tmem + 128u * g + 8u * k, smem_desc(va + 2048u * k, kTcBox, 1024), idO,
+                           (j > 0 || k > 0) ? 1u : 0u);
+            };
+            bool ok = mbar_wait(BAR(kBarQ), 0, abort_flag, p.status) && mbar_wait(BAR(kBarKFull), 0, abort_flag, p.status);
+            if (ok) {
+                tc_fence_after();
+                for (int g = 0; g < ng; ++g) issue_s(g, 0);
+                mma_commit(BAR(kBarKEmpty));
+            }
+            for (int j = 0; ok && j < nkt; ++j) {
+                const int s = j & 1;
+                const bool next = j + 1 < nkt;
+                if (!mbar_wait(BAR(kBarVFull + s), (uint32_t)(j >> 1) & 1u, abort_flag, p.status)) break;
+                for (int g = 0; g < ng && ok; ++g) {
+                    ok = mbar_wait(BAR(kBarP + g), (uint32_t)j & 1u, abort_flag, p.status);
+                    if (ok && next && g == 0)
+                        ok = mbar_wait(BAR(kBarKFull + (s ^ 1)), (uint32_t)((j + 1) >> 1) & 1u, abort_flag, p.status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(g, j);
+                    if (next) {
+                        issue_s(g, j + 1);
+                    } else {
+                        mma_commit(BAR(kBarO + g));
+                    }
+                }
+                if (!ok) break;
+                mma_commit(BAR(kBarVEmpty + s));
+                if (next) mma_commit(BAR(kBarKEmpty + (s ^ 1)));
+            }
+            // every MMA issued has completed before the CTA ends
+            mma_commit(BAR(kBarDrain));
+            mbar_wait(BAR(kBarDrain), 0, abort_flag, p.status, false);
+        }
+        __syncwarp();
+    } else {
+        // ---- softmax warpgroups (and the record encoder)
+        const int g = warp >> 2;
+        if (pair == 0) {
+            stage_thresholds(s_thr, p.thr, tid, kEncWarps * 32);
+            asm volatile("bar.sync 1, %0;" ::"n"(kEncWarps * 32) : "memory");
+            encode_block(p, b, h, q0, min(kTcRows, p.T - q0), s_thr, s_rec[warp], s_vmask[warp], warp, lane, kEncWarps);
+        }
+        if (g < ng)
+            softmax_rows(p, tmem, g, b, hq0 + g, q0, nkt, BAR(kBarS + g), BAR(kBarP + g), BAR(kBarO + g), abort_flag, warp,
+                         lane);
+    }
+#undef BAR
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    }
+}
+
+// ---- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult qr = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+// Tensor map of a row-major [rows][128] fp16 matrix in this GPU's memory,
+// read in boxes of 128 rows x 64 columns with the 128-byte swizzle; rows past
+// the end read as zeros.
+bool rows_map(CUtensorMap* m, const void* base, uint64_t rows) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kTcRows};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -376,18 +652,29 @@ cudaError_t launch_prefill(const bgtq_plan& pl, cudaStream_t s, const void* q, c
                            int32_t* status) {
     static std::mutex mu;
     static bool done[64] = {false};
+    static const bool desc_ok = descriptors_valid();
+    if (!desc_ok) return cudaErrorInvalidValue;
+    // coordinates of the tensor maps and the grid are 32-bit
+    const uint64_t q_rows = (uint64_t)batch * pl.H * pl.G * (uint64_t)t;
+    const int nqb = (t + kTcRows - 1) / kTcRows;
+    const uint64_t units = (uint64_t)batch * pl.H * ((pl.G + 1) / 2);
+    if (q_rows + kTcRows >= (1ull << 31) || nqb > 65535 || units >= (1ull << 31)) return cudaErrorInvalidValue;
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!done[dev]) {
-            const cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       kPfSmem);
+            const cudaError_t e =
+                cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
             if (e != cudaSuccess) return e;
             done[dev] = true;
         }
     }
+    alignas(64) CUtensorMap tq, tk, tv;
+    if (!rows_map(&tq, q, q_rows) || !rows_map(&tk, k, (uint64_t)batch * pl.H * t) ||
+        !rows_map(&tv, v, (uint64_t)batch * pl.H * t))
+        return cudaErrorInvalidValue;
     PfParams p;
     p.q = static_cast<const __half*>(q);
     p.k = static_cast<const __half*>(k);
@@ -411,8 +698,8 @@ cudaError_t launch_prefill(const bgtq_plan& pl, cudaStream_t s, const void* q, c
     p.k_recent = static_cast<__half*>(c.k_recent);
     p.recent = c.recent;
     p.status = status;
-    dim3 grid((unsigned)((t + kPfRows - 1) / kPfRows), (unsigned)(pl.H * pl.G), (unsigned)batch);
-    prefill_kernel<<<grid, kPfWarps * 32, kPfSmem, s>>>(p);
+    const dim3 grid((unsigned)units, (unsigned)nqb, 1);
+    prefill_kernel<<<grid, kTcThreads, kTcSmem, s>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 

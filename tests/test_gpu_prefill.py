@@ -148,7 +148,7 @@ def test_prefill_long_prompt_sampled_rows():
     for i in sorted(set([0, 1, 63, 64, T - 1] + rng.integers(0, T, 12).tolist())):
         for h in range(H):
             want = O.attention(q[0][h * G:(h + 1) * G, i], li[0].k[h][:i + 1], li[0].v[h][:i + 1])
-            check_close(got[0][h * G:(h + 1) * G, i], want)
+            check_close(got[0][h * G:(h + 1) * G, i], want, fp16_out=True)
 
 
 def test_prefill_rejects_a_prompt_longer_than_the_cache():

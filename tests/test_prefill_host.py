@@ -33,11 +33,12 @@ def test_empty_prompt_is_a_no_op():
     (dict(t=200), -3, "capacity"),
     (dict(t=-1), -1, ">= 0"),
     (dict(q=BASE + 8), -1, "16-byte aligned"),
-    (dict(out=BASE + 4), -1, "8-byte aligned"),
+    (dict(out=BASE + 8), -1, "16-byte aligned"),
     (dict(out_dtype=2), -1, "out_dtype"),
     (dict(scale=0.0), -1, "softmax_scale"),
     (dict(scale=float("inf")), -1, "softmax_scale"),
     (dict(batch=70000), -2, "65535"),
+    (dict(batch=65535, t=5000, capacity=1 << 20), -2, "2^31"),
 ])
 def test_bad_arguments_are_rejected(kw, code, frag):
     rc, msg = call(**kw)
