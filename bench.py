@@ -565,7 +565,7 @@ def measure_prefill_attn(w, plan, tokens: int, peaks: dict, stream) -> dict:
     return {"tokens": tokens, "batch": B, "query_heads": Hq, "kv_heads": H, "ms_per_launch": ms,
             "tokens_per_s": B * tokens / (ms / 1000.0), "achieved": tf, "peak": peaks["bf16_tflops"],
             "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"], "bound": "tensor",
-            "flops": "4 * 128 per (query head, row, key <= row): causal Q K^T and P V; fp16 mma.sync, fp32 accumulate",
+            "flops": "4 * 128 per (query head, row, key <= row): causal Q K^T and P V; fp16 tcgen05 MMAs, fp32 accumulators in tensor memory",
             "peak_note": "measured dense bf16 (burst); fp16 has the same nominal tensor rate"}
 
 

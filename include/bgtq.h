@@ -68,6 +68,9 @@ extern "C" {
 #define BGTQ_STATUS_SEQLEN_CAPACITY 2 /* seq_len > capacity or < 0: clamped */
 #define BGTQ_STATUS_PAGE_RANGE 4      /* a page_table entry outside [0, n_pages) was met: writes to that
                                          page skipped, reads use page 0 (output unspecified) */
+#define BGTQ_STATUS_BOUNDS 16         /* library built with BGTQ_DEBUG_BOUNDS only: an index (record slot,
+                                         position against the capacity, page entry, table entry) failed
+                                         its range check; that access was skipped */
 #define BGTQ_STATUS_TIMEOUT 8         /* a wait inside a pipelined kernel gave up after 2 s: that launch
                                          skipped the rest of its work (output unspecified); never expected,
                                          reported instead of hanging the GPU */

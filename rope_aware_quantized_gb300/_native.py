@@ -60,8 +60,14 @@ EXPORTS = {
 }
 
 
+def debug_bounds() -> bool:
+    """BGTQ_DEBUG_BOUNDS=1 in the environment selects the range-checked build
+    of the library (for the whole process)."""
+    return os.environ.get("BGTQ_DEBUG_BOUNDS", "0") not in ("", "0")
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.LIB_DEBUG if debug_bounds() else _build.LIB
 
 
 def lib(build_if_missing: bool = True):
@@ -69,9 +75,9 @@ def lib(build_if_missing: bool = True):
     global _LIB
     if _LIB is not None:
         return _LIB
-    path = _build.LIB
+    path = library_path()
     if build_if_missing:
-        path = _build.build()
+        path = _build.build(debug_bounds=debug_bounds())
     if not os.path.exists(path):
         raise RuntimeError(f"libbgtq.so is not built ({path}); run rope_aware_quantized_gb300.build.build()")
     L = C.CDLL(path)

@@ -17,6 +17,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libbgtq.so")
+# the BGTQ_DEBUG_BOUNDS build: every record and table index range-checked
+# (a failure sets BGTQ_STATUS_BOUNDS and skips the access)
+LIB_DEBUG = os.path.join(BUILD, "debug_bounds", "libbgtq_debug_bounds.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 SOURCES = [
@@ -40,8 +43,8 @@ def nvcc() -> str:
     return exe
 
 
-def _compile(src: str, extra: list, verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD, src + ".o")
+def _compile(src: str, extra: list, verbose_ptxas: bool, outdir: str = BUILD) -> str:
+    obj = os.path.join(outdir, src + ".o")
     cmd = [nvcc(), "-c", os.path.join(CSRC, src), "-o", obj, "-std=c++17", "-O3", "-lineinfo",
            "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include"), "-I", CSRC] + ARCH + extra
     if verbose_ptxas and src.endswith(".cu"):
@@ -62,21 +65,25 @@ def sources_newer_than(path: str) -> bool:
     return any(os.path.getmtime(f) > t for f in files)
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile (if needed) and return the path of libbgtq.so."""
-    if not force and not sources_newer_than(LIB):
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, debug_bounds: bool = False) -> str:
+    """Compile (if needed) and return the path of libbgtq.so (or, with
+    debug_bounds, of the range-checked BGTQ_DEBUG_BOUNDS build)."""
+    lib = LIB_DEBUG if debug_bounds else LIB
+    if not force and not sources_newer_than(lib):
+        return lib
+    outdir = os.path.dirname(lib)
+    os.makedirs(outdir, exist_ok=True)
+    defs = ["-DBGTQ_DEBUG_BOUNDS"] if debug_bounds else []
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s[0], s[1], verbose_ptxas), SOURCES))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s[0], s[1] + defs, verbose_ptxas, outdir), SOURCES))
+    tmp = lib + ".tmp"
     cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH + ["-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv, debug_bounds="--debug-bounds" in sys.argv))

@@ -87,18 +87,44 @@ struct DevTables {
 // of a paged one (page = page_table[b][pos / P]).  K record, norms: index
 // slot; V pair record of the pair holding pos: index slot / 2 (P and the
 // capacity are even, so a pair never straddles two pages).
+#ifdef __CUDACC__
+// Range checks of the BGTQ_DEBUG_BOUNDS build: a failed check ORs
+// BGTQ_STATUS_BOUNDS into the launch's status word and its caller skips the
+// access (no trap).  In the default build every check is `true` and the
+// condition compiles away.
+__device__ __forceinline__ bool debug_in_range(bool ok, int32_t* status) {
+#ifdef BGTQ_DEBUG_BOUNDS
+    if (!ok && status) atomicOr(status, BGTQ_STATUS_BOUNDS);
+    return ok;
+#else
+    (void)ok;
+    (void)status;
+    return true;
+#endif
+}
+#endif
+
 struct CacheMap {
     const int32_t* page_table;  // [B][max_pages], nullptr: contiguous
     int64_t cap;                // positions per sequence (capacity = max_pages * P when paged)
     int64_t max_pages, n_pages;
     int H, lp;                  // lp = log2 P (paged)
+    int batch;                  // sequences of the launch
+    int64_t n_slots;            // record slots: batch H cap, or n_pages H P when paged
+    int32_t* status;            // where a failed range check is reported
 #ifdef __CUDACC__
-    // -1 when the page_table entry is outside [0, n_pages)
+    // -1 when the page_table entry is outside [0, n_pages) (and, in the
+    // BGTQ_DEBUG_BOUNDS build, when b, h, pos or the slot is out of range)
     __device__ __forceinline__ int64_t slot(int b, int h, int64_t pos) const {
+        if (!debug_in_range(b >= 0 && b < batch && h >= 0 && h < H && pos >= 0 && pos < cap, status)) return -1;
         if (!page_table) return ((int64_t)b * H + h) * cap + pos;
         const int32_t pg = page_table[(int64_t)b * max_pages + (pos >> lp)];
-        if (pg < 0 || (int64_t)pg >= n_pages) return -1;
-        return (((int64_t)pg * H + h) << lp) + (pos & ((((int64_t)1) << lp) - 1));
+        if (pg < 0 || (int64_t)pg >= n_pages) {
+            debug_in_range(false, status);
+            return -1;
+        }
+        const int64_t sl = (((int64_t)pg * H + h) << lp) + (pos & ((((int64_t)1) << lp) - 1));
+        return debug_in_range(sl < n_slots, status) ? sl : -1;
     }
 #endif
 };
@@ -111,7 +137,7 @@ cudaError_t launch_prefill(const bgtq_plan& pl, cudaStream_t s, const void* q, c
 // recent-key buffer, paging); sets the thread's error message.
 int check_cache(const bgtq_plan* p, const bgtq_cache* c);
 
-inline CacheMap make_cache_map(const bgtq_cache& c, int H) {
+inline CacheMap make_cache_map(const bgtq_cache& c, int H, int batch, int32_t* status) {
     CacheMap m;
     m.page_table = c.page_table;
     m.cap = c.capacity;
@@ -121,6 +147,9 @@ inline CacheMap make_cache_map(const bgtq_cache& c, int H) {
     m.lp = 0;
     if (c.page_table)
         while (((int64_t)1 << m.lp) < c.page_tokens) ++m.lp;
+    m.batch = batch;
+    m.n_slots = c.page_table ? (int64_t)c.n_pages * H * c.page_tokens : (int64_t)batch * H * c.capacity;
+    m.status = status;
     return m;
 }
 

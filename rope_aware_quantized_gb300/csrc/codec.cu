@@ -49,7 +49,10 @@ __global__ void __launch_bounds__(128) quantize_append_kernel(QParams p) {
     const int ps = p.pos_start[b];
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (ps < 0 || (int64_t)ps + p.t_new > p.cap) {
-        if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_APPEND_CAPACITY);
+        if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0 && p.status) {
+            atomicOr(p.status, BGTQ_STATUS_APPEND_CAPACITY);
+            debug_in_range(false, p.status);  // positions past the capacity
+        }
         return;
     }
     const int64_t end = (int64_t)ps + p.t_new;
@@ -230,7 +233,7 @@ __global__ void __launch_bounds__(128) dequant_kernel(DqParams p) {
                 if (wi + 1 >= 4 * p.bk) win &= 0xffffffffull;
                 const uint32_t field = (uint32_t)(win >> sh) & ((1u << (2 * w)) - 1);
                 const uint32_t c = (j & 1) ? (field >> w) : (field & ((1u << w) - 1));
-                y[i] = __fmul_rn(rho, p.cent[256 * w + c]);
+                y[i] = debug_in_range(w <= kWMax && c < (1u << w), nullptr) ? __fmul_rn(rho, p.cent[256 * w + c]) : 0.0f;
                 pl[i] = ht->plog2[j];
             }
         }
@@ -272,7 +275,7 @@ __global__ void __launch_bounds__(128) dequant_kernel(DqParams p) {
             uint64_t win = rec[warp][wi];
             if (wi + 1 < 8 * p.bv) win |= (uint64_t)rec[warp][wi + 1] << 32;
             const uint32_t c = (uint32_t)(win >> sh) & ((1u << p.bv) - 1);
-            y[i] = __fmul_rn(rho, p.cent[256 * p.bv + c]);
+            y[i] = debug_in_range(p.bv <= kWMax && c < (1u << p.bv), nullptr) ? __fmul_rn(rho, p.cent[256 * p.bv + c]) : 0.0f;
             pl[i] = 7;
         }
         float* out = p.v_out + row * kD;
@@ -307,7 +310,7 @@ cudaError_t launch_quantize_append(const bgtq_plan& pl, cudaStream_t s, const vo
     p.vc = static_cast<uint8_t*>(c.v_codes);
     p.vn = c.v_norm;
     p.cap = c.capacity;
-    p.map = make_cache_map(c, pl.H);
+    p.map = make_cache_map(c, pl.H, batch, status);
     p.heads = pl.dev.heads;
     p.thr = pl.dev.thr;
     p.bk = pl.bk;
@@ -347,7 +350,7 @@ cudaError_t launch_dequant(const bgtq_plan& pl, cudaStream_t s, const bgtq_cache
     p.cap = c.capacity;
     p.t0 = t0;
     p.t1 = t1;
-    p.map = make_cache_map(c, pl.H);
+    p.map = make_cache_map(c, pl.H, batch, nullptr);
     p.b = b;
     p.h = head;
     p.ht = pl.dev.heads + head;

@@ -198,7 +198,10 @@ __global__ void __launch_bounds__(kBulkTok) quantize_append_bulk_kernel(QParams 
     const int ps = p.pos_start[b];
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (ps < 0 || (int64_t)ps + p.t_new > p.cap) {
-        if (blockIdx.x == 0 && h == 0 && tid == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_APPEND_CAPACITY);
+        if (blockIdx.x == 0 && h == 0 && tid == 0 && p.status) {
+            atomicOr(p.status, BGTQ_STATUS_APPEND_CAPACITY);
+            debug_in_range(false, p.status);  // positions past the capacity
+        }
         return;
     }
     const int64_t end = (int64_t)ps + p.t_new;

@@ -150,7 +150,7 @@ cudaError_t launch_decode(const bgtq_plan& pl, cudaStream_t s, const void* q, co
     p.vc = static_cast<uint8_t*>(c.v_codes);
     p.vn = c.v_norm;
     p.cap = c.capacity;
-    p.map = make_cache_map(c, pl.H);
+    p.map = make_cache_map(c, pl.H, batch, status);
     p.seq_lens = seq_lens;
     p.out = out;
     p.out_dtype = out_dtype;

@@ -478,7 +478,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     int seq = p.seq_lens[b];
     if (seq < 0 || (int64_t)seq > p.cap) {
         pdl_wait();
-        if (tid == 0 && split == 0 && h == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_SEQLEN_CAPACITY);
+        if (tid == 0 && split == 0 && h == 0 && p.status) {
+            atomicOr(p.status, BGTQ_STATUS_SEQLEN_CAPACITY);
+            debug_in_range(false, p.status);  // records past the capacity
+        }
         seq = seq < 0 ? 0 : (int)p.cap;
     }
     // Token ranges, newest first: split 0 attends [a0, seq) with a0 the
@@ -509,7 +512,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     }
     if (seq == 0) {
         pdl_wait();
-        if (pos_bad && split == 0 && h == 0 && tid == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_APPEND_CAPACITY);
+        if (pos_bad && split == 0 && h == 0 && tid == 0 && p.status) {
+            atomicOr(p.status, BGTQ_STATUS_APPEND_CAPACITY);
+            debug_in_range(false, p.status);  // a new position past the capacity
+        }
         if (owner) {
             const int64_t sl = new_token_slot(p, b, h, pos);
             if (sl >= 0) append_new_token<BK, BV>(p, el, unit, sl, pos, s_thr, s_enc, warp, lane);
@@ -612,7 +618,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             q_sc[i] = coded ? ht->inv_sqrt[j] * p.scale_log2 : 0.0f;
         }
         uint32_t* src = reinterpret_cast<uint32_t*>(s_stage);
-        const int nw = p.img_lane + p.img_shared;
+        const int nw = debug_in_range(p.img_lane + p.img_shared <= kImageMaxWords, tid == 0 ? p.status : nullptr)
+                           ? p.img_lane + p.img_shared : 0;
         constexpr int kPerThread = (kImageMaxWords + kWarps * 32 - 1) / (kWarps * 32);
         uint32_t v[kPerThread];
 #pragma unroll
@@ -651,7 +658,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     }
 
     pdl_wait();  // q, the cache and the workspace may belong to the previous kernel
-    if (pos_bad && split == 0 && h == 0 && tid == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_APPEND_CAPACITY);
+    if (pos_bad && split == 0 && h == 0 && tid == 0 && p.status) {
+        atomicOr(p.status, BGTQ_STATUS_APPEND_CAPACITY);
+        debug_in_range(false, p.status);  // a new position past the capacity
+    }
     if (owner) {
         int64_t sl;
         if constexpr (kPaged) {

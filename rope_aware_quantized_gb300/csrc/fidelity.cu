@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kMaeWarps * 32) logit_mae_kernel(MaeParams p) 
                 uint64_t win = s_rec[warp][wi];
                 if (wi + 1 < rec_words) win |= (uint64_t)s_rec[warp][wi + 1] << 32;
                 const uint32_t code = (uint32_t)(win >> sh) & ((1u << w) - 1u);
-                y[i] = rho * p.cent[256 * w + code];
+                y[i] = debug_in_range(w <= kWMax && code < (1u << w), nullptr) ? rho * p.cent[256 * w + code] : 0.0f;
             }
         }
         const float kx[4] = {__half2float(__ushort_as_half((unsigned short)(kr.x & 0xffffu))),
@@ -168,7 +168,7 @@ cudaError_t launch_logit_mae(const bgtq_plan& pl, cudaStream_t s, const void* q,
     p.kc = static_cast<const uint8_t*>(c.k_codes);
     p.kn = c.k_norm;
     p.cap = c.capacity;
-    p.map = make_cache_map(c, pl.H);
+    p.map = make_cache_map(c, pl.H, batch, nullptr);
     p.t = t;
     p.H = pl.H;
     p.G = pl.G;
