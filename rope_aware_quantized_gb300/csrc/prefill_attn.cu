@@ -689,7 +689,7 @@ cudaError_t launch_prefill(const bgtq_plan& pl, cudaStream_t s, const void* q, c
     p.kn = c.k_norm;
     p.vc = static_cast<uint8_t*>(c.v_codes);
     p.vn = c.v_norm;
-    p.map = make_cache_map(c, pl.H);
+    p.map = make_cache_map(c, pl.H, batch, status);
     p.heads = pl.dev.heads;
     p.thr = pl.dev.thr;
     p.bk = pl.bk;
