@@ -686,3 +686,42 @@ def prefill_attention(q_fp16, k_fp16, v_fp16, scale: float = 1.0 / math.sqrt(D),
         p = np.exp(s)
         out[:, r0:r1] = np.einsum("gij,jd->gid", p, v[:r1]) / p.sum(axis=2, keepdims=True)
     return out
+
+
+# =============================================================================
+# Chunked prefill onto a non-empty cache (the same next step, a later chunk of
+# a long prompt).  Reading R22: a chunk of C tokens at positions P0 .. P0+C-1
+# of a sequence whose cache already holds P0 packed tokens writes the packed
+# records of its own positions (encoder unchanged: an append at pos_start =
+# P0) and returns, for query row i, one softmax over the P0 cached keys as
+# stored (dequantised, reading R13) and the chunk's keys 0 .. i as given
+# (fp16), values likewise: the prefix is what the cache holds, the chunk is
+# the prompt as given, exactly as a prefill into an empty cache (R21) treats
+# its own tokens.  P0 = 0 is R21.
+# =============================================================================
+
+
+def chunk_prefill_attention(q_fp16, khat_prefix, vhat_prefix, k_fp16, v_fp16, scale: float = 1.0 / math.sqrt(D),
+                            rows: int = 256):
+    """q [G][C][128] (fp16), khat_prefix, vhat_prefix [P0][128] (the cache's
+    dequantised prefix), k, v [C][128] (fp16, the chunk) -> [G][C][128]
+    float64: out[g][i] = sum over keys j of softmax_j(scale q[g][i] . key_j)
+    value_j, keys = the P0 prefix rows then the chunk rows 0 .. i."""
+    q = np.asarray(q_fp16, dtype=np.float16).astype(np.float64)
+    kp = np.asarray(khat_prefix, dtype=np.float64).reshape(-1, D)
+    vp = np.asarray(vhat_prefix, dtype=np.float64).reshape(-1, D)
+    keys = np.concatenate([kp, np.asarray(k_fp16, dtype=np.float16).astype(np.float64)])
+    vals = np.concatenate([vp, np.asarray(v_fp16, dtype=np.float16).astype(np.float64)])
+    p0 = kp.shape[0]
+    G, C = q.shape[0], q.shape[1]
+    out = np.zeros((G, C, D))
+    for r0 in range(0, C, rows):
+        r1 = min(C, r0 + rows)
+        n = p0 + r1  # keys any of these rows can see
+        s = np.einsum("gid,jd->gij", q[:, r0:r1], keys[:n]) * scale
+        visible = np.arange(n)[None, :] <= p0 + np.arange(r0, r1)[:, None]
+        s = np.where(visible[None], s, -np.inf)
+        s = s - s.max(axis=2, keepdims=True)
+        p = np.exp(s)
+        out[:, r0:r1] = np.einsum("gij,jd->gid", p, vals[:n]) / p.sum(axis=2, keepdims=True)
+    return out
