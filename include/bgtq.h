@@ -328,6 +328,39 @@ int bgtq_prefill_attn(const bgtq_plan* plan, void* stream, const void* q_fp16, c
                       float softmax_scale, int32_t* dev_status);
 
 /*
+ * bgtq_prefill_chunk_attn — a later chunk of a long prompt onto a cache that
+ * already holds positions 0 .. P0-1 of each sequence: the packed records of
+ * positions P0 .. P0+c-1 are written (bgtq_quantize_append at pos_start = P0,
+ * bit for bit) and chunk row i attends, in one softmax, the P0 cached keys as
+ * stored (dequantised) and the chunk's keys 0 .. i as given, values likewise.
+ * Source: the packed cache is what earlier chunks left (review §1
+ * "Packed-Cache"); a quantizer fused into attention is future work on the
+ * LogQuant page (section "중요성 및 주장").
+ *   q_fp16       device, [batch][H*G][c][128] half, RoPE applied, 16-byte aligned
+ *   k_fp16, v_fp16  device, [batch][H][c][128] half (the chunk), 16-byte aligned
+ *   c            chunk length, 0 <= c <= capacity
+ *   dev_pos_start  device int32 [batch]: P0 of each sequence; a sequence with
+ *                P0 < 0 or P0 + c > capacity is skipped (nothing written to
+ *                the cache, zero output rows, BGTQ_STATUS_APPEND_CAPACITY)
+ *   cache        host pointer to the layer's descriptor, contiguous or paged,
+ *                without a recent-key buffer
+ *   out          device, [batch][H*G][c][128], half (out_dtype 0) or float
+ *                (1), 16-byte aligned
+ *   softmax_scale  logit scale, e.g. 1/sqrt(128)
+ *   dev_status   device int32 or NULL
+ * Two launches on `stream`: the append, then the attention.  The chunk part
+ * is computed as in bgtq_prefill_attn; the prefix part in the codecs' own
+ * domains (rotated query, raw centroids, norms in fp32) with fp16 hi + lo
+ * splits of the query and of the probabilities, fp32 accumulation.
+ * Errors: INVALID_ARG (pointers, alignment, dtype, scale), CAPACITY (c >
+ * capacity), UNSUPPORTED (a recent-key buffer, bK > 3, bV > 4), CUDA.
+ */
+int bgtq_prefill_chunk_attn(const bgtq_plan* plan, void* stream, const void* q_fp16, const void* k_fp16,
+                            const void* v_fp16, int batch, int c, const int32_t* dev_pos_start,
+                            const bgtq_cache* cache, void* out, int out_dtype, float softmax_scale,
+                            int32_t* dev_status);
+
+/*
  * bgtq_decode_attn_noalloc — bgtq_decode_attn for callers that cannot
  * allocate device memory (a fixed memory budget, an allocator or pool that
  * must not be bypassed, a host runtime without a device allocator).  The

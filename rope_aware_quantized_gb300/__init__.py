@@ -336,6 +336,35 @@ def bgtq_prefill_attn(plan: Plan, q_fp16, k_fp16, v_fp16, cache: Cache, out, sof
                                    C.byref(cache.desc), _ptr(out), out_dtype, scale, _ptr(status)))
 
 
+def bgtq_prefill_chunk_attn(plan: Plan, q_fp16, k_fp16, v_fp16, pos_start, cache: Cache, out,
+                            softmax_scale: float | None = None, status=None, stream=None):
+    """A later chunk of a prompt onto a cache holding pos_start[b] tokens of sequence b: the
+    chunk's packed records into `cache` (an append at pos_start) and attention of every chunk
+    row over the cached prefix (as stored) and the chunk's own K/V so far into `out`.
+    q: [B][H*G][C][128] float16; k, v: [B][H][C][128] float16; pos_start: [B] int32 CUDA
+    tensor; out: like q, float16 or float32."""
+    import torch
+    b, hq, t, d = q_fp16.shape
+    if d != HEAD_DIM or tuple(k_fp16.shape) != (b, plan.n_kv_heads, t, d) or tuple(v_fp16.shape) != tuple(k_fp16.shape):
+        raise ValueError("q must be [B][H*G][C][128], k and v [B][H][C][128]")
+    if tuple(out.shape) != tuple(q_fp16.shape):
+        raise ValueError("out must have the shape of q")
+    if tuple(pos_start.shape) != (b,) or pos_start.dtype != torch.int32:
+        raise ValueError("pos_start must be an int32 tensor of shape [B]")
+    if not all(x.is_contiguous() for x in (q_fp16, k_fp16, v_fp16, out)):
+        raise ValueError("q, k, v and out must be contiguous")
+    if out.dtype == torch.float32:
+        out_dtype = 1
+    elif out.dtype == torch.float16:
+        out_dtype = 0
+    else:
+        raise ValueError("out must be float16 or float32")
+    scale = (1.0 / HEAD_DIM ** 0.5) if softmax_scale is None else softmax_scale
+    _check(lib().bgtq_prefill_chunk_attn(plan.handle, _stream(stream), _ptr(q_fp16), _ptr(k_fp16), _ptr(v_fp16), b,
+                                         t, _ptr(pos_start), C.byref(cache.desc), _ptr(out), out_dtype, scale,
+                                         _ptr(status)))
+
+
 def bgtq_dequant_debug(plan: Plan, cache: Cache, b: int, head: int, t0: int, t1: int, k_out=None, v_out=None,
                        codec_domain: bool = False, stream=None):
     _check(lib().bgtq_dequant_debug(plan.handle, _stream(stream), C.byref(cache.desc), cache.batch, b, head, t0, t1,
@@ -345,6 +374,6 @@ def bgtq_dequant_debug(plan: Plan, cache: Cache, b: int, head: int, t0: int, t1:
 __all__ = [
     "BgtqError", "Plan", "Cache", "CacheView", "bgtq_alloc_bits", "bgtq_plan_create", "bgtq_cache_bytes",
     "bgtq_quantize_append", "bgtq_decode_attn_workspace", "bgtq_decode_attn", "bgtq_decode_step",
-    "bgtq_decode_attn_noalloc", "bgtq_logit_mae",
-    "bgtq_dequant_debug",
+    "bgtq_decode_attn_noalloc", "bgtq_logit_mae", "bgtq_prefill_attn", "bgtq_prefill_chunk_attn",
+    "bgtq_plan_save", "bgtq_plan_load", "bgtq_dequant_debug",
 ]

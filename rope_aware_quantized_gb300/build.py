@@ -33,6 +33,7 @@ SOURCES = [
     ("decode_attn_noalloc.cu", []),
     ("fidelity.cu", []),
     ("prefill_attn.cu", []),
+    ("prefill_chunk.cu", []),
 ]
 
 

@@ -837,6 +837,34 @@ int bgtq_prefill_attn(const bgtq_plan* p, void* stream, const void* q, const voi
     return BGTQ_OK;
 }
 
+int bgtq_prefill_chunk_attn(const bgtq_plan* p, void* stream, const void* q, const void* k, const void* v, int batch,
+                            int t, const int32_t* pos_start, const bgtq_cache* c, void* out, int out_dtype, float scale,
+                            int32_t* status) {
+    if (!p) return set_error(BGTQ_ERR_INVALID_ARG, "plan is NULL");
+    int rc = check_cache(p, c);
+    if (rc) return rc;
+    if (batch < 0 || t < 0) return set_error(BGTQ_ERR_INVALID_ARG, "batch and c must be >= 0");
+    if (t > c->capacity) return set_error(BGTQ_ERR_CAPACITY, "c = %d exceeds the cache capacity", t);
+    if (batch == 0 || t == 0) return BGTQ_OK;
+    if (!q || !k || !v || !out || !pos_start) return set_error(BGTQ_ERR_INVALID_ARG, "NULL pointer");
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15)
+        return set_error(BGTQ_ERR_INVALID_ARG, "q, k and v must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(out) & 15) return set_error(BGTQ_ERR_INVALID_ARG, "out must be 16-byte aligned");
+    if (out_dtype != 0 && out_dtype != 1) return set_error(BGTQ_ERR_INVALID_ARG, "out_dtype must be 0 (half) or 1 (float)");
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return set_error(BGTQ_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
+    if (c->recent > 0)
+        return set_error(BGTQ_ERR_UNSUPPORTED, "chunked prefill onto a cache with a recent-key buffer is not supported");
+    if ((uint64_t)batch * p->H * p->G * (uint64_t)t + 128 >= (1ull << 31))
+        return set_error(BGTQ_ERR_UNSUPPORTED, "batch * query heads * c must stay below 2^31 - 128");
+    if ((rc = check_plan(p))) return rc;
+    if (p->bk > 3 || p->bv > 4) return set_error(BGTQ_ERR_UNSUPPORTED, "chunked prefill supports bK <= 3 and v_bits <= 4");
+    cudaError_t e = launch_quantize_append(*p, (cudaStream_t)stream, k, v, batch, t, pos_start, *c, status);
+    if (e != cudaSuccess) return set_error(BGTQ_ERR_CUDA, "chunk append launch: %s", cudaGetErrorString(e));
+    e = launch_prefill_chunk(*p, (cudaStream_t)stream, q, k, v, batch, t, pos_start, *c, out, out_dtype, scale, status);
+    if (e != cudaSuccess) return set_error(BGTQ_ERR_CUDA, "chunk attention launch: %s", cudaGetErrorString(e));
+    return BGTQ_OK;
+}
+
 int bgtq_logit_mae(const bgtq_plan* p, void* stream, const void* q, const void* k, const bgtq_cache* c, int64_t t,
                    int batch, float scale, float* mae) {
     int rc = check_plan(p);

@@ -132,6 +132,9 @@ struct CacheMap {
 cudaError_t launch_prefill(const bgtq_plan& pl, cudaStream_t s, const void* q, const void* k, const void* v,
                            int batch, int t, const bgtq_cache& c, void* out, int out_dtype, float scale,
                            int32_t* status);
+cudaError_t launch_prefill_chunk(const bgtq_plan& pl, cudaStream_t s, const void* q, const void* k, const void* v,
+                                 int batch, int c, const int32_t* pos_start, const bgtq_cache& cache, void* out,
+                                 int out_dtype, float scale, int32_t* status);
 
 // Host checks of a cache descriptor (buffers, alignment, capacity, the
 // recent-key buffer, paging); sets the thread's error message.

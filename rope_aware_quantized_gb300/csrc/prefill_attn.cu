@@ -40,7 +40,8 @@
 #include <cmath>
 #include <mutex>
 
-#include "encode.cuh"
+#include "prefill_common.cuh"
+#include "tc_common.cuh"
 
 namespace bgtq {
 namespace {
@@ -57,7 +58,6 @@ constexpr uint32_t kOffV = 4 * kTcTile;           // V stage s at + s kTcTile
 constexpr uint32_t kTcSmem = 6 * kTcTile + 1024;  // + room to align the base to 1 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr float kHeadroom = 8.0f;
-constexpr unsigned long long kWaitNs = 2000000000ull;
 
 // mbarriers: tile copies landed (Q, K/V per stage), stages free again,
 // S_g computed, P_g written, O_g final, every MMA done
@@ -74,282 +74,23 @@ enum {
     kNumBars = 16
 };
 
-struct PfParams {
-    const __half* q;  // [B][H*G][T][128]
-    const __half* k;  // [B][H][T][128]
-    const __half* v;
-    void* out;        // [B][H*G][T][128], fp16 or fp32
-    int out_dtype;
-    int T, H, G;
-    float scale_log2;
-    // the packed records of the prompt
-    uint8_t* kc;
-    float* kn;
-    uint8_t* vc;
-    float* vn;
-    CacheMap map;
-    const HeadTab* heads;
-    const float* thr;
-    int bk, bv;
-    float v_inv_sqrt;
-    __half* k_recent;
-    int64_t recent;
-    int32_t* status;
-};
 
-// ---- descriptors (PTX ISA, tcgen05 "Matrix Descriptors" and "Instruction
-// descriptor" tables)
-
-// Shared-memory matrix descriptor: start address, leading and stride byte
-// offsets (each >> 4 in 14 bits at bits 0, 16 and 32), the fixed 0b001 at
-// bits 46-48, base offset 0 (bits 49-51; every pattern starts 1 KB aligned)
-// and the 128-byte swizzle (2) in bits 61-63.
-__host__ __device__ constexpr uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-// Instruction descriptor of kind::f16: dense, fp32 D (bits 4-5 = 1), fp16 A
-// and B (bits 7-9, 10-12 = 0), no negation, A K-major (bit 15 = 0), B K-major
-// (0) or MN-major (1) in bit 16, N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t instr_desc(int m, int n, int b_mn_major) {
-    return (1u << 4) | ((uint32_t)b_mn_major << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
-}
-
-// The descriptors the kernel builds, decoded field by field against the
-// layout above for the extreme addresses it can use (a 1 KB-aligned base
-// anywhere in the 227 KB a CTA can address).
+// The descriptors the kernel builds, checked field by field for the extreme
+// addresses it can use (a 1 KB-aligned base anywhere in the 227 KB a CTA can
+// address).
 bool descriptors_valid() {
-    const uint32_t idS = instr_desc(kTcRows, kTcKeys, 0), idO = instr_desc(kTcRows, kD, 1);
-    for (uint32_t id : {idS, idO}) {
-        const uint32_t n = ((id >> 17) & 0x3Fu) << 3, m = ((id >> 24) & 0x1Fu) << 4;
-        if (m != 128 || n % 16 != 0 || n < 16 || n > 256) return false;       // M = 128: N in 16..256, step 16
-        if (((id >> 4) & 3u) != 1u || ((id >> 7) & 0x3Fu) != 0u) return false;  // fp32 D; fp16 A and B
-        if (((id >> 13) & 7u) != 0u || (id & 0xFu) != 0u) return false;        // no negation, A K-major, dense
-    }
-    if (((idS >> 16) & 1u) != 0u || ((idO >> 16) & 1u) != 1u) return false;
+    if (!instr_desc_ok(instr_desc(kTcRows, kTcKeys, 0), 0) || !instr_desc_ok(instr_desc(kTcRows, kD, 1), 1)) return false;
     constexpr uint32_t kMaxSmem = 227u * 1024u;
-    for (uint32_t base = 0; base + kTcSmem <= kMaxSmem + 1024; base += 1024) {
-        // S operands (K-major: LBO unused, SBO = 8 rows of 128 B), steps of 16 in K
+    for (uint32_t base = 0; base + kTcSmem <= kMaxSmem + 1024; base += 1024)
         for (int k = 0; k < kD / 16; ++k) {
+            // S operands (K-major: LBO unused, SBO = 8 rows of 128 B), steps of 16 in K
             const uint32_t off = (uint32_t)(k >> 2) * kTcBox + (uint32_t)(k & 3) * 32;
-            for (uint32_t a : {base + kOffQ + kTcTile + off, base + kOffK + kTcTile + off}) {
-                const uint64_t d = smem_desc(a, 16, 1024);
-                if (((d & 0x3FFFu) << 4) != a || (((d >> 32) & 0x3FFFu) << 4) != 1024u) return false;
-                if (((d >> 46) & 7u) != 1u || ((d >> 49) & 7u) != 0u || (d >> 61) != 2u) return false;
-            }
+            if (!smem_desc_ok(base + kOffQ + kTcTile + off, 16, 1024) || !smem_desc_ok(base + kOffK + kTcTile + off, 16, 1024))
+                return false;
             // V (MN-major: LBO = the 64-column box stride, SBO = 8 keys of 128 B), steps of 16 keys
-            const uint32_t av = base + kOffV + kTcTile + (uint32_t)k * 2048;
-            const uint64_t d = smem_desc(av, kTcBox, 1024);
-            if (((d & 0x3FFFu) << 4) != av || (((d >> 16) & 0x3FFFu) << 4) != kTcBox) return false;
-            if ((((d >> 32) & 0x3FFFu) << 4) != 1024u || (d >> 61) != 2u) return false;
+            if (!smem_desc_ok(base + kOffV + kTcTile + (uint32_t)k * 2048, kTcBox, 1024)) return false;
         }
-    }
     return true;
-}
-
-// ---- device helpers
-
-__device__ __forceinline__ uint32_t smem_u32(const void* ptr) { return (uint32_t)__cvta_generic_to_shared(ptr); }
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Wait for the phase of parity `parity` of an mbarrier, for kWaitNs at most
-// and not at all once another thread of the CTA gave up (`check_abort`).
-// Giving up sets the status bit and the CTA's abort flag.
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* status,
-                          bool check_abort = true) {
-    if (mbar_try(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (;;) {
-        if (mbar_try(bar, parity)) return true;
-        if (check_abort && *abort_flag) return false;
-        if (global_ns() - t0 > kWaitNs) {
-            *abort_flag = 1;
-            if (status) atomicOr(status, BGTQ_STATUS_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            dst),
-        "l"(map), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
-}
-// A operand from tensor memory
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(
-            d),
-        "r"(a), "l"(b), "r"(idesc), "r"(accumulate));
-}
-// the mbarrier arrives once every MMA this thread issued so far has completed
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// 32 consecutive fp32 columns of the warp's 32 lanes
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
-    uint32_t* r = reinterpret_cast<uint32_t*>(v);
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
-        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
-        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
-    const __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// Encode the keys and values of positions [p0, p0 + n) of (b, h): warp w
-// takes the token pairs w, w + n_warps, ...; the steps are the append
-// kernel's.
-__device__ void encode_block(const PfParams& p, int b, int h, int p0, int n, const float* s_thr,
-                             uint32_t (*s_rec)[8 * kPairMaxW], uint32_t* s_vmask, int warp, int lane, int n_warps) {
-    const HeadTab* ht = p.heads + h;
-    EncLane ek, ev;
-    enc_lane_load(ek, ht, true, p.bv, p.v_inv_sqrt, lane);
-    enc_lane_load(ev, ht, false, p.bv, p.v_inv_sqrt, lane);
-    const size_t row0 = ((size_t)b * p.H + h) * p.T;
-    const size_t unit = (size_t)b * p.H + h;
-    for (int pi = warp; 2 * pi < n; pi += n_warps) {
-        const int pos0 = p0 + 2 * pi;
-        const bool has[2] = {true, 2 * pi + 1 < n};
-        // ---- keys of the pair
-        float x[2][4];
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            const __half* row = p.k + (row0 + pos0 + m) * kD;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) x[m][k] = has[m] ? __fmul_rn(__half2float(row[ek.src[k]]), ek.wh[k]) : 0.0f;
-        }
-        for (int k = lane; k < 2 * 8 * kPairMaxW; k += 32) (&s_rec[0][0])[k] = 0;
-        __syncwarp();
-        int code[2][4];
-        float rho[2];
-        warp_encode_n<2>(x, ek.sg, ek.pl, ek.is, ek.wd, ek.n_coded, s_thr, code, rho);
-#pragma unroll
-        for (int m = 0; m < 2; ++m) pack_k_fields(s_rec[m], code[m], ek, lane);
-        __syncwarp();
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            if (!has[m]) continue;
-            const int pos = pos0 + m;
-            const int64_t sl = p.map.slot(b, h, pos);
-            if (sl < 0) {
-                if (lane == 0 && p.status) atomicOr(p.status, BGTQ_STATUS_PAGE_RANGE);
-                continue;
-            }
-            uint32_t* dst = reinterpret_cast<uint32_t*>(p.kc + sl * (16 * p.bk));
-            if (lane < 4 * p.bk) dst[lane] = s_rec[m][lane];
-            if (lane == 0) p.kn[sl] = rho[m];
-            if (p.recent > 0 && pos >= p.T - p.recent) {
-                // fp16 recent-key ring: the key as given, slot pos mod W
-                const uint2 nat = *(reinterpret_cast<const uint2*>(p.k + (row0 + pos) * kD) + lane);
-                *(reinterpret_cast<uint2*>(p.k_recent + (unit * p.recent + pos % p.recent) * kD) + lane) = nat;
-            }
-        }
-        __syncwarp();
-        // ---- values of the pair: one V record
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            uint2 raw = make_uint2(0u, 0u);
-            if (has[m]) raw = *(reinterpret_cast<const uint2*>(p.v + (row0 + pos0 + m) * kD) + lane);
-            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-            const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-            x[m][0] = a.x;
-            x[m][1] = a.y;
-            x[m][2] = c.x;
-            x[m][3] = c.y;
-        }
-        for (int k = lane; k < 8 * kPairMaxW; k += 32) {
-            s_rec[2][k] = 0;
-            s_vmask[k] = 0;
-        }
-        __syncwarp();
-        warp_encode_n<2>(x, ev.sg, ev.pl, ev.is, ev.wd, kD, s_thr, code, rho);
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-            if (has[m]) pack_v_fields(s_rec[2], s_vmask, code[m], m, p.bv, lane);
-        __syncwarp();
-        const int64_t sl0 = p.map.slot(b, h, pos0);
-        if (sl0 >= 0) {
-            if (lane == 0) {
-                p.vn[sl0] = rho[0];
-                if (has[1]) p.vn[sl0 + 1] = rho[1];
-            }
-            uint32_t* vdst = reinterpret_cast<uint32_t*>(p.vc + (sl0 >> 1) * (32 * p.bv));
-            for (int k = lane; k < 8 * p.bv; k += 32) {
-                if (has[1]) {
-                    vdst[k] = s_rec[2][k];
-                } else {
-                    // a prompt of odd length ends half-way through a pair:
-                    // merge without disturbing the other half
-                    atomicAnd(vdst + k, ~s_vmask[k]);
-                    atomicOr(vdst + k, s_rec[2][k]);
-                }
-            }
-        } else if (lane == 0 && p.status) {
-            atomicOr(p.status, BGTQ_STATUS_PAGE_RANGE);
-        }
-        __syncwarp();
-    }
 }
 
 // Softmax warpgroup g: the online softmax of row r of query head hq0 + g
@@ -595,7 +336,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (pair == 0) {
             stage_thresholds(s_thr, p.thr, tid, kEncWarps * 32);
             asm volatile("bar.sync 1, %0;" ::"n"(kEncWarps * 32) : "memory");
-            encode_block(p, b, h, q0, min(kTcRows, p.T - q0), s_thr, s_rec[warp], s_vmask[warp], warp, lane, kEncWarps);
+            encode_block(p, b, h, q0, min(kTcRows, p.T - q0), 0, p.T, s_thr, s_rec[warp], s_vmask[warp], warp, lane,
+                         kEncWarps);
         }
         if (g < ng)
             softmax_rows(p, tmem, g, b, hq0 + g, q0, nkt, BAR(kBarS + g), BAR(kBarP + g), BAR(kBarO + g), abort_flag, warp,
@@ -608,41 +350,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
     }
-}
-
-// ---- host side
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled() {
-    static std::once_flag once;
-    static EncodeTiledFn fn = nullptr;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult qr = cudaDriverEntryPointSymbolNotFound;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
-            qr == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-        cudaGetLastError();
-    });
-    return fn;
-}
-
-// Tensor map of a row-major [rows][128] fp16 matrix in this GPU's memory,
-// read in boxes of 128 rows x 64 columns with the 128-byte swizzle; rows past
-// the end read as zeros.
-bool rows_map(CUtensorMap* m, const void* base, uint64_t rows) {
-    EncodeTiledFn enc = encode_tiled();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)kTcRows};
-    const cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -672,8 +379,8 @@ cudaError_t launch_prefill(const bgtq_plan& pl, cudaStream_t s, const void* q, c
         }
     }
     alignas(64) CUtensorMap tq, tk, tv;
-    if (!rows_map(&tq, q, q_rows) || !rows_map(&tk, k, (uint64_t)batch * pl.H * t) ||
-        !rows_map(&tv, v, (uint64_t)batch * pl.H * t))
+    if (!rows_map(&tq, q, q_rows, kTcRows) || !rows_map(&tk, k, (uint64_t)batch * pl.H * t, kTcKeys) ||
+        !rows_map(&tv, v, (uint64_t)batch * pl.H * t, kTcKeys))
         return cudaErrorInvalidValue;
     PfParams p;
     p.q = static_cast<const __half*>(q);

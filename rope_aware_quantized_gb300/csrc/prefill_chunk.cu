@@ -1,0 +1,707 @@
+// Chunked prefill: a later chunk of a long prompt onto a cache that already
+// holds the earlier tokens packed.  Query row i of the chunk attends, in one
+// softmax, the P0 cached keys as stored and the chunk's keys 0 .. i as given.
+//
+// Method: "RoPE-Aware Bit Allocation for KV-Cache Quantization" — the packed
+// cache (review §1 "Packed-Cache") is what earlier chunks left; attention
+// over it is the decode path's arithmetic.  Fusing the quantizer into an
+// attention operator is named as future work on the LogQuant page (section
+// "중요성 및 주장").
+//
+// The prefix is attended on the tensor cores in the codecs' own domains.
+// For a key, q . k_hat = rho_k * sum_j q''_j c_j with c_j the centroid of
+// codec coordinate j and q'' = BF(q[perm] * dewhiten * sign * 1/sqrt(piece))
+// (BF: the per-piece butterflies, which are their own transpose); for the
+// values, sum_t p_t v_hat_t = sign * BF(sum_t p_t rho_v,t c_t) / sqrt(128).
+// So a prefix tile is staged as raw centroid values (fp16-exact), the query
+// rows are rotated once per CTA, the key norms scale the logits in fp32, the
+// value norms scale the probabilities, and the output row is taken back to
+// the value dims once, when the chunk's own tiles begin.  Query and
+// probabilities are split into fp16 hi + lo parts (two MMAs each) so that the
+// products keep about 22 bits, as in the decode path; each rotated query row
+// is first scaled by a power of two to below 2^14, undone on its logits.
+//
+// One CTA takes 128 rows of one query head; 10 warps:
+//   warps 0-3  softmax (thread i = row i = tensor-memory lane i)
+//   warps 4-7  dequantise prefix tiles: the packed records of 128 keys into
+//              K and V stages (raw centroid values, 128-byte swizzle)
+//   warp 8     MMA issue (one thread), owner of the tensor memory
+//   warp 9     TMA: Q (again after the prefix, the rotated query having taken
+//              its place), the chunk's K and V tiles
+// Tensor memory: S in two buffers (columns 0 and 128), O at 256; P (hi at
+// the buffer's columns 0-63, lo at 64-127) overwrites the S it came from.
+// MMA order: S(0), S(1), then PV(j), S(j+2) for every tile j.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "bgtq_internal.h"
+#include "tc_common.cuh"
+
+namespace bgtq {
+namespace {
+
+constexpr int kCkRows = 128;
+constexpr int kCkKeys = 128;
+constexpr int kCkThreads = 320;
+constexpr uint32_t kCkTile = 128 * kD * 2;  // 32 KB
+constexpr uint32_t kCkBox = kCkTile / 2;
+constexpr uint32_t kCOffQ = 0;              // Q, or the rotated query's hi part
+constexpr uint32_t kCOffQL = kCkTile;       // the rotated query's lo part
+constexpr uint32_t kCOffK = 2 * kCkTile;    // K stage s at + s kCkTile
+constexpr uint32_t kCOffV = 4 * kCkTile;    // V stage s at + s kCkTile
+constexpr uint32_t kCkSmem = 6 * kCkTile + 1024;
+constexpr int kRawK = 4 * 3 + 1;            // words of a staged K record (bK <= 3) + a zero word
+constexpr int kRawV = 8 * 4 + 1;            // words of a staged V pair record (bV <= 4) + a zero word
+constexpr float kHeadroomC = 8.0f;
+constexpr float kPvScale = 1.0f / 256.0f;   // prefix probabilities * rho_v are stored scaled by this
+
+enum {
+    kCQ = 0,        // Q copied (phase 0), copied again for the chunk's tiles (phase 1)
+    kCQR = 1,       // rotated query written (128 arrivals)
+    kCPSD = 2,      // every prefix S done: the Q region may be reloaded
+    kCPKF = 3,      // prefix K stage s filled (128 arrivals), 3 + s
+    kCPVF = 5,      // prefix V stage s filled
+    kCKF = 7,       // chunk K tile copied (TMA), 7 + s
+    kCVF = 9,
+    kCKE = 11,      // K stage s free again (MMA commit)
+    kCVE = 13,
+    kCS = 15,       // S buffer b computed, 15 + b
+    kCP = 17,       // P of the current tile written (128 arrivals)
+    kCO = 18,       // PV of a tile done (one phase per tile)
+    kCDrain = 19,
+    kCNumBars = 20
+};
+
+struct CkParams {
+    const __half* q;  // [B][H*G][C][128], the chunk's queries
+    const __half* k;  // [B][H][C][128], the chunk's keys and values as given
+    const __half* v;
+    void* out;        // [B][H*G][C][128]
+    int out_dtype;
+    int C, H, G;
+    float scale_log2;
+    const int32_t* pos_start;  // [B]: prefix length P0 of each sequence
+    const uint8_t* kc;
+    const float* kn;
+    const uint8_t* vc;
+    const float* vn;
+    CacheMap map;
+    const HeadTab* heads;
+    const float* cent;  // [9][256]
+    int bk, bv;
+    int32_t* status;
+};
+
+__device__ __forceinline__ uint32_t swz_off(int row, int col) {
+    // element (row, col) of a [128][128] fp16 tile held as two 64-column boxes
+    return (uint32_t)((col >> 6) * kCkBox + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) + (col & 7) * 2);
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+// barrier over n threads that also ANDs a predicate across them
+__device__ __forceinline__ bool named_sync_and(int id, int n, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+// Unnormalised butterflies over 128 values in registers; stage h acts on the
+// pairs (j, j + h) with j < n[h] (the pieces larger than h form that prefix).
+template <bool kAll>
+__device__ __forceinline__ void butterflies128(float (&x)[kD], const int* nh) {
+#pragma unroll
+    for (int st = 0; st < 7; ++st) {
+        const int h = 1 << st;
+        const int lim = kAll ? kD : nh[st];
+#pragma unroll
+        for (int j = 0; j < kD; ++j) {
+            if (j & h) continue;
+            if (kAll || j < lim) {
+                const float a = x[j], b = x[j + h];
+                x[j] = a + b;
+                x[j + h] = a - b;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kCkThreads, 1)
+    chunk_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                 const __grid_constant__ CUtensorMap tv, CkParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t s_bar[kCNumBars];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+    __shared__ __half s_cent[(kWMax + 1) * 256];  // centroids, fp16-exact
+    __shared__ uint32_t s_ktab[kD];               // K code j: bit position | width << 16
+    __shared__ uint8_t s_qperm[kD];               // rotated query: source dim of codec index j
+    __shared__ float s_qscale[kD];                // dewhiten * sign * 1/sqrt(piece) (0 past n_coded)
+    __shared__ float s_vsign[kD];
+    __shared__ int s_nh[8];                       // butterfly stage h = 2^i: pairs j < s_nh[i]
+    __shared__ float s_rho[2][2][kCkKeys];        // stage, (key, value) norms of the prefix keys
+    __shared__ uint32_t s_rawk[kCkKeys][kRawK];   // staged K records
+    __shared__ uint32_t s_rawv[kCkKeys / 2][kRawV];
+
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int hq = (int)blockIdx.x % (p.H * p.G);
+    const int b = (int)blockIdx.x / (p.H * p.G);
+    const int h = hq / p.G;
+    const int nqb = (p.C + kCkRows - 1) / kCkRows;
+    const int qb = nqb - 1 - (int)blockIdx.y;  // heaviest query blocks first
+    const int q0 = qb * kCkRows;
+    const int P0 = p.pos_start[b];
+    const HeadTab* ht = p.heads + h;
+    // a chunk past the capacity: the append flagged it and wrote nothing
+    if (P0 < 0 || (int64_t)P0 + p.C > p.map.cap) {
+        if (tid < kCkRows && q0 + tid < p.C) {
+            const size_t o = (((size_t)b * p.H * p.G + hq) * p.C + q0 + tid) * kD;
+            for (int d = 0; d < kD; ++d) {
+                if (p.out_dtype) static_cast<float*>(p.out)[o + d] = 0.0f;
+                else static_cast<__half*>(p.out)[o + d] = __float2half_rn(0.0f);
+            }
+        }
+        return;
+    }
+    const int np = (P0 + kCkKeys - 1) / kCkKeys;  // prefix tiles
+    const int nc = qb + 1;                        // chunk tiles; the last holds the diagonal
+    const int nt = np + nc;
+    const uint32_t bar0 = smem_u32(&s_bar[0]);
+    volatile int* abort_flag = &s_abort;
+#define CBAR(i) (bar0 + 8u * (uint32_t)(i))
+
+    // ---- set-up: barriers, tensor memory, the head's tables
+    if (tid == 0) {
+        s_abort = 0;
+        for (int i = 0; i < kCNumBars; ++i) {
+            const bool many = i == kCQR || i == kCPKF || i == kCPKF + 1 || i == kCPVF || i == kCPVF + 1 || i == kCP;
+            mbar_init(CBAR(i), many ? kCkRows : 1);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 8) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(512));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    for (int i = tid; i < (kWMax + 1) * 256; i += kCkThreads) s_cent[i] = __float2half_rn(p.cent[i]);
+    const int n_coded = ht->n_coded;
+    for (int j = tid; j < kD; j += kCkThreads) {
+        const int w = j < n_coded ? ht->width[j] : 0;
+        const int bit = w ? ht->pair_bit[j >> 1] + (j & 1) * w : 0;
+        s_ktab[j] = (uint32_t)bit | ((uint32_t)w << 16);
+        s_qperm[j] = ht->perm[j];
+        s_qscale[j] = j < n_coded ? ht->dewhiten[j] * ht->sign_k[j] * ht->inv_sqrt[j] : 0.0f;
+        s_vsign[j] = ht->sign_v[j];
+    }
+    if (warp == 9) {
+        for (int st = 0; st < 7; ++st) {
+            int cnt = 0;
+            for (int j = lane; j < kD; j += 32) cnt += (j < n_coded && (1 << ht->plog2[j]) > (1 << st)) ? 1 : 0;
+            cnt = __reduce_add_sync(0xffffffffu, cnt);
+            if (lane == 0) s_nh[st] = cnt;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    if (warp == 9) {
+        // ---- TMA: Q, Q again after the prefix, the chunk's K/V tiles
+        if (lane == 0) {
+            const int qrow = (b * p.H * p.G + hq) * p.C + q0;
+            const int krow = (b * p.H + h) * p.C;
+            mbar_expect_tx(CBAR(kCQ), kCkTile);
+            for (int x = 0; x < 2; ++x) tma_load_2d(sbase + kCOffQ + x * kCkBox, &tq, 64 * x, qrow, CBAR(kCQ));
+            bool ok = true;
+            if (np > 0) {
+                ok = mbar_wait(CBAR(kCPSD), 0, abort_flag, p.status);
+                if (ok) {
+                    mbar_expect_tx(CBAR(kCQ), kCkTile);
+                    for (int x = 0; x < 2; ++x) tma_load_2d(sbase + kCOffQ + x * kCkBox, &tq, 64 * x, qrow, CBAR(kCQ));
+                }
+            }
+            int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};  // chunk tiles issued per stage (uses - 1)
+            int uses[2] = {0, 0};
+            for (int i = 0; ok && i < nc; ++i) {
+                const int j = np + i, s = j & 1;
+                const uint32_t par = (uint32_t)((j >> 1) - 1) & 1u;
+                if (j >= 2 && !mbar_wait(CBAR(kCKE + s), par, abort_flag, p.status)) break;
+                mbar_expect_tx(CBAR(kCKF + s), kCkTile);
+                for (int x = 0; x < 2; ++x)
+                    tma_load_2d(sbase + kCOffK + s * kCkTile + x * kCkBox, &tk, 64 * x, krow + i * kCkKeys, CBAR(kCKF + s));
+                last_k[s] = uses[s];
+                if (j >= 2 && !mbar_wait(CBAR(kCVE + s), par, abort_flag, p.status)) break;
+                mbar_expect_tx(CBAR(kCVF + s), kCkTile);
+                for (int x = 0; x < 2; ++x)
+                    tma_load_2d(sbase + kCOffV + s * kCkTile + x * kCkBox, &tv, 64 * x, krow + i * kCkKeys, CBAR(kCVF + s));
+                last_v[s] = uses[s];
+                ++uses[s];
+            }
+            // every copy issued has landed before the CTA ends
+            mbar_wait(CBAR(kCQ), np > 0 ? 1u : 0u, abort_flag, p.status, false);
+            for (int s = 0; s < 2; ++s) {
+                if (last_k[s] >= 0) mbar_wait(CBAR(kCKF + s), (uint32_t)last_k[s] & 1u, abort_flag, p.status, false);
+                if (last_v[s] >= 0) mbar_wait(CBAR(kCVF + s), (uint32_t)last_v[s] & 1u, abort_flag, p.status, false);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 8) {
+        // ---- MMA issue
+        if (lane == 0) {
+            constexpr uint32_t idS = instr_desc(kCkRows, kCkKeys, 0);
+            constexpr uint32_t idO = instr_desc(kCkRows, kD, 1);
+            int cnt_pk[2] = {0, 0}, cnt_pv[2] = {0, 0}, cnt_k[2] = {0, 0}, cnt_v[2] = {0, 0};
+            bool ok = mbar_wait(CBAR(kCQ), 0, abort_flag, p.status);
+            if (ok && np > 0) ok = mbar_wait(CBAR(kCQR), 0, abort_flag, p.status);
+            auto issue_s = [&](int j) -> bool {
+                const int s = j & 1;
+                const uint32_t ka = sbase + kCOffK + s * kCkTile, d = tmem + 128u * (uint32_t)s;
+                if (j < np) {
+                    if (!mbar_wait(CBAR(kCPKF + s), (uint32_t)(cnt_pk[s]++) & 1u, abort_flag, p.status)) return false;
+                    tc_fence_after();
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {
+                        const uint32_t qa = sbase + (part ? kCOffQL : kCOffQ);
+#pragma unroll
+                        for (int k = 0; k < kD / 16; ++k) {
+                            const uint32_t off = (uint32_t)(k >> 2) * kCkBox + (uint32_t)(k & 3) * 32;
+                            mma_ss(d, smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), idS, (part | k) ? 1u : 0u);
+                        }
+                    }
+                } else {
+                    if (j == np && np > 0 && !mbar_wait(CBAR(kCQ), 1, abort_flag, p.status)) return false;
+                    if (!mbar_wait(CBAR(kCKF + s), (uint32_t)(cnt_k[s]++) & 1u, abort_flag, p.status)) return false;
+                    tc_fence_after();
+                    const uint32_t qa = sbase + kCOffQ;
+#pragma unroll
+                    for (int k = 0; k < kD / 16; ++k) {
+                        const uint32_t off = (uint32_t)(k >> 2) * kCkBox + (uint32_t)(k & 3) * 32;
+                        mma_ss(d, smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), idS, k > 0 ? 1u : 0u);
+                    }
+                }
+                mma_commit(CBAR(kCS + s));
+                mma_commit(CBAR(kCKE + s));
+                if (j == np - 1) mma_commit(CBAR(kCPSD));
+                return true;
+            };
+            auto issue_pv = [&](int j) -> bool {
+                const int s = j & 1;
+                const uint32_t va = sbase + kCOffV + s * kCkTile, pa = tmem + 128u * (uint32_t)s;
+                if (!mbar_wait(CBAR(kCP), (uint32_t)j & 1u, abort_flag, p.status)) return false;
+                if (j < np) {
+                    if (!mbar_wait(CBAR(kCPVF + s), (uint32_t)(cnt_pv[s]++) & 1u, abort_flag, p.status)) return false;
+                } else {
+                    if (!mbar_wait(CBAR(kCVF + s), (uint32_t)(cnt_v[s]++) & 1u, abort_flag, p.status)) return false;
+                }
+                tc_fence_after();
+                const int parts = j < np ? 2 : 1;
+                for (int part = 0; part < parts; ++part)
+#pragma unroll
+                    for (int k = 0; k < kCkKeys / 16; ++k)
+                        mma_ts(tmem + 256u, pa + 64u * part + 8u * k, smem_desc(va + 2048u * k, kCkBox, 1024), idO,
+                               (j > 0 || part > 0 || k > 0) ? 1u : 0u);
+                mma_commit(CBAR(kCO));
+                mma_commit(CBAR(kCVE + s));
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            if (ok && nt > 1) ok = issue_s(1);
+            for (int j = 0; ok && j < nt; ++j) {
+                ok = issue_pv(j);
+                if (ok && j + 2 < nt) ok = issue_s(j + 2);
+            }
+            mma_commit(CBAR(kCDrain));
+            mbar_wait(CBAR(kCDrain), 0, abort_flag, p.status, false);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ---- prefix tiles from the packed records: thread r takes key r
+        const int r = tid - 128;
+        const int rk = 4 * p.bk, rv = 8 * p.bv;
+        for (int j = 0; j < np; ++j) {
+            const int s = j & 1;
+            if (j >= 2) {
+                // all four warps leave together (they meet at named barriers below)
+                const uint32_t par = (uint32_t)((j >> 1) - 1) & 1u;
+                const bool got = mbar_wait(CBAR(kCKE + s), par, abort_flag, p.status) &&
+                                 mbar_wait(CBAR(kCVE + s), par, abort_flag, p.status);
+                if (!named_sync_and(2, 128, got)) break;
+            }
+            const int pos = j * kCkKeys + r;
+            int64_t sl = -1;
+            if (pos < P0) {
+                sl = p.map.slot(b, h, pos);
+                if (sl < 0 && p.status) atomicOr(p.status, BGTQ_STATUS_PAGE_RANGE);
+            }
+            // raw records into shared memory (the V pair record by the even key)
+            if (sl >= 0) {
+                const uint4* src = reinterpret_cast<const uint4*>(p.kc + sl * (16 * p.bk));
+                for (int i = 0; i < p.bk; ++i) {
+                    const uint4 w4 = src[i];
+                    s_rawk[r][4 * i] = w4.x;
+                    s_rawk[r][4 * i + 1] = w4.y;
+                    s_rawk[r][4 * i + 2] = w4.z;
+                    s_rawk[r][4 * i + 3] = w4.w;
+                }
+            } else {
+                for (int i = 0; i < rk; ++i) s_rawk[r][i] = 0u;
+            }
+            s_rawk[r][rk] = 0u;
+            if ((r & 1) == 0) {
+                if (sl >= 0) {
+                    const uint4* src = reinterpret_cast<const uint4*>(p.vc + (sl >> 1) * (32 * p.bv));
+                    for (int i = 0; i < 2 * p.bv; ++i) {
+                        const uint4 w4 = src[i];
+                        s_rawv[r >> 1][4 * i] = w4.x;
+                        s_rawv[r >> 1][4 * i + 1] = w4.y;
+                        s_rawv[r >> 1][4 * i + 2] = w4.z;
+                        s_rawv[r >> 1][4 * i + 3] = w4.w;
+                    }
+                } else {
+                    for (int i = 0; i < rv; ++i) s_rawv[r >> 1][i] = 0u;
+                }
+                s_rawv[r >> 1][rv] = 0u;
+            }
+            const float rho_k = sl >= 0 ? p.kn[sl] : 0.0f;
+            // the odd key of a pair reads the even key's record: same slot / 2
+            const float rho_v = sl >= 0 ? p.vn[sl] : 0.0f;
+            named_sync(2, 128);
+            // K row r: centroid of codec coordinate jj, codec order
+            const uint32_t krow = sbase + kCOffK + s * kCkTile;
+#pragma unroll 1
+            for (int c8 = 0; c8 < kD / 8; ++c8) {
+                uint32_t packed[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    __half hv[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint32_t t = s_ktab[8 * c8 + 2 * e + u];
+                        const uint32_t w = t >> 16, bit = t & 0xFFFFu;
+                        const uint32_t lo = s_rawk[r][bit >> 5], hi = s_rawk[r][(bit >> 5) + 1];
+                        const uint32_t code = __funnelshift_r(lo, hi, bit & 31u) & ((1u << w) - 1u);
+                        hv[u] = w ? s_cent[w * 256 + code] : __float2half_rn(0.0f);
+                    }
+                    packed[e] = (uint32_t)__half_as_ushort(hv[0]) | ((uint32_t)__half_as_ushort(hv[1]) << 16);
+                }
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(krow + swz_off(r, 8 * c8)), "r"(packed[0]),
+                             "r"(packed[1]), "r"(packed[2]), "r"(packed[3])
+                             : "memory");
+            }
+            // V row r: dim d holds code_even | code_odd << bV at bit 2 bV d
+            const uint32_t vrow = sbase + kCOffV + s * kCkTile;
+            const uint32_t bvv = (uint32_t)p.bv, par_sh = (uint32_t)(r & 1) * bvv;
+#pragma unroll 1
+            for (int c8 = 0; c8 < kD / 8; ++c8) {
+                uint32_t packed[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    __half hv[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint32_t bit = 2u * bvv * (uint32_t)(8 * c8 + 2 * e + u) + par_sh;
+                        const uint32_t lo = s_rawv[r >> 1][bit >> 5], hi = s_rawv[r >> 1][(bit >> 5) + 1];
+                        const uint32_t code = __funnelshift_r(lo, hi, bit & 31u) & ((1u << bvv) - 1u);
+                        hv[u] = s_cent[bvv * 256 + code];
+                    }
+                    packed[e] = (uint32_t)__half_as_ushort(hv[0]) | ((uint32_t)__half_as_ushort(hv[1]) << 16);
+                }
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(vrow + swz_off(r, 8 * c8)), "r"(packed[0]),
+                             "r"(packed[1]), "r"(packed[2]), "r"(packed[3])
+                             : "memory");
+            }
+            s_rho[s][0][r] = rho_k;
+            s_rho[s][1][r] = rho_v;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(CBAR(kCPKF + s));
+            mbar_arrive(CBAR(kCPVF + s));
+            named_sync(2, 128);  // the raw records are read; the next tile may overwrite them
+        }
+    } else {
+        // ---- softmax: thread r owns row q0 + r of the chunk
+        const int r = tid;
+        const int row = q0 + r;  // chunk-local
+        const uint32_t lanes = (uint32_t)(32 * warp) << 16;
+        const float c = p.scale_log2;
+        float q_unscale = 1.0f;  // prefix logits: times this power of two (the rotated query's scaling)
+        bool ok = __all_sync(0xffffffffu, mbar_wait(CBAR(kCQ), 0, abort_flag, p.status));
+        if (ok && np > 0) {
+            // the rotated query q'' (codec order), split into fp16 hi + lo, over Q
+            float x[kD];
+            const uint8_t* qs = smem_raw + (sbase - smem_u32(smem_raw)) + kCOffQ;
+#pragma unroll
+            for (int j = 0; j < kD; ++j) {
+                const float qv = __half2float(*reinterpret_cast<const __half*>(qs + swz_off(r, s_qperm[j] & (kD - 1))));
+                x[j] = qv * s_qscale[j];
+            }
+            int nh[7];
+#pragma unroll
+            for (int st = 0; st < 7; ++st) nh[st] = s_nh[st];
+            butterflies128<false>(x, nh);
+            // the row scaled by a power of two to below 2^14 (the de-whitened
+            // query can leave the fp16 range); the logits take it back exactly
+            float amax = 0.0f;
+#pragma unroll
+            for (int j = 0; j < kD; ++j) amax = fmaxf(amax, fabsf(x[j]));
+            if (amax > 0.0f) {
+                int e2 = 0;
+                frexpf(amax, &e2);  // amax = f 2^e2, f in [0.5, 1)
+                const float up = ldexpf(1.0f, 14 - e2);
+                q_unscale = ldexpf(1.0f, e2 - 14);
+#pragma unroll
+                for (int j = 0; j < kD; ++j) x[j] *= up;
+            }
+#pragma unroll
+            for (int c8 = 0; c8 < kD / 8; ++c8) {
+                uint32_t hp[4], lp[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const __half h0 = __float2half_rn(x[8 * c8 + 2 * e]), h1 = __float2half_rn(x[8 * c8 + 2 * e + 1]);
+                    const __half l0 = __float2half_rn(x[8 * c8 + 2 * e] - __half2float(h0));
+                    const __half l1 = __float2half_rn(x[8 * c8 + 2 * e + 1] - __half2float(h1));
+                    hp[e] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+                    lp[e] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+                }
+                const uint32_t off = swz_off(r, 8 * c8);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + kCOffQ + off), "r"(hp[0]), "r"(hp[1]),
+                             "r"(hp[2]), "r"(hp[3])
+                             : "memory");
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + kCOffQL + off), "r"(lp[0]),
+                             "r"(lp[1]), "r"(lp[2]), "r"(lp[3])
+                             : "memory");
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(CBAR(kCQR));
+        }
+        float m = 0.0f, l = 0.0f;
+        const uint32_t tO = tmem + lanes + 256u;
+        for (int j = 0; ok && j < nt; ++j) {
+            const int s = j & 1;
+            const uint32_t tS = tmem + lanes + 128u * (uint32_t)s;
+            const bool pre = j < np;
+            if (!__all_sync(0xffffffffu, mbar_wait(CBAR(kCS + s), (uint32_t)(j >> 1) & 1u, abort_flag, p.status) &&
+                                             (!pre || mbar_wait(CBAR(kCPKF + s), (uint32_t)(j >> 1) & 1u, abort_flag,
+                                                                p.status)))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float sv[kCkKeys];
+#pragma unroll
+            for (int q4 = 0; q4 < kCkKeys / 32; ++q4) tmem_ld32(tS + 32 * q4, sv + 32 * q4);
+            tmem_wait_ld();
+            if (pre) {
+                const int lim = P0 - 1 - j * kCkKeys;  // keys past the prefix
+#pragma unroll
+                for (int k = 0; k < kCkKeys; ++k) sv[k] = k > lim ? -INFINITY : sv[k] * (s_rho[s][0][k] * q_unscale);
+            } else if (j == nt - 1) {  // the chunk's diagonal tile
+                const int lim = min(row, p.C - 1) - (j - np) * kCkKeys;
+#pragma unroll
+                for (int k = 0; k < kCkKeys; ++k)
+                    if (k > lim) sv[k] = -INFINITY;
+            }
+            float mx[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = sv[i];
+#pragma unroll
+            for (int k = 8; k < kCkKeys; ++k) mx[k & 7] = fmaxf(mx[k & 7], sv[k]);
+            const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * c;
+            float f = 1.0f;
+            bool raise = false;
+            if (j == 0) {
+                m = mt;  // finite: key 0 (of the prefix, or of the chunk) is before every row
+            } else if (mt > m + kHeadroomC) {
+                f = ex2(m - mt);
+                m = mt;
+                l *= f;
+                raise = true;
+            }
+            const bool to_dims = np > 0 && j == np;  // O leaves the value codec domain
+            if (__any_sync(0xffffffffu, raise) || to_dims) {
+                // PV of tile j - 1 must be done before O is touched
+                if (!__all_sync(0xffffffffu, mbar_wait(CBAR(kCO), (uint32_t)(j - 1) & 1u, abort_flag, p.status))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (to_dims) {
+                    float o[kD];
+#pragma unroll
+                    for (int q4 = 0; q4 < kD / 32; ++q4) tmem_ld32(tO + 32 * q4, o + 32 * q4);
+                    tmem_wait_ld();
+                    int nh_all[7];
+                    butterflies128<true>(o, nh_all);
+                    const float g = f * (1.0f / kPvScale) * 0.08838834764831845f;  // 1/sqrt(128)
+#pragma unroll
+                    for (int q4 = 0; q4 < kD / 32; ++q4) {
+                        uint32_t w[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(o[32 * q4 + i] * (g * s_vsign[32 * q4 + i]));
+                        tmem_st32(tO + 32 * q4, w);
+                    }
+                } else {
+#pragma unroll 1
+                    for (int q4 = 0; q4 < kD / 32; ++q4) {
+                        float o[32];
+                        tmem_ld32(tO + 32 * q4, o);
+                        tmem_wait_ld();
+                        uint32_t w[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(o[i] * f);
+                        tmem_st32(tO + 32 * q4, w);
+                    }
+                }
+            }
+            float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (pre) {
+                // keys 64 hf .. 64 hf + 63: hi parts to columns 32 hf, lo parts to 64 + 32 hf
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t hi[32], lo[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int k = 64 * hf + 2 * i;
+                        const float p0 = ex2(fmaf(sv[k], c, -m)), p1 = ex2(fmaf(sv[k + 1], c, -m));
+                        ls[i & 3] += p0 + p1;
+                        const float a = p0 * (s_rho[s][1][k] * kPvScale), bq = p1 * (s_rho[s][1][k + 1] * kPvScale);
+                        const __half ha = __float2half_rn(a), hb = __float2half_rn(bq);
+                        const __half la = __float2half_rn(a - __half2float(ha)), lb = __float2half_rn(bq - __half2float(hb));
+                        hi[i] = (uint32_t)__half_as_ushort(ha) | ((uint32_t)__half_as_ushort(hb) << 16);
+                        lo[i] = (uint32_t)__half_as_ushort(la) | ((uint32_t)__half_as_ushort(lb) << 16);
+                    }
+                    tmem_st32(tS + 32 * hf, hi);
+                    tmem_st32(tS + 64 + 32 * hf, lo);
+                }
+            } else {
+                uint32_t pk[kCkKeys / 2];
+#pragma unroll
+                for (int i = 0; i < kCkKeys / 2; ++i) {
+                    const float p0 = ex2(fmaf(sv[2 * i], c, -m)), p1 = ex2(fmaf(sv[2 * i + 1], c, -m));
+                    ls[i & 3] += p0 + p1;
+                    pk[i] = pack_h2(p0, p1);
+                }
+                tmem_st32(tS, pk);
+                tmem_st32(tS + 32, pk + 32);
+            }
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(CBAR(kCP));
+        }
+        if (ok && __all_sync(0xffffffffu, mbar_wait(CBAR(kCO), (uint32_t)(nt - 1) & 1u, abort_flag, p.status))) {
+            tc_fence_after();
+            const float inv = 1.0f / l;
+            const size_t o0 = (((size_t)b * p.H * p.G + hq) * p.C + row) * kD;
+#pragma unroll 1
+            for (int q4 = 0; q4 < kD / 32; ++q4) {
+                float o[32];
+                tmem_ld32(tO + 32 * q4, o);
+                tmem_wait_ld();
+                if (row >= p.C) continue;
+                if (p.out_dtype) {
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + o0 + 32 * q4);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(p.out) + o0 + 32 * q4);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(pack_h2(o[8 * i] * inv, o[8 * i + 1] * inv),
+                                            pack_h2(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
+                                            pack_h2(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
+                                            pack_h2(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
+                }
+            }
+        }
+    }
+#undef CBAR
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
+    }
+}
+
+// The descriptors the kernel builds, checked field by field for every 1 KB
+// aligned base it can have.
+bool chunk_descriptors_valid() {
+    if (!instr_desc_ok(instr_desc(kCkRows, kCkKeys, 0), 0) || !instr_desc_ok(instr_desc(kCkRows, kD, 1), 1)) return false;
+    constexpr uint32_t kMaxSmem = 227u * 1024u;
+    for (uint32_t base = 0; base + kCkSmem <= kMaxSmem + 1024; base += 1024)
+        for (int k = 0; k < kD / 16; ++k) {
+            const uint32_t off = (uint32_t)(k >> 2) * kCkBox + (uint32_t)(k & 3) * 32;
+            for (uint32_t a : {base + kCOffQ + off, base + kCOffQL + off, base + kCOffK + kCkTile + off})
+                if (!smem_desc_ok(a, 16, 1024)) return false;
+            if (!smem_desc_ok(base + kCOffV + kCkTile + (uint32_t)k * 2048, kCkBox, 1024)) return false;
+        }
+    return true;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_chunk(const bgtq_plan& pl, cudaStream_t s, const void* q, const void* k, const void* v,
+                                 int batch, int c, const int32_t* pos_start, const bgtq_cache& cache, void* out,
+                                 int out_dtype, float scale, int32_t* status) {
+    static std::mutex mu;
+    static bool done[64] = {false};
+    static const bool desc_ok = chunk_descriptors_valid();
+    if (!desc_ok) return cudaErrorInvalidValue;
+    const uint64_t q_rows = (uint64_t)batch * pl.H * pl.G * (uint64_t)c;
+    const int nqb = (c + kCkRows - 1) / kCkRows;
+    if (q_rows + kCkRows >= (1ull << 31) || nqb > 65535 || (uint64_t)batch * pl.H * pl.G >= (1ull << 31))
+        return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!done[dev]) {
+            const cudaError_t e = cudaFuncSetAttribute(chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCkSmem);
+            if (e != cudaSuccess) return e;
+            done[dev] = true;
+        }
+    }
+    alignas(64) CUtensorMap tq, tk, tv;
+    if (!rows_map(&tq, q, q_rows, kCkRows) || !rows_map(&tk, k, (uint64_t)batch * pl.H * c, kCkKeys) ||
+        !rows_map(&tv, v, (uint64_t)batch * pl.H * c, kCkKeys))
+        return cudaErrorInvalidValue;
+    CkParams p;
+    p.q = static_cast<const __half*>(q);
+    p.k = static_cast<const __half*>(k);
+    p.v = static_cast<const __half*>(v);
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.C = c;
+    p.H = pl.H;
+    p.G = pl.G;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.pos_start = pos_start;
+    p.kc = static_cast<const uint8_t*>(cache.k_codes);
+    p.kn = cache.k_norm;
+    p.vc = static_cast<const uint8_t*>(cache.v_codes);
+    p.vn = cache.v_norm;
+    p.map = make_cache_map(cache, pl.H, batch, status);
+    p.heads = pl.dev.heads;
+    p.cent = pl.dev.cent;
+    p.bk = pl.bk;
+    p.bv = pl.bv;
+    p.status = status;
+    const dim3 grid((unsigned)((uint64_t)batch * pl.H * pl.G), (unsigned)nqb, 1);
+    chunk_kernel<<<grid, kCkThreads, kCkSmem, s>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace bgtq

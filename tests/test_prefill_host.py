@@ -43,3 +43,31 @@ def test_empty_prompt_is_a_no_op():
 def test_bad_arguments_are_rejected(kw, code, frag):
     rc, msg = call(**kw)
     assert rc == code and frag in msg, (rc, msg)
+
+
+def chunk_call(t=100, batch=1, q=BASE, out=BASE, pos=BASE, recent=0, capacity=128):
+    plan = bg.bgtq_plan_create(np.full((2, 64), 3, np.uint8), np.ones((2, 64)), 4, 384, 3, 1, host_only=True)
+    desc = bg._native.BgtqCache(BASE, BASE, BASE, BASE, capacity)
+    if recent:
+        desc.k_recent = BASE
+        desc.recent = recent
+    rc = bg.lib().bgtq_prefill_chunk_attn(plan.handle, None, q, BASE, BASE, batch, t, pos, ctypes.byref(desc), out, 0,
+                                          0.088, None)
+    return rc, bg.lib().bgtq_last_error().decode()
+
+
+def test_chunk_valid_arguments_reach_the_plan_check():
+    rc, msg = chunk_call()
+    assert rc == -1 and "host-only" in msg
+
+
+@pytest.mark.parametrize("kw,code,frag", [
+    (dict(t=200), -3, "capacity"),
+    (dict(pos=None), -1, "NULL"),
+    (dict(q=BASE + 8), -1, "16-byte aligned"),
+    (dict(out=BASE + 8), -1, "16-byte aligned"),
+    (dict(recent=16), -2, "recent-key"),
+])
+def test_chunk_bad_arguments_are_rejected(kw, code, frag):
+    rc, msg = chunk_call(**kw)
+    assert rc == code and frag in msg, (rc, msg)
