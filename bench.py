@@ -569,6 +569,55 @@ def measure_prefill_attn(w, plan, tokens: int, peaks: dict, stream) -> dict:
             "peak_note": "measured dense bf16 (burst); fp16 has the same nominal tensor rate"}
 
 
+def measure_chunk_prefill(w, plan, prefix: int, chunk: int, peaks: dict, stream) -> dict:
+    """Chunked prefill (bgtq_prefill_chunk_attn: the chunk's records by the
+    append, then attention of every chunk row over the packed prefix and the
+    chunk's own fp16 K/V) on one layer of the workload's shape: `prefix`
+    cached tokens per sequence, a chunk of `chunk` tokens, fp16 output.
+    Algorithmic work: 4 * 128 flops per (query head, chunk row, visible key),
+    the prefix keys all visible, the chunk's causally."""
+    import torch
+
+    import rope_aware_quantized_gb300 as bg
+
+    B, H, Hq = w.batch, w.n_kv, w.n_q
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(20262)
+    cache = bg.Cache(plan, B, prefix + chunk + ((prefix + chunk) & 1))
+    kp = torch.randn((B, H, prefix, 128), generator=gen, device="cuda").half()
+    vp = torch.randn((B, H, prefix, 128), generator=gen, device="cuda").half()
+    bg.bgtq_quantize_append(plan, kp, vp, torch.zeros(B, dtype=torch.int32, device="cuda"), cache)
+    del kp, vp
+    q = torch.randn((B, Hq, chunk, 128), generator=gen, device="cuda").half()
+    k = torch.randn((B, H, chunk, 128), generator=gen, device="cuda").half()
+    v = torch.randn((B, H, chunk, 128), generator=gen, device="cuda").half()
+    pos = torch.full((B,), prefix, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(6):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            bg.bgtq_prefill_chunk_attn(plan, q, k, v, pos, cache, out, status=status)
+            b.record(stream)
+            times.append((a, b))
+    torch.cuda.synchronize()
+    assert status.item() == 0, f"chunk prefill status {status.item()}"
+    ms = statistics.median(a.elapsed_time(b) for a, b in times[2:])
+    flops = 4.0 * 128 * B * Hq * chunk * (prefix + (chunk + 1) / 2)
+    tf = flops / (ms / 1000.0) / 1e12
+    del q, k, v, out, cache
+    return {"prefix_tokens": prefix, "chunk_tokens": chunk, "batch": B, "query_heads": Hq, "kv_heads": H,
+            "ms_per_call": ms, "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": tf / peaks["bf16_tflops"], "bound": "tensor",
+            "flops": "4 * 128 per (query head, chunk row, visible key); the prefix on tcgen05 with fp16 hi + lo "
+                     "query and probability splits (twice the MMAs of the counted flops), the chunk as the "
+                     "fused prefill",
+            "peak_note": "measured dense bf16 (burst); fp16 has the same nominal tensor rate"}
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -593,10 +642,11 @@ def run_gpu(args):
                                    workloads.plan_seed(w, 0))
         peaks, _ = load_peaks()
         r = measure_prefill_attn(w, plan, args.prefill_tokens, peaks, torch.cuda.Stream())
+        rc = measure_chunk_prefill(w, plan, args.prefill_tokens, args.prefill_tokens // 4, peaks, torch.cuda.Stream())
         if rank == 0:
             print(json.dumps({"metric": "fused_prefill_tflops", "value": r["achieved"], "unit": "TFLOP/s",
                               "config": {"workload": w.name, "prompt_tokens": args.prefill_tokens},
-                              "prefill_attn": r}), flush=True)
+                              "prefill_attn": r, "chunk_prefill": rc}), flush=True)
         return
 
     # device buffers of all layers' per-step inputs/outputs (views per layer)
@@ -709,6 +759,8 @@ def run_gpu(args):
 
     prefill = measure_prefill(w, layers[0].plan, max_len, peaks, stream)
     prefill_attn = measure_prefill_attn(w, layers[0].plan, min(max_len, args.prefill_tokens), peaks, stream)
+    chunk_prefill = measure_chunk_prefill(w, layers[0].plan, min(max_len, args.prefill_tokens),
+                                          min(max_len, args.prefill_tokens) // 4, peaks, stream)
 
     # end to end: pinned host inputs -> device, graph replay, outputs -> host
     hq = torch.empty(q_all.shape, dtype=q_all.dtype, pin_memory=True)
@@ -789,6 +841,7 @@ def run_gpu(args):
         }
         line["append_prefill"] = prefill
         line["prefill_attn"] = prefill_attn
+        line["chunk_prefill"] = chunk_prefill
         if others:
             line["workloads"] = others
         if cpu:
