@@ -328,6 +328,15 @@ int bgtq_prefill_attn(const bgtq_plan* plan, void* stream, const void* q_fp16, c
                       float softmax_scale, int32_t* dev_status);
 
 /*
+ * bgtq_prefill_chunk_workspace — bytes of device scratch that
+ * bgtq_prefill_chunk_attn needs for `batch` sequences whose prefixes are at
+ * most max_prefix tokens: every prefix token's decoded rows (raw centroids,
+ * fp16, K and V) and its two norms, (512 + 8) bytes per (sequence, KV head,
+ * position up to max_prefix rounded up to 128).
+ */
+int bgtq_prefill_chunk_workspace(const bgtq_plan* plan, int batch, int64_t max_prefix, size_t* bytes);
+
+/*
  * bgtq_prefill_chunk_attn — a later chunk of a long prompt onto a cache that
  * already holds positions 0 .. P0-1 of each sequence: the packed records of
  * positions P0 .. P0+c-1 are written (bgtq_quantize_append at pos_start = P0,
@@ -341,24 +350,31 @@ int bgtq_prefill_attn(const bgtq_plan* plan, void* stream, const void* q_fp16, c
  *   c            chunk length, 0 <= c <= capacity
  *   dev_pos_start  device int32 [batch]: P0 of each sequence; a sequence with
  *                P0 < 0 or P0 + c > capacity is skipped (nothing written to
- *                the cache, zero output rows, BGTQ_STATUS_APPEND_CAPACITY)
+ *                the cache, zero output rows, BGTQ_STATUS_APPEND_CAPACITY); one
+ *                with P0 > max_prefix gets zero output rows and
+ *                BGTQ_STATUS_SEQLEN_CAPACITY (its records are still appended)
+ *   max_prefix   host bound of every P0, 0 <= max_prefix <= capacity
  *   cache        host pointer to the layer's descriptor, contiguous or paged,
  *                without a recent-key buffer
  *   out          device, [batch][H*G][c][128], half (out_dtype 0) or float
  *                (1), 16-byte aligned
  *   softmax_scale  logit scale, e.g. 1/sqrt(128)
+ *   workspace    device scratch of bgtq_prefill_chunk_workspace(plan, batch,
+ *                max_prefix) bytes, 256-byte aligned (contents not kept)
  *   dev_status   device int32 or NULL
- * Two launches on `stream`: the append, then the attention.  The chunk part
- * is computed as in bgtq_prefill_attn; the prefix part in the codecs' own
- * domains (rotated query, raw centroids, norms in fp32) with fp16 hi + lo
- * splits of the query and of the probabilities, fp32 accumulation.
- * Errors: INVALID_ARG (pointers, alignment, dtype, scale), CAPACITY (c >
- * capacity), UNSUPPORTED (a recent-key buffer, bK > 3, bV > 4), CUDA.
+ * Three launches on `stream`: the append, the decode of the prefix records
+ * into the workspace (each prefix token once), the attention (tcgen05).  The
+ * chunk part is computed as in bgtq_prefill_attn; the prefix part in the
+ * codecs' own domains (rotated query, raw centroids, norms in fp32) with fp16
+ * hi + lo splits of the query and of the probabilities, fp32 accumulation.
+ * Errors: INVALID_ARG (pointers, alignment, dtype, scale), CAPACITY (c or
+ * max_prefix > capacity), WORKSPACE (too small), UNSUPPORTED (a recent-key
+ * buffer, bK > 3, bV > 4, sizes past 2^31 rows), CUDA.
  */
 int bgtq_prefill_chunk_attn(const bgtq_plan* plan, void* stream, const void* q_fp16, const void* k_fp16,
-                            const void* v_fp16, int batch, int c, const int32_t* dev_pos_start,
-                            const bgtq_cache* cache, void* out, int out_dtype, float softmax_scale,
-                            int32_t* dev_status);
+                            const void* v_fp16, int batch, int c, const int32_t* dev_pos_start, int64_t max_prefix,
+                            const bgtq_cache* cache, void* out, int out_dtype, float softmax_scale, void* workspace,
+                            size_t ws_bytes, int32_t* dev_status);
 
 /*
  * bgtq_decode_attn_noalloc — bgtq_decode_attn for callers that cannot

@@ -336,13 +336,22 @@ def bgtq_prefill_attn(plan: Plan, q_fp16, k_fp16, v_fp16, cache: Cache, out, sof
                                    C.byref(cache.desc), _ptr(out), out_dtype, scale, _ptr(status)))
 
 
+def bgtq_prefill_chunk_workspace(plan: Plan, batch: int, max_prefix: int) -> int:
+    n = C.c_size_t()
+    _check(lib().bgtq_prefill_chunk_workspace(plan.handle, batch, max_prefix, C.byref(n)))
+    return n.value
+
+
 def bgtq_prefill_chunk_attn(plan: Plan, q_fp16, k_fp16, v_fp16, pos_start, cache: Cache, out,
-                            softmax_scale: float | None = None, status=None, stream=None):
+                            max_prefix: int | None = None, workspace=None, softmax_scale: float | None = None,
+                            status=None, stream=None):
     """A later chunk of a prompt onto a cache holding pos_start[b] tokens of sequence b: the
     chunk's packed records into `cache` (an append at pos_start) and attention of every chunk
     row over the cached prefix (as stored) and the chunk's own K/V so far into `out`.
     q: [B][H*G][C][128] float16; k, v: [B][H][C][128] float16; pos_start: [B] int32 CUDA
-    tensor; out: like q, float16 or float32."""
+    tensor; out: like q, float16 or float32.  max_prefix bounds pos_start (read from it when
+    None); workspace: a uint8 CUDA tensor of bgtq_prefill_chunk_workspace bytes (allocated
+    here when None)."""
     import torch
     b, hq, t, d = q_fp16.shape
     if d != HEAD_DIM or tuple(k_fp16.shape) != (b, plan.n_kv_heads, t, d) or tuple(v_fp16.shape) != tuple(k_fp16.shape):
@@ -359,10 +368,15 @@ def bgtq_prefill_chunk_attn(plan: Plan, q_fp16, k_fp16, v_fp16, pos_start, cache
         out_dtype = 0
     else:
         raise ValueError("out must be float16 or float32")
+    if max_prefix is None:
+        max_prefix = max(0, int(pos_start.max().item())) if b else 0
+    if workspace is None:
+        workspace = torch.empty(max(bgtq_prefill_chunk_workspace(plan, b, max_prefix), 1), dtype=torch.uint8,
+                                device=q_fp16.device)
     scale = (1.0 / HEAD_DIM ** 0.5) if softmax_scale is None else softmax_scale
     _check(lib().bgtq_prefill_chunk_attn(plan.handle, _stream(stream), _ptr(q_fp16), _ptr(k_fp16), _ptr(v_fp16), b,
-                                         t, _ptr(pos_start), C.byref(cache.desc), _ptr(out), out_dtype, scale,
-                                         _ptr(status)))
+                                         t, _ptr(pos_start), max_prefix, C.byref(cache.desc), _ptr(out), out_dtype,
+                                         scale, _ptr(workspace), workspace.numel(), _ptr(status)))
 
 
 def bgtq_dequant_debug(plan: Plan, cache: Cache, b: int, head: int, t0: int, t1: int, k_out=None, v_out=None,
@@ -374,6 +388,6 @@ def bgtq_dequant_debug(plan: Plan, cache: Cache, b: int, head: int, t0: int, t1:
 __all__ = [
     "BgtqError", "Plan", "Cache", "CacheView", "bgtq_alloc_bits", "bgtq_plan_create", "bgtq_cache_bytes",
     "bgtq_quantize_append", "bgtq_decode_attn_workspace", "bgtq_decode_attn", "bgtq_decode_step",
-    "bgtq_decode_attn_noalloc", "bgtq_logit_mae", "bgtq_prefill_attn", "bgtq_prefill_chunk_attn",
+    "bgtq_decode_attn_noalloc", "bgtq_logit_mae", "bgtq_prefill_attn", "bgtq_prefill_chunk_workspace", "bgtq_prefill_chunk_attn",
     "bgtq_plan_save", "bgtq_plan_load", "bgtq_dequant_debug",
 ]

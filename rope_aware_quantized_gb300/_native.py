@@ -51,8 +51,10 @@ EXPORTS = {
                                    C.c_void_p, C.c_size_t, C.c_void_p]),
     "bgtq_prefill_attn": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
                                     C.POINTER(BgtqCache), C.c_void_p, C.c_int, C.c_float, C.c_void_p]),
-    "bgtq_prefill_chunk_attn": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p,
-                                    C.POINTER(BgtqCache), C.c_void_p, C.c_int, C.c_float, C.c_void_p]),
+    "bgtq_prefill_chunk_workspace": (C.c_int, [C.c_void_p, C.c_int, C.c_int64, C.POINTER(C.c_size_t)]),
+    "bgtq_prefill_chunk_attn": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
+                                          C.c_void_p, C.c_int64, C.POINTER(BgtqCache), C.c_void_p, C.c_int, C.c_float,
+                                          C.c_void_p, C.c_size_t, C.c_void_p]),
     "bgtq_decode_attn_noalloc": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.POINTER(BgtqCache), C.c_void_p,
                                            C.c_int64, C.c_int, C.c_void_p, C.c_int, C.c_float, C.c_void_p]),
     "bgtq_logit_mae": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.POINTER(BgtqCache), C.c_int64,

@@ -837,14 +837,23 @@ int bgtq_prefill_attn(const bgtq_plan* p, void* stream, const void* q, const voi
     return BGTQ_OK;
 }
 
+int bgtq_prefill_chunk_workspace(const bgtq_plan* p, int batch, int64_t max_prefix, size_t* bytes) {
+    if (!p || !bytes) return set_error(BGTQ_ERR_INVALID_ARG, "NULL pointer");
+    if (batch < 0 || max_prefix < 0) return set_error(BGTQ_ERR_INVALID_ARG, "batch and max_prefix must be >= 0");
+    *bytes = prefill_chunk_workspace_bytes(*p, batch, max_prefix);
+    return BGTQ_OK;
+}
+
 int bgtq_prefill_chunk_attn(const bgtq_plan* p, void* stream, const void* q, const void* k, const void* v, int batch,
-                            int t, const int32_t* pos_start, const bgtq_cache* c, void* out, int out_dtype, float scale,
-                            int32_t* status) {
+                            int t, const int32_t* pos_start, int64_t max_prefix, const bgtq_cache* c, void* out,
+                            int out_dtype, float scale, void* ws, size_t ws_bytes, int32_t* status) {
     if (!p) return set_error(BGTQ_ERR_INVALID_ARG, "plan is NULL");
     int rc = check_cache(p, c);
     if (rc) return rc;
     if (batch < 0 || t < 0) return set_error(BGTQ_ERR_INVALID_ARG, "batch and c must be >= 0");
+    if (max_prefix < 0) return set_error(BGTQ_ERR_INVALID_ARG, "max_prefix must be >= 0");
     if (t > c->capacity) return set_error(BGTQ_ERR_CAPACITY, "c = %d exceeds the cache capacity", t);
+    if (max_prefix > c->capacity) return set_error(BGTQ_ERR_CAPACITY, "max_prefix exceeds the cache capacity");
     if (batch == 0 || t == 0) return BGTQ_OK;
     if (!q || !k || !v || !out || !pos_start) return set_error(BGTQ_ERR_INVALID_ARG, "NULL pointer");
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15)
@@ -854,13 +863,19 @@ int bgtq_prefill_chunk_attn(const bgtq_plan* p, void* stream, const void* q, con
     if (!(scale > 0.0f) || !std::isfinite(scale)) return set_error(BGTQ_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
     if (c->recent > 0)
         return set_error(BGTQ_ERR_UNSUPPORTED, "chunked prefill onto a cache with a recent-key buffer is not supported");
-    if ((uint64_t)batch * p->H * p->G * (uint64_t)t + 128 >= (1ull << 31))
-        return set_error(BGTQ_ERR_UNSUPPORTED, "batch * query heads * c must stay below 2^31 - 128");
+    if ((uint64_t)batch * p->H * p->G * (uint64_t)t + 128 >= (1ull << 31) ||
+        (uint64_t)batch * p->H * (uint64_t)(max_prefix + 128) + 128 >= (1ull << 31))
+        return set_error(BGTQ_ERR_UNSUPPORTED, "batch * query heads * c and batch * heads * max_prefix must stay below 2^31");
+    const size_t need = prefill_chunk_workspace_bytes(*p, batch, max_prefix);
+    if (ws_bytes < need) return set_error(BGTQ_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+    if (need > 0 && (!ws || (reinterpret_cast<uintptr_t>(ws) & 255)))
+        return set_error(BGTQ_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device buffer");
     if ((rc = check_plan(p))) return rc;
     if (p->bk > 3 || p->bv > 4) return set_error(BGTQ_ERR_UNSUPPORTED, "chunked prefill supports bK <= 3 and v_bits <= 4");
     cudaError_t e = launch_quantize_append(*p, (cudaStream_t)stream, k, v, batch, t, pos_start, *c, status);
     if (e != cudaSuccess) return set_error(BGTQ_ERR_CUDA, "chunk append launch: %s", cudaGetErrorString(e));
-    e = launch_prefill_chunk(*p, (cudaStream_t)stream, q, k, v, batch, t, pos_start, *c, out, out_dtype, scale, status);
+    e = launch_prefill_chunk(*p, (cudaStream_t)stream, q, k, v, batch, t, pos_start, max_prefix, *c, out, out_dtype,
+                             scale, ws, status);
     if (e != cudaSuccess) return set_error(BGTQ_ERR_CUDA, "chunk attention launch: %s", cudaGetErrorString(e));
     return BGTQ_OK;
 }

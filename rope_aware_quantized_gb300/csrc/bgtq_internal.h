@@ -132,9 +132,10 @@ struct CacheMap {
 cudaError_t launch_prefill(const bgtq_plan& pl, cudaStream_t s, const void* q, const void* k, const void* v,
                            int batch, int t, const bgtq_cache& c, void* out, int out_dtype, float scale,
                            int32_t* status);
+size_t prefill_chunk_workspace_bytes(const bgtq_plan& pl, int batch, int64_t max_prefix);
 cudaError_t launch_prefill_chunk(const bgtq_plan& pl, cudaStream_t s, const void* q, const void* k, const void* v,
-                                 int batch, int c, const int32_t* pos_start, const bgtq_cache& cache, void* out,
-                                 int out_dtype, float scale, int32_t* status);
+                                 int batch, int c, const int32_t* pos_start, int64_t max_prefix, const bgtq_cache& cache,
+                                 void* out, int out_dtype, float scale, void* ws, int32_t* status);
 
 // Host checks of a cache descriptor (buffers, alignment, capacity, the
 // recent-key buffer, paging); sets the thread's error message.

@@ -13,23 +13,24 @@
 // codec coordinate j and q'' = BF(q[perm] * dewhiten * sign * 1/sqrt(piece))
 // (BF: the per-piece butterflies, which are their own transpose); for the
 // values, sum_t p_t v_hat_t = sign * BF(sum_t p_t rho_v,t c_t) / sqrt(128).
-// So a prefix tile is staged as raw centroid values (fp16-exact), the query
-// rows are rotated once per CTA, the key norms scale the logits in fp32, the
-// value norms scale the probabilities, and the output row is taken back to
-// the value dims once, when the chunk's own tiles begin.  Query and
+// A first kernel decodes each prefix token's packed records once into a
+// workspace: its raw centroids (fp16-exact, codec order) for K and V and its
+// two norms.  The attention kernel copies those rows by TMA like the chunk's
+// own K/V, rotates its query rows once, scales the logits by the key norms in
+// fp32 and the probabilities by the value norms, and takes the output row
+// back to the value dims once, when the chunk's own tiles begin.  Query and
 // probabilities are split into fp16 hi + lo parts (two MMAs each) so that the
 // products keep about 22 bits, as in the decode path; each rotated query row
 // is first scaled by a power of two to below 2^14, undone on its logits.
 //
-// One CTA takes 128 rows of one query head; 10 warps:
+// Attention: one CTA takes 128 rows of one query head; 6 warps:
 //   warps 0-3  softmax (thread i = row i = tensor-memory lane i)
-//   warps 4-7  dequantise prefix tiles: the packed records of 128 keys into
-//              K and V stages (raw centroid values, 128-byte swizzle)
-//   warp 8     MMA issue (one thread), owner of the tensor memory
-//   warp 9     TMA: Q (again after the prefix, the rotated query having taken
-//              its place), the chunk's K and V tiles
-// Tensor memory: S in two buffers (columns 0 and 128), O at 256; P (hi at
-// the buffer's columns 0-63, lo at 64-127) overwrites the S it came from.
+//   warp 4     MMA issue (one thread), owner of the tensor memory
+//   warp 5     TMA: Q (again after the prefix, the rotated query having taken
+//              its place), the prefix tiles and norms, the chunk's K/V tiles
+// Tensor memory: S in two buffers (columns 0 and 128), O at 256; P
+// overwrites the S it came from, 32 keys per 32 columns: the hi parts of the
+// chunk's 16 key pairs in its first 16 columns, the lo parts in the next 16.
 // MMA order: S(0), S(1), then PV(j), S(j+2) for every tile j.
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -46,7 +47,7 @@ namespace {
 
 constexpr int kCkRows = 128;
 constexpr int kCkKeys = 128;
-constexpr int kCkThreads = 320;
+constexpr int kCkThreads = 192;
 constexpr uint32_t kCkTile = 128 * kD * 2;  // 32 KB
 constexpr uint32_t kCkBox = kCkTile / 2;
 constexpr uint32_t kCOffQ = 0;              // Q, or the rotated query's hi part
@@ -56,6 +57,7 @@ constexpr uint32_t kCOffV = 4 * kCkTile;    // V stage s at + s kCkTile
 constexpr uint32_t kCkSmem = 6 * kCkTile + 1024;
 constexpr int kRawK = 4 * 3 + 1;            // words of a staged K record (bK <= 3) + a zero word
 constexpr int kRawV = 8 * 4 + 1;            // words of a staged V pair record (bV <= 4) + a zero word
+constexpr int kMmaWarp = 4, kTmaWarp = 5;
 constexpr float kHeadroomC = 8.0f;
 constexpr float kPvScale = 1.0f / 256.0f;   // prefix probabilities * rho_v are stored scaled by this
 
@@ -63,17 +65,15 @@ enum {
     kCQ = 0,        // Q copied (phase 0), copied again for the chunk's tiles (phase 1)
     kCQR = 1,       // rotated query written (128 arrivals)
     kCPSD = 2,      // every prefix S done: the Q region may be reloaded
-    kCPKF = 3,      // prefix K stage s filled (128 arrivals), 3 + s
-    kCPVF = 5,      // prefix V stage s filled
-    kCKF = 7,       // chunk K tile copied (TMA), 7 + s
-    kCVF = 9,
-    kCKE = 11,      // K stage s free again (MMA commit)
-    kCVE = 13,
-    kCS = 15,       // S buffer b computed, 15 + b
-    kCP = 17,       // P of the current tile written (128 arrivals)
-    kCO = 18,       // PV of a tile done (one phase per tile)
-    kCDrain = 19,
-    kCNumBars = 20
+    kCKF = 3,       // K tile of stage s copied, 3 + s
+    kCVF = 5,       // V tile (and, for a prefix tile, its norms) of stage s copied
+    kCKE = 7,       // K stage s free again (MMA commit)
+    kCVE = 9,
+    kCS = 11,       // S buffer b computed, 11 + b
+    kCP = 13,       // P of the current tile written (128 arrivals)
+    kCO = 14,       // PV of a tile done (one phase per tile)
+    kCDrain = 15,
+    kCNumBars = 16
 };
 
 struct CkParams {
@@ -85,6 +85,14 @@ struct CkParams {
     int C, H, G;
     float scale_log2;
     const int32_t* pos_start;  // [B]: prefix length P0 of each sequence
+    int max_prefix;            // P0 bound of the workspace
+    int pmax;                  // workspace rows per (sequence, head): max_prefix rounded up to 128
+    // the decoded prefix (workspace): raw centroids [B][H][pmax][128] fp16, norms [B][H][pmax]
+    __half* kh;
+    __half* vh;
+    float* rk;
+    float* rv;
+    // the packed cache
     const uint8_t* kc;
     const float* kn;
     const uint8_t* vc;
@@ -101,16 +109,12 @@ __device__ __forceinline__ uint32_t swz_off(int row, int col) {
     return (uint32_t)((col >> 6) * kCkBox + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) + (col & 7) * 2);
 }
 
-__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
-// barrier over n threads that also ANDs a predicate across them
-__device__ __forceinline__ bool named_sync_and(int id, int n, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
-        : "=r"(r)
-        : "r"((uint32_t)v), "r"(id), "r"(n)
-        : "memory");
-    return r != 0;
+// plain (untiled) bulk copy global -> shared completing on an mbarrier; both
+// addresses 16-byte aligned, size a multiple of 16
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
 }
 
 // Unnormalised butterflies over 128 values in registers; stage h acts on the
@@ -133,22 +137,123 @@ __device__ __forceinline__ void butterflies128(float (&x)[kD], const int* nh) {
     }
 }
 
+
+// Decode of the prefix into the workspace: thread r of block (tile, h, b)
+// takes position 128 tile + r; positions from P0 up to the tile's end get
+// zero rows and norms (the attention masks them; zeros keep its MMAs finite).
+__global__ void __launch_bounds__(kCkKeys) chunk_prefix_decode_kernel(CkParams p) {
+    __shared__ __half s_cent[(kWMax + 1) * 256];  // centroids, fp16-exact
+    __shared__ uint32_t s_ktab[kD];               // K code j: bit position | width << 16
+    __shared__ uint32_t s_rawk[kCkKeys][kRawK];   // staged K records
+    __shared__ uint32_t s_rawv[kCkKeys / 2][kRawV];
+    const int r = threadIdx.x, tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int P0 = p.pos_start[b];
+    if (P0 < 0 || P0 > p.max_prefix || (int64_t)P0 + p.C > p.map.cap || tile * kCkKeys >= P0) return;
+    const HeadTab* ht = p.heads + h;
+    for (int i = r; i < (kWMax + 1) * 256; i += kCkKeys) s_cent[i] = __float2half_rn(p.cent[i]);
+    {
+        const int j = r;
+        const int w = j < ht->n_coded ? ht->width[j] : 0;
+        const int bit = w ? ht->pair_bit[j >> 1] + (j & 1) * w : 0;
+        s_ktab[j] = (uint32_t)bit | ((uint32_t)w << 16);
+    }
+    const int rk = 4 * p.bk, rv = 8 * p.bv;
+    const int pos = tile * kCkKeys + r;
+    int64_t sl = -1;
+    if (pos < P0) {
+        sl = p.map.slot(b, h, pos);
+        if (sl < 0 && p.status) atomicOr(p.status, BGTQ_STATUS_PAGE_RANGE);
+    }
+    // raw records into shared memory (the V pair record by the even key)
+    if (sl >= 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.kc + sl * (16 * p.bk));
+        for (int i = 0; i < p.bk; ++i) {
+            const uint4 w4 = src[i];
+            s_rawk[r][4 * i] = w4.x;
+            s_rawk[r][4 * i + 1] = w4.y;
+            s_rawk[r][4 * i + 2] = w4.z;
+            s_rawk[r][4 * i + 3] = w4.w;
+        }
+    } else {
+        for (int i = 0; i < rk; ++i) s_rawk[r][i] = 0u;
+    }
+    s_rawk[r][rk] = 0u;
+    if ((r & 1) == 0) {
+        if (sl >= 0) {
+            const uint4* src = reinterpret_cast<const uint4*>(p.vc + (sl >> 1) * (32 * p.bv));
+            for (int i = 0; i < 2 * p.bv; ++i) {
+                const uint4 w4 = src[i];
+                s_rawv[r >> 1][4 * i] = w4.x;
+                s_rawv[r >> 1][4 * i + 1] = w4.y;
+                s_rawv[r >> 1][4 * i + 2] = w4.z;
+                s_rawv[r >> 1][4 * i + 3] = w4.w;
+            }
+        } else {
+            for (int i = 0; i < rv; ++i) s_rawv[r >> 1][i] = 0u;
+        }
+        s_rawv[r >> 1][rv] = 0u;
+    }
+    __syncthreads();
+    const size_t row = (((size_t)b * p.H + h) * p.pmax + pos);
+    const bool live = sl >= 0;
+    // K row: centroid of codec coordinate jj (codec order)
+    uint4* kdst = reinterpret_cast<uint4*>(p.kh + row * kD);
+#pragma unroll 1
+    for (int c8 = 0; c8 < kD / 8; ++c8) {
+        uint32_t packed[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            __half hv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const uint32_t t = s_ktab[8 * c8 + 2 * e + u];
+                const uint32_t w = t >> 16, bit = t & 0xFFFFu;
+                const uint32_t lo = s_rawk[r][bit >> 5], hi = s_rawk[r][(bit >> 5) + 1];
+                const uint32_t code = __funnelshift_r(lo, hi, bit & 31u) & ((1u << w) - 1u);
+                hv[u] = (w && live) ? s_cent[w * 256 + code] : __float2half_rn(0.0f);
+            }
+            packed[e] = (uint32_t)__half_as_ushort(hv[0]) | ((uint32_t)__half_as_ushort(hv[1]) << 16);
+        }
+        kdst[c8] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    }
+    // V row: dim d holds code_even | code_odd << bV at bit 2 bV d
+    uint4* vdst = reinterpret_cast<uint4*>(p.vh + row * kD);
+    const uint32_t bvv = (uint32_t)p.bv, par_sh = (uint32_t)(r & 1) * bvv;
+#pragma unroll 1
+    for (int c8 = 0; c8 < kD / 8; ++c8) {
+        uint32_t packed[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            __half hv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const uint32_t bit = 2u * bvv * (uint32_t)(8 * c8 + 2 * e + u) + par_sh;
+                const uint32_t lo = s_rawv[r >> 1][bit >> 5], hi = s_rawv[r >> 1][(bit >> 5) + 1];
+                const uint32_t code = __funnelshift_r(lo, hi, bit & 31u) & ((1u << bvv) - 1u);
+                hv[u] = live ? s_cent[bvv * 256 + code] : __float2half_rn(0.0f);
+            }
+            packed[e] = (uint32_t)__half_as_ushort(hv[0]) | ((uint32_t)__half_as_ushort(hv[1]) << 16);
+        }
+        vdst[c8] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    }
+    p.rk[row] = live ? p.kn[sl] : 0.0f;
+    // the odd key of a pair reads the even key's record: same slot / 2
+    p.rv[row] = live ? p.vn[sl] : 0.0f;
+}
+
 __global__ void __launch_bounds__(kCkThreads, 1)
     chunk_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                 const __grid_constant__ CUtensorMap tv, CkParams p) {
+                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tkp,
+                 const __grid_constant__ CUtensorMap tvp, CkParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t s_bar[kCNumBars];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
-    __shared__ __half s_cent[(kWMax + 1) * 256];  // centroids, fp16-exact
-    __shared__ uint32_t s_ktab[kD];               // K code j: bit position | width << 16
     __shared__ uint8_t s_qperm[kD];               // rotated query: source dim of codec index j
     __shared__ float s_qscale[kD];                // dewhiten * sign * 1/sqrt(piece) (0 past n_coded)
     __shared__ float s_vsign[kD];
     __shared__ int s_nh[8];                       // butterfly stage h = 2^i: pairs j < s_nh[i]
-    __shared__ float s_rho[2][2][kCkKeys];        // stage, (key, value) norms of the prefix keys
-    __shared__ uint32_t s_rawk[kCkKeys][kRawK];   // staged K records
-    __shared__ uint32_t s_rawv[kCkKeys / 2][kRawV];
+    __shared__ __align__(16) float s_rho[2][2][kCkKeys];  // stage, (key, value) norms of the prefix keys
 
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -160,8 +265,11 @@ __global__ void __launch_bounds__(kCkThreads, 1)
     const int q0 = qb * kCkRows;
     const int P0 = p.pos_start[b];
     const HeadTab* ht = p.heads + h;
-    // a chunk past the capacity: the append flagged it and wrote nothing
-    if (P0 < 0 || (int64_t)P0 + p.C > p.map.cap) {
+    // a chunk past the capacity (the append flagged it and wrote nothing) or
+    // a prefix past the workspace: zero rows
+    if (P0 < 0 || (int64_t)P0 + p.C > p.map.cap || P0 > p.max_prefix) {
+        if (P0 > p.max_prefix && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && p.status)
+            atomicOr(p.status, BGTQ_STATUS_SEQLEN_CAPACITY);
         if (tid < kCkRows && q0 + tid < p.C) {
             const size_t o = (((size_t)b * p.H * p.G + hq) * p.C + q0 + tid) * kD;
             for (int d = 0; d < kD; ++d) {
@@ -178,31 +286,24 @@ __global__ void __launch_bounds__(kCkThreads, 1)
     volatile int* abort_flag = &s_abort;
 #define CBAR(i) (bar0 + 8u * (uint32_t)(i))
 
-    // ---- set-up: barriers, tensor memory, the head's tables
+    // ---- set-up: barriers, tensor memory, the head's query-rotation tables
     if (tid == 0) {
         s_abort = 0;
-        for (int i = 0; i < kCNumBars; ++i) {
-            const bool many = i == kCQR || i == kCPKF || i == kCPKF + 1 || i == kCPVF || i == kCPVF + 1 || i == kCP;
-            mbar_init(CBAR(i), many ? kCkRows : 1);
-        }
+        for (int i = 0; i < kCNumBars; ++i) mbar_init(CBAR(i), (i == kCQR || i == kCP) ? kCkRows : 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 8) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
                      "r"(512));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
-    for (int i = tid; i < (kWMax + 1) * 256; i += kCkThreads) s_cent[i] = __float2half_rn(p.cent[i]);
     const int n_coded = ht->n_coded;
     for (int j = tid; j < kD; j += kCkThreads) {
-        const int w = j < n_coded ? ht->width[j] : 0;
-        const int bit = w ? ht->pair_bit[j >> 1] + (j & 1) * w : 0;
-        s_ktab[j] = (uint32_t)bit | ((uint32_t)w << 16);
         s_qperm[j] = ht->perm[j];
         s_qscale[j] = j < n_coded ? ht->dewhiten[j] * ht->sign_k[j] * ht->inv_sqrt[j] : 0.0f;
         s_vsign[j] = ht->sign_v[j];
     }
-    if (warp == 9) {
+    if (warp == kTmaWarp) {
         for (int st = 0; st < 7; ++st) {
             int cnt = 0;
             for (int j = lane; j < kD; j += 32) cnt += (j < n_coded && (1 << ht->plog2[j]) > (1 << st)) ? 1 : 0;
@@ -215,78 +316,83 @@ __global__ void __launch_bounds__(kCkThreads, 1)
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
-    if (warp == 9) {
-        // ---- TMA: Q, Q again after the prefix, the chunk's K/V tiles
+    if (warp == kTmaWarp) {
+        // ---- TMA: Q; prefix tiles (decoded rows and their norms); Q again;
+        // the chunk's K/V tiles
         if (lane == 0) {
             const int qrow = (b * p.H * p.G + hq) * p.C + q0;
             const int krow = (b * p.H + h) * p.C;
+            const int prow = (b * p.H + h) * p.pmax;
             mbar_expect_tx(CBAR(kCQ), kCkTile);
             for (int x = 0; x < 2; ++x) tma_load_2d(sbase + kCOffQ + x * kCkBox, &tq, 64 * x, qrow, CBAR(kCQ));
-            bool ok = true;
-            if (np > 0) {
-                ok = mbar_wait(CBAR(kCPSD), 0, abort_flag, p.status);
-                if (ok) {
+            int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
+            int uses[2] = {0, 0};
+            bool q_again = false;
+            for (int j = 0; j < nt; ++j) {
+                const int s = j & 1;
+                const uint32_t par = (uint32_t)((j >> 1) - 1) & 1u;
+                const bool pre = j < np;
+                if (j == np && np > 0) {
+                    if (!mbar_wait(CBAR(kCPSD), 0, abort_flag, p.status)) break;
                     mbar_expect_tx(CBAR(kCQ), kCkTile);
                     for (int x = 0; x < 2; ++x) tma_load_2d(sbase + kCOffQ + x * kCkBox, &tq, 64 * x, qrow, CBAR(kCQ));
+                    q_again = true;
                 }
-            }
-            int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};  // chunk tiles issued per stage (uses - 1)
-            int uses[2] = {0, 0};
-            for (int i = 0; ok && i < nc; ++i) {
-                const int j = np + i, s = j & 1;
-                const uint32_t par = (uint32_t)((j >> 1) - 1) & 1u;
                 if (j >= 2 && !mbar_wait(CBAR(kCKE + s), par, abort_flag, p.status)) break;
                 mbar_expect_tx(CBAR(kCKF + s), kCkTile);
-                for (int x = 0; x < 2; ++x)
-                    tma_load_2d(sbase + kCOffK + s * kCkTile + x * kCkBox, &tk, 64 * x, krow + i * kCkKeys, CBAR(kCKF + s));
+                for (int x = 0; x < 2; ++x) {
+                    if (pre)
+                        tma_load_2d(sbase + kCOffK + s * kCkTile + x * kCkBox, &tkp, 64 * x, prow + j * kCkKeys, CBAR(kCKF + s));
+                    else
+                        tma_load_2d(sbase + kCOffK + s * kCkTile + x * kCkBox, &tk, 64 * x, krow + (j - np) * kCkKeys,
+                                    CBAR(kCKF + s));
+                }
                 last_k[s] = uses[s];
                 if (j >= 2 && !mbar_wait(CBAR(kCVE + s), par, abort_flag, p.status)) break;
-                mbar_expect_tx(CBAR(kCVF + s), kCkTile);
-                for (int x = 0; x < 2; ++x)
-                    tma_load_2d(sbase + kCOffV + s * kCkTile + x * kCkBox, &tv, 64 * x, krow + i * kCkKeys, CBAR(kCVF + s));
+                mbar_expect_tx(CBAR(kCVF + s), kCkTile + (pre ? 2u * kCkKeys * 4u : 0u));
+                for (int x = 0; x < 2; ++x) {
+                    if (pre)
+                        tma_load_2d(sbase + kCOffV + s * kCkTile + x * kCkBox, &tvp, 64 * x, prow + j * kCkKeys, CBAR(kCVF + s));
+                    else
+                        tma_load_2d(sbase + kCOffV + s * kCkTile + x * kCkBox, &tv, 64 * x, krow + (j - np) * kCkKeys,
+                                    CBAR(kCVF + s));
+                }
+                if (pre) {
+                    bulk_copy(smem_u32(&s_rho[s][0][0]), p.rk + (size_t)prow + (size_t)j * kCkKeys, kCkKeys * 4, CBAR(kCVF + s));
+                    bulk_copy(smem_u32(&s_rho[s][1][0]), p.rv + (size_t)prow + (size_t)j * kCkKeys, kCkKeys * 4, CBAR(kCVF + s));
+                }
                 last_v[s] = uses[s];
                 ++uses[s];
             }
             // every copy issued has landed before the CTA ends
-            mbar_wait(CBAR(kCQ), np > 0 ? 1u : 0u, abort_flag, p.status, false);
+            mbar_wait(CBAR(kCQ), q_again ? 1u : 0u, abort_flag, p.status, false);
             for (int s = 0; s < 2; ++s) {
                 if (last_k[s] >= 0) mbar_wait(CBAR(kCKF + s), (uint32_t)last_k[s] & 1u, abort_flag, p.status, false);
                 if (last_v[s] >= 0) mbar_wait(CBAR(kCVF + s), (uint32_t)last_v[s] & 1u, abort_flag, p.status, false);
             }
         }
         __syncwarp();
-    } else if (warp == 8) {
+    } else if (warp == kMmaWarp) {
         // ---- MMA issue
         if (lane == 0) {
             constexpr uint32_t idS = instr_desc(kCkRows, kCkKeys, 0);
             constexpr uint32_t idO = instr_desc(kCkRows, kD, 1);
-            int cnt_pk[2] = {0, 0}, cnt_pv[2] = {0, 0}, cnt_k[2] = {0, 0}, cnt_v[2] = {0, 0};
+            int cnt_k[2] = {0, 0}, cnt_v[2] = {0, 0};
             bool ok = mbar_wait(CBAR(kCQ), 0, abort_flag, p.status);
             if (ok && np > 0) ok = mbar_wait(CBAR(kCQR), 0, abort_flag, p.status);
             auto issue_s = [&](int j) -> bool {
                 const int s = j & 1;
                 const uint32_t ka = sbase + kCOffK + s * kCkTile, d = tmem + 128u * (uint32_t)s;
-                if (j < np) {
-                    if (!mbar_wait(CBAR(kCPKF + s), (uint32_t)(cnt_pk[s]++) & 1u, abort_flag, p.status)) return false;
-                    tc_fence_after();
-#pragma unroll
-                    for (int part = 0; part < 2; ++part) {
-                        const uint32_t qa = sbase + (part ? kCOffQL : kCOffQ);
-#pragma unroll
-                        for (int k = 0; k < kD / 16; ++k) {
-                            const uint32_t off = (uint32_t)(k >> 2) * kCkBox + (uint32_t)(k & 3) * 32;
-                            mma_ss(d, smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), idS, (part | k) ? 1u : 0u);
-                        }
-                    }
-                } else {
-                    if (j == np && np > 0 && !mbar_wait(CBAR(kCQ), 1, abort_flag, p.status)) return false;
-                    if (!mbar_wait(CBAR(kCKF + s), (uint32_t)(cnt_k[s]++) & 1u, abort_flag, p.status)) return false;
-                    tc_fence_after();
-                    const uint32_t qa = sbase + kCOffQ;
+                if (j == np && np > 0 && !mbar_wait(CBAR(kCQ), 1, abort_flag, p.status)) return false;
+                if (!mbar_wait(CBAR(kCKF + s), (uint32_t)(cnt_k[s]++) & 1u, abort_flag, p.status)) return false;
+                tc_fence_after();
+                const int parts = j < np ? 2 : 1;  // the rotated query's hi and lo parts
+                for (int part = 0; part < parts; ++part) {
+                    const uint32_t qa = sbase + (part ? kCOffQL : kCOffQ);
 #pragma unroll
                     for (int k = 0; k < kD / 16; ++k) {
                         const uint32_t off = (uint32_t)(k >> 2) * kCkBox + (uint32_t)(k & 3) * 32;
-                        mma_ss(d, smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), idS, k > 0 ? 1u : 0u);
+                        mma_ss(d, smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), idS, (part | k) ? 1u : 0u);
                     }
                 }
                 mma_commit(CBAR(kCS + s));
@@ -298,18 +404,14 @@ __global__ void __launch_bounds__(kCkThreads, 1)
                 const int s = j & 1;
                 const uint32_t va = sbase + kCOffV + s * kCkTile, pa = tmem + 128u * (uint32_t)s;
                 if (!mbar_wait(CBAR(kCP), (uint32_t)j & 1u, abort_flag, p.status)) return false;
-                if (j < np) {
-                    if (!mbar_wait(CBAR(kCPVF + s), (uint32_t)(cnt_pv[s]++) & 1u, abort_flag, p.status)) return false;
-                } else {
-                    if (!mbar_wait(CBAR(kCVF + s), (uint32_t)(cnt_v[s]++) & 1u, abort_flag, p.status)) return false;
-                }
+                if (!mbar_wait(CBAR(kCVF + s), (uint32_t)(cnt_v[s]++) & 1u, abort_flag, p.status)) return false;
                 tc_fence_after();
                 const int parts = j < np ? 2 : 1;
                 for (int part = 0; part < parts; ++part)
 #pragma unroll
                     for (int k = 0; k < kCkKeys / 16; ++k)
-                        mma_ts(tmem + 256u, pa + 64u * part + 8u * k, smem_desc(va + 2048u * k, kCkBox, 1024), idO,
-                               (j > 0 || part > 0 || k > 0) ? 1u : 0u);
+                        mma_ts(tmem + 256u, pa + 32u * (k >> 1) + 8u * (k & 1) + 16u * part,
+                               smem_desc(va + 2048u * k, kCkBox, 1024), idO, (j > 0 || part > 0 || k > 0) ? 1u : 0u);
                 mma_commit(CBAR(kCO));
                 mma_commit(CBAR(kCVE + s));
                 return true;
@@ -324,109 +426,6 @@ __global__ void __launch_bounds__(kCkThreads, 1)
             mbar_wait(CBAR(kCDrain), 0, abort_flag, p.status, false);
         }
         __syncwarp();
-    } else if (warp >= 4) {
-        // ---- prefix tiles from the packed records: thread r takes key r
-        const int r = tid - 128;
-        const int rk = 4 * p.bk, rv = 8 * p.bv;
-        for (int j = 0; j < np; ++j) {
-            const int s = j & 1;
-            if (j >= 2) {
-                // all four warps leave together (they meet at named barriers below)
-                const uint32_t par = (uint32_t)((j >> 1) - 1) & 1u;
-                const bool got = mbar_wait(CBAR(kCKE + s), par, abort_flag, p.status) &&
-                                 mbar_wait(CBAR(kCVE + s), par, abort_flag, p.status);
-                if (!named_sync_and(2, 128, got)) break;
-            }
-            const int pos = j * kCkKeys + r;
-            int64_t sl = -1;
-            if (pos < P0) {
-                sl = p.map.slot(b, h, pos);
-                if (sl < 0 && p.status) atomicOr(p.status, BGTQ_STATUS_PAGE_RANGE);
-            }
-            // raw records into shared memory (the V pair record by the even key)
-            if (sl >= 0) {
-                const uint4* src = reinterpret_cast<const uint4*>(p.kc + sl * (16 * p.bk));
-                for (int i = 0; i < p.bk; ++i) {
-                    const uint4 w4 = src[i];
-                    s_rawk[r][4 * i] = w4.x;
-                    s_rawk[r][4 * i + 1] = w4.y;
-                    s_rawk[r][4 * i + 2] = w4.z;
-                    s_rawk[r][4 * i + 3] = w4.w;
-                }
-            } else {
-                for (int i = 0; i < rk; ++i) s_rawk[r][i] = 0u;
-            }
-            s_rawk[r][rk] = 0u;
-            if ((r & 1) == 0) {
-                if (sl >= 0) {
-                    const uint4* src = reinterpret_cast<const uint4*>(p.vc + (sl >> 1) * (32 * p.bv));
-                    for (int i = 0; i < 2 * p.bv; ++i) {
-                        const uint4 w4 = src[i];
-                        s_rawv[r >> 1][4 * i] = w4.x;
-                        s_rawv[r >> 1][4 * i + 1] = w4.y;
-                        s_rawv[r >> 1][4 * i + 2] = w4.z;
-                        s_rawv[r >> 1][4 * i + 3] = w4.w;
-                    }
-                } else {
-                    for (int i = 0; i < rv; ++i) s_rawv[r >> 1][i] = 0u;
-                }
-                s_rawv[r >> 1][rv] = 0u;
-            }
-            const float rho_k = sl >= 0 ? p.kn[sl] : 0.0f;
-            // the odd key of a pair reads the even key's record: same slot / 2
-            const float rho_v = sl >= 0 ? p.vn[sl] : 0.0f;
-            named_sync(2, 128);
-            // K row r: centroid of codec coordinate jj, codec order
-            const uint32_t krow = sbase + kCOffK + s * kCkTile;
-#pragma unroll 1
-            for (int c8 = 0; c8 < kD / 8; ++c8) {
-                uint32_t packed[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    __half hv[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const uint32_t t = s_ktab[8 * c8 + 2 * e + u];
-                        const uint32_t w = t >> 16, bit = t & 0xFFFFu;
-                        const uint32_t lo = s_rawk[r][bit >> 5], hi = s_rawk[r][(bit >> 5) + 1];
-                        const uint32_t code = __funnelshift_r(lo, hi, bit & 31u) & ((1u << w) - 1u);
-                        hv[u] = w ? s_cent[w * 256 + code] : __float2half_rn(0.0f);
-                    }
-                    packed[e] = (uint32_t)__half_as_ushort(hv[0]) | ((uint32_t)__half_as_ushort(hv[1]) << 16);
-                }
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(krow + swz_off(r, 8 * c8)), "r"(packed[0]),
-                             "r"(packed[1]), "r"(packed[2]), "r"(packed[3])
-                             : "memory");
-            }
-            // V row r: dim d holds code_even | code_odd << bV at bit 2 bV d
-            const uint32_t vrow = sbase + kCOffV + s * kCkTile;
-            const uint32_t bvv = (uint32_t)p.bv, par_sh = (uint32_t)(r & 1) * bvv;
-#pragma unroll 1
-            for (int c8 = 0; c8 < kD / 8; ++c8) {
-                uint32_t packed[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    __half hv[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const uint32_t bit = 2u * bvv * (uint32_t)(8 * c8 + 2 * e + u) + par_sh;
-                        const uint32_t lo = s_rawv[r >> 1][bit >> 5], hi = s_rawv[r >> 1][(bit >> 5) + 1];
-                        const uint32_t code = __funnelshift_r(lo, hi, bit & 31u) & ((1u << bvv) - 1u);
-                        hv[u] = s_cent[bvv * 256 + code];
-                    }
-                    packed[e] = (uint32_t)__half_as_ushort(hv[0]) | ((uint32_t)__half_as_ushort(hv[1]) << 16);
-                }
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(vrow + swz_off(r, 8 * c8)), "r"(packed[0]),
-                             "r"(packed[1]), "r"(packed[2]), "r"(packed[3])
-                             : "memory");
-            }
-            s_rho[s][0][r] = rho_k;
-            s_rho[s][1][r] = rho_v;
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(CBAR(kCPKF + s));
-            mbar_arrive(CBAR(kCPVF + s));
-            named_sync(2, 128);  // the raw records are read; the next tile may overwrite them
-        }
     } else {
         // ---- softmax: thread r owns row q0 + r of the chunk
         const int r = tid;
@@ -489,34 +488,46 @@ __global__ void __launch_bounds__(kCkThreads, 1)
             const int s = j & 1;
             const uint32_t tS = tmem + lanes + 128u * (uint32_t)s;
             const bool pre = j < np;
+            // a prefix tile's norms arrive with its V tile
             if (!__all_sync(0xffffffffu, mbar_wait(CBAR(kCS + s), (uint32_t)(j >> 1) & 1u, abort_flag, p.status) &&
-                                             (!pre || mbar_wait(CBAR(kCPKF + s), (uint32_t)(j >> 1) & 1u, abort_flag,
+                                             (!pre || mbar_wait(CBAR(kCVF + s), (uint32_t)(j >> 1) & 1u, abort_flag,
                                                                 p.status)))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            // logits of the tile (a whole S row in registers; prefix logits
+            // times the key norms, read four at a time)
+            const int lim = pre ? P0 - 1 - j * kCkKeys                                   // keys past the prefix
+                                : (j == nt - 1 ? min(row, p.C - 1) - (j - np) * kCkKeys  // the chunk's diagonal
+                                               : kCkKeys);
             float sv[kCkKeys];
 #pragma unroll
             for (int q4 = 0; q4 < kCkKeys / 32; ++q4) tmem_ld32(tS + 32 * q4, sv + 32 * q4);
             tmem_wait_ld();
             if (pre) {
-                const int lim = P0 - 1 - j * kCkKeys;  // keys past the prefix
+                const float4* rk4 = reinterpret_cast<const float4*>(&s_rho[s][0][0]);
 #pragma unroll
-                for (int k = 0; k < kCkKeys; ++k) sv[k] = k > lim ? -INFINITY : sv[k] * (s_rho[s][0][k] * q_unscale);
-            } else if (j == nt - 1) {  // the chunk's diagonal tile
-                const int lim = min(row, p.C - 1) - (j - np) * kCkKeys;
+                for (int k4 = 0; k4 < kCkKeys / 4; ++k4) {
+                    const float4 r4 = rk4[k4];
+                    sv[4 * k4] *= r4.x * q_unscale;
+                    sv[4 * k4 + 1] *= r4.y * q_unscale;
+                    sv[4 * k4 + 2] *= r4.z * q_unscale;
+                    sv[4 * k4 + 3] *= r4.w * q_unscale;
+                }
+            }
+            if (lim < kCkKeys - 1) {
 #pragma unroll
                 for (int k = 0; k < kCkKeys; ++k)
                     if (k > lim) sv[k] = -INFINITY;
             }
-            float mx[8];
+            float mxa[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mx[i] = sv[i];
+            for (int i = 0; i < 8; ++i) mxa[i] = sv[i];
 #pragma unroll
-            for (int k = 8; k < kCkKeys; ++k) mx[k & 7] = fmaxf(mx[k & 7], sv[k]);
-            const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * c;
+            for (int k = 8; k < kCkKeys; ++k) mxa[k & 7] = fmaxf(mxa[k & 7], sv[k]);
+            const float mt = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+                                   fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7]))) * c;
             float f = 1.0f;
             bool raise = false;
             if (j == 0) {
@@ -563,36 +574,41 @@ __global__ void __launch_bounds__(kCkThreads, 1)
                     }
                 }
             }
+            // P of each 32-key chunk over that chunk's own 32 columns: hi parts
+            // in its first 16, lo parts (prefix tiles) in the next 16
             float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if (pre) {
-                // keys 64 hf .. 64 hf + 63: hi parts to columns 32 hf, lo parts to 64 + 32 hf
+            const float4* rv4 = reinterpret_cast<const float4*>(&s_rho[s][1][0]);
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t hi[32], lo[32];
+            for (int q4 = 0; q4 < kCkKeys / 32; ++q4) {
+                uint32_t hi[16], lo[16];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int k = 64 * hf + 2 * i;
-                        const float p0 = ex2(fmaf(sv[k], c, -m)), p1 = ex2(fmaf(sv[k + 1], c, -m));
-                        ls[i & 3] += p0 + p1;
-                        const float a = p0 * (s_rho[s][1][k] * kPvScale), bq = p1 * (s_rho[s][1][k + 1] * kPvScale);
-                        const __half ha = __float2half_rn(a), hb = __float2half_rn(bq);
-                        const __half la = __float2half_rn(a - __half2float(ha)), lb = __float2half_rn(bq - __half2float(hb));
-                        hi[i] = (uint32_t)__half_as_ushort(ha) | ((uint32_t)__half_as_ushort(hb) << 16);
-                        lo[i] = (uint32_t)__half_as_ushort(la) | ((uint32_t)__half_as_ushort(lb) << 16);
+                for (int i2 = 0; i2 < 8; ++i2) {
+                    const int k = 32 * q4 + 4 * i2;
+                    float pv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        pv[e] = ex2(fmaf(sv[k + e], c, -m));
+                        ls[e] += pv[e];
                     }
-                    tmem_st32(tS + 32 * hf, hi);
-                    tmem_st32(tS + 64 + 32 * hf, lo);
-                }
-            } else {
-                uint32_t pk[kCkKeys / 2];
+                    if (pre) {
+                        const float4 r4 = rv4[k / 4];
+                        const float a[4] = {pv[0] * (r4.x * kPvScale), pv[1] * (r4.y * kPvScale), pv[2] * (r4.z * kPvScale),
+                                            pv[3] * (r4.w * kPvScale)};
 #pragma unroll
-                for (int i = 0; i < kCkKeys / 2; ++i) {
-                    const float p0 = ex2(fmaf(sv[2 * i], c, -m)), p1 = ex2(fmaf(sv[2 * i + 1], c, -m));
-                    ls[i & 3] += p0 + p1;
-                    pk[i] = pack_h2(p0, p1);
+                        for (int e2 = 0; e2 < 2; ++e2) {
+                            const __half ha = __float2half_rn(a[2 * e2]), hb = __float2half_rn(a[2 * e2 + 1]);
+                            const __half la = __float2half_rn(a[2 * e2] - __half2float(ha));
+                            const __half lb = __float2half_rn(a[2 * e2 + 1] - __half2float(hb));
+                            hi[2 * i2 + e2] = (uint32_t)__half_as_ushort(ha) | ((uint32_t)__half_as_ushort(hb) << 16);
+                            lo[2 * i2 + e2] = (uint32_t)__half_as_ushort(la) | ((uint32_t)__half_as_ushort(lb) << 16);
+                        }
+                    } else {
+                        hi[2 * i2] = pack_h2(pv[0], pv[1]);
+                        hi[2 * i2 + 1] = pack_h2(pv[2], pv[3]);
+                    }
                 }
-                tmem_st32(tS, pk);
-                tmem_st32(tS + 32, pk + 32);
+                tmem_st16(tS + 32 * q4, hi);
+                if (pre) tmem_st16(tS + 32 * q4 + 16, lo);
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             tmem_wait_st();
@@ -629,7 +645,7 @@ __global__ void __launch_bounds__(kCkThreads, 1)
 #undef CBAR
     tc_fence_before();
     __syncthreads();
-    if (warp == 8) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
     }
@@ -650,18 +666,28 @@ bool chunk_descriptors_valid() {
     return true;
 }
 
+int64_t chunk_pmax(int64_t max_prefix) { return (max_prefix + kCkKeys - 1) / kCkKeys * kCkKeys; }
+
 }  // namespace
 
+size_t prefill_chunk_workspace_bytes(const bgtq_plan& pl, int batch, int64_t max_prefix) {
+    const size_t rows = (size_t)batch * pl.H * (size_t)chunk_pmax(max_prefix);
+    return rows * (2 * kD * sizeof(__half) + 2 * sizeof(float));
+}
+
 cudaError_t launch_prefill_chunk(const bgtq_plan& pl, cudaStream_t s, const void* q, const void* k, const void* v,
-                                 int batch, int c, const int32_t* pos_start, const bgtq_cache& cache, void* out,
-                                 int out_dtype, float scale, int32_t* status) {
+                                 int batch, int c, const int32_t* pos_start, int64_t max_prefix, const bgtq_cache& cache,
+                                 void* out, int out_dtype, float scale, void* ws, int32_t* status) {
     static std::mutex mu;
     static bool done[64] = {false};
     static const bool desc_ok = chunk_descriptors_valid();
     if (!desc_ok) return cudaErrorInvalidValue;
+    const int64_t pmax = chunk_pmax(max_prefix);
     const uint64_t q_rows = (uint64_t)batch * pl.H * pl.G * (uint64_t)c;
+    const uint64_t p_rows = (uint64_t)batch * pl.H * (uint64_t)pmax;
     const int nqb = (c + kCkRows - 1) / kCkRows;
-    if (q_rows + kCkRows >= (1ull << 31) || nqb > 65535 || (uint64_t)batch * pl.H * pl.G >= (1ull << 31))
+    if (q_rows + kCkRows >= (1ull << 31) || p_rows + kCkKeys >= (1ull << 31) || nqb > 65535 ||
+        (uint64_t)batch * pl.H * pl.G >= (1ull << 31) || pmax / kCkKeys > 0x7fffffff)
         return cudaErrorInvalidValue;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -674,10 +700,6 @@ cudaError_t launch_prefill_chunk(const bgtq_plan& pl, cudaStream_t s, const void
             done[dev] = true;
         }
     }
-    alignas(64) CUtensorMap tq, tk, tv;
-    if (!rows_map(&tq, q, q_rows, kCkRows) || !rows_map(&tk, k, (uint64_t)batch * pl.H * c, kCkKeys) ||
-        !rows_map(&tv, v, (uint64_t)batch * pl.H * c, kCkKeys))
-        return cudaErrorInvalidValue;
     CkParams p;
     p.q = static_cast<const __half*>(q);
     p.k = static_cast<const __half*>(k);
@@ -689,6 +711,13 @@ cudaError_t launch_prefill_chunk(const bgtq_plan& pl, cudaStream_t s, const void
     p.G = pl.G;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.pos_start = pos_start;
+    p.max_prefix = (int)max_prefix;
+    p.pmax = (int)pmax;
+    char* w = static_cast<char*>(ws);
+    p.kh = reinterpret_cast<__half*>(w);
+    p.vh = reinterpret_cast<__half*>(w + p_rows * kD * sizeof(__half));
+    p.rk = reinterpret_cast<float*>(w + 2 * p_rows * kD * sizeof(__half));
+    p.rv = p.rk + p_rows;
     p.kc = static_cast<const uint8_t*>(cache.k_codes);
     p.kn = cache.k_norm;
     p.vc = static_cast<const uint8_t*>(cache.v_codes);
@@ -699,8 +728,22 @@ cudaError_t launch_prefill_chunk(const bgtq_plan& pl, cudaStream_t s, const void
     p.bk = pl.bk;
     p.bv = pl.bv;
     p.status = status;
+    alignas(64) CUtensorMap tq, tk, tv, tkp, tvp;
+    if (!rows_map(&tq, q, q_rows, kCkRows) || !rows_map(&tk, k, (uint64_t)batch * pl.H * c, kCkKeys) ||
+        !rows_map(&tv, v, (uint64_t)batch * pl.H * c, kCkKeys))
+        return cudaErrorInvalidValue;
+    if (pmax > 0) {
+        if (!rows_map(&tkp, p.kh, p_rows, kCkKeys) || !rows_map(&tvp, p.vh, p_rows, kCkKeys)) return cudaErrorInvalidValue;
+        const dim3 dgrid((unsigned)(pmax / kCkKeys), (unsigned)pl.H, (unsigned)batch);
+        chunk_prefix_decode_kernel<<<dgrid, kCkKeys, 0, s>>>(p);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    } else {
+        tkp = tk;  // no prefix tiles: never read
+        tvp = tv;
+    }
     const dim3 grid((unsigned)((uint64_t)batch * pl.H * pl.G), (unsigned)nqb, 1);
-    chunk_kernel<<<grid, kCkThreads, kCkSmem, s>>>(tq, tk, tv, p);
+    chunk_kernel<<<grid, kCkThreads, kCkSmem, s>>>(tq, tk, tv, tkp, tvp, p);
     return cudaGetLastError();
 }
 

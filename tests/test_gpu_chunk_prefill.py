@@ -72,8 +72,9 @@ def run_chunk(plan, cache, li, p0s, C, q, out_dtype=torch.float32):
     vc = np.stack([l.v[:, p0:p0 + C] for l, p0 in zip(li, p0s)])
     out = torch.full(q.shape, float("nan"), dtype=out_dtype, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(bg.bgtq_prefill_chunk_workspace(plan, B, max(p0s)) + 1, dtype=torch.uint8, device="cuda")
     bg.bgtq_prefill_chunk_attn(plan, dev(q), dev(np.ascontiguousarray(kc)), dev(np.ascontiguousarray(vc)),
-                               dev(np.asarray(p0s, np.int32)), cache, out, status=st)
+                               dev(np.asarray(p0s, np.int32)), cache, out, max_prefix=max(p0s), workspace=ws, status=st)
     torch.cuda.synchronize()
     return out.float().cpu().numpy().astype(np.float64), int(st.item())
 
@@ -148,8 +149,24 @@ def test_a_chunk_past_the_capacity_is_skipped_and_flagged():
     out = torch.full(q.shape, 7.0, dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     bg.bgtq_prefill_chunk_attn(plan, dev(q), dev(li[0].k[None, :, :C]), dev(li[0].v[None, :, :C]),
-                               dev(np.array([190], np.int32)), cache, out, status=st)
+                               dev(np.array([190], np.int32)), cache, out, max_prefix=190, status=st)
     torch.cuda.synchronize()
     assert st.item() & 1
     assert torch.count_nonzero(out) == 0
     assert torch.count_nonzero(cache.k_norm) == 0
+
+
+def test_a_prefix_past_max_prefix_is_flagged():
+    H, G, C, P0 = 1, 2, 32, 300
+    li, plan, heads = build(6, H, G, P0 + C)
+    cache = new_cache(plan, 1, P0 + C)
+    bg.bgtq_quantize_append(plan, dev(li[0].k[None, :, :P0]), dev(li[0].v[None, :, :P0]), dev(np.array([0], np.int32)),
+                            cache)
+    q = chunk_queries([type("L", (), {"k": li[0].k[:, P0:]})()], G, C, 13)
+    out = torch.full(q.shape, 7.0, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bg.bgtq_prefill_chunk_attn(plan, dev(q), dev(li[0].k[None, :, P0:]), dev(li[0].v[None, :, P0:]),
+                               dev(np.array([P0], np.int32)), cache, out, max_prefix=256, status=st)
+    torch.cuda.synchronize()
+    assert st.item() & 2
+    assert torch.count_nonzero(out) == 0

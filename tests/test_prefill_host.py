@@ -45,15 +45,23 @@ def test_bad_arguments_are_rejected(kw, code, frag):
     assert rc == code and frag in msg, (rc, msg)
 
 
-def chunk_call(t=100, batch=1, q=BASE, out=BASE, pos=BASE, recent=0, capacity=128):
+def chunk_call(t=100, batch=1, q=BASE, out=BASE, pos=BASE, recent=0, capacity=128, max_prefix=16, ws=BASE,
+               ws_bytes=1 << 30):
     plan = bg.bgtq_plan_create(np.full((2, 64), 3, np.uint8), np.ones((2, 64)), 4, 384, 3, 1, host_only=True)
     desc = bg._native.BgtqCache(BASE, BASE, BASE, BASE, capacity)
     if recent:
         desc.k_recent = BASE
         desc.recent = recent
-    rc = bg.lib().bgtq_prefill_chunk_attn(plan.handle, None, q, BASE, BASE, batch, t, pos, ctypes.byref(desc), out, 0,
-                                          0.088, None)
+    rc = bg.lib().bgtq_prefill_chunk_attn(plan.handle, None, q, BASE, BASE, batch, t, pos, max_prefix,
+                                          ctypes.byref(desc), out, 0, 0.088, ws, ws_bytes, None)
     return rc, bg.lib().bgtq_last_error().decode()
+
+
+def test_chunk_workspace_size():
+    plan = bg.bgtq_plan_create(np.full((2, 64), 3, np.uint8), np.ones((2, 64)), 4, 384, 3, 1, host_only=True)
+    # (512 + 8) bytes per (sequence, KV head, position up to max_prefix rounded up to 128)
+    assert bg.bgtq_prefill_chunk_workspace(plan, 3, 300) == 3 * 2 * 384 * 520
+    assert bg.bgtq_prefill_chunk_workspace(plan, 1, 0) == 0
 
 
 def test_chunk_valid_arguments_reach_the_plan_check():
@@ -67,6 +75,10 @@ def test_chunk_valid_arguments_reach_the_plan_check():
     (dict(q=BASE + 8), -1, "16-byte aligned"),
     (dict(out=BASE + 8), -1, "16-byte aligned"),
     (dict(recent=16), -2, "recent-key"),
+    (dict(max_prefix=200), -3, "max_prefix"),
+    (dict(max_prefix=-1), -1, "max_prefix"),
+    (dict(ws_bytes=100), -4, "workspace"),
+    (dict(ws=BASE + 64), -1, "256-byte"),
 ])
 def test_chunk_bad_arguments_are_rejected(kw, code, frag):
     rc, msg = chunk_call(**kw)
