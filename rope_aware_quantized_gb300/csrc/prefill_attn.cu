@@ -10,11 +10,13 @@
 // future work on the LogQuant page (section "중요성 및 주장").
 //
 // One CTA takes 128 query rows of two query heads that share a KV head, so
-// that both attend the same K/V tiles; 10 warps:
+// that both attend the same K/V tiles; 12 warps:
 //   warps 0-3, 4-7  softmax warpgroups: thread i of warpgroup g owns row i of
 //                   query head g, which is lane i of tensor memory
 //   warp 8          issues the MMAs (one thread) and owns the tensor memory
 //   warp 9          issues the TMA copies (one thread)
+//   warps 10-11     encode the packed records of a share of the block's
+//                   positions while the others attend
 // Tensor memory, 512 columns of fp32: S_g = Q_g K^T at columns 128 g, the
 // output accumulator O_g at 256 + 128 g.  The softmax writes P_g (fp16, two
 // per column) over the first 64 columns of S_g and O_g += P_g V reads its A
@@ -27,9 +29,9 @@
 // softmax is online in the log2 domain; a row's running maximum is raised
 // (and its O rescaled in tensor memory) only when a tile's maximum exceeds
 // it by more than kHeadroom, so a probability never exceeds 2^kHeadroom.
-// The CTAs of the first pair of query heads of each KV head also encode the
-// keys and values of their 128 positions, with the warp encoder steps of the
-// append kernel (records bit-identical to an append of the same tokens).
+// The records of a block's 128 positions are encoded, with the warp encoder
+// steps of the append kernel (bit-identical to an append of the same tokens),
+// by the encoder warps of the KV head's CTAs of that block, an even share each.
 // Every wait is bounded: after kWaitNs it sets BGTQ_STATUS_TIMEOUT, the CTA
 // skips the rest of its work, lets its copies and MMAs land and frees its
 // tensor memory.
@@ -48,8 +50,9 @@ namespace {
 
 constexpr int kTcRows = 128;                      // query rows per warpgroup (tensor-memory lanes)
 constexpr int kTcKeys = 128;                      // keys per tile
-constexpr int kTcThreads = 320;                   // two softmax warpgroups, the MMA warp, the TMA warp
-constexpr int kEncWarps = 8;                      // warps that encode the block's records
+constexpr int kTcThreads = 384;                   // two softmax warpgroups, the MMA warp, the TMA warp, 2 encoder warps
+constexpr int kEncWarps = 2;                      // warps that encode records alongside the attention
+constexpr int kEncWarp0 = 10;
 constexpr uint32_t kTcTile = kTcRows * kD * 2;    // one 128 x 128 fp16 tile: 32 KB
 constexpr uint32_t kTcBox = kTcTile / 2;          // one 64-column box of it (128 rows x 128 B)
 constexpr uint32_t kOffQ = 0;                     // Q_g at + g kTcTile
@@ -330,15 +333,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_wait(BAR(kBarDrain), 0, abort_flag, p.status, false);
         }
         __syncwarp();
-    } else {
-        // ---- softmax warpgroups (and the record encoder)
-        const int g = warp >> 2;
-        if (pair == 0) {
-            stage_thresholds(s_thr, p.thr, tid, kEncWarps * 32);
+    } else if (warp >= kEncWarp0) {
+        // ---- record encoder: the block's 128 positions are shared out over
+        // the CTAs of the KV head's query-head pairs (an even share each, so a
+        // V pair record is never split); encoded while the others attend
+        const int n = min(kTcRows, p.T - q0);
+        const int share = ((n + npair - 1) / npair + 1) & ~1;
+        const int e0 = pair * share, e1 = min(n, e0 + share);
+        if (e0 < e1) {
+            const int ew = warp - kEncWarp0;
+            stage_thresholds(s_thr, p.thr, tid - kEncWarp0 * 32, kEncWarps * 32);
             asm volatile("bar.sync 1, %0;" ::"n"(kEncWarps * 32) : "memory");
-            encode_block(p, b, h, q0, min(kTcRows, p.T - q0), 0, p.T, s_thr, s_rec[warp], s_vmask[warp], warp, lane,
-                         kEncWarps);
+            encode_block(p, b, h, q0 + e0, e1 - e0, 0, p.T, s_thr, s_rec[ew], s_vmask[ew], ew, lane, kEncWarps);
         }
+    } else {
+        // ---- softmax warpgroups
+        const int g = warp >> 2;
         if (g < ng)
             softmax_rows(p, tmem, g, b, hq0 + g, q0, nkt, BAR(kBarS + g), BAR(kBarP + g), BAR(kBarO + g), abort_flag, warp,
                          lane);
