@@ -179,10 +179,11 @@ cudaError_t launch_decode(const bgtq_plan& pl, cudaStream_t s, const void* q, co
     p.recent = c.recent;
     dim3 grid((unsigned)sp.n_split, (unsigned)pl.H, (unsigned)batch);
     // the fast instances decode codes of width >= 4 only in each lane's
-    // kFastWide widest slots; the general instance in any slot
+    // kFastWide widest slots; the general instance in any slot, and it takes
+    // a recent-key window longer than kWinPre
     bool any_wide = false;
     for (const HeadTab& ht : pl.heads) any_wide |= ht.n_wide > kFastWide;
-    const int kind = any_wide ? 2 : (c.recent > 0 ? 1 : 0);
+    const int kind = any_wide ? 2 : (c.recent > 0 ? (c.recent <= kWinPre ? 1 : 2) : 0);
     if (c.page_table) return launch_decode_paged(p, grid, s, kind, pl.bk, pl.bv);
     const int key = pl.bk * 10 + pl.bv;
     switch (key) {

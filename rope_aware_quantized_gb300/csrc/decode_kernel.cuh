@@ -97,6 +97,7 @@ constexpr int kTile = 16;         // tokens per warp iteration; splits start on 
 constexpr int kCluster = 8;       // CTAs per thread-block cluster (consecutive splits of one head)
 constexpr int kMaxClusters = 64;  // clusters per (sequence, head)
 constexpr int64_t kMaxSplitTokens = 4096;  // longest token split of one CTA
+constexpr int kWinPre = 256;               // longest fp16 key window of the precomputed-logit instance (1)
 constexpr int kMaxTilesPerWarp = (int)(kMaxSplitTokens / (kWarps * 16));  // 16-token tiles of one warp
 constexpr int kPartStride = 2 + kD;  // m, l, acc[128] per query head
 // leading slots (width order 0, 8, 1, 9, ...) that may hold codes of width >= 4
@@ -442,14 +443,17 @@ struct BoolTag {
 };
 
 // Instances (kKind): 0 = fast (slots 0 and 8 alone may hold codes wider
-// than the pair tables; no recent-key buffer), 1 = fast with the fp16
-// recent-key buffer, 2 = general (any slot wide) with the buffer; kPaged:
+// than the pair tables; no recent-key buffer), 1 = fast with an fp16
+// recent-key buffer of at most kWinPre keys (their exact logits computed
+// ahead of the main loop), 2 = general (any slot wide, any buffer); kPaged:
 // the cache is paged.  The buffer and paging paths are separate instances
 // so that the instances without them carry none of their code.
 template <int BK, int BV, int kKind, bool kPaged>
 __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) {
     constexpr int NW = kKind == 2 ? 16 : kFastWide;  // leading slots that may hold codes of width >= 4
-    constexpr bool kWinPath = kKind >= 1;
+    constexpr bool kWinPath = kKind >= 1;  // fp16 recent-key buffer supported
+    constexpr bool kWinPre1 = kKind == 1;  // its logits computed ahead (window <= kWinPre)
+    constexpr bool kWinLoop = kKind == 2;  // its tiles in a second loop
     extern __shared__ __align__(16) uint8_t dsmem[];
     uint32_t* s_tab = reinterpret_cast<uint32_t*>(dsmem);
     float (*s_q)[kD] = reinterpret_cast<float (*)[kD]>(dsmem + p.img_bytes);
@@ -459,6 +463,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     __shared__ float s_thr[kThrCompact];                 // fused step: encoder thresholds
     __shared__ uint32_t s_enc[3][8 * kPairMaxW];          // fused step: records being assembled
     __shared__ uint2 s_qo[8][32];                         // recent-key buffer: A fragments of q as given
+    __shared__ float s_wlog[kWinPre1 ? 8 : 1][kWinPre1 ? kWinPre : 1];  // instance 1: exact window logits (log2 domain)
     __shared__ int64_t s_pslot[kPaged ? kWarps : 1][kPaged ? kMaxTilesPerWarp : 1];  // paged: tile slots
     // after the main loop the table region holds the per-warp partials of
     // the 8 query heads (m, l, acc[128]) that the cluster reads
@@ -540,6 +545,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     const int t_begin = !active ? seq : split == 0 ? a0 : max(0, a0 - split * p.tps);
     const int t_end = !active ? seq : split == 0 ? seq : a0 - (split - 1) * p.tps;
     const int wstart = p.recent > 0 ? max(0, seq - (int)p.recent) : seq;  // first position of the fp16 keys
+    const int wlo = max(t_begin, wstart);  // the range's first window token (instance 1: s_wlog column 0)
     // record bases: the (sequence, head) row of a contiguous cache (token
     // slot = position), the pools of a paged one (token slot per tile)
     constexpr bool paged = kPaged;
@@ -662,6 +668,54 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         atomicOr(p.status, BGTQ_STATUS_APPEND_CAPACITY);
         debug_in_range(false, p.status);  // a new position past the capacity
     }
+    // instance 1: the exact logits (q as given . k, on the tensor cores) of
+    // the range's window tokens (at most kWinPre), all their key loads in
+    // flight at once; the main loop takes them from shared memory.  Warps
+    // w0, w0 + stride, ... take the 8-token groups w0, w0 + stride, ...; the
+    // new token's key is read as given (its ring slot is being written).
+    const bool win_pre = kWinPre1 && p.recent > 0 && active && t_end > wstart;
+    auto window_logits = [&](int w0, int stride) {
+        const __half* qh = p.q + ((size_t)b * p.H * G + (size_t)h * G) * kD;
+        uint2 qo[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint32_t* qw = reinterpret_cast<const uint32_t*>(qh + (size_t)min(g, G - 1) * kD + 16 * c + 2 * t);
+            qo[c] = g < G ? make_uint2(__ldg(qw), __ldg(qw + 4)) : make_uint2(0u, 0u);
+        }
+        const int nwt = min(t_end - wlo, kWinPre);
+        // four 8-token groups per round, their key loads issued together
+        for (int g0 = w0; 8 * g0 < nwt; g0 += 4 * stride) {
+            uint32_t kb[4][8][2];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int tk = min(wlo + 8 * (g0 + u * stride) + g, seq - 1);
+                const __half* krow = (p.k_new != nullptr && tk == pos)
+                                         ? p.k_new + unit * kD
+                                         : p.k_recent + (unit * (size_t)p.recent + (size_t)(tk % p.recent)) * kD;
+                const uint32_t* kr = reinterpret_cast<const uint32_t*>(krow + 2 * t);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    kb[u][c][0] = __ldcg(kr + 8 * c);
+                    kb[u][c][1] = __ldcg(kr + 8 * c + 4);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int grp = g0 + u * stride;
+                float s16[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t af[4] = {qo[c].x, 0u, qo[c].y, 0u};
+                    mma16816(s16, af, kb[u][c][0], kb[u][c][1]);
+                }
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int col = 8 * grp + 2 * t + e;
+                    if (col < nwt) s_wlog[g][col] = s16[e] * p.scale_log2;
+                }
+            }
+        }
+    };
     if (owner) {
         int64_t sl;
         if constexpr (kPaged) {
@@ -670,7 +724,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         } else {
             sl = p.map.slot(b, h, pos);
         }
-        if (sl >= 0) append_new_token<BK, BV>(p, el, unit, sl, pos, s_thr, s_enc, warp, lane);
+        if (sl >= 0) append_new_token<BK, BV>(p, el, unit, sl, pos, s_thr, s_enc, warp, lane);  // warps 0, 1
+        if (win_pre && warp >= 2) window_logits(warp - 2, kWarps - 2);
         __syncthreads();  // the new token's records are written before any warp stages them
     }
     // the first kStages - 1 tiles of every warp are copied while the queries
@@ -737,7 +792,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
         // fp16 recent-key buffer: the query heads as given (fp16) as mma A
         // fragments, rows 0..7 = heads (rows 8..15 zero), k-chunk c = dims
         // 16c..16c+15; warp w builds chunks 2w, 2w + 1
-        if (kWinPath && p.recent > 0 && t_end > wstart) {
+        if (kWinLoop && p.recent > 0 && t_end > wstart) {
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 const int c = 2 * warp + k;
@@ -746,6 +801,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
             }
         }
         __syncthreads();  // s_q, s_qunscale, the table image (and a fused step's new token) are complete
+        if (win_pre && !owner) {  // (the appending CTA computed them during its append)
+            window_logits(warp, kWarps);
+            __syncthreads();
+        }
     }
     const float q_unscale = s_qunscale[g];
     uint32_t qa[8][4];
@@ -808,7 +867,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int tok = T0 + 8 * nt + 2 * t + e;
-                const float v = (sacc[nt][e] + sacc[nt][2 + e]) * (tr.rk[nt][e] * q_unscale);
+                float v = (sacc[nt][e] + sacc[nt][2 + e]) * (tr.rk[nt][e] * q_unscale);
+                if constexpr (kWinPre1) {
+                    if (tok >= wstart && tok < t_end) v = s_wlog[g][(tok - wlo) & (kWinPre - 1)];
+                }
                 lg[nt][e] = tok < t_end ? v : -INFINITY;
             }
         if constexpr (kWin) {
@@ -897,12 +959,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(DecodeParams p) 
     // the tiles that reach into the fp16 recent-key buffer are the warp's
     // last few; the loop over the others carries no trace of the buffer
     int n_fast = n_tiles;
-    if (kWinPath && p.recent > 0) {
+    if (kWinLoop && p.recent > 0) {
         const int d = wstart - kTile - T0w;
         n_fast = d < 0 ? 0 : min(n_tiles, d / kStep + 1);
     }
     for (int k = 0; k < n_fast; ++k) step(k, BoolTag<false>{});
-    if constexpr (kWinPath)
+    if constexpr (kWinLoop)
         for (int k = n_fast; k < n_tiles; ++k) step(k, BoolTag<true>{});
     cp_async_wait<0>();
     }  // active
