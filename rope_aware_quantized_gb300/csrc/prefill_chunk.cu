@@ -23,10 +23,11 @@
 // products keep about 22 bits, as in the decode path; each rotated query row
 // is first scaled by a power of two to below 2^14, undone on its logits.
 //
-// Attention: one CTA takes 128 rows of one query head; 6 warps:
-//   warps 0-3  softmax (thread i = row i = tensor-memory lane i)
-//   warp 4     MMA issue (one thread), owner of the tensor memory
-//   warp 5     TMA: Q (again after the prefix, the rotated query having taken
+// Attention: one CTA takes 128 rows of one query head; 10 warps:
+//   warps 0-3, 4-7  softmax warpgroups on the same rows (thread i = row i =
+//              tensor-memory lane i), each taking 64 of a tile's 128 keys
+//   warp 8     MMA issue (one thread), owner of the tensor memory
+//   warp 9     TMA: Q (again after the prefix, the rotated query having taken
 //              its place), the prefix tiles and norms, the chunk's K/V tiles
 // Tensor memory: S in two buffers (columns 0 and 128), O at 256; P
 // overwrites the S it came from, 32 keys per 32 columns: the hi parts of the
@@ -47,7 +48,7 @@ namespace {
 
 constexpr int kCkRows = 128;
 constexpr int kCkKeys = 128;
-constexpr int kCkThreads = 192;
+constexpr int kCkThreads = 320;
 constexpr uint32_t kCkTile = 128 * kD * 2;  // 32 KB
 constexpr uint32_t kCkBox = kCkTile / 2;
 constexpr uint32_t kCOffQ = 0;              // Q, or the rotated query's hi part
@@ -57,7 +58,7 @@ constexpr uint32_t kCOffV = 4 * kCkTile;    // V stage s at + s kCkTile
 constexpr uint32_t kCkSmem = 6 * kCkTile + 1024;
 constexpr int kRawK = 4 * 3 + 1;            // words of a staged K record (bK <= 3) + a zero word
 constexpr int kRawV = 8 * 4 + 1;            // words of a staged V pair record (bV <= 4) + a zero word
-constexpr int kMmaWarp = 4, kTmaWarp = 5;
+constexpr int kMmaWarp = 8, kTmaWarp = 9;
 constexpr float kHeadroomC = 8.0f;
 constexpr float kPvScale = 1.0f / 256.0f;   // prefix probabilities * rho_v are stored scaled by this
 
@@ -115,6 +116,18 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+// barrier over n threads that also ANDs a predicate across them
+__device__ __forceinline__ bool named_sync_and(int id, int n, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
 }
 
 // Unnormalised butterflies over 128 values in registers; stage h acts on the
@@ -254,6 +267,9 @@ __global__ void __launch_bounds__(kCkThreads, 1)
     __shared__ float s_vsign[kD];
     __shared__ int s_nh[8];                       // butterfly stage h = 2^i: pairs j < s_nh[i]
     __shared__ __align__(16) float s_rho[2][2][kCkKeys];  // stage, (key, value) norms of the prefix keys
+    __shared__ float s_mx[2][2][kCkRows];                 // row maxima of each warpgroup's half (tile parity)
+    __shared__ float s_lsum[2][kCkRows];                  // row sums of each warpgroup's half
+    __shared__ float s_qun[kCkRows];                      // the rotated query rows' power-of-two scaling
 
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -289,7 +305,7 @@ __global__ void __launch_bounds__(kCkThreads, 1)
     // ---- set-up: barriers, tensor memory, the head's query-rotation tables
     if (tid == 0) {
         s_abort = 0;
-        for (int i = 0; i < kCNumBars; ++i) mbar_init(CBAR(i), (i == kCQR || i == kCP) ? kCkRows : 1);
+        for (int i = 0; i < kCNumBars; ++i) mbar_init(CBAR(i), i == kCQR ? kCkRows : i == kCP ? 2 * kCkRows : 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == kMmaWarp) {
@@ -427,88 +443,99 @@ __global__ void __launch_bounds__(kCkThreads, 1)
         }
         __syncwarp();
     } else {
-        // ---- softmax: thread r owns row q0 + r of the chunk
-        const int r = tid;
+        // ---- softmax: two warpgroups on the same rows; warpgroup hw takes
+        // keys 64 hw .. 64 hw + 63 of every tile, thread r of each row q0 + r
+        // of the chunk.  They exchange row maxima (and, at the end, row sums)
+        // through shared memory and take every go/stop decision together at
+        // named barrier 1 (an AND over both), so neither can be left waiting.
+        const int hw = warp >> 2;
+        const int r = tid & (kCkRows - 1);
         const int row = q0 + r;  // chunk-local
-        const uint32_t lanes = (uint32_t)(32 * warp) << 16;
+        const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
         const float c = p.scale_log2;
         float q_unscale = 1.0f;  // prefix logits: times this power of two (the rotated query's scaling)
-        bool ok = __all_sync(0xffffffffu, mbar_wait(CBAR(kCQ), 0, abort_flag, p.status));
+        bool ok = named_sync_and(1, 2 * kCkRows, mbar_wait(CBAR(kCQ), 0, abort_flag, p.status));
         if (ok && np > 0) {
-            // the rotated query q'' (codec order), split into fp16 hi + lo, over Q
-            float x[kD];
-            const uint8_t* qs = smem_raw + (sbase - smem_u32(smem_raw)) + kCOffQ;
-#pragma unroll
-            for (int j = 0; j < kD; ++j) {
-                const float qv = __half2float(*reinterpret_cast<const __half*>(qs + swz_off(r, s_qperm[j] & (kD - 1))));
-                x[j] = qv * s_qscale[j];
-            }
-            int nh[7];
-#pragma unroll
-            for (int st = 0; st < 7; ++st) nh[st] = s_nh[st];
-            butterflies128<false>(x, nh);
-            // the row scaled by a power of two to below 2^14 (the de-whitened
-            // query can leave the fp16 range); the logits take it back exactly
-            float amax = 0.0f;
-#pragma unroll
-            for (int j = 0; j < kD; ++j) amax = fmaxf(amax, fabsf(x[j]));
-            if (amax > 0.0f) {
-                int e2 = 0;
-                frexpf(amax, &e2);  // amax = f 2^e2, f in [0.5, 1)
-                const float up = ldexpf(1.0f, 14 - e2);
-                q_unscale = ldexpf(1.0f, e2 - 14);
-#pragma unroll
-                for (int j = 0; j < kD; ++j) x[j] *= up;
-            }
-#pragma unroll
-            for (int c8 = 0; c8 < kD / 8; ++c8) {
-                uint32_t hp[4], lp[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const __half h0 = __float2half_rn(x[8 * c8 + 2 * e]), h1 = __float2half_rn(x[8 * c8 + 2 * e + 1]);
-                    const __half l0 = __float2half_rn(x[8 * c8 + 2 * e] - __half2float(h0));
-                    const __half l1 = __float2half_rn(x[8 * c8 + 2 * e + 1] - __half2float(h1));
-                    hp[e] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
-                    lp[e] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+            if (hw == 0) {
+                // the rotated query q'' (codec order), split into fp16 hi + lo, over Q
+                float x[kD];
+                const uint8_t* qs = smem_raw + (sbase - smem_u32(smem_raw)) + kCOffQ;
+    #pragma unroll
+                for (int j = 0; j < kD; ++j) {
+                    const float qv = __half2float(*reinterpret_cast<const __half*>(qs + swz_off(r, s_qperm[j] & (kD - 1))));
+                    x[j] = qv * s_qscale[j];
                 }
-                const uint32_t off = swz_off(r, 8 * c8);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + kCOffQ + off), "r"(hp[0]), "r"(hp[1]),
-                             "r"(hp[2]), "r"(hp[3])
-                             : "memory");
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + kCOffQL + off), "r"(lp[0]),
-                             "r"(lp[1]), "r"(lp[2]), "r"(lp[3])
-                             : "memory");
+                int nh[7];
+    #pragma unroll
+                for (int st = 0; st < 7; ++st) nh[st] = s_nh[st];
+                butterflies128<false>(x, nh);
+                // the row scaled by a power of two to below 2^14 (the de-whitened
+                // query can leave the fp16 range); the logits take it back exactly
+                float amax = 0.0f;
+    #pragma unroll
+                for (int j = 0; j < kD; ++j) amax = fmaxf(amax, fabsf(x[j]));
+                if (amax > 0.0f) {
+                    int e2 = 0;
+                    frexpf(amax, &e2);  // amax = f 2^e2, f in [0.5, 1)
+                    const float up = ldexpf(1.0f, 14 - e2);
+                    q_unscale = ldexpf(1.0f, e2 - 14);
+    #pragma unroll
+                    for (int j = 0; j < kD; ++j) x[j] *= up;
+                }
+    #pragma unroll
+                for (int c8 = 0; c8 < kD / 8; ++c8) {
+                    uint32_t hp[4], lp[4];
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __half h0 = __float2half_rn(x[8 * c8 + 2 * e]), h1 = __float2half_rn(x[8 * c8 + 2 * e + 1]);
+                        const __half l0 = __float2half_rn(x[8 * c8 + 2 * e] - __half2float(h0));
+                        const __half l1 = __float2half_rn(x[8 * c8 + 2 * e + 1] - __half2float(h1));
+                        hp[e] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+                        lp[e] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+                    }
+                    const uint32_t off = swz_off(r, 8 * c8);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + kCOffQ + off), "r"(hp[0]), "r"(hp[1]),
+                                 "r"(hp[2]), "r"(hp[3])
+                                 : "memory");
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + kCOffQL + off), "r"(lp[0]),
+                                 "r"(lp[1]), "r"(lp[2]), "r"(lp[3])
+                                 : "memory");
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive(CBAR(kCQR));
+                s_qun[r] = q_unscale;
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(CBAR(kCQR));
+            named_sync(1, 2 * kCkRows);
+            q_unscale = s_qun[r];
         }
-        float m = 0.0f, l = 0.0f;
+        float m = 0.0f, l = 0.0f;  // l: this warpgroup's half of the row sum
         const uint32_t tO = tmem + lanes + 256u;
-        for (int j = 0; ok && j < nt; ++j) {
+        // (the combined decision below is the loop's only exit: a warpgroup
+        // never leaves alone)
+        for (int j = 0; j < nt; ++j) {
             const int s = j & 1;
             const uint32_t tS = tmem + lanes + 128u * (uint32_t)s;
             const bool pre = j < np;
             // a prefix tile's norms arrive with its V tile
-            if (!__all_sync(0xffffffffu, mbar_wait(CBAR(kCS + s), (uint32_t)(j >> 1) & 1u, abort_flag, p.status) &&
-                                             (!pre || mbar_wait(CBAR(kCVF + s), (uint32_t)(j >> 1) & 1u, abort_flag,
-                                                                p.status)))) {
+            const bool got = ok && mbar_wait(CBAR(kCS + s), (uint32_t)(j >> 1) & 1u, abort_flag, p.status) &&
+                             (!pre || mbar_wait(CBAR(kCVF + s), (uint32_t)(j >> 1) & 1u, abort_flag, p.status));
+            if (!named_sync_and(1, 2 * kCkRows, got)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            // logits of the tile (a whole S row in registers; prefix logits
-            // times the key norms, read four at a time)
-            const int lim = pre ? P0 - 1 - j * kCkKeys                                   // keys past the prefix
-                                : (j == nt - 1 ? min(row, p.C - 1) - (j - np) * kCkKeys  // the chunk's diagonal
-                                               : kCkKeys);
-            float sv[kCkKeys];
-#pragma unroll
-            for (int q4 = 0; q4 < kCkKeys / 32; ++q4) tmem_ld32(tS + 32 * q4, sv + 32 * q4);
+            const int k0 = 64 * hw;  // the warpgroup's first key of the tile
+            const int lim = (pre ? P0 - 1 - j * kCkKeys                                    // keys past the prefix
+                                 : (j == nt - 1 ? min(row, p.C - 1) - (j - np) * kCkKeys   // the chunk's diagonal
+                                                : kCkKeys)) - k0;
+            float sv[64];
+            tmem_ld32(tS + k0, sv);
+            tmem_ld32(tS + k0 + 32, sv + 32);
             tmem_wait_ld();
             if (pre) {
-                const float4* rk4 = reinterpret_cast<const float4*>(&s_rho[s][0][0]);
+                const float4* rk4 = reinterpret_cast<const float4*>(&s_rho[s][0][k0]);
 #pragma unroll
-                for (int k4 = 0; k4 < kCkKeys / 4; ++k4) {
+                for (int k4 = 0; k4 < 16; ++k4) {
                     const float4 r4 = rk4[k4];
                     sv[4 * k4] *= r4.x * q_unscale;
                     sv[4 * k4 + 1] *= r4.y * q_unscale;
@@ -516,18 +543,21 @@ __global__ void __launch_bounds__(kCkThreads, 1)
                     sv[4 * k4 + 3] *= r4.w * q_unscale;
                 }
             }
-            if (lim < kCkKeys - 1) {
+            if (lim < 63) {
 #pragma unroll
-                for (int k = 0; k < kCkKeys; ++k)
+                for (int k = 0; k < 64; ++k)
                     if (k > lim) sv[k] = -INFINITY;
             }
             float mxa[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) mxa[i] = sv[i];
 #pragma unroll
-            for (int k = 8; k < kCkKeys; ++k) mxa[k & 7] = fmaxf(mxa[k & 7], sv[k]);
-            const float mt = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
-                                   fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7]))) * c;
+            for (int k = 8; k < 64; ++k) mxa[k & 7] = fmaxf(mxa[k & 7], sv[k]);
+            const float hmax = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+                                     fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
+            s_mx[s][hw][r] = hmax;
+            named_sync(1, 2 * kCkRows);
+            const float mt = fmaxf(hmax, s_mx[s][hw ^ 1][r]) * c;
             float f = 1.0f;
             bool raise = false;
             if (j == 0) {
@@ -539,51 +569,54 @@ __global__ void __launch_bounds__(kCkThreads, 1)
                 raise = true;
             }
             const bool to_dims = np > 0 && j == np;  // O leaves the value codec domain
-            if (__any_sync(0xffffffffu, raise) || to_dims) {
-                // PV of tile j - 1 must be done before O is touched
-                if (!__all_sync(0xffffffffu, mbar_wait(CBAR(kCO), (uint32_t)(j - 1) & 1u, abort_flag, p.status))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (to_dims) {
-                    float o[kD];
-#pragma unroll
-                    for (int q4 = 0; q4 < kD / 32; ++q4) tmem_ld32(tO + 32 * q4, o + 32 * q4);
-                    tmem_wait_ld();
-                    int nh_all[7];
-                    butterflies128<true>(o, nh_all);
-                    const float g = f * (1.0f / kPvScale) * 0.08838834764831845f;  // 1/sqrt(128)
-#pragma unroll
-                    for (int q4 = 0; q4 < kD / 32; ++q4) {
-                        uint32_t w[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(o[32 * q4 + i] * (g * s_vsign[32 * q4 + i]));
-                        tmem_st32(tO + 32 * q4, w);
-                    }
+            if (to_dims || __any_sync(0xffffffffu, raise)) {
+                // PV of tile j - 1 must be done before O is touched; warpgroup 0
+                // takes the whole row when it changes domain, else each its half
+                if (to_dims && hw == 1) {
+                    // (nothing: warpgroup 0 rescales the whole row with the transform)
+                } else if (!__all_sync(0xffffffffu, mbar_wait(CBAR(kCO), (uint32_t)(j - 1) & 1u, abort_flag, p.status))) {
+                    ok = false;  // both leave at the next tile's decision
                 } else {
-#pragma unroll 1
-                    for (int q4 = 0; q4 < kD / 32; ++q4) {
-                        float o[32];
-                        tmem_ld32(tO + 32 * q4, o);
-                        tmem_wait_ld();
-                        uint32_t w[32];
+                    tc_fence_after();
+                    if (to_dims) {
+                        float o[kD];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(o[i] * f);
-                        tmem_st32(tO + 32 * q4, w);
+                        for (int q4 = 0; q4 < kD / 32; ++q4) tmem_ld32(tO + 32 * q4, o + 32 * q4);
+                        tmem_wait_ld();
+                        int nh_all[7];
+                        butterflies128<true>(o, nh_all);
+                        const float g = f * (1.0f / kPvScale) * 0.08838834764831845f;  // 1/sqrt(128)
+#pragma unroll
+                        for (int q4 = 0; q4 < kD / 32; ++q4) {
+                            uint32_t w[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(o[32 * q4 + i] * (g * s_vsign[32 * q4 + i]));
+                            tmem_st32(tO + 32 * q4, w);
+                        }
+                    } else {
+#pragma unroll 1
+                        for (int q4 = 2 * hw; q4 < 2 * hw + 2; ++q4) {
+                            float o[32];
+                            tmem_ld32(tO + 32 * q4, o);
+                            tmem_wait_ld();
+                            uint32_t w[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(o[i] * f);
+                            tmem_st32(tO + 32 * q4, w);
+                        }
                     }
                 }
             }
-            // P of each 32-key chunk over that chunk's own 32 columns: hi parts
-            // in its first 16, lo parts (prefix tiles) in the next 16
+            // P of each 32-key chunk of the half over that chunk's own 32
+            // columns: hi parts in its first 16, lo parts (prefix tiles) in the next 16
             float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const float4* rv4 = reinterpret_cast<const float4*>(&s_rho[s][1][0]);
+            const float4* rv4 = reinterpret_cast<const float4*>(&s_rho[s][1][k0]);
 #pragma unroll
-            for (int q4 = 0; q4 < kCkKeys / 32; ++q4) {
+            for (int qh = 0; qh < 2; ++qh) {
                 uint32_t hi[16], lo[16];
 #pragma unroll
                 for (int i2 = 0; i2 < 8; ++i2) {
-                    const int k = 32 * q4 + 4 * i2;
+                    const int k = 32 * qh + 4 * i2;
                     float pv[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -607,20 +640,23 @@ __global__ void __launch_bounds__(kCkThreads, 1)
                         hi[2 * i2 + 1] = pack_h2(pv[2], pv[3]);
                     }
                 }
-                tmem_st16(tS + 32 * q4, hi);
-                if (pre) tmem_st16(tS + 32 * q4 + 16, lo);
+                tmem_st16(tS + k0 + 32 * qh, hi);
+                if (pre) tmem_st16(tS + k0 + 32 * qh + 16, lo);
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(CBAR(kCP));
         }
-        if (ok && __all_sync(0xffffffffu, mbar_wait(CBAR(kCO), (uint32_t)(nt - 1) & 1u, abort_flag, p.status))) {
+        // the row sums of both halves; the output row, 64 columns per warpgroup
+        s_lsum[hw][r] = l;
+        const bool fin = ok && mbar_wait(CBAR(kCO), (uint32_t)(nt - 1) & 1u, abort_flag, p.status);
+        if (named_sync_and(1, 2 * kCkRows, fin)) {
             tc_fence_after();
-            const float inv = 1.0f / l;
+            const float inv = 1.0f / (s_lsum[0][r] + s_lsum[1][r]);
             const size_t o0 = (((size_t)b * p.H * p.G + hq) * p.C + row) * kD;
 #pragma unroll 1
-            for (int q4 = 0; q4 < kD / 32; ++q4) {
+            for (int q4 = 2 * hw; q4 < 2 * hw + 2; ++q4) {
                 float o[32];
                 tmem_ld32(tO + 32 * q4, o);
                 tmem_wait_ld();
