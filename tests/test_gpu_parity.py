@@ -205,7 +205,7 @@ def test_decode_fp16_output_and_split_invariance():
         outs.append(got[0])
     assert np.abs(outs[0] - outs[2]).max() < 1e-4
     got16, _ = decode(plan, cache, q, lens, T, out_dtype=torch.float16)
-    check_close(got16[0], want, extra_abs=np.abs(want).max() * 2.0 ** -11)
+    check_close(got16[0], want, fp16_out=True)
 
 
 @pytest.mark.parametrize("qmul", [60.0, 1e-3])
