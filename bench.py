@@ -644,10 +644,11 @@ def run_gpu(args):
         peaks, _ = load_peaks()
         r = measure_prefill_attn(w, plan, args.prefill_tokens, peaks, torch.cuda.Stream())
         rc = measure_chunk_prefill(w, plan, args.prefill_tokens, args.prefill_tokens // 4, peaks, torch.cuda.Stream())
+        ra = measure_prefill(w, plan, max_len, peaks, torch.cuda.Stream())
         if rank == 0:
             print(json.dumps({"metric": "fused_prefill_tflops", "value": r["achieved"], "unit": "TFLOP/s",
                               "config": {"workload": w.name, "prompt_tokens": args.prefill_tokens},
-                              "prefill_attn": r, "chunk_prefill": rc}), flush=True)
+                              "prefill_attn": r, "chunk_prefill": rc, "append_prefill": ra}), flush=True)
         return
 
     # device buffers of all layers' per-step inputs/outputs (views per layer)

@@ -219,6 +219,13 @@ int bgtq_plan_load(bgtq_plan** out, const void* buf, size_t bytes, int flags);
 int bgtq_plan_get_codebook(const bgtq_plan* plan, int width, const float** centroids, const float** thresholds,
                            int* n_levels);
 
+/* Codes of n quotients u at one width (0..8) through the plan's code-search
+ * cell tables, on the host: the number of width-`width` thresholds <= u[i]
+ * (TQ-MSE's nearest-centroid rule, review §1 Key Terms; the bulk encoder
+ * takes its codes from the same tables).  u, codes: host arrays of n floats /
+ * int32; NaN is INVALID_ARG.  For checking the tables against a plain count. */
+int bgtq_plan_code(const bgtq_plan* plan, int width, const float* u, int64_t n, int32_t* codes);
+
 /* Byte sizes of one layer's cache buffers for `batch` sequences of `capacity`
  * tokens (capacity even); for a paged cache, of the pools: batch = n_pages,
  * capacity = page_tokens.  Host only. */

@@ -118,6 +118,14 @@ class Plan:
         thr = np.ctypeslib.as_array(tp, shape=(max(n.value - 1, 0),)).copy() if n.value > 1 else np.zeros(0, np.float32)
         return cent, thr
 
+    def code(self, width: int, u) -> np.ndarray:
+        """Codes of the quotients u at one width through the plan's code-search
+        cell tables (host): the number of thresholds <= u."""
+        uu = np.ascontiguousarray(np.asarray(u, dtype=np.float32).reshape(-1))
+        out = np.empty(uu.shape, dtype=np.int32)
+        _check(lib().bgtq_plan_code(self.handle, width, uu.ctypes.data, uu.size, out.ctypes.data))
+        return out
+
 
 def bgtq_plan_create(block_bits, energy, group: int, bits_per_key: int, v_bits: int, seed: int,
                      rope_layout: int = 0, host_only: bool = False) -> Plan:

@@ -39,6 +39,7 @@ EXPORTS = {
     "bgtq_plan_get_head": (C.c_int, [C.c_void_p, C.c_int, C.POINTER(BgtqHeadTables)]),
     "bgtq_plan_get_codebook": (C.c_int, [C.c_void_p, C.c_int, C.POINTER(C.POINTER(C.c_float)),
                                          C.POINTER(C.POINTER(C.c_float)), C.POINTER(C.c_int)]),
+    "bgtq_plan_code": (C.c_int, [C.c_void_p, C.c_int, C.c_void_p, C.c_int64, C.c_void_p]),
     "bgtq_cache_bytes": (C.c_int, [C.c_void_p, C.c_int, C.c_int64, C.POINTER(C.c_size_t),
                                    C.POINTER(C.c_size_t), C.POINTER(C.c_size_t)]),
     "bgtq_quantize_append": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,

@@ -298,6 +298,7 @@ static void free_dev(bgtq_plan* p) {
     if (p->dev.cent) cudaFree(p->dev.cent);
     if (p->dev.thr) cudaFree(p->dev.thr);
     if (p->dev.img_src) cudaFree(p->dev.img_src);
+    if (p->dev.cells) cudaFree(p->dev.cells);
     p->dev = DevTables{};
 }
 
@@ -461,6 +462,86 @@ static int build_codebooks(bgtq_plan* p) {
     return BGTQ_OK;
 }
 
+// Code-search cell tables.  The code of a quotient u at width w is the number
+// of width-w thresholds <= u.  The bulk encoder maps u to a cell by
+// cell(u) = round(s * sat(a u + b)) (two correctly rounded fused
+// multiply-adds, the second adding 1.5 * 2^23 so that the integer is the low
+// bits of the result), a non-decreasing function of u.  A threshold whose cell
+// is below cell(u) is then <= u and one whose cell is above is > u; so when
+// no two thresholds share a cell, the code is base(c) + [t_c <= u] for
+// c = cell(u), with base(c) the number of thresholds in the cells below c and
+// t_c the threshold in c (+inf if none).  The cell count is raised until every
+// threshold has a cell of its own, checked with the arithmetic of the device.
+static uint32_t f2u(float f) {
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    return u;
+}
+
+static float u2f(uint32_t u) {
+    float f;
+    std::memcpy(&f, &u, 4);
+    return f;
+}
+
+static int cell_of(float u, float a, float b, float s) {
+    float v = std::fmaf(u, a, b);
+    v = v < 0.0f ? 0.0f : (v > 1.0f ? 1.0f : v);  // sat (no NaN reaches here)
+    return (int)(f2u(std::fmaf(v, s, 12582912.0f)) - kCellMagicBits);
+}
+
+static int build_cells(bgtq_plan* p) {
+    std::vector<uint32_t> hdr(kCellHdr, 0u), ent;
+    for (int w = 0; w <= kWMax; ++w) {
+        const std::vector<float>& t = p->thr[w];
+        const int n = (int)t.size();
+        float a = 0.0f, b = 0.0f, s = 0.0f;
+        std::vector<int> cell(n);
+        if (n > 0) {
+            double gap = 1.0;
+            for (int i = 0; i + 1 < n; ++i) gap = std::min(gap, (double)t[i + 1] - (double)t[i]);
+            if (!(gap > 0.0)) return set_error(BGTQ_ERR_UNSUPPORTED, "width %d: repeated threshold", w);
+            const double lo = (double)t[0] - gap, hi = (double)t[n - 1] + gap;
+            bool ok = false;
+            for (int cells = (int)std::ceil((hi - lo) / (0.9 * gap)) + 1; cells <= kCellMaxEntries; cells += cells / 16 + 1) {
+                a = (float)(1.0 / (hi - lo));
+                b = (float)(-lo / (hi - lo));
+                s = (float)(cells - 1);
+                ok = true;
+                for (int i = 0; i < n && ok; ++i) {
+                    cell[i] = cell_of(t[i], a, b, s);
+                    ok = cell[i] >= 0 && cell[i] < cells && (i == 0 || cell[i] > cell[i - 1]);
+                }
+                if (ok) break;
+            }
+            if (!ok) return set_error(BGTQ_ERR_UNSUPPORTED, "width %d: no cell table", w);
+        }
+        const int cells = (int)s + 1;
+        hdr[4 * w] = f2u(a);
+        hdr[4 * w + 1] = f2u(b);
+        hdr[4 * w + 2] = f2u(s);
+        hdr[4 * w + 3] = (uint32_t)(ent.size() / 2);
+        for (int c = 0, i = 0; c < cells; ++c) {
+            while (i < n && cell[i] < c) ++i;  // i = thresholds in cells below c
+            ent.push_back(i < n && cell[i] == c ? f2u(t[i]) : f2u(INFINITY));
+            ent.push_back((uint32_t)i);
+        }
+    }
+    if (ent.size() / 2 > (size_t)kCellMaxEntries) return set_error(BGTQ_ERR_UNSUPPORTED, "cell tables too large");
+    p->cells = hdr;
+    p->cells.insert(p->cells.end(), ent.begin(), ent.end());
+    return BGTQ_OK;
+}
+
+// The code of u at width w through the cell tables (host copy of the bulk
+// encoder's search; the tests compare it with a plain threshold count).
+static int cell_code(const bgtq_plan* p, int w, float u) {
+    const uint32_t* h = p->cells.data() + 4 * w;
+    const int c = cell_of(u, u2f(h[0]), u2f(h[1]), u2f(h[2]));
+    const uint32_t* e = p->cells.data() + kCellHdr + 2 * ((size_t)h[3] + (size_t)c);
+    return (int)e[1] + (u2f(e[0]) <= u ? 1 : 0);
+}
+
 template <class T>
 static cudaError_t upload(T** dst, const T* src, size_t n) {
     cudaError_t e = cudaMalloc((void**)dst, n * sizeof(T));
@@ -481,7 +562,8 @@ static int upload_plan(bgtq_plan* p) {
     if ((e = upload(&p->dev.heads, p->heads.data(), p->heads.size())) != cudaSuccess ||
         (e = upload(&p->dev.cent, cent.data(), cent.size())) != cudaSuccess ||
         (e = upload(&p->dev.thr, thr.data(), thr.size())) != cudaSuccess ||
-        (e = upload(&p->dev.img_src, p->img_src.data(), p->img_src.size())) != cudaSuccess) {
+        (e = upload(&p->dev.img_src, p->img_src.data(), p->img_src.size())) != cudaSuccess ||
+        (e = upload(&p->dev.cells, p->cells.data(), p->cells.size())) != cudaSuccess) {
         free_dev(p);
         return set_error(BGTQ_ERR_CUDA, "plan upload: %s", cudaGetErrorString(e));
     }
@@ -582,6 +664,7 @@ int bgtq_plan_create(bgtq_plan** out, int head_dim, int n_kv_heads, int group, i
     p->piece.resize(n_kv_heads);
     p->slot_off.resize(n_kv_heads);
     int rc = build_codebooks(p);
+    if (rc == BGTQ_OK) rc = build_cells(p);
     for (int h = 0; rc == BGTQ_OK && h < n_kv_heads; ++h) rc = build_head(p, h, block_bits + h * kNB, energy + h * kNB);
     if (rc == BGTQ_OK) {
         // decode tables: widest code of all heads (keys) and of the values
@@ -728,6 +811,16 @@ int bgtq_plan_get_codebook(const bgtq_plan* p, int width, const float** cent, co
     *cent = p->cent[width].data();
     *thr = p->thr[width].data();
     *n_levels = (int)p->cent[width].size();
+    return BGTQ_OK;
+}
+
+int bgtq_plan_code(const bgtq_plan* p, int width, const float* u, int64_t n, int32_t* codes) {
+    if (!p || (n > 0 && (!u || !codes))) return set_error(BGTQ_ERR_INVALID_ARG, "NULL pointer");
+    if (width < 0 || width > kWMax || n < 0) return set_error(BGTQ_ERR_INVALID_ARG, "width or count out of range");
+    for (int64_t i = 0; i < n; ++i) {
+        if (std::isnan(u[i])) return set_error(BGTQ_ERR_INVALID_ARG, "NaN quotient at %lld", (long long)i);
+        codes[i] = cell_code(p, width, u[i]);
+    }
     return BGTQ_OK;
 }
 

@@ -80,7 +80,18 @@ struct DevTables {
     float* cent = nullptr;        // [9][256] centroids (fp16-exact floats)
     float* thr = nullptr;         // [9][256] thresholds (first 2^w - 1 used)
     uint32_t* img_src = nullptr;  // [kImageMaxWords] decode tables: per-lane entries, then shared words
+    uint32_t* cells = nullptr;    // code-search cell tables (layout: kCellHdr)
 };
+
+// Code-search cell tables of the bulk encoder (built with the codebooks).
+// Words: for each width w = 0..8 four words (a, b, s as float bits, index of
+// the width's first entry), then the entries, two words each (threshold as
+// float bits, +inf if none; number of thresholds in the cells below).  The
+// cell of a quotient u at width w is round(s * sat(a u + b)), found as the
+// low bits of fma(sat(fma(u, a, b)), s, 1.5 * 2^23).
+constexpr int kCellHdr = 4 * (kWMax + 1);
+constexpr int kCellMaxEntries = 1536;
+constexpr uint32_t kCellMagicBits = 0x4B400000u;  // bits of 1.5 * 2^23
 
 // Where the records of (sequence b, head h, position pos) live: token slot
 // (b H + h) capacity + pos of a contiguous cache, or (page H + h) P + pos mod P
@@ -169,6 +180,7 @@ struct bgtq_plan {
     std::vector<uint8_t> in_bits;   // the plan's defining inputs, kept for bgtq_plan_save:
     std::vector<double> in_energy;  // block widths and energies [H][64]
     std::vector<uint32_t> img_src;  // decode table entries (see single_base)
+    std::vector<uint32_t> cells;    // code-search cell tables (kCellHdr words, then the entries)
     int img_ws = 0;                 // widest code the decode tables cover
     // inspection copies (bgtq_plan_get_head)
     std::vector<std::vector<int8_t>> sign_k8, sign_v8;

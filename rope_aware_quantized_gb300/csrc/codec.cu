@@ -313,6 +313,8 @@ cudaError_t launch_quantize_append(const bgtq_plan& pl, cudaStream_t s, const vo
     p.map = make_cache_map(c, pl.H, batch, status);
     p.heads = pl.dev.heads;
     p.thr = pl.dev.thr;
+    p.cells = pl.dev.cells;
+    p.cell_words = (int)pl.cells.size();
     p.bk = pl.bk;
     p.bv = pl.bv;
     p.v_inv_sqrt = (float)(1.0 / std::sqrt((double)kD));
@@ -327,10 +329,11 @@ cudaError_t launch_quantize_append(const bgtq_plan& pl, cudaStream_t s, const vo
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     // Bulk appends (prefill) take the token-per-thread kernel, which reads
-    // whole fp16 rows with 16-byte loads; small appends (decode) and other
-    // widths the warp-per-token kernel.
+    // whole fp16 rows with 16-byte loads (its grid's z holds two blocks per
+    // sequence); small appends (decode), other widths and batches of more
+    // than 32767 sequences the warp-per-token kernel.
     const bool aligned = ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15) == 0;
-    if (t_new >= kBulkMinTokens && aligned && pl.bk >= 1 && pl.bk <= 3 && pl.bv >= 1 && pl.bv <= 4)
+    if (t_new >= kBulkMinTokens && aligned && pl.bk >= 1 && pl.bk <= 3 && pl.bv >= 1 && pl.bv <= 4 && batch <= 32767)
         return launch_quantize_append_bulk(p, pl.bk, pl.bv, batch, s);
     const int64_t pairs = (int64_t)t_new / 2 + 1;
     const int64_t per_block = kPairsPerBlock;

@@ -29,15 +29,18 @@ namespace {
 // larger than h form the prefix [0, E_h) of the codec order, pieces being laid
 // out by decreasing size and aligned to their size), the 1/sqrt(piece)
 // scaling, the 32-partial norm tree, the quotient and the threshold count; so
-// codes and norms are identical to the warp encoder's.
+// codes and norms are identical to the warp encoder's.  A token's 128
+// coordinates stay in registers from the gather to the codes; each code is
+// one lookup in the cell tables (see cell_code), so no loop indexes them at
+// run time.
 constexpr int kBulkTok = 128;
-// Per-thread column of 129 words in dynamic shared memory (the odd stride
-// keeps the threads of a warp on distinct banks): first the fp16 key row,
-// then the rotated coordinates that the code loops read back.  The quotients
-// u = y / rho use the token's reciprocal of rho (see quot), and the code
-// searches run at the width of each rotation piece.
-constexpr int kColWords = 129;
-constexpr int kBulkDynSmem = kBulkTok * kColWords * 4;
+constexpr int kBulkMinBlocks = 3;  // resident blocks per SM the register budget is cut for
+// Per-thread fp16 key row in dynamic shared memory: 64 words + 1 (the odd
+// stride keeps the threads of a warp on distinct banks); the plan's cell
+// tables follow the rows.
+constexpr int kRowWords = 65;
+constexpr int kBulkRowBytes = kBulkTok * kRowWords * 4;
+constexpr int kBulkPairBatch = 8;  // key pairs whose codes are computed before their fields are merged
 
 // The quotient y / rho correctly rounded, as __fdiv_rn gives it, from the
 // correctly rounded reciprocal r = 1/rho (r = 0 when rho = 0, which makes the
@@ -56,15 +59,28 @@ __device__ __forceinline__ float quot(float y, float rho, float r) {
     return __fmaf_rn(e1, r, q1);
 }
 
-// Code of quotient u at width W: the number of width-W thresholds <= u, by
-// binary search over the sorted thresholds tb (= s_thr + 2^W - 1).
-template <int W>
-__device__ __forceinline__ uint32_t code_w(float u, const float* tb) {
-    int c = 0;
-#pragma unroll
-    for (int k = W - 1; k >= 0; --k)
-        if (tb[c + (1 << k) - 1] <= u) c += 1 << k;
-    return (uint32_t)c;
+// Code of quotient u (the number of thresholds <= u) from a width's cell
+// table: cell c = round(s sat(a u + b)), the low bits of
+// fma(sat(fma(u, a, b)), s, 1.5 2^23) (a non-decreasing function of u, so
+// every threshold of a lower cell is <= u and every one of a higher cell is
+// > u); each cell holds at most one threshold t_c (+inf if none) and the
+// count base_c of the thresholds below it, and the code is base_c + [t_c <= u].
+// tab = shared address of the width's first entry - 8 x the bits of 1.5 2^23
+// (mod 2^32), so the entry address is tab + 8 x the bits of the second fma.
+// The load is a plain function of its address (the tables do not change
+// while the kernel runs); its address depends on data loaded after the
+// tables were staged, which orders it after the staging.
+__device__ __forceinline__ uint32_t cell_code(float u, float a, float b, float s, uint32_t tab) {
+    const float v = __saturatef(__fmaf_rn(u, a, b));
+    const uint32_t addr = tab + ((uint32_t)__float_as_int(__fmaf_rn(v, s, 12582912.0f)) << 3);
+    uint32_t th, base;
+    asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(th), "=r"(base) : "r"(addr));
+    return base + (__uint_as_float(th) <= u ? 1u : 0u);
+}
+
+// OR into a shared-memory word without reading it back
+__device__ __forceinline__ void red_or_shared(uint32_t addr, uint32_t v) {
+    asm volatile("red.shared.or.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // Butterfly stage H over the first e coordinates (e a multiple of 2H).  Small
@@ -131,67 +147,50 @@ __device__ __forceinline__ float bulk_rotate_norm(float (&z)[kD], int n, const i
     return __fsqrt_rn(__fdiv_rn(part[0], (float)n));
 }
 
-// Codes and packing of the key pairs of one rotation piece (codec coordinates
-// [j0, j0 + n), all of width W) into the thread's record: four pairs at a time
-// so that their threshold searches overlap.
-template <int W>
-__device__ __forceinline__ void bulk_key_piece(const float* col, int j0, int n, float rho, float r, const float* s_thr,
-                                               const uint16_t* s_pbit, uint32_t* rec) {
-    const float* tb = s_thr + (1 << W) - 1;
-    const int m1 = (j0 + n) >> 1;
-    for (int m0 = j0 >> 1; m0 < m1; m0 += 4) {
-        uint32_t f[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int m = min(m0 + q, m1 - 1);
-            f[q] = code_w<W>(quot(col[2 * m], rho, r), tb) | (code_w<W>(quot(col[2 * m + 1], rho, r), tb) << W);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            if (m0 + q >= m1) break;
-            const int bit = s_pbit[m0 + q];
-            const int wi = bit >> 5, sh = bit & 31;
-            rec[wi] |= f[q] << sh;
-            if (sh + 2 * W > 32) rec[wi + 1] |= f[q] >> (32 - sh);
-        }
-    }
-}
-
 template <int BK, int BV>
-__global__ void __launch_bounds__(kBulkTok) quantize_append_bulk_kernel(QParams p) {
-    __shared__ float s_thr[kThrCompact];
+__global__ void __launch_bounds__(kBulkTok, kBulkMinBlocks) quantize_append_bulk_kernel(QParams p) {
     __shared__ float2 s_pw[kD];  // keys: (whitening x sign, source dim) per codec coordinate (0 past n_coded)
     __shared__ float s_is[kD];   // 1/sqrt(piece) (keys)
     __shared__ float s_sv[kD];   // value signs
-    __shared__ uint8_t s_width[kD];
-    __shared__ uint8_t s_plog2[kD];
-    __shared__ uint16_t s_pbit[kNB];
+    __shared__ uint4 s_cp[kNB];  // key pair m: a, b, s of its width's cell table (float bits), table base
+    __shared__ uint32_t s_pk[kNB];  // key pair m: bit position in the record | width << 16
     __shared__ int s_end[7];
     __shared__ uint32_t s_rec[kBulkTok * (4 * BK + 1)];
-    __shared__ uint32_t s_vrec[kBulkTok * (8 * BV + 1)];
-    extern __shared__ float s_col[];
+    extern __shared__ __align__(16) uint32_t s_dyn[];
+    uint32_t* const s_cell = s_dyn + kBulkTok * kRowWords;  // the plan's cell tables
     const int tid = threadIdx.x;
-    const int h = blockIdx.y, b = blockIdx.z;
+    // blockIdx.z: the key blocks of every sequence, then the value blocks
+    // (blocks are dispatched in that order, so an SM runs one half of the code
+    // at a time)
+    const int nbz = (int)gridDim.z >> 1;
+    const bool is_v = (int)blockIdx.z >= nbz;
+    const int h = blockIdx.y, b = (int)blockIdx.z - (is_v ? nbz : 0);
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- plan-static set-up (thread tid prepares codec coordinate tid)
     const HeadTab* ht = p.heads + h;
     const int nc = ht->n_coded;
-    stage_thresholds(s_thr, p.thr, tid, kBulkTok);
+    for (int i = tid; i < p.cell_words; i += kBulkTok) s_cell[i] = __ldg(p.cells + i);
     {
         const int j = tid;
         const bool coded = j < nc;
         s_pw[j] = make_float2(coded ? __fmul_rn(ht->whiten[j], ht->sign_k[j]) : 0.0f, __int_as_float((int)ht->perm[j]));
         s_is[j] = ht->inv_sqrt[j];
         s_sv[j] = ht->sign_v[j];
-        s_width[j] = coded ? ht->width[j] : 0;
-        s_plog2[j] = coded ? ht->plog2[j] : 0;
-        if (j < kNB) s_pbit[j] = ht->pair_bit[j];
         if (j < 7) {
             int e = 0;
             for (int i = 0; i < nc; ++i) e += (1 << ht->plog2[i]) > (1 << j);
             s_end[j] = e;
         }
+    }
+    const uint32_t cell_base = (uint32_t)__cvta_generic_to_shared(s_cell + kCellHdr);
+    __syncthreads();
+    if (!is_v && tid < kNB) {
+        const int m = tid;
+        const int w = 2 * m < nc ? ht->width[2 * m] : 0;
+        const uint32_t* hd = s_cell + 4 * w;
+        s_cp[m] = make_uint4(hd[0], hd[1], hd[2], cell_base + 8u * hd[3] - 8u * kCellMagicBits);
+        s_pk[m] = (uint32_t)ht->pair_bit[m] | ((uint32_t)w << 16);
     }
     __syncthreads();
     // pos_start is read before the wait: no kernel of this library writes it
@@ -210,12 +209,12 @@ __global__ void __launch_bounds__(kBulkTok) quantize_append_bulk_kernel(QParams 
     const size_t unit = (size_t)b * p.H + h;
     const int64_t sl = act ? p.map.slot(b, h, pos) : 0;  // record location of token `pos`
     if (sl < 0 && p.status) atomicOr(p.status, BGTQ_STATUS_PAGE_RANGE);
-    float* col = s_col + tid * kColWords;
 
     // ---- key of token `pos`
-    if (act) {
+    if (!is_v) {
+        if (!act) return;
+        uint32_t* row = s_dyn + tid * kRowWords;
         const uint4* src = reinterpret_cast<const uint4*>(p.k + (unit * p.t_new + (size_t)(pos - ps)) * kD);
-        uint32_t* row = reinterpret_cast<uint32_t*>(col);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const uint4 w4 = __ldg(src + i);
@@ -239,34 +238,43 @@ __global__ void __launch_bounds__(kBulkTok) quantize_append_bulk_kernel(QParams 
         }
         const float rho = bulk_rotate_norm<false>(z, nc, s_end, s_is, p.v_inv_sqrt);
         const float r = rho > 0.0f ? __frcp_rn(rho) : 0.0f;
-        // the rotated coordinates go back to the column (the row is no longer
-        // needed): the code loops below index them at run time
-#pragma unroll
-        for (int j = 0; j < kD; ++j) col[j] = z[j];
         uint32_t* rec = s_rec + tid * (4 * BK + 1);
 #pragma unroll
         for (int i = 0; i < 4 * BK; ++i) rec[i] = 0;
-        // rotation pieces in codec order, each of one width (uniform loop)
-        for (int j = 0; j < nc;) {
-            const int w = s_width[j], n = 1 << s_plog2[j];
-            switch (w) {
-                case 1: bulk_key_piece<1>(col, j, n, rho, r, s_thr, s_pbit, rec); break;
-                case 2: bulk_key_piece<2>(col, j, n, rho, r, s_thr, s_pbit, rec); break;
-                case 3: bulk_key_piece<3>(col, j, n, rho, r, s_thr, s_pbit, rec); break;
-                case 4: bulk_key_piece<4>(col, j, n, rho, r, s_thr, s_pbit, rec); break;
-                case 5: bulk_key_piece<5>(col, j, n, rho, r, s_thr, s_pbit, rec); break;
-                case 6: bulk_key_piece<6>(col, j, n, rho, r, s_thr, s_pbit, rec); break;
-                case 7: bulk_key_piece<7>(col, j, n, rho, r, s_thr, s_pbit, rec); break;
-                default: bulk_key_piece<8>(col, j, n, rho, r, s_thr, s_pbit, rec); break;
+        const uint32_t rec_a = (uint32_t)__cvta_generic_to_shared(rec);
+        // key pairs in codec order, a batch at a time: codes first (their
+        // lookups overlap), then the fields OR-ed into the record
+#pragma unroll
+        for (int m0 = 0; m0 < kNB; m0 += kBulkPairBatch) {
+            if (2 * m0 >= nc) break;
+            uint32_t f[kBulkPairBatch], pk[kBulkPairBatch];
+#pragma unroll
+            for (int q = 0; q < kBulkPairBatch; ++q) {
+                const int m = m0 + q;
+                const uint4 cp = s_cp[m];
+                pk[q] = s_pk[m];
+                const float a = __uint_as_float(cp.x), bb = __uint_as_float(cp.y), sc = __uint_as_float(cp.z);
+                const uint32_t c0 = cell_code(quot(z[2 * m], rho, r), a, bb, sc, cp.w);
+                const uint32_t c1 = cell_code(quot(z[2 * m + 1], rho, r), a, bb, sc, cp.w);
+                f[q] = c0 | (c1 << (pk[q] >> 16));
             }
-            j += n;
+#pragma unroll
+            for (int q = 0; q < kBulkPairBatch; ++q) {
+                if (2 * (m0 + q) >= nc) break;
+                const uint32_t w = pk[q] >> 16, bit = pk[q] & 0xffffu;
+                const uint32_t wa = rec_a + 4u * (bit >> 5), sh = bit & 31u;
+                red_or_shared(wa, f[q] << sh);
+                if (sh + 2u * w > 32u) red_or_shared(wa + 4u, f[q] >> (32u - sh));
+            }
         }
+        asm volatile("" ::: "memory");
         if (sl >= 0) {
             uint4* dst = reinterpret_cast<uint4*>(p.kc + sl * (16 * BK));
 #pragma unroll
             for (int i = 0; i < BK; ++i) dst[i] = make_uint4(rec[4 * i], rec[4 * i + 1], rec[4 * i + 2], rec[4 * i + 3]);
             p.kn[sl] = rho;
         }
+        return;
     }
 
     // ---- value of token `pos`: the thread pair (even, odd) shares a record
@@ -293,29 +301,18 @@ __global__ void __launch_bounds__(kBulkTok) quantize_append_bulk_kernel(QParams 
         }
         rho_v = bulk_rotate_norm<true>(z, kD, s_end, s_is, p.v_inv_sqrt);
         const float r = rho_v > 0.0f ? __frcp_rn(rho_v) : 0.0f;
-#pragma unroll
-        for (int j = 0; j < kD; ++j) col[j] = z[j];
+        const uint32_t* hd = s_cell + 4 * BV;
+        const float a = __uint_as_float(hd[0]), bb = __uint_as_float(hd[1]), sc = __uint_as_float(hd[2]);
+        const uint32_t tab = cell_base + 8u * hd[3] - 8u * kCellMagicBits;
         // fields as for an even token (code of dim j at bit 2 BV j), shifted up
-        // by BV for an odd one; 16 dims (BV words of the record) at a time
-        const float* tb = s_thr + (1 << BV) - 1;
-        uint32_t* vr = s_vrec + tid * (8 * BV + 1);
-#pragma unroll 1
-        for (int g = 0; g < 8; ++g) {
-            uint32_t wds[BV];
+        // by BV for an odd one
 #pragma unroll
-            for (int i = 0; i < BV; ++i) wds[i] = 0;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint32_t c = code_w<BV>(quot(col[16 * g + i], rho_v, r), tb);
-                const int bit = 2 * BV * i;  // compile-time after unrolling
-                wds[bit >> 5] |= c << (bit & 31);
-                if ((bit & 31) + BV > 32) wds[(bit >> 5) + 1] |= c >> (32 - (bit & 31));
-            }
-#pragma unroll
-            for (int i = 0; i < BV; ++i) vr[BV * g + i] = wds[i];
+        for (int j = 0; j < kD; ++j) {
+            const uint32_t c = cell_code(quot(z[j], rho_v, r), a, bb, sc, tab);
+            const int bit = 2 * BV * j;  // compile-time after unrolling
+            vw[bit >> 5] |= c << (bit & 31);
+            if ((bit & 31) + BV > 32) vw[(bit >> 5) + 1] |= c >> (32 - (bit & 31));
         }
-#pragma unroll
-        for (int i = 0; i < kW; ++i) vw[i] = vr[i];
         if (par) {
 #pragma unroll
             for (int i = kW - 1; i >= 0; --i) vw[i] = (vw[i] << BV) | (i ? vw[i - 1] >> (32 - BV) : 0u);
@@ -373,12 +370,15 @@ cudaError_t launch_bulk_bk_impl(const QParams& p, int bv, int batch, cudaStream_
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     // blocks start at even positions: one more token covers an odd start
-    cfg.gridDim = dim3((unsigned)(((int64_t)p.t_new + 1 + kBulkTok - 1) / kBulkTok), (unsigned)p.H, (unsigned)batch);
+    // z: key blocks of every sequence, then value blocks
+    if (2 * (int64_t)batch > 65535) return cudaErrorInvalidValue;
+    cfg.gridDim = dim3((unsigned)(((int64_t)p.t_new + 1 + kBulkTok - 1) / kBulkTok), (unsigned)p.H, (unsigned)(2 * batch));
     cfg.blockDim = dim3(kBulkTok, 1, 1);
-    cfg.dynamicSmemBytes = kBulkDynSmem;
+    const int dyn = kBulkRowBytes + 4 * p.cell_words;
+    cfg.dynamicSmemBytes = (size_t)dyn;
     auto go = [&](auto kernel) -> cudaError_t {
-        // the per-thread columns exceed the 48 KB default: raise it (cheap; idempotent)
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkDynSmem);
+        // the key rows and cell tables may exceed the 48 KB default: raise it (cheap; idempotent)
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
         return e != cudaSuccess ? e : cudaLaunchKernelEx(&cfg, kernel, p);
     };
     switch (bv) {

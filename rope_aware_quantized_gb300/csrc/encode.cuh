@@ -30,6 +30,8 @@ struct QParams {
     CacheMap map;      // record location of (sequence, head, position)
     const HeadTab* heads;
     const float* thr;
+    const uint32_t* cells;  // code-search cell tables (bulk kernel)
+    int cell_words;
     int bk, bv;
     float v_inv_sqrt;
     int32_t* status;

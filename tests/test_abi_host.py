@@ -84,6 +84,41 @@ def test_codebooks_match_oracle_bit_exactly():
         assert np.array_equal(thr, othr), w
 
 
+def _ulp_walk(t, n):
+    """float32 values t and the n neighbours on each side of t."""
+    t = np.float32(t)
+    out, a, b = [t], t, t
+    for _ in range(n):
+        a = np.nextafter(a, np.float32(-np.inf))
+        b = np.nextafter(b, np.float32(np.inf))
+        out += [a, b]
+    return np.array(out, np.float32)
+
+
+def test_code_search_cells_equal_threshold_count():
+    """The bulk encoder takes each code from a cell table (one lookup and one
+    comparison) instead of a search; its host copy must give the number of
+    thresholds <= u (TQ-MSE's nearest-centroid rule with the oracle's tie
+    rule) for every quotient: uniform draws over the whole quotient range
+    [-sqrt(128), sqrt(128)] and past it, and every float within 300 ulps of
+    every threshold, where a cell boundary or a tie would show."""
+    bits = np.full((1, 64), 3, np.uint8)
+    plan = bg.bgtq_plan_create(bits, np.ones((1, 64)), 4, 384, 3, 1, host_only=True)
+    rng = np.random.default_rng(7)
+    for w in range(0, 9):
+        _, thr = O.codebooks()[w]
+        u = [rng.uniform(-12.0, 12.0, 100000).astype(np.float32),
+             np.array([0.0, -0.0, 11.3138, -11.3138, 1e30, -1e30, 3.4e38, -3.4e38, 1e-40, -1e-40], np.float32)]
+        u += [_ulp_walk(t, 300) for t in thr]
+        u = np.concatenate(u)
+        want = np.searchsorted(thr, u, side="right")  # thresholds <= u
+        assert np.array_equal(plan.code(w, u), want), w
+    with pytest.raises(bg.BgtqError):
+        plan.code(3, np.array([np.nan], np.float32))
+    with pytest.raises(bg.BgtqError):
+        plan.code(9, np.zeros(1, np.float32))
+
+
 @pytest.mark.parametrize("seed,bits_per_key,v_bits,layout", [(11, 384, 3, 0), (12, 256, 2, 0), (13, 384, 2, 1),
                                                              (14, 128, 1, 0)])
 def test_plan_tables_match_oracle(seed, bits_per_key, v_bits, layout):
