@@ -119,6 +119,23 @@ __device__ __forceinline__ void bulk_stage(float (&z)[kD], int e) {
     }
 }
 
+// Node (L, m) of the norm tree: partial L after the sums of the levels above
+// m (m = 32: the leaf, coordinates 4L..4L+3 scaled, squared and summed, the
+// scaled coordinates written back); node (L, m) = node (L, 2m) + node (L + m, 2m).
+template <bool kFull, int M>
+__device__ __forceinline__ float norm_tree(float (&z)[kD], int L, const float* s_is, float v_inv_sqrt) {
+    if constexpr (M == 32) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) z[4 * L + i] = __fmul_rn(z[4 * L + i], kFull ? v_inv_sqrt : s_is[4 * L + i]);
+        return __fadd_rn(__fadd_rn(__fmul_rn(z[4 * L], z[4 * L]), __fmul_rn(z[4 * L + 1], z[4 * L + 1])),
+                         __fadd_rn(__fmul_rn(z[4 * L + 2], z[4 * L + 2]), __fmul_rn(z[4 * L + 3], z[4 * L + 3])));
+    } else {
+        const float a = norm_tree<kFull, 2 * M>(z, L, s_is, v_inv_sqrt);
+        const float b = norm_tree<kFull, 2 * M>(z, L + M, s_is, v_inv_sqrt);
+        return __fadd_rn(a, b);
+    }
+}
+
 // Rotation pieces of one token held by one thread (stage h applies to the
 // coordinates [0, end[h]); kFull: one piece of 128), the 1/sqrt(piece)
 // scaling and the norm tree; returns rho = sqrt(sum y^2 / n).
@@ -132,19 +149,11 @@ __device__ __forceinline__ float bulk_rotate_norm(float (&z)[kD], int n, const i
     bulk_stage<16, kFull>(z, kFull ? kD : s_end[4]);
     bulk_stage<32, kFull>(z, kFull ? kD : s_end[5]);
     bulk_stage<64, kFull>(z, kFull ? kD : s_end[6]);
-    float part[32];
-#pragma unroll
-    for (int L = 0; L < 32; ++L) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) z[4 * L + i] = __fmul_rn(z[4 * L + i], kFull ? v_inv_sqrt : s_is[4 * L + i]);
-        part[L] = __fadd_rn(__fadd_rn(__fmul_rn(z[4 * L], z[4 * L]), __fmul_rn(z[4 * L + 1], z[4 * L + 1])),
-                            __fadd_rn(__fmul_rn(z[4 * L + 2], z[4 * L + 2]), __fmul_rn(z[4 * L + 3], z[4 * L + 3])));
-    }
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1)
-#pragma unroll
-        for (int L = 0; L < m; ++L) part[L] = __fadd_rn(part[L], part[L + m]);
-    return __fsqrt_rn(__fdiv_rn(part[0], (float)n));
+    // partial L = the scaled coordinates 4L..4L+3 squared and summed; the tree
+    // adds partial L + m to partial L for m = 16, 8, 4, 2, 1.  Evaluated depth
+    // first (each sum as soon as both of its operands exist), which keeps few
+    // partials live and leaves every sum and its operands as they are.
+    return __fsqrt_rn(__fdiv_rn(norm_tree<kFull, 1>(z, 0, s_is, v_inv_sqrt), (float)n));
 }
 
 template <int BK, int BV>
@@ -177,10 +186,15 @@ __global__ void __launch_bounds__(kBulkTok, kBulkMinBlocks) quantize_append_bulk
         s_pw[j] = make_float2(coded ? __fmul_rn(ht->whiten[j], ht->sign_k[j]) : 0.0f, __int_as_float((int)ht->perm[j]));
         s_is[j] = ht->inv_sqrt[j];
         s_sv[j] = ht->sign_v[j];
-        if (j < 7) {
-            int e = 0;
-            for (int i = 0; i < nc; ++i) e += (1 << ht->plog2[i]) > (1 << j);
-            s_end[j] = e;
+        // E_h = coordinates in pieces larger than h (a prefix: pieces are laid
+        // out by decreasing size); written by the last such coordinate, or by
+        // thread 0 when there is none
+        const int sz = coded ? 1 << ht->plog2[j] : 0;
+        const int sz1 = j + 1 < nc ? 1 << ht->plog2[j + 1] : 0;
+#pragma unroll
+        for (int st = 0; st < 7; ++st) {
+            if (sz > (1 << st) && sz1 <= (1 << st)) s_end[st] = j + 1;
+            if (j == 0 && sz <= (1 << st)) s_end[st] = 0;
         }
     }
     const uint32_t cell_base = (uint32_t)__cvta_generic_to_shared(s_cell + kCellHdr);
@@ -342,9 +356,13 @@ __global__ void __launch_bounds__(kBulkTok, kBulkMinBlocks) quantize_append_bulk
         for (int i = 0; i < kW; ++i) mask[i] = 0;
 #pragma unroll
         for (int j = 0; j < kD; ++j) {
-            const int bit = 2 * BV * j + par * BV;
+            const int bit = 2 * BV * j;  // the even token's fields; shifted up by BV for an odd one
             mask[bit >> 5] |= m1 << (bit & 31);
             if ((bit & 31) + BV > 32) mask[(bit >> 5) + 1] |= m1 >> (32 - (bit & 31));
+        }
+        if (par) {
+#pragma unroll
+            for (int i = kW - 1; i >= 0; --i) mask[i] = (mask[i] << BV) | (i ? mask[i - 1] >> (32 - BV) : 0u);
         }
 #pragma unroll
         for (int i = 0; i < kW; ++i) {
