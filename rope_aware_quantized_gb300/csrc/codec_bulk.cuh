@@ -84,9 +84,10 @@ __device__ __forceinline__ float quot(float y, float rho, float r) {
 __device__ __forceinline__ uint32_t cell_code(float u, float a, float b, float s, uint32_t tab) {
     const float v = __saturatef(__fmaf_rn(u, a, b));
     const uint32_t addr = tab + ((uint32_t)__float_as_int(__fmaf_rn(v, s, 12582912.0f)) << 3);
-    uint32_t th, base;
+    uint32_t th, base, le;
     asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(th), "=r"(base) : "r"(addr));
-    return base + (__uint_as_float(th) <= u ? 1u : 0u);
+    asm("set.le.u32.f32 %0, %1, %2;" : "=r"(le) : "f"(__uint_as_float(th)), "f"(u));  // all ones when t_c <= u
+    return base - le;
 }
 
 // OR into a shared-memory word without reading it back
@@ -233,15 +234,14 @@ __device__ __forceinline__ void bulk_key_half(const QParams& p, int nc, int hf, 
             const float a = __uint_as_float(c4.x), bb = __uint_as_float(c4.y), sc = __uint_as_float(c4.z);
             const uint32_t c0 = cell_code(quot(z[2 * (q0 + q)], rho, r), a, bb, sc, c4.w);
             const uint32_t c1 = cell_code(quot(z[2 * (q0 + q) + 1], rho, r), a, bb, sc, c4.w);
-            f[q] = c0 | (c1 << (pq[q] >> 16));
+            f[q] = c0 | (c1 << ((pq[q] >> 16) & 15u));
         }
 #pragma unroll
         for (int q = 0; q < kBulkPairBatch; ++q) {
             if (2 * (32 * hf + q0 + q) >= nc) break;
-            const uint32_t w = pq[q] >> 16, bit = pq[q] & 0xffffu;
-            const uint32_t wa = rec_a + 4u * (bit >> 5), sh = bit & 31u;
+            const uint32_t wa = rec_a + (pq[q] & 0xffu), sh = (pq[q] >> 8) & 31u;
             red_or_shared(wa, f[q] << sh);
-            if (sh + 2u * w > 32u) red_or_shared(wa + 4u, f[q] >> (32u - sh));
+            if (pq[q] >> 31) red_or_shared(wa + 4u, f[q] >> (32u - sh));
         }
     }
     __syncwarp();
@@ -361,7 +361,9 @@ __global__ void __launch_bounds__(kBulkThreads, kBulkMinBlocks) quantize_append_
     __shared__ float s_is[2 * kFRow];    // 1/sqrt(piece) (keys)
     __shared__ float s_sv[2 * kFRow];    // value signs
     __shared__ uint4 s_cp[2 * kCpRow];   // key pair m: a, b, s of its width's cell table (float bits), table base
-    __shared__ uint32_t s_pk[2 * kPkRow];  // key pair m: bit position in the record | width << 16
+    // key pair m: byte offset of its first record word | bit shift in it << 8 |
+    // width << 16 | field continues in the next word << 31
+    __shared__ uint32_t s_pk[2 * kPkRow];
     __shared__ int s_end[7];
     __shared__ uint32_t s_rec[kBulkTok * (4 * BK + 1)];
     extern __shared__ __align__(16) uint32_t s_dyn[];
@@ -400,7 +402,8 @@ __global__ void __launch_bounds__(kBulkThreads, kBulkMinBlocks) quantize_append_
         const int w = 2 * m < nc ? ht->width[2 * m] : 0;
         const uint32_t* hd = s_cell + 4 * w;
         s_cp[mc] = make_uint4(hd[0], hd[1], hd[2], cell_base + 8u * hd[3] - 8u * kCellMagicBits);
-        s_pk[mk] = (uint32_t)ht->pair_bit[m] | ((uint32_t)w << 16);
+        const uint32_t bit = ht->pair_bit[m];  // the pair's 2w-bit field starts here
+        s_pk[mk] = 4u * (bit >> 5) | (bit & 31u) << 8 | (uint32_t)w << 16 | (uint32_t)((bit & 31u) + 2u * w > 32u) << 31;
     }
     __syncthreads();
     // pos_start is read before the wait: no kernel of this library writes it
