@@ -250,8 +250,9 @@ __global__ void __launch_bounds__(kCkKeys) chunk_prefix_decode_kernel(CkParams p
         vdst[c8] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     }
     p.rk[row] = live ? p.kn[sl] : 0.0f;
-    // the odd key of a pair reads the even key's record: same slot / 2
-    p.rv[row] = live ? p.vn[sl] : 0.0f;
+    // the value norm times kPvScale (a power of two: exact), the factor the
+    // attention gives each prefix probability
+    p.rv[row] = live ? p.vn[sl] * kPvScale : 0.0f;
 }
 
 __global__ void __launch_bounds__(kCkThreads, 1)
@@ -532,15 +533,18 @@ __global__ void __launch_bounds__(kCkThreads, 1)
             tmem_ld32(tS + k0, sv);
             tmem_ld32(tS + k0 + 32, sv + 32);
             tmem_wait_ld();
+            // a prefix logit is S rho_k q_unscale: S rho_k here, q_unscale in
+            // the tile's log2 scale (a positive factor: the maxima commute)
+            const float cj = pre ? c * q_unscale : c;
             if (pre) {
                 const float4* rk4 = reinterpret_cast<const float4*>(&s_rho[s][0][k0]);
 #pragma unroll
                 for (int k4 = 0; k4 < 16; ++k4) {
                     const float4 r4 = rk4[k4];
-                    sv[4 * k4] *= r4.x * q_unscale;
-                    sv[4 * k4 + 1] *= r4.y * q_unscale;
-                    sv[4 * k4 + 2] *= r4.z * q_unscale;
-                    sv[4 * k4 + 3] *= r4.w * q_unscale;
+                    sv[4 * k4] *= r4.x;
+                    sv[4 * k4 + 1] *= r4.y;
+                    sv[4 * k4 + 2] *= r4.z;
+                    sv[4 * k4 + 3] *= r4.w;
                 }
             }
             if (lim < 63) {
@@ -557,7 +561,7 @@ __global__ void __launch_bounds__(kCkThreads, 1)
                                      fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
             s_mx[s][hw][r] = hmax;
             named_sync(1, 2 * kCkRows);
-            const float mt = fmaxf(hmax, s_mx[s][hw ^ 1][r]) * c;
+            const float mt = fmaxf(hmax, s_mx[s][hw ^ 1][r]) * cj;
             float f = 1.0f;
             bool raise = false;
             if (j == 0) {
@@ -620,20 +624,21 @@ __global__ void __launch_bounds__(kCkThreads, 1)
                     float pv[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        pv[e] = ex2(fmaf(sv[k + e], c, -m));
+                        pv[e] = ex2(fmaf(sv[k + e], cj, -m));
                         ls[e] += pv[e];
                     }
                     if (pre) {
+                        // P' = p rho_v / 256 (the norms are stored scaled), split
+                        // into fp16 hi + lo two at a time
                         const float4 r4 = rv4[k / 4];
-                        const float a[4] = {pv[0] * (r4.x * kPvScale), pv[1] * (r4.y * kPvScale), pv[2] * (r4.z * kPvScale),
-                                            pv[3] * (r4.w * kPvScale)};
+                        const float a[4] = {pv[0] * r4.x, pv[1] * r4.y, pv[2] * r4.z, pv[3] * r4.w};
 #pragma unroll
                         for (int e2 = 0; e2 < 2; ++e2) {
-                            const __half ha = __float2half_rn(a[2 * e2]), hb = __float2half_rn(a[2 * e2 + 1]);
-                            const __half la = __float2half_rn(a[2 * e2] - __half2float(ha));
-                            const __half lb = __float2half_rn(a[2 * e2 + 1] - __half2float(hb));
-                            hi[2 * i2 + e2] = (uint32_t)__half_as_ushort(ha) | ((uint32_t)__half_as_ushort(hb) << 16);
-                            lo[2 * i2 + e2] = (uint32_t)__half_as_ushort(la) | ((uint32_t)__half_as_ushort(lb) << 16);
+                            const __half2 h2 = __floats2half2_rn(a[2 * e2], a[2 * e2 + 1]);
+                            const float2 hf = __half22float2(h2);
+                            const __half2 l2 = __floats2half2_rn(a[2 * e2] - hf.x, a[2 * e2 + 1] - hf.y);
+                            hi[2 * i2 + e2] = *reinterpret_cast<const uint32_t*>(&h2);
+                            lo[2 * i2 + e2] = *reinterpret_cast<const uint32_t*>(&l2);
                         }
                     } else {
                         hi[2 * i2] = pack_h2(pv[0], pv[1]);
