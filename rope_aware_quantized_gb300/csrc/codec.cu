@@ -328,7 +328,7 @@ cudaError_t launch_quantize_append(const bgtq_plan& pl, cudaStream_t s, const vo
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    // Bulk appends (prefill) take the token-per-thread kernel, which reads
+    // Bulk appends (prefill) take the two-lanes-per-token kernel, which reads
     // whole fp16 rows with 16-byte loads (its grid's z holds two blocks per
     // sequence); small appends (decode), other widths and batches of more
     // than 32767 sequences the warp-per-token kernel.

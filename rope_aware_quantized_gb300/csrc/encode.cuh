@@ -40,7 +40,7 @@ struct QParams {
 };
 
 // Appends at least this long (and of the widths below) take the
-// token-per-thread bulk kernel; it launches it on `s`.
+// two-lanes-per-token bulk kernel; it launches it on `s`.
 constexpr int kBulkMinTokens = 64;
 cudaError_t launch_quantize_append_bulk(const QParams& p, int bk, int bv, int batch, cudaStream_t s);
 
