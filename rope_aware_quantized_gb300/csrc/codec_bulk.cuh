@@ -26,8 +26,8 @@ namespace {
 // consecutive positions from an even position, so the two tokens of every V
 // pair record are neighbouring lanes of one half.  All threads of a block
 // share one (sequence, head); blockIdx.z runs over the key blocks of every
-// sequence and then the value blocks (blocks are dispatched in that order, so
-// an SM runs one half of the code at a time).  The arithmetic is the
+// sequence and then the value blocks (the hardware dispatches blocks in about
+// that order, so an SM mostly runs one half of the code at a time).  The arithmetic is the
 // encoder's, operation for operation: whitening then signs (one product, as
 // the sign is +-1), the butterfly stages of each rotation piece (the pieces
 // larger than h form the prefix [0, E_h) of the codec order, pieces being laid
@@ -46,12 +46,13 @@ constexpr int kBulkMinBlocks = 5;  // resident blocks per SM the register budget
 constexpr int kRowWords = 65;
 constexpr int kBulkRowBytes = kBulkTok * kRowWords * 4;
 constexpr int kBulkPairBatch = 8;  // key pairs whose codes are computed before their fields are merged
-// Per-half tables are two rows whose second starts 16 banks after the first,
-// so the two halves of a warp read them without bank conflicts.
-constexpr int kPwRow = 72;   // float2
-constexpr int kFRow = 80;    // float
-constexpr int kCpRow = 34;   // uint4
-constexpr int kPkRow = 48;   // uint32
+// Per-half tables are two rows, the second offset from the first so that the
+// two halves of a warp, reading entry i of their own rows at once, hit
+// distinct banks: 16 banks for 4- and 8-byte entries, 8 for 16-byte ones.
+constexpr int kPwRow = 72;   // float2: 144 words
+constexpr int kFRow = 80;    // float: 80 words
+constexpr int kCpRow = 34;   // uint4: 136 words
+constexpr int kPkRow = 48;   // uint32: 48 words
 
 // The quotient y / rho correctly rounded, as __fdiv_rn gives it, from the
 // correctly rounded reciprocal r = 1/rho (r = 0 when rho = 0, which makes the
