@@ -27,11 +27,13 @@
 //   warps 0-3, 4-7  softmax warpgroups on the same rows (thread i = row i =
 //              tensor-memory lane i), each taking 64 of a tile's 128 keys
 //   warp 8     MMA issue (one thread), owner of the tensor memory
-//   warp 9     TMA: Q (again after the prefix, the rotated query having taken
-//              its place), the prefix tiles and norms, the chunk's K/V tiles
-// Tensor memory: S in two buffers (columns 0 and 128), O at 256; P
-// overwrites the S it came from, 32 keys per 32 columns: the hi parts of the
-// chunk's 16 key pairs in its first 16 columns, the lo parts in the next 16.
+//   warp 9     TMA: Q, the prefix tiles and norms, the chunk's K/V tiles
+// Tensor memory: S in two buffers (columns 0 and 128), O at 256, the rotated
+// query's hi and lo parts at 384 and 448 (the A operand of the prefix S
+// MMAs, so that only the key tile is read from shared memory; the chunk's
+// own tiles take Q from shared memory); P overwrites the S it came from, 32
+// keys per 32 columns: the hi parts of the chunk's 16 key pairs in its first
+// 16 columns, the lo parts in the next 16.
 // MMA order: S(0), S(1), then PV(j), S(j+2) for every tile j.
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -51,11 +53,11 @@ constexpr int kCkKeys = 128;
 constexpr int kCkThreads = 320;
 constexpr uint32_t kCkTile = 128 * kD * 2;  // 32 KB
 constexpr uint32_t kCkBox = kCkTile / 2;
-constexpr uint32_t kCOffQ = 0;              // Q, or the rotated query's hi part
-constexpr uint32_t kCOffQL = kCkTile;       // the rotated query's lo part
-constexpr uint32_t kCOffK = 2 * kCkTile;    // K stage s at + s kCkTile
-constexpr uint32_t kCOffV = 4 * kCkTile;    // V stage s at + s kCkTile
-constexpr uint32_t kCkSmem = 6 * kCkTile + 1024;
+constexpr uint32_t kCOffQ = 0;              // Q
+constexpr uint32_t kCOffK = kCkTile;        // K stage s at + s kCkTile
+constexpr uint32_t kCOffV = 3 * kCkTile;    // V stage s at + s kCkTile
+constexpr uint32_t kCkSmem = 5 * kCkTile + 1024;
+constexpr uint32_t kCColQ = 384;            // tensor-memory columns of the rotated query (hi; lo at + 64)
 constexpr int kRawK = 4 * 3 + 1;            // words of a staged K record (bK <= 3) + a zero word
 constexpr int kRawV = 8 * 4 + 1;            // words of a staged V pair record (bV <= 4) + a zero word
 constexpr int kMmaWarp = 8, kTmaWarp = 9;
@@ -63,18 +65,17 @@ constexpr float kHeadroomC = 8.0f;
 constexpr float kPvScale = 1.0f / 256.0f;   // prefix probabilities * rho_v are stored scaled by this
 
 enum {
-    kCQ = 0,        // Q copied (phase 0), copied again for the chunk's tiles (phase 1)
-    kCQR = 1,       // rotated query written (128 arrivals)
-    kCPSD = 2,      // every prefix S done: the Q region may be reloaded
-    kCKF = 3,       // K tile of stage s copied, 3 + s
-    kCVF = 5,       // V tile (and, for a prefix tile, its norms) of stage s copied
-    kCKE = 7,       // K stage s free again (MMA commit)
-    kCVE = 9,
-    kCS = 11,       // S buffer b computed, 11 + b
-    kCP = 13,       // P of the current tile written (128 arrivals)
-    kCO = 14,       // PV of a tile done (one phase per tile)
-    kCDrain = 15,
-    kCNumBars = 16
+    kCQ = 0,        // Q copied
+    kCQR = 1,       // rotated query written to tensor memory (128 arrivals)
+    kCKF = 2,       // K tile of stage s copied, 2 + s
+    kCVF = 4,       // V tile (and, for a prefix tile, its norms) of stage s copied
+    kCKE = 6,       // K stage s free again (MMA commit)
+    kCVE = 8,
+    kCS = 10,       // S buffer b computed, 10 + b
+    kCP = 12,       // P of the current tile written (256 arrivals)
+    kCO = 13,       // PV of a tile done (one phase per tile)
+    kCDrain = 14,
+    kCNumBars = 15
 };
 
 struct CkParams {
@@ -334,8 +335,8 @@ __global__ void __launch_bounds__(kCkThreads, 1)
     const uint32_t tmem = s_tmem;
 
     if (warp == kTmaWarp) {
-        // ---- TMA: Q; prefix tiles (decoded rows and their norms); Q again;
-        // the chunk's K/V tiles
+        // ---- TMA: Q; prefix tiles (decoded rows and their norms); the
+        // chunk's K/V tiles
         if (lane == 0) {
             const int qrow = (b * p.H * p.G + hq) * p.C + q0;
             const int krow = (b * p.H + h) * p.C;
@@ -344,17 +345,10 @@ __global__ void __launch_bounds__(kCkThreads, 1)
             for (int x = 0; x < 2; ++x) tma_load_2d(sbase + kCOffQ + x * kCkBox, &tq, 64 * x, qrow, CBAR(kCQ));
             int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
             int uses[2] = {0, 0};
-            bool q_again = false;
             for (int j = 0; j < nt; ++j) {
                 const int s = j & 1;
                 const uint32_t par = (uint32_t)((j >> 1) - 1) & 1u;
                 const bool pre = j < np;
-                if (j == np && np > 0) {
-                    if (!mbar_wait(CBAR(kCPSD), 0, abort_flag, p.status)) break;
-                    mbar_expect_tx(CBAR(kCQ), kCkTile);
-                    for (int x = 0; x < 2; ++x) tma_load_2d(sbase + kCOffQ + x * kCkBox, &tq, 64 * x, qrow, CBAR(kCQ));
-                    q_again = true;
-                }
                 if (j >= 2 && !mbar_wait(CBAR(kCKE + s), par, abort_flag, p.status)) break;
                 mbar_expect_tx(CBAR(kCKF + s), kCkTile);
                 for (int x = 0; x < 2; ++x) {
@@ -382,7 +376,7 @@ __global__ void __launch_bounds__(kCkThreads, 1)
                 ++uses[s];
             }
             // every copy issued has landed before the CTA ends
-            mbar_wait(CBAR(kCQ), q_again ? 1u : 0u, abort_flag, p.status, false);
+            mbar_wait(CBAR(kCQ), 0u, abort_flag, p.status, false);
             for (int s = 0; s < 2; ++s) {
                 if (last_k[s] >= 0) mbar_wait(CBAR(kCKF + s), (uint32_t)last_k[s] & 1u, abort_flag, p.status, false);
                 if (last_v[s] >= 0) mbar_wait(CBAR(kCVF + s), (uint32_t)last_v[s] & 1u, abort_flag, p.status, false);
@@ -400,21 +394,26 @@ __global__ void __launch_bounds__(kCkThreads, 1)
             auto issue_s = [&](int j) -> bool {
                 const int s = j & 1;
                 const uint32_t ka = sbase + kCOffK + s * kCkTile, d = tmem + 128u * (uint32_t)s;
-                if (j == np && np > 0 && !mbar_wait(CBAR(kCQ), 1, abort_flag, p.status)) return false;
                 if (!mbar_wait(CBAR(kCKF + s), (uint32_t)(cnt_k[s]++) & 1u, abort_flag, p.status)) return false;
                 tc_fence_after();
-                const int parts = j < np ? 2 : 1;  // the rotated query's hi and lo parts
-                for (int part = 0; part < parts; ++part) {
-                    const uint32_t qa = sbase + (part ? kCOffQL : kCOffQ);
+                if (j < np) {
+                    // the rotated query's hi and lo parts from tensor memory
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int k = 0; k < kD / 16; ++k) {
+                            const uint32_t off = (uint32_t)(k >> 2) * kCkBox + (uint32_t)(k & 3) * 32;
+                            mma_ts(d, tmem + kCColQ + 64u * (uint32_t)part + 8u * (uint32_t)k, smem_desc(ka + off, 16, 1024),
+                                   idS, (part | k) ? 1u : 0u);
+                        }
+                } else {
 #pragma unroll
                     for (int k = 0; k < kD / 16; ++k) {
                         const uint32_t off = (uint32_t)(k >> 2) * kCkBox + (uint32_t)(k & 3) * 32;
-                        mma_ss(d, smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), idS, (part | k) ? 1u : 0u);
+                        mma_ss(d, smem_desc(sbase + kCOffQ + off, 16, 1024), smem_desc(ka + off, 16, 1024), idS, k ? 1u : 0u);
                     }
                 }
                 mma_commit(CBAR(kCS + s));
                 mma_commit(CBAR(kCKE + s));
-                if (j == np - 1) mma_commit(CBAR(kCPSD));
                 return true;
             };
             auto issue_pv = [&](int j) -> bool {
@@ -483,26 +482,25 @@ __global__ void __launch_bounds__(kCkThreads, 1)
     #pragma unroll
                     for (int j = 0; j < kD; ++j) x[j] *= up;
                 }
+                // into tensor memory, row r = lane r: column kCColQ + c holds
+                // dims 2c, 2c + 1 of the hi part, kCColQ + 64 + c of the lo part
+                const uint32_t tq_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kCColQ;
     #pragma unroll
-                for (int c8 = 0; c8 < kD / 8; ++c8) {
-                    uint32_t hp[4], lp[4];
+                for (int c16 = 0; c16 < kD / 32; ++c16) {
+                    uint32_t hp[16], lp[16];
     #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const __half h0 = __float2half_rn(x[8 * c8 + 2 * e]), h1 = __float2half_rn(x[8 * c8 + 2 * e + 1]);
-                        const __half l0 = __float2half_rn(x[8 * c8 + 2 * e] - __half2float(h0));
-                        const __half l1 = __float2half_rn(x[8 * c8 + 2 * e + 1] - __half2float(h1));
+                    for (int e = 0; e < 16; ++e) {
+                        const __half h0 = __float2half_rn(x[32 * c16 + 2 * e]), h1 = __float2half_rn(x[32 * c16 + 2 * e + 1]);
+                        const __half l0 = __float2half_rn(x[32 * c16 + 2 * e] - __half2float(h0));
+                        const __half l1 = __float2half_rn(x[32 * c16 + 2 * e + 1] - __half2float(h1));
                         hp[e] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
                         lp[e] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
                     }
-                    const uint32_t off = swz_off(r, 8 * c8);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + kCOffQ + off), "r"(hp[0]), "r"(hp[1]),
-                                 "r"(hp[2]), "r"(hp[3])
-                                 : "memory");
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + kCOffQL + off), "r"(lp[0]),
-                                 "r"(lp[1]), "r"(lp[2]), "r"(lp[3])
-                                 : "memory");
+                    tmem_st16(tq_row + 16u * (uint32_t)c16, hp);
+                    tmem_st16(tq_row + 64u + 16u * (uint32_t)c16, lp);
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                tmem_wait_st();
+                tc_fence_before();
                 mbar_arrive(CBAR(kCQR));
                 s_qun[r] = q_unscale;
             }
@@ -700,7 +698,7 @@ bool chunk_descriptors_valid() {
     for (uint32_t base = 0; base + kCkSmem <= kMaxSmem + 1024; base += 1024)
         for (int k = 0; k < kD / 16; ++k) {
             const uint32_t off = (uint32_t)(k >> 2) * kCkBox + (uint32_t)(k & 3) * 32;
-            for (uint32_t a : {base + kCOffQ + off, base + kCOffQL + off, base + kCOffK + kCkTile + off})
+            for (uint32_t a : {base + kCOffQ + off, base + kCOffK + kCkTile + off})
                 if (!smem_desc_ok(a, 16, 1024)) return false;
             if (!smem_desc_ok(base + kCOffV + kCkTile + (uint32_t)k * 2048, kCkBox, 1024)) return false;
         }
