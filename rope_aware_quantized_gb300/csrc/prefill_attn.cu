@@ -117,7 +117,8 @@ __device__ __forceinline__ void softmax_rows(const PfParams& p, uint32_t tmem, i
         float s[kTcKeys];
 #pragma unroll
         for (int q = 0; q < kTcKeys / 32; ++q) tmem_ld32(tS + 32 * q, s + 32 * q);
-        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < kTcKeys / 32; ++q) tmem_wait_ld32(s + 32 * q);
         if (j == nkt - 1) {  // the diagonal tile: keys after the row, and past the prompt
             const int lim = min(row, p.T - 1) - j * kTcKeys;
 #pragma unroll
@@ -148,7 +149,7 @@ __device__ __forceinline__ void softmax_rows(const PfParams& p, uint32_t tmem, i
             for (int q = 0; q < kD / 32; ++q) {
                 float o[32];
                 tmem_ld32(tO + 32 * q, o);
-                tmem_wait_ld();
+                tmem_wait_ld32(o);
                 uint32_t w[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(o[i] * f);
@@ -179,7 +180,7 @@ __device__ __forceinline__ void softmax_rows(const PfParams& p, uint32_t tmem, i
     for (int q = 0; q < kD / 32; ++q) {
         float o[32];
         tmem_ld32(tO + 32 * q, o);
-        tmem_wait_ld();
+        tmem_wait_ld32(o);
         if (row >= p.T) continue;
         if (p.out_dtype) {
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + o0 + 32 * q);

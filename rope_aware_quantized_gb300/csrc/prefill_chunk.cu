@@ -41,6 +41,7 @@
 
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "bgtq_internal.h"
 #include "tc_common.cuh"
@@ -509,32 +510,34 @@ __global__ void __launch_bounds__(kCkThreads, 1)
         }
         float m = 0.0f, l = 0.0f;  // l: this warpgroup's half of the row sum
         const uint32_t tO = tmem + lanes + 256u;
-        // (the combined decision below is the loop's only exit: a warpgroup
-        // never leaves alone)
-        for (int j = 0; j < nt; ++j) {
+        // Tile j of the prefix (kPre) or of the chunk.  The combined decision
+        // at its first named barrier is the only way out (false: both
+        // warpgroups leave), so a warpgroup never leaves alone.
+        auto tile = [&](int j, auto pre_tag) -> bool {
+            constexpr bool kPre = decltype(pre_tag)::value;
             const int s = j & 1;
             const uint32_t tS = tmem + lanes + 128u * (uint32_t)s;
-            const bool pre = j < np;
             // a prefix tile's norms arrive with its V tile
             const bool got = ok && mbar_wait(CBAR(kCS + s), (uint32_t)(j >> 1) & 1u, abort_flag, p.status) &&
-                             (!pre || mbar_wait(CBAR(kCVF + s), (uint32_t)(j >> 1) & 1u, abort_flag, p.status));
+                             (!kPre || mbar_wait(CBAR(kCVF + s), (uint32_t)(j >> 1) & 1u, abort_flag, p.status));
             if (!named_sync_and(1, 2 * kCkRows, got)) {
                 ok = false;
-                break;
+                return false;
             }
             tc_fence_after();
             const int k0 = 64 * hw;  // the warpgroup's first key of the tile
-            const int lim = (pre ? P0 - 1 - j * kCkKeys                                    // keys past the prefix
-                                 : (j == nt - 1 ? min(row, p.C - 1) - (j - np) * kCkKeys   // the chunk's diagonal
-                                                : kCkKeys)) - k0;
+            const int lim = (kPre ? P0 - 1 - j * kCkKeys                                    // keys past the prefix
+                                  : (j == nt - 1 ? min(row, p.C - 1) - (j - np) * kCkKeys   // the chunk's diagonal
+                                                 : kCkKeys)) - k0;
             float sv[64];
             tmem_ld32(tS + k0, sv);
             tmem_ld32(tS + k0 + 32, sv + 32);
-            tmem_wait_ld();
+            tmem_wait_ld32(sv);
+            tmem_wait_ld32(sv + 32);
             // a prefix logit is S rho_k q_unscale: S rho_k here, q_unscale in
             // the tile's log2 scale (a positive factor: the maxima commute)
-            const float cj = pre ? c * q_unscale : c;
-            if (pre) {
+            const float cj = kPre ? c * q_unscale : c;
+            if constexpr (kPre) {
                 const float4* rk4 = reinterpret_cast<const float4*>(&s_rho[s][0][k0]);
 #pragma unroll
                 for (int k4 = 0; k4 < 16; ++k4) {
@@ -570,42 +573,21 @@ __global__ void __launch_bounds__(kCkThreads, 1)
                 l *= f;
                 raise = true;
             }
-            const bool to_dims = np > 0 && j == np;  // O leaves the value codec domain
-            if (to_dims || __any_sync(0xffffffffu, raise)) {
-                // PV of tile j - 1 must be done before O is touched; warpgroup 0
-                // takes the whole row when it changes domain, else each its half
-                if (to_dims && hw == 1) {
-                    // (nothing: warpgroup 0 rescales the whole row with the transform)
-                } else if (!__all_sync(0xffffffffu, mbar_wait(CBAR(kCO), (uint32_t)(j - 1) & 1u, abort_flag, p.status))) {
+            if (__any_sync(0xffffffffu, raise)) {
+                // PV of tile j - 1 must be done before the warpgroup rescales its half of O
+                if (!__all_sync(0xffffffffu, mbar_wait(CBAR(kCO), (uint32_t)(j - 1) & 1u, abort_flag, p.status))) {
                     ok = false;  // both leave at the next tile's decision
                 } else {
                     tc_fence_after();
-                    if (to_dims) {
-                        float o[kD];
-#pragma unroll
-                        for (int q4 = 0; q4 < kD / 32; ++q4) tmem_ld32(tO + 32 * q4, o + 32 * q4);
-                        tmem_wait_ld();
-                        int nh_all[7];
-                        butterflies128<true>(o, nh_all);
-                        const float g = f * (1.0f / kPvScale) * 0.08838834764831845f;  // 1/sqrt(128)
-#pragma unroll
-                        for (int q4 = 0; q4 < kD / 32; ++q4) {
-                            uint32_t w[32];
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(o[32 * q4 + i] * (g * s_vsign[32 * q4 + i]));
-                            tmem_st32(tO + 32 * q4, w);
-                        }
-                    } else {
 #pragma unroll 1
-                        for (int q4 = 2 * hw; q4 < 2 * hw + 2; ++q4) {
-                            float o[32];
-                            tmem_ld32(tO + 32 * q4, o);
-                            tmem_wait_ld();
-                            uint32_t w[32];
+                    for (int q4 = 2 * hw; q4 < 2 * hw + 2; ++q4) {
+                        float o[32];
+                        tmem_ld32(tO + 32 * q4, o);
+                        tmem_wait_ld32(o);
+                        uint32_t w[32];
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(o[i] * f);
-                            tmem_st32(tO + 32 * q4, w);
-                        }
+                        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(o[i] * f);
+                        tmem_st32(tO + 32 * q4, w);
                     }
                 }
             }
@@ -625,7 +607,7 @@ __global__ void __launch_bounds__(kCkThreads, 1)
                         pv[e] = ex2(fmaf(sv[k + e], cj, -m));
                         ls[e] += pv[e];
                     }
-                    if (pre) {
+                    if constexpr (kPre) {
                         // P' = p rho_v / 256 (the norms are stored scaled), split
                         // into fp16 hi + lo two at a time
                         const float4 r4 = rv4[k / 4];
@@ -644,13 +626,51 @@ __global__ void __launch_bounds__(kCkThreads, 1)
                     }
                 }
                 tmem_st16(tS + k0 + 32 * qh, hi);
-                if (pre) tmem_st16(tS + k0 + 32 * qh + 16, lo);
+                if constexpr (kPre) tmem_st16(tS + k0 + 32 * qh + 16, lo);
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(CBAR(kCP));
+            return true;
+        };
+        for (int j = 0; j < np; ++j)
+            if (!tile(j, std::true_type{})) break;
+        if (np > 0) {  // (uniform; the chunk has at least one tile)
+            // O leaves the value codec domain before the chunk's own tiles:
+            // warpgroup 0 takes the whole row once PV of the last prefix tile
+            // is done; both then pass one combined decision, so that neither
+            // touches O before the transform is complete
+            bool good = ok;
+            if (hw == 0 && good) {
+                good = __all_sync(0xffffffffu, mbar_wait(CBAR(kCO), (uint32_t)(np - 1) & 1u, abort_flag, p.status));
+                if (good) {
+                    tc_fence_after();
+                    float o[kD];
+#pragma unroll
+                    for (int q4 = 0; q4 < kD / 32; ++q4) tmem_ld32(tO + 32 * q4, o + 32 * q4);
+#pragma unroll
+                    for (int q4 = 0; q4 < kD / 32; ++q4) tmem_wait_ld32(o + 32 * q4);
+                    int nh_all[7];
+                    butterflies128<true>(o, nh_all);
+                    const float g = (1.0f / kPvScale) * 0.08838834764831845f;  // 1/sqrt(128)
+#pragma unroll
+                    for (int q4 = 0; q4 < kD / 32; ++q4) {
+                        uint32_t w[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(o[32 * q4 + i] * (g * s_vsign[32 * q4 + i]));
+                        tmem_st32(tO + 32 * q4, w);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                }
+            }
+            ok = named_sync_and(1, 2 * kCkRows, good);
+            tc_fence_after();
         }
+        if (ok)
+            for (int j = np; j < nt; ++j)
+                if (!tile(j, std::false_type{})) break;
         // the row sums of both halves; the output row, 64 columns per warpgroup
         s_lsum[hw][r] = l;
         const bool fin = ok && mbar_wait(CBAR(kCO), (uint32_t)(nt - 1) & 1u, abort_flag, p.status);
@@ -662,7 +682,7 @@ __global__ void __launch_bounds__(kCkThreads, 1)
             for (int q4 = 2 * hw; q4 < 2 * hw + 2; ++q4) {
                 float o[32];
                 tmem_ld32(tO + 32 * q4, o);
-                tmem_wait_ld();
+                tmem_wait_ld32(o);
                 if (row >= p.C) continue;
                 if (p.out_dtype) {
                     float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + o0 + 32 * q4);
