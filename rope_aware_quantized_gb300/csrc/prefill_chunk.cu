@@ -74,9 +74,12 @@ enum {
     kCVE = 8,
     kCS = 10,       // S buffer b computed, 10 + b
     kCP = 12,       // P of the current tile written (256 arrivals)
-    kCO = 13,       // PV of a tile done (one phase per tile)
-    kCDrain = 14,
-    kCNumBars = 15
+    kCO = 13,       // PV of a tile done (one phase per tile; waited on only at a tile
+                    // whose S wait proves PV of the tile before last done, so that the
+                    // parity names one phase)
+    kCDrain = 14,   // every MMA done (one phase)
+    kCOPre = 15,    // PV of the last prefix tile done (one phase)
+    kCNumBars = 16
 };
 
 struct CkParams {
@@ -431,6 +434,7 @@ __global__ void __launch_bounds__(kCkThreads, 1)
                                smem_desc(va + 2048u * k, kCkBox, 1024), idO, (j > 0 || part > 0 || k > 0) ? 1u : 0u);
                 mma_commit(CBAR(kCO));
                 mma_commit(CBAR(kCVE + s));
+                if (j == np - 1) mma_commit(CBAR(kCOPre));
                 return true;
             };
             if (ok) ok = issue_s(0);
@@ -529,35 +533,36 @@ __global__ void __launch_bounds__(kCkThreads, 1)
             const int lim = (kPre ? P0 - 1 - j * kCkKeys                                    // keys past the prefix
                                   : (j == nt - 1 ? min(row, p.C - 1) - (j - np) * kCkKeys   // the chunk's diagonal
                                                  : kCkKeys)) - k0;
-            float sv[64];
-            tmem_ld32(tS + k0, sv);
-            tmem_ld32(tS + k0 + 32, sv + 32);
-            tmem_wait_ld32(sv);
-            tmem_wait_ld32(sv + 32);
             // a prefix logit is S rho_k q_unscale: S rho_k here, q_unscale in
             // the tile's log2 scale (a positive factor: the maxima commute)
             const float cj = kPre ? c * q_unscale : c;
-            if constexpr (kPre) {
-                const float4* rk4 = reinterpret_cast<const float4*>(&s_rho[s][0][k0]);
-#pragma unroll
-                for (int k4 = 0; k4 < 16; ++k4) {
-                    const float4 r4 = rk4[k4];
-                    sv[4 * k4] *= r4.x;
-                    sv[4 * k4 + 1] *= r4.y;
-                    sv[4 * k4 + 2] *= r4.z;
-                    sv[4 * k4 + 3] *= r4.w;
-                }
-            }
-            if (lim < 63) {
-#pragma unroll
-                for (int k = 0; k < 64; ++k)
-                    if (k > lim) sv[k] = -INFINITY;
-            }
+            float sv[64];
             float mxa[8];
+            tmem_ld32(tS + k0, sv);
+            tmem_wait_ld32(sv);
+            tmem_ld32(tS + k0 + 32, sv + 32);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mxa[i] = sv[i];
+            for (int hh = 0; hh < 2; ++hh) {
+                if (hh == 1) tmem_wait_ld32(sv + 32);
+                if constexpr (kPre) {
+                    const float4* rk4 = reinterpret_cast<const float4*>(&s_rho[s][0][k0 + 32 * hh]);
 #pragma unroll
-            for (int k = 8; k < 64; ++k) mxa[k & 7] = fmaxf(mxa[k & 7], sv[k]);
+                    for (int k4 = 0; k4 < 8; ++k4) {
+                        const float4 r4 = rk4[k4];
+                        sv[32 * hh + 4 * k4] *= r4.x;
+                        sv[32 * hh + 4 * k4 + 1] *= r4.y;
+                        sv[32 * hh + 4 * k4 + 2] *= r4.z;
+                        sv[32 * hh + 4 * k4 + 3] *= r4.w;
+                    }
+                }
+                if (lim < 32 * hh + 31) {
+#pragma unroll
+                    for (int k = 32 * hh; k < 32 * hh + 32; ++k)
+                        if (k > lim) sv[k] = -INFINITY;
+                }
+#pragma unroll
+                for (int k = 32 * hh; k < 32 * hh + 32; ++k) mxa[k & 7] = k < 8 ? sv[k] : fmaxf(mxa[k & 7], sv[k]);
+            }
             const float hmax = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
                                      fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
             s_mx[s][hw][r] = hmax;
@@ -574,7 +579,9 @@ __global__ void __launch_bounds__(kCkThreads, 1)
                 raise = true;
             }
             if (__any_sync(0xffffffffu, raise)) {
-                // PV of tile j - 1 must be done before the warpgroup rescales its half of O
+                // PV of tile j - 1 must be done before the warpgroup rescales its half
+                // of O (S of this tile was issued after PV of tile j - 2, so kCO is at
+                // phase j - 1 or past it and the parity names that phase)
                 if (!__all_sync(0xffffffffu, mbar_wait(CBAR(kCO), (uint32_t)(j - 1) & 1u, abort_flag, p.status))) {
                     ok = false;  // both leave at the next tile's decision
                 } else {
@@ -643,7 +650,7 @@ __global__ void __launch_bounds__(kCkThreads, 1)
             // touches O before the transform is complete
             bool good = ok;
             if (hw == 0 && good) {
-                good = __all_sync(0xffffffffu, mbar_wait(CBAR(kCO), (uint32_t)(np - 1) & 1u, abort_flag, p.status));
+                good = __all_sync(0xffffffffu, mbar_wait(CBAR(kCOPre), 0u, abort_flag, p.status));
                 if (good) {
                     tc_fence_after();
                     float o[kD];
@@ -673,7 +680,9 @@ __global__ void __launch_bounds__(kCkThreads, 1)
                 if (!tile(j, std::false_type{})) break;
         // the row sums of both halves; the output row, 64 columns per warpgroup
         s_lsum[hw][r] = l;
-        const bool fin = ok && mbar_wait(CBAR(kCO), (uint32_t)(nt - 1) & 1u, abort_flag, p.status);
+        // (the drain barrier has one phase: PV of the tile before last may
+        // still run here, which a parity wait on kCO could not tell apart)
+        const bool fin = ok && mbar_wait(CBAR(kCDrain), 0u, abort_flag, p.status);
         if (named_sync_and(1, 2 * kCkRows, fin)) {
             tc_fence_after();
             const float inv = 1.0f / (s_lsum[0][r] + s_lsum[1][r]);
