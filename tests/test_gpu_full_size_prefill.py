@@ -8,8 +8,8 @@ the benchmark times, checked on samples the oracle computes one by one.
   the oracle's encoder bit for bit.
 * bgtq_prefill_chunk_attn of an 8192-token chunk onto 32768 cached tokens of
   the same layer (16 query heads, fp16 output, the workspace sized by
-  bgtq_prefill_chunk_workspace): sampled rows of two query heads (one per KV
-  head; the first row, tile edges, the last row) against the oracle's float64
+  bgtq_prefill_chunk_workspace): the first row of every warp of every query
+  block and the last row, of one query head per KV head, against the oracle's float64
   attention over the dequantised prefix and the chunk's own keys 0 .. i, within
   the decode tolerance (an fp16 output may differ by half a binary16 ulp more);
   the chunk's own records equal one append of them.
@@ -86,15 +86,17 @@ def test_chunk_of_8192_onto_32768_cached_sampled_rows():
     assert st.item() == 0
     got = out.float().cpu().numpy().astype(np.float64)
     assert np.all(np.isfinite(got))
-    rows = [0, 1, 127, 128, 4095, 4096, C - 2, C - 1]
+    # the first row of every warp of every query block (a fault confined to one
+    # warp's tensor-memory lanes shows in it), and the last row
+    rows = list(range(0, C, 32)) + [C - 1]
     for h, hs in enumerate(heads):
         enc = O.encode_head(hs, li.k[h][:P0], li.v[h][:P0])
-        for gq in (h * G, h * G + G - 1):
-            for i in rows:
-                keys = np.concatenate([enc["khat"], li.k[h][P0:P0 + i + 1].astype(np.float64)])
-                vals = np.concatenate([enc["vhat"], li.v[h][P0:P0 + i + 1].astype(np.float64)])
-                want = O.attention(q[0, gq, i][None], keys, vals)
-                check_close(got[0, gq, i][None], want, fp16_out=True)
+        gq = h * G + h  # query head h of KV head h
+        for i in rows:
+            keys = np.concatenate([enc["khat"], li.k[h][P0:P0 + i + 1].astype(np.float64)])
+            vals = np.concatenate([enc["vhat"], li.v[h][P0:P0 + i + 1].astype(np.float64)])
+            want = O.attention(q[0, gq, i][None], keys, vals)
+            check_close(got[0, gq, i][None], want, fp16_out=True)
     # the chunk's records: an append of the chunk's tokens at P0
     kc, vc, kn, vn = cache_arrays(plan, cache, H, BPK // 128, VB)
     for h, hs in enumerate(heads):
