@@ -35,6 +35,10 @@
 // keys per 32 columns: the hi parts of the chunk's 16 key pairs in its first
 // 16 columns, the lo parts in the next 16.
 // MMA order: S(0), S(1), then PV(j), S(j+2) for every tile j.
+// Waits on O: a rescale at tile j waits for PV(j - 1) on the per-tile PV
+// barrier (its parity names one phase there, S(j) having been issued after
+// PV(j - 2)); the move to the value dims after the prefix and the final read
+// wait on barriers committed once (PV of the last prefix tile; every MMA).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
