@@ -177,22 +177,13 @@ __device__ __forceinline__ float half_scale_norm(float (&z)[64], int n, const fl
 template <int BK>
 __device__ __forceinline__ void bulk_key_half(const QParams& p, int nc, int hf, const int* s_end, const float2* pw,
                                               const float* is, const uint4* cp, const uint32_t* pk, uint32_t* row,
-                                              uint32_t* rec, bool act, size_t unit, int ps, int64_t pos, int64_t end,
-                                              int64_t sl) {
-    uint4 w4[8];
-    if (act) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.k + (unit * p.t_new + (size_t)(pos - ps)) * kD) + 8 * hf;
+                                              uint32_t* rec, const uint4 (&w4)[8], bool act, size_t unit, int64_t pos,
+                                              int64_t end, int64_t sl) {
+    if (act && p.recent > 0 && pos >= end - p.recent) {
+        // fp16 recent-key ring: the key as given, slot pos mod W
+        uint4* rdst = reinterpret_cast<uint4*>(p.k_recent + (unit * p.recent + pos % p.recent) * kD) + 8 * hf;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) w4[i] = __ldg(src + i);
-        if (p.recent > 0 && pos >= end - p.recent) {
-            // fp16 recent-key ring: the key as given, slot pos mod W
-            uint4* rdst = reinterpret_cast<uint4*>(p.k_recent + (unit * p.recent + pos % p.recent) * kD) + 8 * hf;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) rdst[i] = w4[i];
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) w4[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = 0; i < 8; ++i) rdst[i] = w4[i];
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -263,27 +254,20 @@ __device__ __forceinline__ void bulk_key_half(const QParams& p, int nc, int hf, 
 // (even, odd token: lanes l, l ^ 1) of a half shares those words.  Every lane
 // of the warp takes part.
 template <int BV>
-__device__ __forceinline__ void bulk_value_half(const QParams& p, int hf, int par, const int* s_end, const float* sv,
-                                                const uint32_t* s_cell, uint32_t cell_base, bool act, size_t unit,
-                                                int ps, int64_t pos, int64_t end, int64_t sl) {
+__device__ __forceinline__ void bulk_value_half(const QParams& p, int hf, int par, const float* sv,
+                                                const uint32_t* s_cell, uint32_t cell_base, const uint4 (&w4)[8],
+                                                bool act, int ps, int64_t pos, int64_t end, int64_t sl) {
     float z[64];
-    if (act) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.v + (unit * p.t_new + (size_t)(pos - ps)) * kD) + 8 * hf;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint4 w4 = __ldg(src + i);
+    for (int i = 0; i < 8; ++i) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t wk = k == 0 ? w4.x : k == 1 ? w4.y : k == 2 ? w4.z : w4.w;
-                const float f0 = __half2float(__ushort_as_half((unsigned short)(wk & 0xffffu)));
-                const float f1 = __half2float(__ushort_as_half((unsigned short)(wk >> 16)));
-                z[8 * i + 2 * k] = __fmul_rn(f0, sv[8 * i + 2 * k]);
-                z[8 * i + 2 * k + 1] = __fmul_rn(f1, sv[8 * i + 2 * k + 1]);
-            }
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t wk = k == 0 ? w4[i].x : k == 1 ? w4[i].y : k == 2 ? w4[i].z : w4[i].w;
+            const float f0 = __half2float(__ushort_as_half((unsigned short)(wk & 0xffffu)));
+            const float f1 = __half2float(__ushort_as_half((unsigned short)(wk >> 16)));
+            z[8 * i + 2 * k] = __fmul_rn(f0, sv[8 * i + 2 * k]);
+            z[8 * i + 2 * k + 1] = __fmul_rn(f1, sv[8 * i + 2 * k + 1]);
         }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) z[i] = 0.0f;
     }
     half_stage<1, true>(z, 64);
     half_stage<2, true>(z, 64);
@@ -374,6 +358,35 @@ __global__ void __launch_bounds__(kBulkThreads, kBulkMinBlocks) quantize_append_
     const bool is_v = (int)blockIdx.z >= nbz;
     const int h = blockIdx.y, b = (int)blockIdx.z - (is_v ? nbz : 0);
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // pos_start is read before the wait: no kernel of this library writes it
+    const int ps = p.pos_start[b];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (ps < 0 || (int64_t)ps + p.t_new > p.cap) {
+        if (blockIdx.x == 0 && h == 0 && tid == 0 && p.status) {
+            atomicOr(p.status, BGTQ_STATUS_APPEND_CAPACITY);
+            debug_in_range(false, p.status);  // positions past the capacity
+        }
+        return;
+    }
+    const int warp = tid >> 5, lane = tid & 31, hf = lane >> 4;
+    const int tk = 16 * warp + (lane & 15);  // the block's token of this lane
+    const int64_t end = (int64_t)ps + p.t_new;
+    const int64_t pos = (int64_t)(ps & ~1) + (int64_t)blockIdx.x * kBulkTok + tk;
+    const bool act = pos >= ps && pos < end;
+    const size_t unit = (size_t)b * p.H + h;
+    // this half of the token's fp16 row (zeros for an inactive token): issued
+    // first, so that the plan-static set-up below runs while it is in flight
+    uint4 w4[8];
+    if (act) {
+        const __half* x = is_v ? p.v : p.k;
+        const uint4* src = reinterpret_cast<const uint4*>(x + (unit * p.t_new + (size_t)(pos - ps)) * kD) + 8 * hf;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w4[i] = __ldg(src + i);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w4[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    const int64_t sl = act ? p.map.slot(b, h, pos) : 0;  // record location of token `pos`
 
     // ---- plan-static set-up (thread tid prepares codec coordinate tid)
     const HeadTab* ht = p.heads + h;
@@ -407,29 +420,12 @@ __global__ void __launch_bounds__(kBulkThreads, kBulkMinBlocks) quantize_append_
         s_pk[mk] = 4u * (bit >> 5) | (bit & 31u) << 8 | (uint32_t)w << 16 | (uint32_t)((bit & 31u) + 2u * w > 32u) << 31;
     }
     __syncthreads();
-    // pos_start is read before the wait: no kernel of this library writes it
-    const int ps = p.pos_start[b];
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (ps < 0 || (int64_t)ps + p.t_new > p.cap) {
-        if (blockIdx.x == 0 && h == 0 && tid == 0 && p.status) {
-            atomicOr(p.status, BGTQ_STATUS_APPEND_CAPACITY);
-            debug_in_range(false, p.status);  // positions past the capacity
-        }
-        return;
-    }
-    const int warp = tid >> 5, lane = tid & 31, hf = lane >> 4;
-    const int tk = 16 * warp + (lane & 15);  // the block's token of this lane
-    const int64_t end = (int64_t)ps + p.t_new;
-    const int64_t pos = (int64_t)(ps & ~1) + (int64_t)blockIdx.x * kBulkTok + tk;
-    const bool act = pos >= ps && pos < end;
-    const size_t unit = (size_t)b * p.H + h;
-    const int64_t sl = act ? p.map.slot(b, h, pos) : 0;  // record location of token `pos`
     if (sl < 0 && p.status && hf == 0) atomicOr(p.status, BGTQ_STATUS_PAGE_RANGE);
     if (!is_v)
         bulk_key_half<BK>(p, nc, hf, s_end, s_pw + hf * kPwRow, s_is + hf * kFRow, s_cp + hf * kCpRow, s_pk + hf * kPkRow,
-                          s_dyn + tk * kRowWords, s_rec + tk * (4 * BK + 1), act, unit, ps, pos, end, sl);
+                          s_dyn + tk * kRowWords, s_rec + tk * (4 * BK + 1), w4, act, unit, pos, end, sl);
     else
-        bulk_value_half<BV>(p, hf, tk & 1, s_end, s_sv + hf * kFRow, s_cell, cell_base, act, unit, ps, pos, end, sl);
+        bulk_value_half<BV>(p, hf, tk & 1, s_sv + hf * kFRow, s_cell, cell_base, w4, act, ps, pos, end, sl);
 }
 
 }  // namespace
