@@ -45,6 +45,7 @@ constexpr int kBulkMinBlocks = 5;  // resident blocks per SM the register budget
 // tables follow the rows.
 constexpr int kRowWords = 65;
 constexpr int kBulkRowBytes = kBulkTok * kRowWords * 4;
+constexpr int kCellBatch = 5;      // 16-byte cell-table loads a thread has in flight during the set-up
 constexpr int kBulkPairBatch = 8;  // key pairs whose codes are computed before their fields are merged
 // Per-half tables are two rows, the second offset from the first so that the
 // two halves of a warp, reading entry i of their own rows at once, hit
@@ -391,7 +392,23 @@ __global__ void __launch_bounds__(kBulkThreads, kBulkMinBlocks) quantize_append_
     // ---- plan-static set-up (thread tid prepares codec coordinate tid)
     const HeadTab* ht = p.heads + h;
     const int nc = ht->n_coded;
-    for (int i = tid; i < p.cell_words; i += kBulkThreads) s_cell[i] = __ldg(p.cells + i);
+    {
+        // the cell tables, 16 bytes at a time: every thread's first kCellBatch
+        // loads are issued before any store (one round trip for tables of up
+        // to kCellBatch x 2 KB), then what is left, then the last 0-3 words
+        const int n4 = p.cell_words >> 2;
+        const uint4* src4 = reinterpret_cast<const uint4*>(p.cells);
+        uint4* dst4 = reinterpret_cast<uint4*>(s_cell);
+        uint4 t[kCellBatch];
+#pragma unroll
+        for (int k = 0; k < kCellBatch; ++k)
+            if (tid + k * kBulkThreads < n4) t[k] = __ldg(src4 + tid + k * kBulkThreads);
+#pragma unroll
+        for (int k = 0; k < kCellBatch; ++k)
+            if (tid + k * kBulkThreads < n4) dst4[tid + k * kBulkThreads] = t[k];
+        for (int i = tid + kCellBatch * kBulkThreads; i < n4; i += kBulkThreads) dst4[i] = __ldg(src4 + i);
+        if (tid < p.cell_words - 4 * n4) s_cell[4 * n4 + tid] = __ldg(p.cells + 4 * n4 + tid);
+    }
     {
         const int j = tid, jh = (j >> 6) * kPwRow + (j & 63), jf = (j >> 6) * kFRow + (j & 63);
         const bool coded = j < nc;
