@@ -150,6 +150,19 @@ def test_plan_tables_match_oracle(seed, bits_per_key, v_bits, layout):
         assert np.array_equal(t["slot_offset"], np.array(off))
 
 
+def test_lane_layout_hand_example_mixed_widths_in_the_library():
+    """The library's K record layout for K2 with blocks 0-15 at 3 bits, 16-31
+    at 1 and 32-63 at 2: the slots and offsets worked by hand from the rule
+    (the oracle's test of the same example derives them step by step)."""
+    bits = np.array([[3] * 16 + [1] * 16 + [2] * 32], np.uint8)
+    plan = bg.bgtq_plan_create(bits, np.ones((1, 64)), 4, 256, 2, 1, host_only=True)
+    t = plan.head_tables(0)
+    for ln in range(4):
+        assert list(t["slot_pair"][ln]) == [32 + ln, 40 + ln, ln, 8 + ln, 16 + ln, 24 + ln, 48 + ln, 56 + ln,
+                                            36 + ln, 44 + ln, 4 + ln, 12 + ln, 20 + ln, 28 + ln, 52 + ln, 60 + ln]
+        assert list(t["slot_offset"][ln]) == [0, 6, 12, 16, 20, 24, 28, 30, 32, 38, 44, 48, 52, 56, 60, 62]
+
+
 def test_infeasible_lane_layout_is_reported_by_both():
     bits = np.zeros((1, 64), np.uint8)
     bits[0, :9] = 7

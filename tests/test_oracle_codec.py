@@ -241,3 +241,37 @@ def test_lane_layout_hand_example_uniform_widths():
             m = sp[t][s]
             want = (2 * m % 4) | (((2 * m + 1) % 4) << 2)
             assert (word >> (4 * s)) & 0xF == want
+
+
+def test_lane_layout_hand_example_mixed_widths():
+    """K2 with three width classes, worked by hand from the rule.  Blocks 0-15
+    get 3 bits, 16-31 get 1, 32-63 get 2.  Codec order (pieces by size, then
+    width): the 64-piece of width 2 (blocks 32-63) is codec pairs 0-31, the
+    32-piece of width 3 (blocks 0-15) pairs 32-47, the 32-piece of width 1
+    (blocks 16-31) pairs 48-63.  Ranks by (width desc, index): pairs 32-47
+    are ranks 0-15, pairs 0-31 ranks 16-47, pairs 48-63 ranks 48-63.  Lane t
+    scans ranks = t (mod 4) first: 4 of width 3, 8 of width 2 and 4 of width 1,
+    16 pairs whose widths sum to 32 = 16 bK, so it takes exactly those.  In
+    the lane, sorted a_0..a_15 = 32+t, 36+t, 40+t, 44+t, t, 4+t, ..., 28+t,
+    48+t, ..., 60+t; slots take a_0, a_2, ..., a_14 then a_1, ..., a_15, and
+    the fields (2w bits) of slots 0-7 are 6, 6, 4, 4, 4, 4, 2, 2 bits long."""
+    bits = np.array([3] * 16 + [1] * 16 + [2] * 32)
+    kc = O.k_codec(bits, np.ones(O.NB), 1, 0)
+    sp, off, wd = O.k_lane_layout(kc, 2)
+    assert wd == [2] * 32 + [3] * 16 + [1] * 16
+    for t in range(4):
+        assert sp[t] == [32 + t, 40 + t, t, 8 + t, 16 + t, 24 + t, 48 + t, 56 + t,
+                         36 + t, 44 + t, 4 + t, 12 + t, 20 + t, 28 + t, 52 + t, 60 + t]
+        assert off[t] == [0, 6, 12, 16, 20, 24, 28, 30, 32, 38, 44, 48, 52, 56, 60, 62]
+    # pair m's codes: (m >> 2) and (m >> 2) + 3, each mod 2^w.  Lane 0, slots
+    # 0-7 (pairs 32, 40, 0, 8, 16, 24, 48, 56): fields 0 | 3 << 3 = 24,
+    # 2 | 5 << 3 = 42, 0 | 3 << 2 = 12, 2 | 1 << 2 = 6, 12, 6, 0 | 1 << 1 = 2, 2
+    # at bits 0, 6, 12, 16, 20, 24, 28, 30: 0xA6C6CA98 in the record's word 0
+    codes = np.zeros((1, 128), dtype=np.int64)
+    for m in range(64):
+        mask = (1 << wd[m]) - 1
+        codes[0, 2 * m] = (m >> 2) & mask
+        codes[0, 2 * m + 1] = ((m >> 2) + 3) & mask
+    rec = O.pack_k(codes, kc, 2).view("<u4")[0]
+    assert int(rec[0]) == 0xA6C6CA98
+    assert np.array_equal(O.unpack_k(O.pack_k(codes, kc, 2), kc, 2), codes)
