@@ -39,6 +39,10 @@
 // barrier (its parity names one phase there, S(j) having been issued after
 // PV(j - 2)); the move to the value dims after the prefix and the final read
 // wait on barriers committed once (PV of the last prefix tile; every MMA).
+// The P barrier: the MMA thread waits for P(j) right after issuing S(j + 1),
+// and the softmax can arrive P(j + 1) only once S(j + 1) has run and been
+// read, so its phase is never two ahead of that wait (were it, the wait would
+// run out and report the call as failed; no output would be wrong).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
