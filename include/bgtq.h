@@ -223,7 +223,8 @@ int bgtq_plan_get_codebook(const bgtq_plan* plan, int width, const float** centr
  * cell tables, on the host: the number of width-`width` thresholds <= u[i]
  * (TQ-MSE's nearest-centroid rule, review §1 Key Terms; the bulk encoder
  * takes its codes from the same tables).  u, codes: host arrays of n floats /
- * int32; NaN is INVALID_ARG.  For checking the tables against a plain count. */
+ * int32; a NaN is INVALID_ARG (the codes of the quotients before it are then
+ * written, the rest not).  For checking the tables against a plain count. */
 int bgtq_plan_code(const bgtq_plan* plan, int width, const float* u, int64_t n, int32_t* codes);
 
 /* Byte sizes of one layer's cache buffers for `batch` sequences of `capacity`
